@@ -1,0 +1,500 @@
+"""Benchmark: one KIVI decode step over the Llama-2-7B-shaped 2-bit cache.
+
+Workload (default): batch 8, 32 heads (MHA), d_h 128, K/V 2-bit, G 32,
+R 128, context 4096 with 3968 packed + 128 fp16 tokens for K and for V.
+A step is the whole hot path: quantize-append of the new token (V eviction
+quantized per token, K into the ring), decode attention over the cache, and
+the K block flush that the append left due -- all through the C ABI.  The
+cache lengths are reset after each step so every step sees the same state.
+
+value    = effective KV GB/s = algorithmic bytes read by the attention
+           (packed codes + fp16 scales/zeros + fp16 ring) / device step time
+roofline = the decode-attention kernel alone: the same bytes / its own
+           CUDA-event duration, against the measured HBM copy bandwidth
+e2e      = the same metric through the plain API calls with the step's
+           inputs copied from pinned host memory and the output read back
+L2 is flushed (256 MiB write) between timed steps: the cache (114 MB) would
+otherwise sit in the 129 MB L2.
+
+--impl reference times the CPU oracle (plain C + Python) on a bounded sample
+of the same workload (one (batch, kv-head) slice per step), scaled to the
+full step.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "decode-attn µs/step and effective KV GB/s (% of GB300 HBM peak), 2-bit"
+UNIT = "GB/s"
+WORKLOAD = "llama2_7b"
+
+
+def algorithmic_bytes(w, nk, nkr, nv, nvr):
+    """Bytes the attention must read: codes + fp16 scale/zero + fp16 ring."""
+    P = w["batch"] * w["h_kv"]
+    d, G, b = w["d"], w["G"], w["bits"]
+    per = nk * d * b // 8 + (nk // G) * d * 2 * 2 + nkr * d * 2
+    per += nv * d * b // 8 + nv * (d // G) * 2 * 2 + nvr * d * 2
+    return P * per
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_kv_cache_kivi_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("kvq_decode") or name.endswith((".h", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per decode launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "kvq_decode_llama2_7b.md")
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in txt.splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_hash")):
+            k, v = line.split(":", 1)
+            vals[k.strip().strip("-* `")] = v.strip().strip("`")
+    if vals.get("source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def setup_workload(w, device):
+    import torch
+    from quantized_kv_cache_kivi_gb300 import kvq, synth
+
+    B, Hq, H, d, G, R, bits = w["batch"], w["h_q"], w["h_kv"], w["d"], w["G"], w["R"], w["bits"]
+    L = w["n_packed"] + w["n_resid"]
+    cache = kvq.alloc_cache(B, H, Hq, d, G, R, [(bits, L + R)], device=device)
+    K, V = synth.kv_block(w["seed"], B, H, L - 1, d, w["n_out"], w["factor"])
+    kd = torch.from_numpy(K).to(device)
+    vd = torch.from_numpy(V).to(device)
+    st = kvq.kvq_quantize_append(cache, kd, vd)
+    if st == kvq.KVQ_FLUSH_DUE:
+        kvq.kvq_flush_residual(cache)
+    del kd, vd
+    torch.cuda.synchronize()
+    return cache
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from quantized_kv_cache_kivi_gb300 import kvq, synth
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    w = synth.WORKLOADS[WORKLOAD]
+    B, Hq, H, d = w["batch"], w["h_q"], w["h_kv"], w["d"]
+    cache = setup_workload(w, device)
+    c = cache.c
+    snap = (c.seg[0].nk, c.seg[0].nv, c.nkr, c.nvr, c.k_ring_start, c.v_ring_start)
+
+    def reset():
+        c.seg[0].nk, c.seg[0].nv, c.nkr, c.nvr, c.k_ring_start, c.v_ring_start = snap
+
+    n_in = args.steps + args.warmup
+    pool = 64  # distinct new tokens / queries cycled through the steps
+    kn, vn = synth.kv_block(w["seed"] + 100, B, H, pool, d, w["n_out"], w["factor"])
+    kn = torch.from_numpy(np.ascontiguousarray(kn.transpose(2, 0, 1, 3))).to(device)  # [pool][B][H][d]
+    vn = torch.from_numpy(np.ascontiguousarray(vn.transpose(2, 0, 1, 3))).to(device)
+    qp = torch.from_numpy(np.stack([synth.q_block(w["seed"], B, Hq, d, step=i)
+                                    for i in range(pool)])).to(device)
+    k_in = torch.empty(B, H, 1, d, dtype=torch.float16, device=device)
+    v_in = torch.empty_like(k_in)
+    q_in = torch.empty(B, Hq, d, dtype=torch.float16, device=device)
+    out = torch.empty_like(q_in)
+    ws = torch.zeros(kvq.kvq_workspace_bytes(cache, kvq.KVQ_MAX_SPLITS), dtype=torch.uint8,
+                     device=device)
+    l2 = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def stage_inputs(i):
+        j = i % pool
+        k_in.copy_(kn[j].unsqueeze(2))
+        v_in.copy_(vn[j].unsqueeze(2))
+        q_in.copy_(qp[j])
+
+    def step_append():
+        st = kvq.kvq_quantize_append(cache, k_in, v_in)
+        assert st == kvq.KVQ_FLUSH_DUE
+
+    def step_attn():
+        kvq.kvq_decode_attention(cache, q_in, out, ws)
+
+    def step_flush():
+        kvq.kvq_flush_residual(cache)
+
+    # attention reads the state right after the append (flush deferred)
+    reset()
+    stage_inputs(0)
+    step_append()
+    attn_state = (c.seg[0].nk, c.nkr, c.seg[0].nv, c.nvr)
+    step_attn()
+    step_flush()
+    reset()
+    torch.cuda.synchronize()
+    attn_bytes = algorithmic_bytes(w, *attn_state)
+
+    # capture the three calls as CUDA graphs (same lengths every step)
+    graphs = None
+    if not args.no_graph:
+        try:
+            graphs = []
+            for fn in (step_append, step_attn, step_flush):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn()
+                graphs.append(g)
+            reset()
+        except Exception as e:  # fall back to plain calls, and say so
+            print("graph capture failed (%s); timing plain calls" % e, file=sys.stderr)
+            graphs = None
+            reset()
+            torch.cuda.synchronize()
+
+    def run_step():
+        if graphs is not None:
+            for g in graphs:
+                g.replay()
+        else:
+            step_append()
+            step_attn()
+            step_flush()
+            reset()
+
+    for i in range(args.warmup):
+        l2.fill_(i & 255)
+        stage_inputs(i)
+        run_step()
+        if graphs is None:
+            reset()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.2)
+    stream = torch.cuda.current_stream()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        l2.fill_(i & 255)
+        stage_inputs(args.warmup + i)
+        e = ev[i]
+        if graphs is not None:
+            e[0].record(stream)
+            graphs[0].replay()
+            e[1].record(stream)
+            graphs[1].replay()
+            e[2].record(stream)
+            graphs[2].replay()
+            e[3].record(stream)
+        else:
+            e[0].record(stream)
+            step_append()
+            e[1].record(stream)
+            step_attn()
+            e[2].record(stream)
+            step_flush()
+            e[3].record(stream)
+            reset()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    step_ms = np.array([e[0].elapsed_time(e[3]) for e in ev])
+    attn_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    app_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    fl_ms = np.array([e[2].elapsed_time(e[3]) for e in ev])
+    total_ms = float(step_ms.sum())
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the plain API: pinned host inputs in, output back
+    kh_pool = kn.unsqueeze(3).cpu().pin_memory()  # [pool][B][H][1][d]
+    vh_pool = vn.unsqueeze(3).cpu().pin_memory()
+    qh_pool = qp.cpu().pin_memory()
+    oh = torch.empty(B, Hq, d, dtype=torch.float16).pin_memory()
+    e2e_s = []
+    n_e2e = min(args.steps, 500)
+    for i in range(n_e2e):
+        j = i % pool
+        kh, vh, qh = kh_pool[j], vh_pool[j], qh_pool[j]
+        l2.fill_(i & 255)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        k_in.copy_(kh, non_blocking=True)
+        v_in.copy_(vh, non_blocking=True)
+        q_in.copy_(qh, non_blocking=True)
+        step_append()
+        step_attn()
+        step_flush()
+        oh.copy_(out, non_blocking=True)
+        stream.synchronize()
+        e2e_s.append(time.perf_counter() - t0)
+        reset()
+    err = kvq.kvq_workspace_error(ws)
+    if err:
+        raise RuntimeError("decode kernel reported a timed-out wait")
+    e2e_step = float(np.mean(e2e_s))
+    return dict(w=w, attn_bytes=attn_bytes, total_ms=total_ms, step_ms=step_ms, attn_ms=attn_ms,
+                app_ms=app_ms, fl_ms=fl_ms, clocks=clocks, t_wall=t_wall, e2e_step=e2e_step,
+                graphs=graphs is not None, attn_state=attn_state,
+                h2d=(k_in.numel() + v_in.numel() + q_in.numel()) * 2,
+                d2h=oh.numel() * 2)
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+class OracleStep:
+    """One (batch, kv-head) slice of the workload's step, run by the oracle:
+    Algorithm 1 decoding update (flush deferred), fp64 attention over the
+    serialized cache, then the K flush; the state is restored afterwards."""
+
+    def __init__(self, w, b, h):
+        import oracle
+        from quantized_kv_cache_kivi_gb300 import synth
+        self.oracle = oracle
+        self.w = w
+        d, G, R, bits = w["d"], w["G"], w["R"], w["bits"]
+        L = w["n_packed"] + w["n_resid"]
+        K = synth.keys(w["seed"], b, h, L, d, w["n_out"], w["factor"])
+        V = synth.values(w["seed"], b, h, L, d)
+        self.head = oracle.KiviHead(d, G, R, bits)
+        self.head.prefill(K[:L - 1], V[:L - 1])
+        self.tk, self.tv = K[L - 1], V[L - 1]
+        gq = w["h_q"] // w["h_kv"]
+        self.q = synth.queries(w["seed"], b, w["h_q"], d)[h * gq:(h + 1) * gq]
+        self.cap = L + R
+
+    def run(self):
+        import copy
+        o = self.oracle
+        w = self.w
+        saved = copy.copy(self.head.__dict__)
+        saved = {k: (list(v) if isinstance(v, list) else v) for k, v in saved.items()}
+        hd = self.head
+        hd.decode_update(self.tk, self.tv, flush_k=False)
+        segs, kr, vr = o.head_buffers(hd, [self.cap])
+        K, V = o.dequant_head(segs, kr, vr, len(hd.kr), len(hd.vr), hd.krs, hd.vrs, w["d"], w["G"],
+                              w["R"])
+        out = o.attention_head(K, V, self.q.astype(np.float64), 1.0 / math.sqrt(w["d"]))
+        hd.flush_k()
+        self.head.__dict__.update(saved)
+        return out
+
+
+def oracle_rate(n_pairs_sample, seconds, warm=1):
+    """Time the oracle's per-slice step; returns (s per slice-step, steps, slices)."""
+    from quantized_kv_cache_kivi_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    steps = [OracleStep(w, i % w["batch"], (7 * i) % w["h_kv"]) for i in range(n_pairs_sample)]
+    for s in steps[:warm]:
+        s.run()
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        for s in steps:
+            s.run()
+            n += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    return (time.perf_counter() - t0) / n, n, len(steps)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.lib()
+    from quantized_kv_cache_kivi_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    P = w["batch"] * w["h_kv"]
+    step = OracleStep(w, 0, 0)
+    for _ in range(args.warmup):
+        step.run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step.run()
+        times.append(time.perf_counter() - t0)
+    per_slice = float(np.mean(times))
+    full_step_s = per_slice * P
+    nb = algorithmic_bytes(w, w["n_packed"], w["n_resid"], w["n_packed"], w["n_resid"])
+    value = nb / full_step_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": full_step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "llama2_7b: batch 8, 32 heads, d_h 128, 3968 packed + 128 fp16 "
+                   "tokens (K and V), 2-bit, G 32, R 128",
+                   "sample": "one (batch, kv-head) slice per step, scaled x%d" % P},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d steps of one slice of %d" % (args.steps, P)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from quantized_kv_cache_kivi_gb300 import kvq
+    kvq.lib()
+    r = run_ours(args, rank, world, local_rank)
+    w = r["w"]
+    total_bytes = r["attn_bytes"] * args.steps * world
+    value = total_bytes / (r["total_ms"] * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    attn_mean_ms = float(np.mean(r["attn_ms"]))
+    achieved = r["attn_bytes"] / (attn_mean_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": float(np.mean(r["step_ms"])), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": "llama2_7b: batch 8, 32 heads (MHA), d_h 128, 3968 packed + 128 fp16 "
+                        "tokens for K and V, 2-bit, G 32, R 128; step = quantize-append + "
+                        "decode attention + K flush",
+            "l2": "flushed between steps (256 MiB write)",
+            "graphs": r["graphs"], "parallelism": "replicas" if world > 1 else "single",
+            "us_per_step": float(np.mean(r["step_ms"])) * 1e3,
+            "us_attention": attn_mean_ms * 1e3,
+            "us_append": float(np.mean(r["app_ms"])) * 1e3,
+            "us_flush": float(np.mean(r["fl_ms"])) * 1e3,
+            "attn_state": dict(zip(("nk", "nkr", "nv", "nvr"), r["attn_state"])),
+            "algorithmic_bytes_per_step": r["attn_bytes"],
+            "wall_s_timed": r["t_wall"],
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "peak_kind": peak_kind, "kernel": "kvq decode_kernel<128,1>"},
+        "e2e": {"value": r["attn_bytes"] / r["e2e_step"] / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "us_per_step": r["e2e_step"] * 1e6},
+        "gpu_launches": 3 * args.steps,
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        import oracle
+        oracle.lib()
+        per, n, ns = oracle_rate(4, args.cpu_seconds)
+        P = w["batch"] * w["h_kv"]
+        v = r["attn_bytes"] / (per * P) / 1e9
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": "%d slice-steps over %d of %d (batch, kv-head) slices, "
+                                          "scaled to the full step" % (n, ns, P)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,616 @@
+// The C ABI of include/kvq.h: argument validation, planning of the launches
+// (token runs, tiles, splits, append bookkeeping), and the launches.  All
+// state lives in the caller's kvq_cache struct and device buffers.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kvq_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvq_status fail(kvq_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+kvq_status fail(kvq_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+kvq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ---------------------------------------------------------------------------
+// cache validation
+// ---------------------------------------------------------------------------
+kvq_status validate_cache(const kvq_cache* c) {
+  if (!c) return fail(KVQ_ERR_INVALID_ARG, "cache is NULL");
+  if (c->batch < 1 || c->h_kv < 1 || c->h_q < 1)
+    return fail(KVQ_ERR_INVALID_ARG, "batch, h_kv, h_q must be >= 1");
+  if (c->h_q % c->h_kv != 0) return fail(KVQ_ERR_INVALID_ARG, "h_q must be a multiple of h_kv");
+  if (c->h_q / c->h_kv > kvq::kMaxGq)
+    return fail(KVQ_ERR_UNSUPPORTED, "more than %d query heads per kv head", kvq::kMaxGq);
+  if (c->d_h != 64 && c->d_h != 128) return fail(KVQ_ERR_UNSUPPORTED, "d_h must be 64 or 128");
+  const int G = c->group;
+  if (G != 16 && G != 32 && G != 64 && G != 128)
+    return fail(KVQ_ERR_UNSUPPORTED, "group must be 16, 32, 64 or 128");
+  if (c->d_h % G != 0) return fail(KVQ_ERR_INVALID_ARG, "d_h must be a multiple of group");
+  if (c->resid_cap < G || c->resid_cap % G != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "resid_cap must be a positive multiple of group");
+  if (c->policy != KVQ_POLICY_KIVI && c->policy != KVQ_POLICY_FP16_TAIL)
+    return fail(KVQ_ERR_INVALID_ARG, "unknown policy %d", c->policy);
+  if (!std::isfinite(c->sm_scale)) return fail(KVQ_ERR_INVALID_ARG, "sm_scale is not finite");
+  if (c->n_seg < 1 || c->n_seg > KVQ_MAX_SEGMENTS)
+    return fail(KVQ_ERR_INVALID_ARG, "n_seg must be in 1..%d", KVQ_MAX_SEGMENTS);
+  if (!c->k_resid || !c->v_resid || !aligned16(c->k_resid) || !aligned16(c->v_resid))
+    return fail(KVQ_ERR_INVALID_ARG, "residual rings must be non-NULL and 16-byte aligned");
+  const int R = c->resid_cap;
+  if (c->nkr < 0 || c->nkr > R || c->nvr < 0 || c->nvr > R)
+    return fail(KVQ_ERR_INVALID_ARG, "nkr/nvr must be in 0..resid_cap");
+  if (c->k_ring_start < 0 || c->k_ring_start >= R || c->v_ring_start < 0 || c->v_ring_start >= R)
+    return fail(KVQ_ERR_INVALID_ARG, "ring starts must be in 0..resid_cap-1");
+  long long lk = c->nkr, lv = c->nvr;
+  for (int s = 0; s < c->n_seg; ++s) {
+    const kvq_segment& g = c->seg[s];
+    if (g.bits != 2 && g.bits != 4 && g.bits != 8)
+      return fail(KVQ_ERR_UNSUPPORTED, "segment %d: bits must be 2, 4 or 8", s);
+    if (g.capacity < 0 || g.capacity % G != 0)
+      return fail(KVQ_ERR_INVALID_ARG, "segment %d: capacity must be a multiple of group", s);
+    if (g.nk < 0 || g.nk > g.capacity || g.nv < 0 || g.nv > g.capacity || g.nk % G != 0)
+      return fail(KVQ_ERR_INVALID_ARG, "segment %d: bad nk/nv", s);
+    if (s + 1 < c->n_seg && g.nk != g.nv)
+      return fail(KVQ_ERR_INVALID_ARG, "segment %d: only the last segment may have nk != nv", s);
+    const void* p[6] = {g.k_codes, g.k_scale, g.k_zero, g.v_codes, g.v_scale, g.v_zero};
+    for (int i = 0; i < 6; ++i)
+      if (g.capacity > 0 && (!p[i] || !aligned16(p[i])))
+        return fail(KVQ_ERR_INVALID_ARG, "segment %d: buffers must be non-NULL, 16-byte aligned", s);
+    lk += g.nk;
+    lv += g.nv;
+  }
+  if (lk != lv) return fail(KVQ_ERR_INVALID_ARG, "K and V describe %lld vs %lld tokens", lk, lv);
+  if (lk > INT_MAX / 2) return fail(KVQ_ERR_INVALID_ARG, "too many tokens");
+  return KVQ_OK;
+}
+
+kvq::SegDev seg_dev(const kvq_segment& g) {
+  kvq::SegDev d;
+  d.kc = static_cast<const uint8_t*>(g.k_codes);
+  d.ks = static_cast<const __half*>(g.k_scale);
+  d.kz = static_cast<const __half*>(g.k_zero);
+  d.vc = static_cast<const uint8_t*>(g.v_codes);
+  d.vs = static_cast<const __half*>(g.v_scale);
+  d.vz = static_cast<const __half*>(g.v_zero);
+  d.bits = g.bits;
+  d.cap = g.capacity;
+  return d;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n > 0 ? n : 148;
+}
+
+// ---------------------------------------------------------------------------
+// decode planning: runs of uniform (K source, V source), tiles, splits
+// ---------------------------------------------------------------------------
+struct Piece {
+  int seg;  // -1 ring
+  int u0;
+  int len;
+};
+
+int tile_bytes(int tile, int kbits, int vbits, int d, int G) {
+  auto a16 = [](int x) { return (x + 15) & ~15; };
+  int b = a16(tile * d * kbits / 8) + a16(tile * d * vbits / 8);
+  if (kbits != 16) b += 2 * ((tile + G - 1) / G + 1) * d * 2;
+  if (vbits != 16) b += 2 * a16(tile * (d / G) * 2);
+  return b;
+}
+
+int choose_tile(int kbits, int vbits, int d, int G, int gq) {
+  for (int tile = 128; tile >= 32; tile >>= 1) {
+    if (tile_bytes(tile, kbits, vbits, d, G) > kvq::kStageBytes) continue;
+    if (kbits != 16 && ((tile + G - 1) / G + 1) * gq * d * 4 > kvq::kQsBytes) continue;
+    return tile;
+  }
+  return 0;
+}
+
+kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>& tile_cost) {
+  std::vector<Piece> kp, vp;
+  for (int s = 0; s < c->n_seg; ++s) {
+    if (c->seg[s].nk > 0) kp.push_back({s, 0, c->seg[s].nk});
+    if (c->seg[s].nv > 0) vp.push_back({s, 0, c->seg[s].nv});
+  }
+  if (c->nkr > 0) kp.push_back({-1, 0, c->nkr});
+  if (c->nvr > 0) vp.push_back({-1, 0, c->nvr});
+  const int gq = c->h_q / c->h_kv;
+  a.n_runs = 0;
+  a.n_tiles = 0;
+  tile_cost.clear();
+  size_t i = 0, j = 0;
+  int oi = 0, oj = 0;  // offsets consumed inside kp[i], vp[j]
+  while (i < kp.size() && j < vp.size()) {
+    const int len = std::min(kp[i].len - oi, vp[j].len - oj);
+    if (a.n_runs >= kvq::kMaxRuns) return fail(KVQ_ERR_UNSUPPORTED, "too many token runs");
+    kvq::Run& r = a.runs[a.n_runs++];
+    r.seg_k = kp[i].seg;
+    r.seg_v = vp[j].seg;
+    r.u0_k = kp[i].u0 + oi;
+    r.u0_v = vp[j].u0 + oj;
+    r.len = len;
+    const int kb = r.seg_k >= 0 ? c->seg[r.seg_k].bits : 16;
+    const int vb = r.seg_v >= 0 ? c->seg[r.seg_v].bits : 16;
+    r.tile = choose_tile(kb, vb, c->d_h, c->group, gq);
+    if (r.tile == 0) return fail(KVQ_ERR_UNSUPPORTED, "no tile size fits shared memory");
+    r.groups = (r.tile + c->group - 1) / c->group + 1;
+    r.tile0 = a.n_tiles;
+    const int nt = (len + r.tile - 1) / r.tile;
+    for (int t = 0; t < nt; ++t) {
+      const int n = std::min(r.tile, len - t * r.tile);
+      tile_cost.push_back(tile_bytes(n, kb, vb, c->d_h, c->group));
+    }
+    a.n_tiles += nt;
+    oi += len;
+    oj += len;
+    if (oi == kp[i].len) { ++i; oi = 0; }
+    if (oj == vp[j].len) { ++j; oj = 0; }
+  }
+  return KVQ_OK;
+}
+
+// Splits per (batch, kv head): minimise the per-SM load model
+// ceil(pairs * s / SMs) * (1/s + f), f = fixed cost of one CTA relative to a
+// whole head's stream; ties go to fewer splits.
+int choose_splits(int n_pairs, int n_tiles, int max_splits) {
+  const int n_sm = sm_count();
+  const int cap = std::min(std::min(max_splits, n_tiles), KVQ_MAX_SPLITS);
+  const double f = 0.02;
+  int best = 1;
+  double best_t = 1e300;
+  for (int s = 1; s <= cap; ++s) {
+    const double rounds = std::ceil((double)n_pairs * s / n_sm);
+    const double t = rounds * (1.0 / s + f);
+    if (t < best_t * (1.0 - 1e-9)) {
+      best_t = t;
+      best = s;
+    }
+  }
+  return best;
+}
+
+// Walk every tile of the first and the last (batch, kv head) through the same
+// geometry the kernel uses and check each bulk copy before anything launches:
+// 16-byte alignment, source inside its buffer's documented extent, the stage
+// and the scaled-query table large enough, and the copies adding up to the
+// byte count the tile's mbarrier expects (so no wait can be left short).
+kvq_status verify_decode_plan(const kvq_cache* c, const kvq::DecodeArgs& a, int n_pairs) {
+  const size_t P = (size_t)n_pairs, D = (size_t)a.d, G = (size_t)a.G, R = (size_t)a.R;
+  for (int which = 0; which < 2; ++which) {
+    const size_t pair = which == 0 ? 0 : P - 1;
+    for (int t = 0; t < a.n_tiles; ++t) {
+      const kvq::TileInfo ti = kvq::tile_info(a, t);
+      if (ti.n < 1 || ti.n > 128) return fail(KVQ_ERR_UNSUPPORTED, "tile %d has %d tokens", t, ti.n);
+      if (ti.bytes > (uint32_t)kvq::kStageBytes)
+        return fail(KVQ_ERR_UNSUPPORTED, "tile %d needs %u stage bytes", t, ti.bytes);
+      if (ti.kseg >= 0 && (size_t)ti.ng * a.gq * D * 4 > (size_t)kvq::kQsBytes)
+        return fail(KVQ_ERR_UNSUPPORTED, "tile %d: scaled-query table too small", t);
+      kvq::BulkCopy cp[8];
+      const int n = kvq::tile_copies(a, pair, t, ti, cp);
+      uint64_t sum = 0;
+      for (int i = 0; i < n; ++i) {
+        const kvq::BulkCopy& k = cp[i];
+        const uint8_t* base;
+        size_t size;
+        if (k.buf >= 6) {
+          base = static_cast<const uint8_t*>(k.buf == 6 ? c->k_resid : c->v_resid);
+          size = P * R * D * 2;
+        } else {
+          const kvq_segment& g = c->seg[k.seg];
+          const size_t cap = (size_t)g.capacity, rb = D * g.bits / 8;
+          const void* ptrs[6] = {g.k_codes, g.k_scale, g.k_zero, g.v_codes, g.v_scale, g.v_zero};
+          const size_t sizes[6] = {P * cap * rb, P * (cap / G) * D * 2, P * (cap / G) * D * 2,
+                                   P * cap * rb, P * cap * (D / G) * 2, P * cap * (D / G) * 2};
+          base = static_cast<const uint8_t*>(ptrs[k.buf]);
+          size = sizes[k.buf];
+        }
+        const uint8_t* src = static_cast<const uint8_t*>(k.src);
+        if (k.bytes == 0 || k.bytes % 16 || (uintptr_t)src % 16 || k.dst_off % 16)
+          return fail(KVQ_ERR_INVALID_ARG, "tile %d copy %d: misaligned (%u bytes)", t, i, k.bytes);
+        if (src < base || src + k.bytes > base + size)
+          return fail(KVQ_ERR_INVALID_ARG, "tile %d copy %d: outside its buffer", t, i);
+        if ((uint64_t)k.dst_off + k.bytes > ti.bytes)
+          return fail(KVQ_ERR_INVALID_ARG, "tile %d copy %d: outside the stage", t, i);
+        sum += k.bytes;
+      }
+      if (sum != ti.bytes)
+        return fail(KVQ_ERR_INVALID_ARG, "tile %d: copies %llu != expected %u bytes", t,
+                    (unsigned long long)sum, ti.bytes);
+    }
+  }
+  return KVQ_OK;
+}
+
+size_t ws_fixed(int n_pairs) {
+  return kvq::kWorkspaceHeader + (((size_t)n_pairs * 4 + 255) / 256) * 256;
+}
+
+// ---------------------------------------------------------------------------
+// append bookkeeping (KIVI Algorithm 1 over T pushed tokens)
+// ---------------------------------------------------------------------------
+kvq_status append_kivi(kvq_cache* c, const void* k_new, const void* v_new, int T,
+                       cudaStream_t st) {
+  const int R = c->resid_cap, G = c->group;
+  kvq_segment& last = c->seg[c->n_seg - 1];
+  kvq::AppendArgs a{};
+  a.batch = c->batch;
+  a.h_kv = c->h_kv;
+  a.d = c->d_h;
+  a.G = G;
+  a.R = R;
+  a.T = T;
+  a.k_new = static_cast<const __half*>(k_new);
+  a.v_new = static_cast<const __half*>(v_new);
+  a.kr = static_cast<__half*>(c->k_resid);
+  a.vr = static_cast<__half*>(c->v_resid);
+  a.dst = seg_dev(last);
+  a.bits = last.bits;
+  int fb = 0, evict = 0;
+  bool flush_due = false;
+  if (c->policy == KVQ_POLICY_KIVI) {
+    // K: blocks of R pushed tokens are quantized; a block ending exactly at
+    // the last token is left for kvq_flush_residual.
+    const long long pushed = (long long)c->nkr + T;
+    long long nb = pushed / R;
+    if (nb >= 1 && pushed % R == 0) {
+      flush_due = true;
+      --nb;
+    }
+    fb = (int)nb;
+    // V: everything but the newest R pushed tokens is quantized.
+    evict = (int)std::max(0LL, (long long)c->nvr + T - R);
+  } else {
+    if (c->nkr + T > R || c->nvr + T > R)
+      return fail(KVQ_ERR_CAPACITY, "fp16 ring full: %d + %d tokens > resid_cap %d",
+                  std::max(c->nkr, c->nvr), T, R);
+  }
+  if ((long long)last.nk + (long long)fb * R > last.capacity ||
+      (long long)last.nv + evict > last.capacity)
+    return fail(KVQ_ERR_CAPACITY, "last segment full (capacity %d)", last.capacity);
+  a.k_groups = fb * R / G;
+  a.k_nk0 = last.nk;
+  a.ksrc = {c->nkr, c->k_ring_start};
+  a.k_ring_groups = std::min(a.k_groups, (c->nkr + G - 1) / G);
+  a.v_evict = evict;
+  a.v_nv0 = last.nv;
+  a.vsrc = {c->nvr, c->v_ring_start};
+  a.v_ring_tokens = std::min(evict, c->nvr);
+  a.k_first_ring = std::max(0, fb * R - c->nkr);
+  a.k_slot0 = c->k_ring_start + c->nkr;
+  a.v_first_ring = std::max(0, evict - c->nvr);
+  a.v_slot0 = c->v_ring_start + c->nvr;
+  const int in_k = a.k_groups - a.k_ring_groups;
+  const int in_v = a.v_evict - a.v_ring_tokens;
+  a.chunks = (in_k + in_v > 0) ? 1 + std::min(256, in_k + (in_v + 63) / 64) : 1;
+  if (a.chunks == 2 && a.k_ring_groups == 0 && a.v_ring_tokens == 0 && a.k_first_ring >= T &&
+      a.v_first_ring >= T)
+    a.chunks = 1;
+  const cudaError_t e = kvq::launch_append(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  // new lengths
+  last.nk += fb * R;
+  c->nkr = c->nkr + T - fb * R;
+  last.nv += evict;
+  c->v_ring_start = (c->v_ring_start + evict) % R;
+  c->nvr = c->nvr + T - evict;
+  return flush_due ? KVQ_FLUSH_DUE : KVQ_OK;
+}
+
+kvq_status append_plan(kvq_cache* c, const void* k_new, const void* v_new, int T,
+                       const kvq_window_plan* p, cudaStream_t st) {
+  const int R = c->resid_cap, G = c->group;
+  if (c->policy != KVQ_POLICY_FP16_TAIL)
+    return fail(KVQ_ERR_INVALID_ARG, "a window plan needs policy KVQ_POLICY_FP16_TAIL");
+  if (p->window < G || p->window % G != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "window must be a positive multiple of group");
+  if (p->n_windows < 0 || p->n_windows > kvq::kMaxWindowJobs)
+    return fail(KVQ_ERR_UNSUPPORTED, "n_windows must be in 0..%d", kvq::kMaxWindowJobs);
+  if ((long long)p->n_windows * p->window > T)
+    return fail(KVQ_ERR_INVALID_ARG, "windows exceed the %d input tokens", T);
+  if (p->n_windows > 0 && (!p->bits || !p->perm))
+    return fail(KVQ_ERR_INVALID_ARG, "plan bits/perm are NULL");
+  std::vector<char> seen(p->n_windows, 0);
+  for (int i = 0; i < p->n_windows; ++i) {
+    const int w = p->perm[i];
+    if (w < 0 || w >= p->n_windows || seen[w]) return fail(KVQ_ERR_INVALID_ARG, "perm is not a permutation");
+    seen[w] = 1;
+    const int b = p->bits[w];
+    if (b != 2 && b != 4 && b != 8 && b != 16) return fail(KVQ_ERR_INVALID_ARG, "window bits must be 2/4/8/16");
+  }
+  kvq::IngestArgs a{};
+  a.batch = c->batch;
+  a.h_kv = c->h_kv;
+  a.d = c->d_h;
+  a.G = G;
+  a.R = R;
+  a.T = T;
+  a.S = p->window;
+  a.k_new = static_cast<const __half*>(k_new);
+  a.v_new = static_cast<const __half*>(v_new);
+  a.kr = static_cast<__half*>(c->k_resid);
+  a.vr = static_cast<__half*>(c->v_resid);
+  for (int s = 0; s < c->n_seg; ++s) a.seg[s] = seg_dev(c->seg[s]);
+  a.krs_push = c->k_ring_start + c->nkr;
+  a.vrs_push = c->v_ring_start + c->nvr;
+  std::vector<int> add(c->n_seg, 0);
+  int ring = 0;
+  a.n_jobs = p->n_windows;
+  for (int i = 0; i < p->n_windows; ++i) {
+    const int w = p->perm[i];
+    kvq::WindowJob& job = a.jobs[i];
+    job.src_token = w * p->window;
+    if (p->bits[w] == 16) {
+      job.seg = -1;
+      job.dst = ring;
+      ring += p->window;
+      continue;
+    }
+    int s = 0;
+    while (s < c->n_seg && c->seg[s].bits != p->bits[w]) ++s;
+    if (s == c->n_seg) return fail(KVQ_ERR_INVALID_ARG, "no segment of width %d", (int)p->bits[w]);
+    if (c->seg[s].nk != c->seg[s].nv)
+      return fail(KVQ_ERR_INVALID_ARG, "segment %d has nk != nv", s);
+    job.seg = s;
+    job.dst = c->seg[s].nk + add[s];
+    add[s] += p->window;
+  }
+  a.tail_src = p->n_windows * p->window;
+  a.tail_len = T - a.tail_src;
+  a.tail_dst = ring;
+  ring += a.tail_len;
+  for (int s = 0; s < c->n_seg; ++s)
+    if ((long long)c->seg[s].nk + add[s] > c->seg[s].capacity)
+      return fail(KVQ_ERR_CAPACITY, "segment %d full (capacity %d)", s, c->seg[s].capacity);
+  if (c->nkr + ring > R || c->nvr + ring > R)
+    return fail(KVQ_ERR_CAPACITY, "fp16 ring full: %d more tokens", ring);
+  const cudaError_t e = kvq::launch_ingest(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "ingest launch");
+  for (int s = 0; s < c->n_seg; ++s) {
+    c->seg[s].nk += add[s];
+    c->seg[s].nv += add[s];
+  }
+  c->nkr += ring;
+  c->nvr += ring;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_FLUSH_DUE: return "flush due: the K residual holds resid_cap tokens";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_CAPACITY: return "capacity exceeded";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+const char* kvq_last_error_string(void) { return g_last_error.c_str(); }
+
+kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* v_new, int32_t T,
+                               const kvq_window_plan* plan, void* stream) {
+  kvq_status st = validate_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (T < 0) return fail(KVQ_ERR_INVALID_ARG, "T must be >= 0");
+  if (T == 0) return KVQ_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+    return fail(KVQ_ERR_INVALID_ARG, "k_new/v_new must be non-NULL and 16-byte aligned");
+  if (plan) return append_plan(cache, k_new, v_new, T, plan, as_stream(stream));
+  return append_kivi(cache, k_new, v_new, T, as_stream(stream));
+}
+
+kvq_status kvq_flush_residual(kvq_cache* cache, void* stream) {
+  kvq_status st = validate_cache(cache);
+  if (st != KVQ_OK) return st;
+  const int G = cache->group, R = cache->resid_cap;
+  const int n = (cache->nkr / G) * G;
+  if (n == 0) return KVQ_OK;
+  kvq_segment& last = cache->seg[cache->n_seg - 1];
+  if ((long long)last.nk + n > last.capacity)
+    return fail(KVQ_ERR_CAPACITY, "last segment full (capacity %d)", last.capacity);
+  kvq::AppendArgs a{};
+  a.batch = cache->batch;
+  a.h_kv = cache->h_kv;
+  a.d = cache->d_h;
+  a.G = G;
+  a.R = R;
+  a.kr = static_cast<__half*>(cache->k_resid);
+  a.dst = seg_dev(last);
+  a.bits = last.bits;
+  a.k_groups = n / G;
+  a.k_nk0 = last.nk;
+  a.ksrc = {INT_MAX, cache->k_ring_start};
+  const cudaError_t e = kvq::launch_flush(a, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "flush launch");
+  last.nk += n;
+  cache->nkr -= n;
+  cache->k_ring_start = (cache->k_ring_start + n) % R;
+  return KVQ_OK;
+}
+
+size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t max_splits) {
+  if (!cache || cache->batch < 1 || cache->h_kv < 1 || cache->h_q < cache->h_kv) return 0;
+  if (max_splits < 1) max_splits = 1;
+  if (max_splits > KVQ_MAX_SPLITS) max_splits = KVQ_MAX_SPLITS;
+  const int n_pairs = cache->batch * cache->h_kv;
+  const int gq = cache->h_q / cache->h_kv;
+  size_t b = ws_fixed(n_pairs);
+  if (max_splits > 1) b += (size_t)n_pairs * max_splits * gq * (cache->d_h + 2) * sizeof(float);
+  return b;
+}
+
+kvq_status kvq_workspace_init(void* ws, size_t bytes, void* stream) {
+  if (!ws || bytes == 0) return fail(KVQ_ERR_INVALID_ARG, "workspace is NULL/empty");
+  const cudaError_t e = cudaMemsetAsync(ws, 0, bytes, as_stream(stream));
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "workspace memset");
+}
+
+kvq_status kvq_workspace_error(const void* ws, int32_t* err_out, void* stream) {
+  if (!ws || !err_out) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
+  cudaError_t e = cudaMemcpyAsync(err_out, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, as_stream(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "reading the workspace error word");
+}
+
+kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out, void* ws,
+                                size_t ws_bytes, void* stream) {
+  kvq_status st = validate_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!q || !out || !aligned16(q) || !aligned16(out))
+    return fail(KVQ_ERR_INVALID_ARG, "q/out must be non-NULL and 16-byte aligned");
+  const int n_pairs = cache->batch * cache->h_kv;
+  if (!ws || !aligned16(ws) || ws_bytes < ws_fixed(n_pairs))
+    return fail(KVQ_ERR_WORKSPACE, "workspace needs at least %zu bytes", ws_fixed(n_pairs));
+  cudaStream_t s = as_stream(stream);
+  const int gq = cache->h_q / cache->h_kv;
+  kvq::DecodeArgs a{};
+  std::vector<int> cost;
+  st = plan_decode(cache, a, cost);
+  if (st != KVQ_OK) return st;
+  if (a.n_tiles == 0) {
+    const size_t bytes = (size_t)cache->batch * cache->h_q * cache->d_h * 2;
+    const cudaError_t e = cudaMemsetAsync(out, 0, bytes, s);
+    return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "zero output");
+  }
+  const size_t per_split = (size_t)n_pairs * gq * (cache->d_h + 2) * sizeof(float);
+  const int ws_splits = (int)std::min<size_t>(KVQ_MAX_SPLITS, (ws_bytes - ws_fixed(n_pairs)) / per_split);
+  const int S = choose_splits(n_pairs, a.n_tiles, std::max(1, ws_splits));
+  // split boundaries with equal byte cost: split k ends at the first tile
+  // whose cost midpoint passes k/S of the head's bytes
+  std::vector<long long> prefix(a.n_tiles + 1, 0);
+  for (int t = 0; t < a.n_tiles; ++t) prefix[t + 1] = prefix[t] + cost[t];
+  const long long total = prefix[a.n_tiles];
+  a.n_splits = S;
+  a.split_tile[0] = 0;
+  for (int k = 1; k < S; ++k) {
+    const long long target = total * k / S;
+    int t = a.split_tile[k - 1] + 1;
+    while (t < a.n_tiles && 2 * prefix[t] + cost[t] <= 2 * target) ++t;
+    a.split_tile[k] = std::min(t, a.n_tiles - (S - k));
+  }
+  a.split_tile[S] = a.n_tiles;
+  for (int k = 1; k <= S; ++k)
+    if (a.split_tile[k] <= a.split_tile[k - 1])
+      return fail(KVQ_ERR_UNSUPPORTED, "split planning failed");
+  a.batch = cache->batch;
+  a.h_kv = cache->h_kv;
+  a.gq = gq;
+  a.d = cache->d_h;
+  a.G = cache->group;
+  a.R = cache->resid_cap;
+  a.scale_log2 = cache->sm_scale * 1.4426950408889634f;
+  a.n_seg = cache->n_seg;
+  for (int i = 0; i < cache->n_seg; ++i) a.seg[i] = seg_dev(cache->seg[i]);
+  a.kr = static_cast<const __half*>(cache->k_resid);
+  a.vr = static_cast<const __half*>(cache->v_resid);
+  a.krs = cache->k_ring_start;
+  a.vrs = cache->v_ring_start;
+  a.q = static_cast<const __half*>(q);
+  a.out = static_cast<__half*>(out);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.err = reinterpret_cast<int*>(w);
+  a.counters = reinterpret_cast<int*>(w + kvq::kWorkspaceHeader);
+  a.part = reinterpret_cast<float*>(w + ws_fixed(n_pairs));
+  st = verify_decode_plan(cache, a, n_pairs);
+  if (st != KVQ_OK) return st;
+  const cudaError_t e = kvq::launch_decode(a, n_pairs, s);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "decode launch");
+}
+
+size_t kvq_window_assign_workspace_bytes(int32_t batch, int32_t h_kv, int32_t d_h, int32_t M,
+                                         int32_t S) {
+  if (batch < 1 || h_kv < 1 || d_h < 1 || S < 1 || M < S) return 0;
+  const size_t nw = (size_t)M / S;
+  auto a256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  return a256((size_t)batch * h_kv * d_h * 8) + a256((size_t)batch * nw * 16) + a256(nw * 8) +
+         a256(nw) + a256(nw * 4);
+}
+
+kvq_status kvq_window_assign(const void* keys, const void* text_keys, int32_t batch, int32_t h_kv,
+                             int32_t d_h, int32_t M, int32_t S, int32_t N, float frac8,
+                             float frac4, int32_t first_window_fp16, void* ws, size_t ws_bytes,
+                             int8_t* bits_out, int32_t* perm_out, double* sim_out, void* stream) {
+  if (!keys || !text_keys || !bits_out || !perm_out)
+    return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
+  if (batch < 1 || h_kv < 1 || d_h < 1 || S < 1 || M < S || N < 1)
+    return fail(KVQ_ERR_INVALID_ARG, "bad sizes");
+  if (!(frac8 >= 0.f && frac4 >= 0.f && frac8 + frac4 <= 1.f))
+    return fail(KVQ_ERR_INVALID_ARG, "fractions must be >= 0 and sum to <= 1");
+  const size_t need = kvq_window_assign_workspace_bytes(batch, h_kv, d_h, M, S);
+  if (!ws || !aligned16(ws) || ws_bytes < need)
+    return fail(KVQ_ERR_WORKSPACE, "window workspace needs %zu bytes", need);
+  const int nw = M / S;
+  const int ranked = nw - (first_window_fp16 ? 1 : 0);
+  int n8 = (int)std::floor((double)frac8 * ranked);
+  int n4 = (int)std::floor((double)frac4 * ranked);
+  n8 = std::min(n8, ranked);
+  n4 = std::min(n4, ranked - n8);
+  auto a256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  kvq::WindowArgs a{};
+  a.keys = static_cast<const __half*>(keys);
+  a.text = static_cast<const __half*>(text_keys);
+  a.batch = batch;
+  a.h_kv = h_kv;
+  a.d = d_h;
+  a.M = M;
+  a.S = S;
+  a.N = N;
+  a.n8 = n8;
+  a.n4 = n4;
+  a.first_fp16 = first_window_fp16 ? 1 : 0;
+  size_t off = 0;
+  a.tsum = reinterpret_cast<double*>(w + off);
+  off += a256((size_t)batch * h_kv * d_h * 8);
+  a.wstat = reinterpret_cast<double*>(w + off);
+  off += a256((size_t)batch * nw * 16);
+  a.sim = reinterpret_cast<double*>(w + off);
+  off += a256((size_t)nw * 8);
+  a.bits = reinterpret_cast<int8_t*>(w + off);
+  off += a256((size_t)nw);
+  a.perm = reinterpret_cast<int32_t*>(w + off);
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = kvq::launch_window_assign(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "window assign launch");
+  e = cudaMemcpyAsync(bits_out, a.bits, nw, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(perm_out, a.perm, (size_t)nw * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && sim_out)
+    e = cudaMemcpyAsync(sim_out, a.sim, (size_t)nw * 8, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "window assign copy-back");
+}
+
+}  // extern "C"

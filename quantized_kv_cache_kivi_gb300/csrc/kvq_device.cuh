@@ -1,0 +1,132 @@
+// Device helpers: the quantizer's arithmetic, and the bulk-copy / mbarrier
+// primitives of the decode pipeline (sm_100+ PTX).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace kvq {
+
+// ---------------------------------------------------------------------------
+// The quantizer (KIVI "方法细节": Q(X) = round((X - z) / s), X' = Q s + z;
+// WindowQuant §3.3.3 Eq.14/16: s = (max - min)/(qmax - qmin), clamp to
+// [0, 2^b - 1]).  Expression order fixed so codes, scales and zeros are
+// reproducible bit for bit: fp32 subtract, IEEE divide, fp16 round-to-nearest
+// of s, z = min (exact), codes from the fp16-rounded s, rint half-to-even.
+// ---------------------------------------------------------------------------
+struct QParams {
+  float s;  // fp16-rounded scale as fp32
+  float z;  // zero point (the minimum) as fp32
+  __half sh, zh;
+};
+
+__device__ __forceinline__ QParams qparams(float mn, float mx, int bits) {
+  const float qmax = (float)((1 << bits) - 1);
+  QParams p;
+  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+  p.sh = __float2half_rn(s32);
+  p.zh = __float2half_rn(mn);
+  p.s = __half2float(p.sh);
+  p.z = __half2float(p.zh);
+  return p;
+}
+
+__device__ __forceinline__ uint32_t qcode(float x, const QParams& p, int bits) {
+  if (p.s == 0.0f) return 0u;
+  const float qmax = (float)((1 << bits) - 1);
+  float r = rintf(__fdiv_rn(__fsub_rn(x, p.z), p.s));
+  r = fminf(fmaxf(r, 0.0f), qmax);
+  return (uint32_t)r;
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory address, mbarrier and 1-D bulk copy (TMA engine, no tensor map)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier for at most ~2^31 SM clocks (about a
+// second).  Returns false on timeout; the caller records the error and stops.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > (1ll << 31)) return false;
+  }
+  return true;
+}
+
+// global -> shared bulk copy completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Packed fp32 pair arithmetic (sm_100+): two lanes of fp32 per instruction.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(*reinterpret_cast<unsigned long long*>(&d))
+      : "l"(*reinterpret_cast<unsigned long long*>(&a)),
+        "l"(*reinterpret_cast<unsigned long long*>(&b)),
+        "l"(*reinterpret_cast<unsigned long long*>(&c)));
+  return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(*reinterpret_cast<unsigned long long*>(&d))
+      : "l"(*reinterpret_cast<unsigned long long*>(&a)),
+        "l"(*reinterpret_cast<unsigned long long*>(&b)));
+  return d;
+}
+
+// Code of `bits` width at bit position `pos` of word w, as an exact fp32
+// value times 2^pos: (w & mask) is OR-ed into the mantissa of 2^23, and 2^23
+// is subtracted.  Exact while the masked field stays below 2^23 (pos <= 21
+// for 2-bit fields).
+__device__ __forceinline__ float field_scaled(uint32_t w, uint32_t mask) {
+  return __uint_as_float((w & mask) | 0x4B000000u) - 8388608.0f;
+}
+
+}  // namespace kvq

@@ -1,0 +1,246 @@
+// Internal launch descriptors shared by the host planner (kvq_api.cu) and the
+// kernels.  Everything is passed to kernels by value; nothing here allocates.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kMaxRuns = 20;        // token runs of uniform (K source, V source)
+constexpr int kMaxGq = 8;           // query heads per kv head handled by one CTA
+constexpr int kDecodeThreads = 256; // threads of a decode CTA
+constexpr int kStageBytes = 20480;  // one pipeline stage of staged tile data
+constexpr int kStages = 3;          // pipeline depth
+constexpr int kQsBytes = 16384;     // per-tile scaled-query table (K groups)
+constexpr int kWorkspaceHeader = 256;  // error word + padding at workspace start
+
+// One packed segment as the kernels see it (base pointers of the whole array).
+struct SegDev {
+  const uint8_t* kc;
+  const __half* ks;
+  const __half* kz;
+  const uint8_t* vc;
+  const __half* vs;
+  const __half* vz;
+  int bits;
+  int cap;
+};
+
+// A run of consecutive attention positions whose K comes from one source and
+// whose V comes from one source.  seg_* = segment index, or -1 for the ring.
+// u0_* = first packed row (segment source) or first ring index (ring source).
+struct Run {
+  int seg_k, seg_v;
+  int u0_k, u0_v;
+  int len;    // tokens in the run
+  int tile;   // tokens per tile
+  int tile0;  // index of the run's first tile among the head's tiles
+  int groups; // max K scale groups one tile of this run touches (packed K)
+};
+
+struct DecodeArgs {
+  int batch, h_kv, gq, d, G, R;
+  float scale_log2;  // sm_scale * log2(e)
+  int n_seg;
+  SegDev seg[KVQ_MAX_SEGMENTS];
+  const __half* kr;
+  const __half* vr;
+  int krs, vrs;
+  int n_runs;
+  Run runs[kMaxRuns];
+  int n_tiles;   // tiles per (batch, kv head)
+  int n_splits;  // CTAs per (batch, kv head)
+  int split_tile[KVQ_MAX_SPLITS + 1];
+  const __half* q;
+  __half* out;
+  float* part;   // [pairs][splits][gq][d + 2]  (o..., m, l)
+  int* counters; // [pairs]
+  int* err;      // device error word
+};
+
+// Where the rows of a K group / V token come from during an append:
+// push index p < n_old reads ring slot (start + p) % R, otherwise input row
+// (p - n_old) of the new tokens.
+struct RowSrc {
+  int n_old;
+  int start;
+};
+
+struct AppendArgs {
+  int batch, h_kv, d, G, R, T;
+  const __half* k_new;  // [B][H][T][d]
+  const __half* v_new;
+  __half* kr;           // ring [B][H][R][d]
+  __half* vr;
+  // destination: last segment (KIVI) or the plan's segment
+  SegDev dst;
+  int bits;
+  // K side: groups of G pushed tokens to quantize into packed rows nk0 + p
+  int k_groups;         // number of groups (flushed tokens / G)
+  int k_nk0;            // packed K rows already valid
+  RowSrc ksrc;
+  int k_ring_groups;    // groups that read at least one old ring token
+  // V side: pushed tokens p < v_evict are quantized into packed row nv0 + p
+  int v_evict;
+  int v_nv0;
+  RowSrc vsrc;
+  int v_ring_tokens;    // evicted tokens that come from the old ring
+  // ring writes of new tokens: K new token j (j >= k_first_ring) -> slot
+  // (k_slot0 + j) % R, likewise V
+  int k_first_ring, k_slot0;
+  int v_first_ring, v_slot0;
+  int chunks;           // CTAs per (batch, kv head); chunk 0 does ring work
+};
+
+struct WindowJob {   // one window of the WindowQuant ingest plan
+  int src_token;     // first input token of the window
+  int seg;           // destination segment, -1 = fp16 ring
+  int dst;           // first packed row (segment) or ring push index (ring)
+};
+
+constexpr int kMaxWindowJobs = 512;
+
+struct IngestArgs {
+  int batch, h_kv, d, G, R, T, S;
+  const __half* k_new;
+  const __half* v_new;
+  __half* kr;
+  __half* vr;
+  SegDev seg[KVQ_MAX_SEGMENTS];
+  int krs_push, vrs_push;  // ring slot of push index 0 (start + count)
+  int n_jobs;              // windows; tail handled as job n_jobs
+  int tail_src, tail_len, tail_dst;
+  WindowJob jobs[kMaxWindowJobs];
+};
+
+// ---------------------------------------------------------------------------
+// Tile geometry and the bulk copies that stage one tile in shared memory.
+// Used by the decode kernel to issue its copies and by the host to check,
+// before any launch, that every copy stays inside its buffer.
+// ---------------------------------------------------------------------------
+struct TileInfo {
+  int n;           // tokens in the tile
+  int kseg, vseg;  // source segment, -1 = ring
+  int ku0, vu0;    // first packed row / first ring index
+  int g0, ng;      // first K scale group, groups touched (packed K)
+  int kbits, vbits;
+  uint32_t k_off, ks_off, kz_off, v_off, vs_off, vz_off, bytes;
+};
+
+__host__ __device__ inline uint32_t align16u(uint32_t x) { return (x + 15u) & ~15u; }
+
+__host__ __device__ inline TileInfo tile_info(const DecodeArgs& a, int t) {
+  int r = 0;
+  while (r + 1 < a.n_runs && a.runs[r + 1].tile0 <= t) ++r;
+  const Run& run = a.runs[r];
+  const int D = a.d;
+  const int pos0 = (t - run.tile0) * run.tile;
+  TileInfo ti;
+  ti.n = run.len - pos0 < run.tile ? run.len - pos0 : run.tile;
+  ti.kseg = run.seg_k;
+  ti.vseg = run.seg_v;
+  ti.ku0 = run.u0_k + pos0;
+  ti.vu0 = run.u0_v + pos0;
+  ti.kbits = ti.kseg >= 0 ? a.seg[ti.kseg].bits : 16;
+  ti.vbits = ti.vseg >= 0 ? a.seg[ti.vseg].bits : 16;
+  uint32_t off = 0;
+  ti.k_off = off;
+  off += align16u((uint32_t)ti.n * (uint32_t)(D * ti.kbits / 8));
+  if (ti.kseg >= 0) {
+    ti.g0 = ti.ku0 / a.G;
+    ti.ng = (ti.ku0 + ti.n - 1) / a.G - ti.g0 + 1;
+    ti.ks_off = off;
+    off += (uint32_t)ti.ng * D * 2;
+    ti.kz_off = off;
+    off += (uint32_t)ti.ng * D * 2;
+  } else {
+    ti.g0 = ti.ng = 0;
+    ti.ks_off = ti.kz_off = off;
+  }
+  ti.v_off = off;
+  off += align16u((uint32_t)ti.n * (uint32_t)(D * ti.vbits / 8));
+  if (ti.vseg >= 0) {
+    const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.G) * 2u);
+    ti.vs_off = off;
+    off += sb;
+    ti.vz_off = off;
+    off += sb;
+  } else {
+    ti.vs_off = ti.vz_off = off;
+  }
+  ti.bytes = off;
+  return ti;
+}
+
+struct BulkCopy {
+  const void* src;
+  uint32_t dst_off;  // offset inside the stage
+  uint32_t bytes;
+  int buf;           // which buffer: 0..5 = segment k_codes,k_scale,k_zero,v_codes,v_scale,v_zero; 6/7 = K/V ring
+  int seg;
+};
+
+// The (at most 8) bulk copies that stage tile t of (batch, kv head) `pair`.
+__host__ __device__ inline int tile_copies(const DecodeArgs& a, size_t pair, int t,
+                                           const TileInfo& ti, BulkCopy* cp) {
+  const int D = a.d;
+  int n = 0;
+  if (ti.kseg >= 0) {
+    const SegDev& s = a.seg[ti.kseg];
+    const int rb = D * s.bits / 8;
+    cp[n++] = {s.kc + (pair * s.cap + ti.ku0) * rb, ti.k_off, (uint32_t)(ti.n * rb), 0, ti.kseg};
+    const size_t gbase = (pair * (size_t)(s.cap / a.G) + ti.g0) * D;
+    cp[n++] = {s.ks + gbase, ti.ks_off, (uint32_t)(ti.ng * D * 2), 1, ti.kseg};
+    cp[n++] = {s.kz + gbase, ti.kz_off, (uint32_t)(ti.ng * D * 2), 2, ti.kseg};
+  } else {
+    const int s0 = (a.krs + ti.ku0) % a.R;
+    const int n1 = ti.n < a.R - s0 ? ti.n : a.R - s0;
+    const __half* ring = a.kr + pair * (size_t)a.R * D;
+    cp[n++] = {ring + (size_t)s0 * D, ti.k_off, (uint32_t)(n1 * D * 2), 6, -1};
+    if (n1 < ti.n)
+      cp[n++] = {ring, ti.k_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2), 6, -1};
+  }
+  if (ti.vseg >= 0) {
+    const SegDev& s = a.seg[ti.vseg];
+    const int rb = D * s.bits / 8;
+    cp[n++] = {s.vc + (pair * s.cap + ti.vu0) * rb, ti.v_off, (uint32_t)(ti.n * rb), 3, ti.vseg};
+    const size_t sbase = (pair * (size_t)s.cap + ti.vu0) * (D / a.G);
+    const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.G) * 2u);
+    cp[n++] = {s.vs + sbase, ti.vs_off, sb, 4, ti.vseg};
+    cp[n++] = {s.vz + sbase, ti.vz_off, sb, 5, ti.vseg};
+  } else {
+    const int s0 = (a.vrs + ti.vu0) % a.R;
+    const int n1 = ti.n < a.R - s0 ? ti.n : a.R - s0;
+    const __half* ring = a.vr + pair * (size_t)a.R * D;
+    cp[n++] = {ring + (size_t)s0 * D, ti.v_off, (uint32_t)(n1 * D * 2), 7, -1};
+    if (n1 < ti.n)
+      cp[n++] = {ring, ti.v_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2), 7, -1};
+  }
+  return n;
+}
+
+// kernels' launchers (return cudaGetLastError())
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_flush(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int n_pairs, cudaStream_t s);
+size_t decode_smem_bytes(int gq, int d);
+
+struct WindowArgs {
+  const __half* keys;  // [B][H][M][d]
+  const __half* text;  // [B][H][N][d]
+  int batch, h_kv, d, M, S, N;
+  int n8, n4, first_fp16;
+  double* tsum;        // [B][H*d]
+  double* wstat;       // [B][n_win][2] (dot with text sum, squared norm)
+  double* sim;         // [n_win]
+  int8_t* bits;        // [n_win] device
+  int32_t* perm;       // [n_win] device
+};
+cudaError_t launch_window_assign(const WindowArgs& a, cudaStream_t s);
+
+}  // namespace kvq

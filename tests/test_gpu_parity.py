@@ -1,0 +1,311 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Codes, scales, zeros and ring contents must be bit-exact; attention outputs
+within 2e-3 max-abs-relative of the oracle's fp64 result on the same
+dequantized values."""
+import numpy as np
+import pytest
+
+from kvq_testutil import TOL, KiviPair, kv, max_abs_rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # collected on CPU too, never run there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from quantized_kv_cache_kivi_gb300 import kvq, synth  # noqa: E402
+import oracle  # noqa: E402
+
+
+def _q(seed, B, Hq, d, step=0):
+    return synth.q_block(seed, B, Hq, d, step)
+
+
+# ---------------------------------------------------------------------------
+# codec + Algorithm 1 state: bit-exact
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d,G,R,bits", [(128, 32, 64, 2), (128, 64, 128, 4), (128, 32, 32, 8),
+                                        (64, 16, 32, 2), (64, 32, 64, 4), (64, 64, 64, 8)])
+def test_prefill_and_decode_bit_exact(d, G, R, bits):
+    B, H = 2, 3
+    pair = KiviPair(B, H, H, d, G, R, bits, cap=1024)
+    l = 5 * R + 7  # several flush blocks and a ragged residual
+    K, V = kv(11, B, H, l + 3 * R, d)
+    pair.prefill(K[:, :, :l], V[:, :, :l])
+    pair.assert_buffers_bit_exact()
+    # decode steps crossing K flushes and V evictions
+    for t in range(l, l + R + 5):
+        pair.append(K[:, :, t:t + 1], V[:, :, t:t + 1])
+    pair.assert_buffers_bit_exact()
+    # a bulk append of several blocks in one call
+    pair.append(K[:, :, l + R + 5:], V[:, :, l + R + 5:])
+    pair.assert_buffers_bit_exact()
+
+
+def test_short_prompt_and_partial_flush_bit_exact():
+    """l < R (nothing of V quantized), then a partial K flush that moves the
+    ring start, then more appends wrapping the ring."""
+    B, H, d, G, R = 1, 2, 128, 32, 128
+    pair = KiviPair(B, H, H, d, G, R, 2, cap=512)
+    K, V = kv(12, B, H, 400, d)
+    pair.prefill(K[:, :, :50], V[:, :, :50])
+    pair.assert_buffers_bit_exact()
+    pair.flush()  # 32 of the 50 K residual tokens
+    assert pair.gpu.c.k_ring_start == 32
+    pair.assert_buffers_bit_exact()
+    for t in range(50, 200, 7):
+        pair.append(K[:, :, t:t + 7], V[:, :, t:t + 7])
+        pair.assert_buffers_bit_exact()
+
+
+def test_deferred_flush_state_bit_exact():
+    """append returns FLUSH_DUE with a full ring; the caller flushes later."""
+    B, H, d, G, R = 1, 2, 128, 32, 64
+    pair = KiviPair(B, H, H, d, G, R, 2, cap=512)
+    K, V = kv(13, B, H, 3 * R, d)
+    pair.prefill(K[:, :, :R + 10], V[:, :, :R + 10])
+    st = pair.append(K[:, :, R + 10:2 * R], V[:, :, R + 10:2 * R], flush=False)
+    assert st == kvq.KVQ_FLUSH_DUE and pair.gpu.c.nkr == R
+    pair.assert_buffers_bit_exact()
+    pair.flush()
+    pair.assert_buffers_bit_exact()
+
+
+# ---------------------------------------------------------------------------
+# attention parity
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d,G,R,bits,gq", [(128, 32, 128, 2, 1), (128, 64, 128, 4, 4),
+                                           (128, 32, 64, 8, 2), (64, 16, 32, 2, 1),
+                                           (128, 32, 128, 2, 7), (64, 32, 64, 4, 8)])
+def test_attention_parity(d, G, R, bits, gq):
+    B, H = 2, 2
+    pair = KiviPair(B, H, H * gq, d, G, R, bits, cap=2048)
+    l = 1500 + R // 2
+    K, V = kv(21 + bits, B, H, l + 40, d)
+    pair.prefill(K[:, :, :l], V[:, :, :l])
+    q = _q(5, B, H * gq, d)
+    assert pair.attention_error(q) < TOL
+    for t in range(l, l + 40, 13):  # steps with a mixed K-packed / V-fp16 stretch
+        pair.append(K[:, :, t:t + 13], V[:, :, t:t + 13], flush=False)
+        assert pair.attention_error(_q(6 + t, B, H * gq, d)) < TOL
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 64])
+def test_attention_split_counts(splits):
+    """The merge of split partials gives the same result for any split count."""
+    B, H, d, G, R = 1, 2, 128, 32, 128
+    pair = KiviPair(B, H, H, d, G, R, 2, cap=4096)
+    K, V = kv(31, B, H, 3000, d)
+    pair.prefill(K, V)
+    q = _q(7, B, H, d)
+    assert pair.attention_error(q, ws_splits=splits) < TOL
+
+
+def test_attention_edge_cases():
+    B, H, d, G, R = 1, 1, 128, 32, 32
+    q = _q(9, B, H, d)
+    # one token (ring only)
+    pair = KiviPair(B, H, H, d, G, R, 2, cap=256)
+    K, V = kv(41, B, H, 300, d)
+    pair.prefill(K[:, :, :1], V[:, :, :1])
+    out = pair.gpu_attention(q)
+    assert max_abs_rel(out[0, 0], V[0, 0, 0].astype(np.float64)) < TOL
+    # fewer tokens than R, then exactly R (flush due), then ring wrap-around
+    for n in (5, R - 1):
+        pair.append(K[:, :, pair.gpu.c.nkr:n], V[:, :, pair.gpu.c.nkr:n])
+        assert pair.attention_error(q) < TOL
+    pair.append(K[:, :, R - 1:R], V[:, :, R - 1:R], flush=False)
+    assert pair.gpu.c.nkr == R
+    assert pair.attention_error(q) < TOL
+    pair.flush()
+    assert pair.attention_error(q) < TOL
+    for t in range(R, R + 70):
+        pair.append(K[:, :, t:t + 1], V[:, :, t:t + 1])
+    assert pair.gpu.c.v_ring_start != 0
+    assert pair.attention_error(q) < TOL
+
+
+def test_empty_cache_gives_zero():
+    c = kvq.alloc_cache(2, 2, 4, 128, 32, 64, [(2, 256)])
+    q = torch.randn(2, 4, 128, device="cuda").half()
+    out = torch.full_like(q, 7.0)
+    ws = torch.zeros(kvq.kvq_workspace_bytes(c, 4), dtype=torch.uint8, device="cuda")
+    kvq.kvq_decode_attention(c, q, out, ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
+
+
+def test_bad_arguments_launch_nothing():
+    c = kvq.alloc_cache(1, 1, 1, 128, 32, 64, [(2, 256)])
+    q = torch.zeros(1, 1, 128, device="cuda").half()
+    out = torch.zeros_like(q)
+    ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_decode_attention(c, q, out, ws)
+    assert e.value.status == kvq.KVQ_ERR_WORKSPACE
+    c.c.seg[0].bits = 3
+    ws = torch.zeros(kvq.kvq_workspace_bytes(c, 1), dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_decode_attention(c, q, out, ws)
+    assert e.value.status == kvq.KVQ_ERR_UNSUPPORTED
+    c.c.seg[0].bits = 2
+    k = torch.zeros(1, 1, 300, 128, device="cuda").half()
+    with pytest.raises(kvq.KvqError) as e:  # 300 tokens overflow a 256-token segment
+        kvq.kvq_quantize_append(c, k, k)
+    assert e.value.status == kvq.KVQ_ERR_CAPACITY
+    assert c.c.nkr == 0 and c.c.seg[0].nk == 0  # state untouched
+
+
+# ---------------------------------------------------------------------------
+# the workloads (tiny in full; large ones on sampled heads)
+# ---------------------------------------------------------------------------
+def _kivi_workload(name, heads=None, state="resid_full"):
+    w = synth.WORKLOADS[name]
+    B, Hq, H, d, G, R, bits = w["batch"], w["h_q"], w["h_kv"], w["d"], w["G"], w["R"], w["bits"]
+    L = w["n_packed"] + w["n_resid"]
+    pair = KiviPair(B, H, Hq, d, G, R, bits, cap=L + R, heads=heads)
+    seed = w["seed"]
+    K = np.empty((B, H, L, d), np.float16)
+    V = np.empty((B, H, L, d), np.float16)
+    for b in range(B):
+        for h in range(H):
+            K[b, h] = synth.keys(seed, b, h, L, d, w["n_out"], w["factor"])
+            V[b, h] = synth.values(seed, b, h, L, d)
+    # prefill L-1 tokens, then the new token arrives: the timed state has
+    # n_packed packed + n_resid fp16 tokens for both K and V (flush deferred)
+    pair.prefill(K[:, :, :L - 1], V[:, :, :L - 1])
+    pair.append(K[:, :, L - 1:], V[:, :, L - 1:], flush=False)
+    return pair, w
+
+
+def test_workload_tiny_full():
+    pair, w = _kivi_workload("tiny")
+    c = pair.gpu.c
+    assert (c.seg[0].nk, c.nkr, c.seg[0].nv, c.nvr) == (256, 16, 256, 16)
+    pair.assert_buffers_bit_exact()
+    q = synth.q_block(w["seed"], w["batch"], w["h_q"], w["d"])
+    assert pair.attention_error(q) < TOL
+
+
+def test_workload_llama2_7b_sampled_heads():
+    heads = [(0, 0), (3, 17), (7, 31)]
+    pair, w = _kivi_workload("llama2_7b", heads=heads)
+    c = pair.gpu.c
+    assert (c.seg[0].nk, c.nkr, c.seg[0].nv, c.nvr) == (3968, 128, 3968, 128)
+    pair.assert_buffers_bit_exact()
+    q = synth.q_block(w["seed"], w["batch"], w["h_q"], w["d"])
+    assert pair.attention_error(q) < TOL
+    pair.flush()  # the step's deferred K flush
+    pair.assert_buffers_bit_exact()
+    assert pair.attention_error(q) < TOL
+
+
+@pytest.mark.parametrize("heads", [[(0, 0), (15, 7)]])
+def test_workload_llama3_8b_gqa_sampled_heads(heads):
+    pair, w = _kivi_workload("llama3_8b_gqa", heads=heads)
+    pair.flush()
+    pair.assert_buffers_bit_exact()
+    q = synth.q_block(w["seed"], w["batch"], w["h_q"], w["d"])
+    assert pair.attention_error(q) < TOL
+
+
+def test_streaming_reduced():
+    """The streaming workload's recipe at reduced batch and prompt: every step
+    appends one token (flushing K every R) and attends; outputs checked at
+    every step, buffers at the end."""
+    w = synth.WORKLOADS["streaming"]
+    B, H, d, G, R, bits = 2, 4, w["d"], w["G"], w["R"], w["bits"]
+    prompt, steps = 512, 3 * R + 5
+    pair = KiviPair(B, H, H, d, G, R, bits, cap=prompt + steps + R)
+    K, V = kv(w["seed"], B, H, prompt, d, w["n_out"], w["factor"])
+    pair.prefill(K, V)
+    worst = 0.0
+    for s in range(steps):
+        k1, v1 = kv(w["seed"], B, H, 1, d, w["n_out"], w["factor"], step=s + 1)
+        pair.append(k1, v1)
+        worst = max(worst, pair.attention_error(_q(w["seed"], B, H, d, step=s + 1)))
+    assert worst < TOL
+    pair.assert_buffers_bit_exact()
+
+
+# ---------------------------------------------------------------------------
+# WindowQuant: assignment, reordered ingest, mixed-width attention
+# ---------------------------------------------------------------------------
+def test_window_assign_matches_oracle():
+    w = synth.WORKLOADS["windowquant_llava_ov"]
+    vis, txt = synth.window_keys(w["seed"], w["batch"], w["h_kv"], w["n_win"], w["S"],
+                                 w["n_text"], w["d"])
+    bits, perm, sim = kvq.kvq_window_assign(to_dev(vis), to_dev(txt), w["S"], w["frac8"], w["frac4"])
+    osim = oracle.window_sims(vis, txt, w["S"])
+    obits, operm = oracle.window_assign(osim, w["frac8"], w["frac4"])
+    assert np.allclose(sim, osim, rtol=0, atol=1e-12)
+    assert np.array_equal(bits, obits) and np.array_equal(perm, operm)
+    assert [(bits == b).sum() for b in (8, 4, 2)] == [6, 19, 39]
+    bits16, perm16, _ = kvq.kvq_window_assign(to_dev(vis), to_dev(txt), w["S"], 0.1, 0.3, True)
+    ob16, op16 = oracle.window_assign(osim, 0.1, 0.3, first_window_fp16=True)
+    assert np.array_equal(bits16, ob16) and np.array_equal(perm16, op16)
+
+
+def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False):
+    vis, txt = synth.window_keys(seed, B, H, n_win, S, n_text, d)
+    M = n_win * S
+    Vv = np.stack([np.stack([synth.values(seed, b, h, M, d) for h in range(H)]) for b in range(B)])
+    Vt = np.stack([np.stack([synth.values(seed + 1, b, h, n_text, d) for h in range(H)])
+                   for b in range(B)])
+    sim = oracle.window_sims(vis, txt, S)
+    bits, perm = oracle.window_assign(sim, 0.1, 0.3, first_window_fp16=first16)
+    caps = [(b, int(((bits == b).sum() * S + G - 1) // G * G) or G) for b in (8, 4, 2)]
+    R = 128 if not first16 else S + 128
+    c = kvq.alloc_cache(B, H, H * gq, d, G, R, caps, policy=kvq.KVQ_POLICY_FP16_TAIL)
+    plan = kvq.make_plan(S, bits, perm)
+    tail = 5  # vision tokens past the last whole window stay fp16
+    extra_k = np.concatenate([vis, vis[:, :, :tail]], axis=2)
+    extra_v = np.concatenate([Vv, Vv[:, :, :tail]], axis=2)
+    kvq.kvq_quantize_append(c, to_dev(extra_k), to_dev(extra_v), plan=plan)
+    kvq.kvq_quantize_append(c, to_dev(txt), to_dev(Vt))
+    heads = {}
+    for b in range(B):
+        for h in range(H):
+            o = oracle.Segmented(d, G, R, [8, 4, 2])
+            o.ingest_windows(extra_k[b, h], extra_v[b, h], S, bits, perm)
+            o.append_fp16(txt[b, h], Vt[b, h])
+            heads[(b, h)] = o
+    return c, heads, caps, R
+
+
+@pytest.mark.parametrize("first16", [False, True])
+def test_windowquant_ingest_and_attention(first16):
+    n_win, S, n_text, B, H, gq, d, G = 16, 64, 24, 2, 2, 7, 128, 32
+    c, heads, caps, R = _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed=3, first16=first16)
+    torch.cuda.synchronize()
+    P = B * H
+    q = synth.q_block(9, B, H * gq, d)
+    qd = to_dev(q)
+    out = torch.empty_like(qd)
+    ws = torch.zeros(kvq.kvq_workspace_bytes(c, 64), dtype=torch.uint8, device="cuda")
+    kvq.kvq_decode_attention(c, qd, out, ws)
+    got = out.cpu().numpy()
+    errs = []
+    for (b, h), o in heads.items():
+        p = b * H + h
+        segs, kr, vr = oracle.head_buffers(o, [cap for _, cap in caps])
+        for s, seg in enumerate(segs):
+            t = c.t["seg%d" % s]
+            bits, cap = caps[s]
+            rb = d * bits // 8
+            n = c.c.seg[s].nk
+            assert n == seg["nk"] == c.c.seg[s].nv
+            kc = t["k_codes"].cpu().numpy().reshape(P, cap, rb)[p, :n]
+            assert np.array_equal(kc, seg["k_codes"][:n])
+            ks = t["k_scale"].cpu().numpy().view(np.uint16).reshape(P, cap // G, d)[p, :n // G]
+            assert np.array_equal(ks, seg["k_scale"][:n // G])
+            vc = t["v_codes"].cpu().numpy().reshape(P, cap, rb)[p, :n]
+            assert np.array_equal(vc, seg["v_codes"][:n])
+            vz = t["v_zero"].cpu().numpy().view(np.uint16).reshape(P, cap, d // G)[p, :n]
+            assert np.array_equal(vz, seg["v_zero"][:n])
+        assert c.c.nkr == len(o.kr) and c.c.nvr == len(o.vr)
+        K, V = oracle.dequant_head(segs, kr, vr, len(o.kr), len(o.vr), 0, 0, d, G, R)
+        ref = oracle.attention_head(K, V, q[b, h * gq:(h + 1) * gq].astype(np.float64), c.c.sm_scale)
+        errs.append(max_abs_rel(got[b, h * gq:(h + 1) * gq], ref))
+    assert max(errs) < TOL
