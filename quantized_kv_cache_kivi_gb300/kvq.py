@@ -208,7 +208,8 @@ class Cache:
 
 def alloc_cache(batch, h_kv, h_q, d_h, group, resid_cap, segments, policy=KVQ_POLICY_KIVI,
                 sm_scale=None, device="cuda"):
-    """segments: list of (bits, capacity).  Buffers are zero-filled."""
+    """segments: list of (bits, capacity); each capacity is rounded up to a
+    multiple of ``group`` (the layout kvq.h requires).  Buffers are zero-filled."""
     import torch
     c = kvq_cache()
     c.batch, c.h_kv, c.h_q, c.d_h, c.group = batch, h_kv, h_q, d_h, group
@@ -218,6 +219,7 @@ def alloc_cache(batch, h_kv, h_q, d_h, group, resid_cap, segments, policy=KVQ_PO
     tensors = {}
     P = batch * h_kv
     for i, (bits, cap) in enumerate(segments):
+        cap = -(-int(cap) // group) * group
         rb = d_h * bits // 8
         t = dict(
             k_codes=torch.zeros(P * cap * rb, dtype=torch.uint8, device=device),

@@ -33,8 +33,8 @@ class KiviPair:
                  heads=None):
         self.batch, self.h_kv, self.h_q, self.d, self.G, self.R, self.bits = \
             batch, h_kv, h_q, d, G, R, bits
-        self.cap = cap
         self.gpu = kvq.alloc_cache(batch, h_kv, h_q, d, G, R, [(bits, cap)], policy=policy)
+        self.cap = self.gpu.c.seg[0].capacity
         # oracle heads (optionally only a sample of (b, h) pairs)
         self.heads = heads if heads is not None else [(b, h) for b in range(batch)
                                                       for h in range(h_kv)]

@@ -150,8 +150,8 @@ def test_bad_arguments_launch_nothing():
         kvq.kvq_decode_attention(c, q, out, ws)
     assert e.value.status == kvq.KVQ_ERR_UNSUPPORTED
     c.c.seg[0].bits = 2
-    k = torch.zeros(1, 1, 300, 128, device="cuda").half()
-    with pytest.raises(kvq.KvqError) as e:  # 300 tokens overflow a 256-token segment
+    k = torch.zeros(1, 1, 400, 128, device="cuda").half()
+    with pytest.raises(kvq.KvqError) as e:  # 384 flushed K tokens overflow 256 slots
         kvq.kvq_quantize_append(c, k, k)
     assert e.value.status == kvq.KVQ_ERR_CAPACITY
     assert c.c.nkr == 0 and c.c.seg[0].nk == 0  # state untouched
@@ -182,7 +182,9 @@ def _kivi_workload(name, heads=None, state="resid_full"):
 def test_workload_tiny_full():
     pair, w = _kivi_workload("tiny")
     c = pair.gpu.c
-    assert (c.seg[0].nk, c.nkr, c.seg[0].nv, c.nvr) == (256, 16, 256, 16)
+    # K: 256 packed + 16 fp16 as the workload states; V follows Algorithm 1
+    # and keeps the newest R = 32 tokens fp16
+    assert (c.seg[0].nk, c.nkr, c.seg[0].nv, c.nvr) == (256, 16, 240, 32)
     pair.assert_buffers_bit_exact()
     q = synth.q_block(w["seed"], w["batch"], w["h_q"], w["d"])
     assert pair.attention_error(q) < TOL
