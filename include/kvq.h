@@ -212,6 +212,28 @@ kvq_status kvq_window_assign(const void* keys, const void* text_keys,
                              void* workspace, size_t ws_bytes, int8_t* bits_out,
                              int32_t* perm_out, double* sim_out, void* stream);
 
+/* Decode attention without a caller workspace (no counterpart in the pages).
+ *
+ * Same computation, arguments and result as kvq_decode_attention, for callers
+ * that cannot allocate device memory: for instance a custom-operator or
+ * plugin interface that passes only the input and output tensors, or a
+ * process whose device memory belongs to another allocator, where calling
+ * cudaMalloc is not allowed or would stall the device.  The workspace lives
+ * instead in a static array of KVQ_NOALLOC_SCRATCH_BYTES inside the library,
+ * allocated once per GPU that loads the library and kept until the process
+ * exits; the call allocates nothing.
+ *
+ * - The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ * - A cache whose batch * h_kv needs more than the array holds is rejected
+ *   with KVQ_ERR_CAPACITY (kvq_last_error_string says so) before any launch.
+ * - All calls share the one array, and it keeps the previous call's contents
+ *   (each call clears the part that must start at zero, on `stream`).  Calls
+ *   whose work can overlap on the GPU race on it: serialize them. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+kvq_status kvq_decode_attention_noalloc(const kvq_cache* cache, const void* q,
+                                        void* out, void* stream);
+
 /* Static description of a status code. */
 const char* kvq_status_string(kvq_status status);
 

@@ -403,6 +403,11 @@ kvq_status append_plan(kvq_cache* c, const void* k_new, const void* v_new, int T
 
 }  // namespace
 
+namespace kvq {
+void set_last_error(const char* msg) { g_last_error = msg; }
+kvq_status check_cache(const kvq_cache* c) { return validate_cache(c); }
+}  // namespace kvq
+
 extern "C" {
 
 const char* kvq_status_string(kvq_status s) {

@@ -223,6 +223,10 @@ __host__ __device__ inline int tile_copies(const DecodeArgs& a, size_t pair, int
   return n;
 }
 
+// host helpers of kvq_api.cu used by other entry points
+void set_last_error(const char* msg);
+kvq_status check_cache(const kvq_cache* c);
+
 // kernels' launchers (return cudaGetLastError())
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_flush(const AppendArgs& a, cudaStream_t s);

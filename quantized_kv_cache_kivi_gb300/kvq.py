@@ -71,6 +71,8 @@ def lib():
         L.kvq_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
         L.kvq_decode_attention.argtypes = [cp, _P, _P, _P, ctypes.c_size_t, _P]
         L.kvq_workspace_error.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
+        L.kvq_decode_attention_noalloc.argtypes = [cp, _P, _P, _P]
+        L.kvq_decode_attention_noalloc.restype = ctypes.c_int
         L.kvq_window_assign_workspace_bytes.argtypes = [ctypes.c_int32] * 5
         L.kvq_window_assign_workspace_bytes.restype = ctypes.c_size_t
         L.kvq_window_assign.argtypes = [_P, _P] + [ctypes.c_int32] * 6 + \
@@ -143,6 +145,13 @@ def kvq_decode_attention(cache, q, out, ws, stream=None):
     st = lib().kvq_decode_attention(ctypes.byref(cache.c), _ptr(q), _ptr(out), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream))
     return _check(st, "kvq_decode_attention")
+
+
+def kvq_decode_attention_noalloc(cache, q, out, stream=None):
+    """kvq_decode_attention with the library's static scratch (no workspace)."""
+    st = lib().kvq_decode_attention_noalloc(ctypes.byref(cache.c), _ptr(q), _ptr(out),
+                                            _stream(stream))
+    return _check(st, "kvq_decode_attention_noalloc")
 
 
 def kvq_workspace_error(ws, stream=None):
