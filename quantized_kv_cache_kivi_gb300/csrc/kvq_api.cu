@@ -124,6 +124,27 @@ int tile_bytes(int tile, int kbits, int vbits, int d, int G) {
   return b;
 }
 
+// Tile of the one-query-head kernel: nw consumer warps x wt tokens each,
+// the largest that fits one stage and the scaled-query table.
+// Among equal token counts, more warps (a smaller slice) wins.
+void choose_tile_mha(int kbits, int vbits, int d, int G, int* tile, int* wt) {
+  *tile = *wt = 0;
+  int best_nw = 0;
+  for (int w = 32; w >= 8; w >>= 1) {
+    for (int nw = kvq::kMhaConsumerWarps; nw >= 1; --nw) {
+      const int t = w * nw;
+      if (tile_bytes(t, kbits, vbits, d, G) > kvq::kMhaStageBytes) continue;
+      if (kbits != 16 && (t + G - 1) / G + 1 > kvq::kMhaMaxGroups) continue;
+      if (t > *tile || (t == *tile && nw > best_nw)) {
+        *tile = t;
+        *wt = w;
+        best_nw = nw;
+      }
+      break;
+    }
+  }
+}
+
 int choose_tile(int kbits, int vbits, int d, int G, int gq) {
   for (int tile = 128; tile >= 32; tile >>= 1) {
     if (tile_bytes(tile, kbits, vbits, d, G) > kvq::kStageBytes) continue;
@@ -133,7 +154,8 @@ int choose_tile(int kbits, int vbits, int d, int G, int gq) {
   return 0;
 }
 
-kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>& tile_cost) {
+kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>& tile_cost,
+                       bool mha) {
   std::vector<Piece> kp, vp;
   for (int s = 0; s < c->n_seg; ++s) {
     if (c->seg[s].nk > 0) kp.push_back({s, 0, c->seg[s].nk});
@@ -158,7 +180,9 @@ kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>&
     r.len = len;
     const int kb = r.seg_k >= 0 ? c->seg[r.seg_k].bits : 16;
     const int vb = r.seg_v >= 0 ? c->seg[r.seg_v].bits : 16;
-    r.tile = choose_tile(kb, vb, c->d_h, c->group, gq);
+    r.wt = 0;
+    if (mha) choose_tile_mha(kb, vb, c->d_h, c->group, &r.tile, &r.wt);
+    else r.tile = choose_tile(kb, vb, c->d_h, c->group, gq);
     if (r.tile == 0) return fail(KVQ_ERR_UNSUPPORTED, "no tile size fits shared memory");
     r.groups = (r.tile + c->group - 1) / c->group + 1;
     r.tile0 = a.n_tiles;
@@ -201,22 +225,37 @@ int choose_splits(int n_pairs, int n_tiles, int max_splits) {
 // 16-byte alignment, source inside its buffer's documented extent, the stage
 // and the scaled-query table large enough, and the copies adding up to the
 // byte count the tile's mbarrier expects (so no wait can be left short).
-kvq_status verify_decode_plan(const kvq_cache* c, const kvq::DecodeArgs& a, int n_pairs) {
+kvq_status verify_decode_plan(const kvq_cache* c, const kvq::DecodeArgs& a, int n_pairs,
+                              bool mha) {
+  const uint32_t stage_cap = mha ? (uint32_t)kvq::kMhaStageBytes : (uint32_t)kvq::kStageBytes;
   const size_t P = (size_t)n_pairs, D = (size_t)a.d, G = (size_t)a.G, R = (size_t)a.R;
   for (int which = 0; which < 2; ++which) {
     const size_t pair = which == 0 ? 0 : P - 1;
     for (int t = 0; t < a.n_tiles; ++t) {
       const kvq::TileInfo ti = kvq::tile_info(a, t);
-      if (ti.n < 1 || ti.n > 128) return fail(KVQ_ERR_UNSUPPORTED, "tile %d has %d tokens", t, ti.n);
-      if (ti.bytes > (uint32_t)kvq::kStageBytes)
+      if (ti.n < 1 || ti.n > (mha ? 8 * 32 : 128))
+        return fail(KVQ_ERR_UNSUPPORTED, "tile %d has %d tokens", t, ti.n);
+      if (ti.bytes > stage_cap)
         return fail(KVQ_ERR_UNSUPPORTED, "tile %d needs %u stage bytes", t, ti.bytes);
-      if (ti.kseg >= 0 && (size_t)ti.ng * a.gq * D * 4 > (size_t)kvq::kQsBytes)
+      if (!mha && ti.kseg >= 0 && (size_t)ti.ng * a.gq * D * 4 > (size_t)kvq::kQsBytes)
         return fail(KVQ_ERR_UNSUPPORTED, "tile %d: scaled-query table too small", t);
-      kvq::BulkCopy cp[8];
-      const int n = kvq::tile_copies(a, pair, t, ti, cp);
+      if (mha && ti.kseg >= 0 && ti.ng > kvq::kMhaMaxGroups)
+        return fail(KVQ_ERR_UNSUPPORTED, "tile %d: %d K groups > %d", t, ti.ng, kvq::kMhaMaxGroups);
+      struct Copy {
+        const void* src;
+        uint32_t dst_off, bytes;
+        int buf, seg;
+      } cp[8];
+      int n = 0;
+      kvq::for_each_tile_copy(a, pair, ti, [&](const void* src, uint32_t off, uint32_t bytes,
+                                               int buf, int seg) {
+        if (n < 8) cp[n] = {src, off, bytes, buf, seg};
+        ++n;
+      });
+      if (n > 8) return fail(KVQ_ERR_UNSUPPORTED, "tile %d: %d copies", t, n);
       uint64_t sum = 0;
       for (int i = 0; i < n; ++i) {
-        const kvq::BulkCopy& k = cp[i];
+        const Copy& k = cp[i];
         const uint8_t* base;
         size_t size;
         if (k.buf >= 6) {
@@ -503,7 +542,10 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   const int gq = cache->h_q / cache->h_kv;
   kvq::DecodeArgs a{};
   std::vector<int> cost;
-  st = plan_decode(cache, a, cost);
+  // one query head per kv head, one segment, each lane's channel quarter
+  // inside one V group: the specialised kernel
+  const bool mha = gq == 1 && cache->n_seg == 1 && cache->group >= cache->d_h / 4;
+  st = plan_decode(cache, a, cost, mha);
   if (st != KVQ_OK) return st;
   if (a.n_tiles == 0) {
     const size_t bytes = (size_t)cache->batch * cache->h_q * cache->d_h * 2;
@@ -535,6 +577,8 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   a.gq = gq;
   a.d = cache->d_h;
   a.G = cache->group;
+  a.log2G = 0;
+  while ((1 << a.log2G) < a.G) ++a.log2G;
   a.R = cache->resid_cap;
   a.scale_log2 = cache->sm_scale * 1.4426950408889634f;
   a.n_seg = cache->n_seg;
@@ -549,9 +593,10 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   a.err = reinterpret_cast<int*>(w);
   a.counters = reinterpret_cast<int*>(w + kvq::kWorkspaceHeader);
   a.part = reinterpret_cast<float*>(w + ws_fixed(n_pairs));
-  st = verify_decode_plan(cache, a, n_pairs);
+  st = verify_decode_plan(cache, a, n_pairs, mha);
   if (st != KVQ_OK) return st;
-  const cudaError_t e = kvq::launch_decode(a, n_pairs, s);
+  const cudaError_t e = mha ? kvq::launch_decode_mha(a, n_pairs, cache->seg[0].bits, s)
+                            : kvq::launch_decode(a, n_pairs, s);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "decode launch");
 }
 

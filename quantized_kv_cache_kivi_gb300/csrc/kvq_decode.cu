@@ -30,10 +30,10 @@ constexpr int NT = kDecodeThreads;
 __device__ void issue_tile(const DecodeArgs& a, size_t pair, int t, uint8_t* stage,
                            uint64_t* bar) {
   const TileInfo ti = tile_info(a, t);
-  BulkCopy cp[8];
-  const int n = tile_copies(a, pair, t, ti, cp);
   mbar_arrive_expect_tx(bar, ti.bytes);
-  for (int i = 0; i < n; ++i) bulk_g2s(stage + cp[i].dst_off, cp[i].src, cp[i].bytes, bar);
+  for_each_tile_copy(a, pair, ti, [&](const void* src, uint32_t off, uint32_t bytes, int, int) {
+    bulk_g2s(stage + off, src, bytes, bar);
+  });
 }
 
 // Code j (0..7) of a chunk of 8 codes held in `w` (bits per code `B`), as fp32.

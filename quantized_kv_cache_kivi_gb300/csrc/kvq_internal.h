@@ -17,6 +17,12 @@ constexpr int kStageBytes = 20480;  // one pipeline stage of staged tile data
 constexpr int kStages = 3;          // pipeline depth
 constexpr int kQsBytes = 16384;     // per-tile scaled-query table (K groups)
 constexpr int kWorkspaceHeader = 256;  // error word + padding at workspace start
+// one-query-head (MHA) kernel: 7 consumer warps + 1 producer warp (2 CTAs and
+// 16 warps per SM, so each thread may hold 128 registers)
+constexpr int kMhaConsumerWarps = 7;
+constexpr int kMhaStageBytes = 25600;   // staged tile data per pipeline stage
+constexpr int kMhaMaxGroups = 16;       // K scale groups one tile may touch
+constexpr int kMhaQtabBytes = kMhaMaxGroups * 4 * 36 * 4;  // scaled-query rows per stage
 
 // One packed segment as the kernels see it (base pointers of the whole array).
 struct SegDev {
@@ -40,10 +46,12 @@ struct Run {
   int tile;   // tokens per tile
   int tile0;  // index of the run's first tile among the head's tiles
   int groups; // max K scale groups one tile of this run touches (packed K)
+  int wt;     // tokens per consumer-warp slice (one-query-head kernel)
 };
 
 struct DecodeArgs {
   int batch, h_kv, gq, d, G, R;
+  int log2G;         // G is a power of two
   float scale_log2;  // sm_scale * log2(e)
   int n_seg;
   SegDev seg[KVQ_MAX_SEGMENTS];
@@ -176,51 +184,42 @@ __host__ __device__ inline TileInfo tile_info(const DecodeArgs& a, int t) {
   return ti;
 }
 
-struct BulkCopy {
-  const void* src;
-  uint32_t dst_off;  // offset inside the stage
-  uint32_t bytes;
-  int buf;           // which buffer: 0..5 = segment k_codes,k_scale,k_zero,v_codes,v_scale,v_zero; 6/7 = K/V ring
-  int seg;
-};
-
-// The (at most 8) bulk copies that stage tile t of (batch, kv head) `pair`.
-__host__ __device__ inline int tile_copies(const DecodeArgs& a, size_t pair, int t,
-                                           const TileInfo& ti, BulkCopy* cp) {
+// Visit the (at most 8) bulk copies that stage tile `ti` of (batch, kv head)
+// `pair`: f(src, dst_off, bytes, buf, seg) with buf 0..5 = segment k_codes,
+// k_scale, k_zero, v_codes, v_scale, v_zero and 6/7 = the K/V ring.
+template <class F>
+__host__ __device__ inline void for_each_tile_copy(const DecodeArgs& a, size_t pair,
+                                                   const TileInfo& ti, F&& f) {
   const int D = a.d;
-  int n = 0;
   if (ti.kseg >= 0) {
     const SegDev& s = a.seg[ti.kseg];
     const int rb = D * s.bits / 8;
-    cp[n++] = {s.kc + (pair * s.cap + ti.ku0) * rb, ti.k_off, (uint32_t)(ti.n * rb), 0, ti.kseg};
+    f(s.kc + (pair * s.cap + ti.ku0) * rb, ti.k_off, (uint32_t)(ti.n * rb), 0, ti.kseg);
     const size_t gbase = (pair * (size_t)(s.cap / a.G) + ti.g0) * D;
-    cp[n++] = {s.ks + gbase, ti.ks_off, (uint32_t)(ti.ng * D * 2), 1, ti.kseg};
-    cp[n++] = {s.kz + gbase, ti.kz_off, (uint32_t)(ti.ng * D * 2), 2, ti.kseg};
+    f(s.ks + gbase, ti.ks_off, (uint32_t)(ti.ng * D * 2), 1, ti.kseg);
+    f(s.kz + gbase, ti.kz_off, (uint32_t)(ti.ng * D * 2), 2, ti.kseg);
   } else {
     const int s0 = (a.krs + ti.ku0) % a.R;
     const int n1 = ti.n < a.R - s0 ? ti.n : a.R - s0;
     const __half* ring = a.kr + pair * (size_t)a.R * D;
-    cp[n++] = {ring + (size_t)s0 * D, ti.k_off, (uint32_t)(n1 * D * 2), 6, -1};
-    if (n1 < ti.n)
-      cp[n++] = {ring, ti.k_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2), 6, -1};
+    f(ring + (size_t)s0 * D, ti.k_off, (uint32_t)(n1 * D * 2), 6, -1);
+    if (n1 < ti.n) f(ring, ti.k_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2), 6, -1);
   }
   if (ti.vseg >= 0) {
     const SegDev& s = a.seg[ti.vseg];
     const int rb = D * s.bits / 8;
-    cp[n++] = {s.vc + (pair * s.cap + ti.vu0) * rb, ti.v_off, (uint32_t)(ti.n * rb), 3, ti.vseg};
+    f(s.vc + (pair * s.cap + ti.vu0) * rb, ti.v_off, (uint32_t)(ti.n * rb), 3, ti.vseg);
     const size_t sbase = (pair * (size_t)s.cap + ti.vu0) * (D / a.G);
     const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.G) * 2u);
-    cp[n++] = {s.vs + sbase, ti.vs_off, sb, 4, ti.vseg};
-    cp[n++] = {s.vz + sbase, ti.vz_off, sb, 5, ti.vseg};
+    f(s.vs + sbase, ti.vs_off, sb, 4, ti.vseg);
+    f(s.vz + sbase, ti.vz_off, sb, 5, ti.vseg);
   } else {
     const int s0 = (a.vrs + ti.vu0) % a.R;
     const int n1 = ti.n < a.R - s0 ? ti.n : a.R - s0;
     const __half* ring = a.vr + pair * (size_t)a.R * D;
-    cp[n++] = {ring + (size_t)s0 * D, ti.v_off, (uint32_t)(n1 * D * 2), 7, -1};
-    if (n1 < ti.n)
-      cp[n++] = {ring, ti.v_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2), 7, -1};
+    f(ring + (size_t)s0 * D, ti.v_off, (uint32_t)(n1 * D * 2), 7, -1);
+    if (n1 < ti.n) f(ring, ti.v_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2), 7, -1);
   }
-  return n;
 }
 
 // host helpers of kvq_api.cu used by other entry points
@@ -233,6 +232,8 @@ cudaError_t launch_flush(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int n_pairs, cudaStream_t s);
 size_t decode_smem_bytes(int gq, int d);
+cudaError_t launch_decode_mha(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s);
+size_t decode_mha_smem_bytes();
 
 struct WindowArgs {
   const __half* keys;  // [B][H][M][d]
