@@ -145,6 +145,27 @@ void choose_tile_mha(int kbits, int vbits, int d, int G, int* tile, int* wt) {
   }
 }
 
+// Tile of the tensor-core kernel: nw <= 4 consumer warps x wt tokens each
+// (wt a multiple of 16), the largest that fits one stage and the K operand
+// table; among equal token counts, more warps win.
+void choose_tile_tc(int kbits, int vbits, int d, int G, int* tile, int* wt) {
+  *tile = *wt = 0;
+  int best_nw = 0;
+  for (int w = 64; w >= 16; w -= 16) {
+    for (int nw = kvq::kTcConsumerWarps; nw >= 1; --nw) {
+      const int t = w * nw;
+      if (tile_bytes(t, kbits, vbits, d, G) > kvq::kTcStageBytes) continue;
+      if (kbits != 16 && (t + G - 1) / G + 1 > kvq::kTcMaxGroups) continue;
+      if (t > *tile || (t == *tile && nw > best_nw)) {
+        *tile = t;
+        *wt = w;
+        best_nw = nw;
+      }
+      break;
+    }
+  }
+}
+
 int choose_tile(int kbits, int vbits, int d, int G, int gq) {
   for (int tile = 128; tile >= 32; tile >>= 1) {
     if (tile_bytes(tile, kbits, vbits, d, G) > kvq::kStageBytes) continue;
@@ -154,8 +175,10 @@ int choose_tile(int kbits, int vbits, int d, int G, int gq) {
   return 0;
 }
 
+enum Kernel { K_GENERAL = 0, K_MHA = 1, K_TC = 2 };
+
 kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>& tile_cost,
-                       bool mha) {
+                       int kern) {
   std::vector<Piece> kp, vp;
   for (int s = 0; s < c->n_seg; ++s) {
     if (c->seg[s].nk > 0) kp.push_back({s, 0, c->seg[s].nk});
@@ -170,7 +193,11 @@ kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>&
   size_t i = 0, j = 0;
   int oi = 0, oj = 0;  // offsets consumed inside kp[i], vp[j]
   while (i < kp.size() && j < vp.size()) {
-    const int len = std::min(kp[i].len - oi, vp[j].len - oj);
+    int len = std::min(kp[i].len - oi, vp[j].len - oj);
+    // the tensor-core kernel applies one K group per 16-token sub-tile: a
+    // packed-K run that starts off a multiple of 16 gets a short head run
+    const int uk = kp[i].u0 + oi;
+    if (kern == K_TC && kp[i].seg >= 0 && uk % 16 != 0) len = std::min(len, 16 - uk % 16);
     if (a.n_runs >= kvq::kMaxRuns) return fail(KVQ_ERR_UNSUPPORTED, "too many token runs");
     kvq::Run& r = a.runs[a.n_runs++];
     r.seg_k = kp[i].seg;
@@ -181,7 +208,8 @@ kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>&
     const int kb = r.seg_k >= 0 ? c->seg[r.seg_k].bits : 16;
     const int vb = r.seg_v >= 0 ? c->seg[r.seg_v].bits : 16;
     r.wt = 0;
-    if (mha) choose_tile_mha(kb, vb, c->d_h, c->group, &r.tile, &r.wt);
+    if (kern == K_TC) choose_tile_tc(kb, vb, c->d_h, c->group, &r.tile, &r.wt);
+    else if (kern == K_MHA) choose_tile_mha(kb, vb, c->d_h, c->group, &r.tile, &r.wt);
     else r.tile = choose_tile(kb, vb, c->d_h, c->group, gq);
     if (r.tile == 0) return fail(KVQ_ERR_UNSUPPORTED, "no tile size fits shared memory");
     r.groups = (r.tile + c->group - 1) / c->group + 1;
@@ -226,8 +254,12 @@ int choose_splits(int n_pairs, int n_tiles, int max_splits) {
 // and the scaled-query table large enough, and the copies adding up to the
 // byte count the tile's mbarrier expects (so no wait can be left short).
 kvq_status verify_decode_plan(const kvq_cache* c, const kvq::DecodeArgs& a, int n_pairs,
-                              bool mha) {
-  const uint32_t stage_cap = mha ? (uint32_t)kvq::kMhaStageBytes : (uint32_t)kvq::kStageBytes;
+                              int kern) {
+  const bool mha = kern != K_GENERAL;
+  const uint32_t stage_cap = kern == K_TC    ? (uint32_t)kvq::kTcStageBytes
+                             : kern == K_MHA ? (uint32_t)kvq::kMhaStageBytes
+                                             : (uint32_t)kvq::kStageBytes;
+  const int max_groups = kern == K_TC ? kvq::kTcMaxGroups : kvq::kMhaMaxGroups;
   const size_t P = (size_t)n_pairs, D = (size_t)a.d, G = (size_t)a.G, R = (size_t)a.R;
   for (int which = 0; which < 2; ++which) {
     const size_t pair = which == 0 ? 0 : P - 1;
@@ -239,8 +271,8 @@ kvq_status verify_decode_plan(const kvq_cache* c, const kvq::DecodeArgs& a, int 
         return fail(KVQ_ERR_UNSUPPORTED, "tile %d needs %u stage bytes", t, ti.bytes);
       if (!mha && ti.kseg >= 0 && (size_t)ti.ng * a.gq * D * 4 > (size_t)kvq::kQsBytes)
         return fail(KVQ_ERR_UNSUPPORTED, "tile %d: scaled-query table too small", t);
-      if (mha && ti.kseg >= 0 && ti.ng > kvq::kMhaMaxGroups)
-        return fail(KVQ_ERR_UNSUPPORTED, "tile %d: %d K groups > %d", t, ti.ng, kvq::kMhaMaxGroups);
+      if (mha && ti.kseg >= 0 && ti.ng > max_groups)
+        return fail(KVQ_ERR_UNSUPPORTED, "tile %d: %d K groups > %d", t, ti.ng, max_groups);
       struct Copy {
         const void* src;
         uint32_t dst_off, bytes;
@@ -544,8 +576,10 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   std::vector<int> cost;
   // one query head per kv head, one segment, each lane's channel quarter
   // inside one V group: the specialised kernel
-  const bool mha = gq == 1 && cache->n_seg == 1 && cache->group >= cache->d_h / 4;
-  st = plan_decode(cache, a, cost, mha);
+  int kern = K_GENERAL;
+  if (gq == 1 && cache->n_seg == 1 && cache->group >= cache->d_h / 4)
+    kern = cache->d_h == 128 ? K_TC : K_MHA;
+  st = plan_decode(cache, a, cost, kern);
   if (st != KVQ_OK) return st;
   if (a.n_tiles == 0) {
     const size_t bytes = (size_t)cache->batch * cache->h_q * cache->d_h * 2;
@@ -593,10 +627,11 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   a.err = reinterpret_cast<int*>(w);
   a.counters = reinterpret_cast<int*>(w + kvq::kWorkspaceHeader);
   a.part = reinterpret_cast<float*>(w + ws_fixed(n_pairs));
-  st = verify_decode_plan(cache, a, n_pairs, mha);
+  st = verify_decode_plan(cache, a, n_pairs, kern);
   if (st != KVQ_OK) return st;
-  const cudaError_t e = mha ? kvq::launch_decode_mha(a, n_pairs, cache->seg[0].bits, s)
-                            : kvq::launch_decode(a, n_pairs, s);
+  const cudaError_t e = kern == K_TC    ? kvq::launch_decode_tc(a, n_pairs, cache->seg[0].bits, s)
+                        : kern == K_MHA ? kvq::launch_decode_mha(a, n_pairs, cache->seg[0].bits, s)
+                                        : kvq::launch_decode(a, n_pairs, s);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "decode launch");
 }
 

@@ -23,6 +23,13 @@ constexpr int kMhaConsumerWarps = 7;
 constexpr int kMhaStageBytes = 25600;   // staged tile data per pipeline stage
 constexpr int kMhaMaxGroups = 16;       // K scale groups one tile may touch
 constexpr int kMhaQtabBytes = kMhaMaxGroups * 4 * 36 * 4;  // scaled-query rows per stage
+// tensor-core one-query-head kernel (d_h = 128): 4 consumer warps + 1
+// producer, 4 stages, two CTAs per SM
+constexpr int kTcConsumerWarps = 4;
+constexpr int kTcStages = 4;
+constexpr int kTcStageBytes = 19456;
+constexpr int kTcMaxGroups = 8;                      // K groups one tile may touch
+constexpr int kTcKtabBytes = kTcMaxGroups * 512;     // K operand table per stage
 
 // One packed segment as the kernels see it (base pointers of the whole array).
 struct SegDev {
@@ -233,6 +240,7 @@ cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int n_pairs, cudaStream_t s);
 size_t decode_smem_bytes(int gq, int d);
 cudaError_t launch_decode_mha(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s);
 size_t decode_mha_smem_bytes();
 
 struct WindowArgs {

@@ -15,8 +15,6 @@ namespace kvq {
 namespace {
 
 constexpr int kQuantThreads = 128;
-constexpr int kMaxG = 128;
-constexpr int kMaxD = 128;
 
 struct PairPtrs {
   const __half* in_k;  // new tokens of this (batch, kv head)
@@ -33,28 +31,36 @@ __device__ __forceinline__ const __half* src_row(const __half* ring, const __hal
 
 // Quantize one K group (G pushed tokens starting at push index p0, all D
 // channels, one group per channel) into packed rows [row0, row0 + G) and
-// scale/zero row `grow` of the destination segment.  Whole block.
+// scale/zero row `grow` of the destination segment.  Whole block.  The G
+// source rows are first staged in shared memory with 16-byte loads (all in
+// flight at once), then each thread reduces and quantizes one channel.
 template <int D>
 __device__ void quant_k_group(const SegDev& dst, int bits, int G, int R, size_t pair,
                               const __half* ring, const __half* in, const RowSrc& src, int p0,
-                              int row0, int grow, uint8_t (*codes_s)[kMaxD]) {
+                              int row0, int grow, __half* xs, uint8_t* codes_s) {
   const int tid = threadIdx.x;
+  constexpr int kVec = D * 2 / 16;  // 16-byte vectors per row
+  for (int idx = tid; idx < G * kVec; idx += blockDim.x) {
+    const int i = idx / kVec, v = idx % kVec;
+    reinterpret_cast<int4*>(xs + (size_t)i * D)[v] =
+        reinterpret_cast<const int4*>(src_row<D>(ring, in, R, src, p0 + i))[v];
+  }
+  __syncthreads();
   for (int c = tid; c < D; c += blockDim.x) {
-    float mn = __half2float(src_row<D>(ring, in, R, src, p0)[c]);
+    float mn = __half2float(xs[c]);
     float mx = mn;
     for (int i = 1; i < G; ++i) {
-      const float v = __half2float(src_row<D>(ring, in, R, src, p0 + i)[c]);
+      const float v = __half2float(xs[(size_t)i * D + c]);
       mn = fminf(mn, v);
       mx = fmaxf(mx, v);
     }
     const QParams qp = qparams(mn, mx, bits);
+    const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
     const size_t gidx = (pair * (size_t)(dst.cap / G) + grow) * D + c;
     const_cast<__half*>(dst.ks)[gidx] = qp.sh;
     const_cast<__half*>(dst.kz)[gidx] = qp.zh;
-    for (int i = 0; i < G; ++i) {
-      const float v = __half2float(src_row<D>(ring, in, R, src, p0 + i)[c]);
-      codes_s[i][c] = (uint8_t)qcode(v, qp, bits);
-    }
+    for (int i = 0; i < G; ++i)
+      codes_s[(size_t)i * D + c] = (uint8_t)qcode_fast(__half2float(xs[(size_t)i * D + c]), qp, rcp, bits);
   }
   __syncthreads();
   const int per_word = 32 / bits;
@@ -64,7 +70,7 @@ __device__ void quant_k_group(const SegDev& dst, int bits, int G, int R, size_t 
   for (int idx = tid; idx < G * words; idx += blockDim.x) {
     const int i = idx / words, w = idx % words;
     uint32_t word = 0;
-    for (int j = 0; j < per_word; ++j) word |= (uint32_t)codes_s[i][w * per_word + j] << (j * bits);
+    for (int j = 0; j < per_word; ++j) word |= (uint32_t)codes_s[(size_t)i * D + w * per_word + j] << (j * bits);
     reinterpret_cast<uint32_t*>(base + (size_t)i * rb)[w] = word;
   }
   __syncthreads();
@@ -94,8 +100,9 @@ __device__ void quant_v_token(const SegDev& dst, int bits, int G, size_t pair, c
   }
   if (!active) return;
   const QParams qp = qparams(mn, mx, bits);
+  const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
   uint32_t packed = 0;
-  for (int j = 0; j < 4; ++j) packed |= qcode(v[j], qp, bits) << (j * bits);
+  for (int j = 0; j < 4; ++j) packed |= qcode_fast(v[j], qp, rcp, bits) << (j * bits);
   const int rb = D * bits / 8;
   uint8_t* rowp = const_cast<uint8_t*>(dst.vc) + (pair * (size_t)dst.cap + row) * rb;
   if (bits == 2) rowp[lane] = (uint8_t)packed;
@@ -122,7 +129,9 @@ __device__ void copy_to_ring(__half* ring, int R, int slot0, const __half* src, 
 
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs a) {
-  __shared__ uint8_t codes_s[kMaxG][kMaxD];
+  extern __shared__ __align__(16) uint8_t qsm[];
+  __half* xs = reinterpret_cast<__half*>(qsm);
+  uint8_t* codes_s = qsm + (size_t)a.G * D * 2;
   const size_t pair = blockIdx.x;
   const int chunk = blockIdx.y;
   const __half* in_k = a.k_new + pair * (size_t)a.T * D;
@@ -135,7 +144,7 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
     // work that reads old ring slots, before any new token lands in the ring
     for (int gi = 0; gi < a.k_ring_groups; ++gi)
       quant_k_group<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
-                       a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, codes_s);
+                       a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, xs, codes_s);
     for (int p = warp; p < a.v_ring_tokens; p += nwarps)
       quant_v_token<D>(a.dst, a.bits, a.G, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
                        a.v_nv0 + p);
@@ -154,7 +163,7 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
   if (a.chunks > 1 && chunk == 0) return;
   for (int gi = a.k_ring_groups + me; gi < a.k_groups; gi += workers)
     quant_k_group<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
-                     a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, codes_s);
+                     a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, xs, codes_s);
   for (int p = a.v_ring_tokens + me * nwarps + warp; p < a.v_evict; p += workers * nwarps)
     quant_v_token<D>(a.dst, a.bits, a.G, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
                      a.v_nv0 + p);
@@ -163,18 +172,22 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
 // K flush: group blockIdx.y of the ring's oldest tokens.
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) flush_kernel(const AppendArgs a) {
-  __shared__ uint8_t codes_s[kMaxG][kMaxD];
+  extern __shared__ __align__(16) uint8_t qsm[];
+  __half* xs = reinterpret_cast<__half*>(qsm);
+  uint8_t* codes_s = qsm + (size_t)a.G * D * 2;
   const size_t pair = blockIdx.x;
   const int gi = blockIdx.y;
   const __half* ring_k = a.kr + pair * (size_t)a.R * D;
   quant_k_group<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, nullptr, a.ksrc, gi * a.G,
-                   a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, codes_s);
+                   a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, xs, codes_s);
 }
 
 // WindowQuant ingest: block (pair, job); job n_jobs is the fp16 tail.
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs a) {
-  __shared__ uint8_t codes_s[kMaxG][kMaxD];
+  extern __shared__ __align__(16) uint8_t qsm[];
+  __half* xs = reinterpret_cast<__half*>(qsm);
+  uint8_t* codes_s = qsm + (size_t)a.G * D * 2;
   const size_t pair = blockIdx.x;
   const int j = blockIdx.y;
   const __half* in_k = a.k_new + pair * (size_t)a.T * D;
@@ -199,7 +212,7 @@ __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs 
   const __half* wk = in_k + (size_t)job.src_token * D;
   for (int gi = 0; gi < a.S / a.G; ++gi)
     quant_k_group<D>(dst, dst.bits, a.G, a.R, pair, nullptr, wk, src, gi * a.G, job.dst + gi * a.G,
-                     job.dst / a.G + gi, codes_s);
+                     job.dst / a.G + gi, xs, codes_s);
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int p = warp; p < a.S; p += nwarps)
     quant_v_token<D>(dst, dst.bits, a.G, pair, in_v + (size_t)(job.src_token + p) * D, job.dst + p);
@@ -207,25 +220,53 @@ __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs 
 
 }  // namespace
 
+size_t quant_smem(int G, int d) { return (size_t)G * d * 3; }
+
+template <class K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   dim3 grid(a.batch * a.h_kv, a.chunks);
-  if (a.d == 128) append_kernel<128><<<grid, kQuantThreads, 0, s>>>(a);
-  else append_kernel<64><<<grid, kQuantThreads, 0, s>>>(a);
+  const size_t sm = quant_smem(a.G, a.d);
+  cudaError_t e;
+  if (a.d == 128) {
+    if ((e = set_smem(append_kernel<128>, sm)) != cudaSuccess) return e;
+    append_kernel<128><<<grid, kQuantThreads, sm, s>>>(a);
+  } else {
+    if ((e = set_smem(append_kernel<64>, sm)) != cudaSuccess) return e;
+    append_kernel<64><<<grid, kQuantThreads, sm, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_flush(const AppendArgs& a, cudaStream_t s) {
   if (a.k_groups <= 0) return cudaSuccess;
   dim3 grid(a.batch * a.h_kv, a.k_groups);
-  if (a.d == 128) flush_kernel<128><<<grid, kQuantThreads, 0, s>>>(a);
-  else flush_kernel<64><<<grid, kQuantThreads, 0, s>>>(a);
+  const size_t sm = quant_smem(a.G, a.d);
+  cudaError_t e;
+  if (a.d == 128) {
+    if ((e = set_smem(flush_kernel<128>, sm)) != cudaSuccess) return e;
+    flush_kernel<128><<<grid, kQuantThreads, sm, s>>>(a);
+  } else {
+    if ((e = set_smem(flush_kernel<64>, sm)) != cudaSuccess) return e;
+    flush_kernel<64><<<grid, kQuantThreads, sm, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s) {
   dim3 grid(a.batch * a.h_kv, a.n_jobs + 1);
-  if (a.d == 128) ingest_kernel<128><<<grid, kQuantThreads, 0, s>>>(a);
-  else ingest_kernel<64><<<grid, kQuantThreads, 0, s>>>(a);
+  const size_t sm = quant_smem(a.G, a.d);
+  cudaError_t e;
+  if (a.d == 128) {
+    if ((e = set_smem(ingest_kernel<128>, sm)) != cudaSuccess) return e;
+    ingest_kernel<128><<<grid, kQuantThreads, sm, s>>>(a);
+  } else {
+    if ((e = set_smem(ingest_kernel<64>, sm)) != cudaSuccess) return e;
+    ingest_kernel<64><<<grid, kQuantThreads, sm, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
