@@ -13,8 +13,10 @@ roofline = the decode-attention kernel alone: the same bytes / its own
            CUDA-event duration, against the measured HBM copy bandwidth
 e2e      = the same metric through the plain API calls with the step's
            inputs copied from pinned host memory and the output read back
-L2 is flushed (256 MiB write) between timed steps: the cache (114 MB) would
-otherwise sit in the 129 MB L2.
+L2 is flushed between timed steps: the cache (114 MB) would otherwise sit in
+the 129 MB L2.  The flush writes a 256 MiB buffer and then reads another
+256 MiB buffer, so the timed step starts with no cache data in L2 and no
+dirty lines from the flush itself left to write back.
 
 --impl reference times the CPU oracle (plain C + Python) on a bounded sample
 of the same workload (one (batch, kv-head) slice per step), scaled to the
@@ -186,6 +188,11 @@ def run_ours(args, rank, world, local_rank):
     ws = torch.zeros(kvq.kvq_workspace_bytes(cache, kvq.KVQ_MAX_SPLITS), dtype=torch.uint8,
                      device=device)
     l2 = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    l2r = torch.ones(256 << 20, dtype=torch.uint8, device=device)
+
+    def flush_l2(i):
+        l2.fill_(i & 255)
+        l2r.sum()
 
     def stage_inputs(i):
         j = i % pool
@@ -242,7 +249,7 @@ def run_ours(args, rank, world, local_rank):
             reset()
 
     for i in range(args.warmup):
-        l2.fill_(i & 255)
+        flush_l2(i)
         stage_inputs(i)
         run_step()
         if graphs is None:
@@ -258,7 +265,7 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
-        l2.fill_(i & 255)
+        flush_l2(i)
         stage_inputs(args.warmup + i)
         e = ev[i]
         if graphs is not None:
@@ -304,7 +311,7 @@ def run_ours(args, rank, world, local_rank):
     for i in range(n_e2e):
         j = i % pool
         kh, vh, qh = kh_pool[j], vh_pool[j], qh_pool[j]
-        l2.fill_(i & 255)
+        flush_l2(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         k_in.copy_(kh, non_blocking=True)
@@ -462,7 +469,7 @@ def main():
             "workload": "llama2_7b: batch 8, 32 heads (MHA), d_h 128, 3968 packed + 128 fp16 "
                         "tokens for K and V, 2-bit, G 32, R 128; step = quantize-append + "
                         "decode attention + K flush",
-            "l2": "flushed between steps (256 MiB write)",
+            "l2": "flushed between steps (256 MiB write, then 256 MiB read)",
             "graphs": r["graphs"], "parallelism": "replicas" if world > 1 else "single",
             "us_per_step": float(np.mean(r["step_ms"])) * 1e3,
             "us_attention": attn_mean_ms * 1e3,

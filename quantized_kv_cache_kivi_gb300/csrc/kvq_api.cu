@@ -148,21 +148,16 @@ void choose_tile_mha(int kbits, int vbits, int d, int G, int* tile, int* wt) {
 // Tile of the tensor-core kernel: nw <= 4 consumer warps x wt tokens each
 // (wt a multiple of 16), the largest that fits one stage and the K operand
 // table; among equal token counts, more warps win.
+// Tile of the tensor-core kernel: the most tokens (a multiple of the 32-token
+// unit) that fit one stage and the K operand table.
 void choose_tile_tc(int kbits, int vbits, int d, int G, int* tile, int* wt) {
   *tile = *wt = 0;
-  int best_nw = 0;
-  for (int w = 64; w >= 16; w -= 16) {
-    for (int nw = kvq::kTcConsumerWarps; nw >= 1; --nw) {
-      const int t = w * nw;
-      if (tile_bytes(t, kbits, vbits, d, G) > kvq::kTcStageBytes) continue;
-      if (kbits != 16 && (t + G - 1) / G + 1 > kvq::kTcMaxGroups) continue;
-      if (t > *tile || (t == *tile && nw > best_nw)) {
-        *tile = t;
-        *wt = w;
-        best_nw = nw;
-      }
-      break;
-    }
+  for (int t = 256; t >= 32; t -= 32) {
+    if (tile_bytes(t, kbits, vbits, d, G) > kvq::kTcStageBytes) continue;
+    if (kbits != 16 && (t + G - 1) / G + 1 > kvq::kTcMaxGroups) continue;
+    *tile = t;
+    *wt = 32;
+    return;
   }
 }
 
@@ -194,10 +189,10 @@ kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>&
   int oi = 0, oj = 0;  // offsets consumed inside kp[i], vp[j]
   while (i < kp.size() && j < vp.size()) {
     int len = std::min(kp[i].len - oi, vp[j].len - oj);
-    // the tensor-core kernel applies one K group per 16-token sub-tile: a
-    // packed-K run that starts off a multiple of 16 gets a short head run
+    // the tensor-core kernel applies one K group (G >= 32) per 32-token unit:
+    // a packed-K run that starts off a multiple of 32 gets a short head run
     const int uk = kp[i].u0 + oi;
-    if (kern == K_TC && kp[i].seg >= 0 && uk % 16 != 0) len = std::min(len, 16 - uk % 16);
+    if (kern == K_TC && kp[i].seg >= 0 && uk % 32 != 0) len = std::min(len, 32 - uk % 32);
     if (a.n_runs >= kvq::kMaxRuns) return fail(KVQ_ERR_UNSUPPORTED, "too many token runs");
     kvq::Run& r = a.runs[a.n_runs++];
     r.seg_k = kp[i].seg;
@@ -248,6 +243,34 @@ int choose_splits(int n_pairs, int n_tiles, int max_splits) {
   return best;
 }
 
+// CTA owning global tile g when T tiles are cut into N equal contiguous
+// ranges [floor(i T / N), floor((i + 1) T / N)) (the tensor-core kernel's
+// stream-K split; the kernel uses the same formula).
+long long tc_owner(long long g, long long T, long long N) { return ((g + 1) * N + T - 1) / T - 1; }
+
+// Bound on the ranges that cover one pair, for N ranges over n_pairs x
+// n_tiles tiles: every range holds at least floor(T / N) tiles.
+int tc_max_pieces(int n_pairs, int n_tiles, int N) {
+  const long long T = (long long)n_pairs * n_tiles;
+  const long long per = T / N;
+  if (T % N == 0 && per % n_tiles == 0) return 1;  // ranges are whole pairs
+  return (int)std::min<long long>(N, (n_tiles - 1 + per - 1) / per + 1);
+}
+
+// Persistent grid of the tensor-core kernel: as many CTAs as fit on the GPU
+// at once (never more than tiles), fewer while some pair could be cut into
+// more partial records than the workspace holds; one CTA per pair needs none.
+int tc_grid(int n_pairs, int n_tiles, int records) {
+  const long long T = (long long)n_pairs * n_tiles;
+  const int cap = std::max(records, 1);
+  int N = (int)std::min<long long>(T, (long long)sm_count() * kvq::decode_tc_ctas_per_sm());
+  while (tc_max_pieces(n_pairs, n_tiles, N) > cap) {
+    if (N <= n_pairs) return n_pairs;
+    N = std::max(n_pairs, N - std::max(1, N / 32));
+  }
+  return N;
+}
+
 // Walk every tile of the first and the last (batch, kv head) through the same
 // geometry the kernel uses and check each bulk copy before anything launches:
 // 16-byte alignment, source inside its buffer's documented extent, the stage
@@ -271,6 +294,8 @@ kvq_status verify_decode_plan(const kvq_cache* c, const kvq::DecodeArgs& a, int 
         return fail(KVQ_ERR_UNSUPPORTED, "tile %d needs %u stage bytes", t, ti.bytes);
       if (!mha && ti.kseg >= 0 && (size_t)ti.ng * a.gq * D * 4 > (size_t)kvq::kQsBytes)
         return fail(KVQ_ERR_UNSUPPORTED, "tile %d: scaled-query table too small", t);
+      if (kern == K_TC && ti.kseg >= 0 && ti.ku0 % 32 != 0 && ti.ku0 / 32 != (ti.ku0 + ti.n - 1) / 32)
+        return fail(KVQ_ERR_UNSUPPORTED, "tile %d: 32-token unit spans two K groups", t);
       if (mha && ti.kseg >= 0 && ti.ng > max_groups)
         return fail(KVQ_ERR_UNSUPPORTED, "tile %d: %d K groups > %d", t, ti.ng, max_groups);
       struct Copy {
@@ -588,13 +613,22 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   }
   const size_t per_split = (size_t)n_pairs * gq * (cache->d_h + 2) * sizeof(float);
   const int ws_splits = (int)std::min<size_t>(KVQ_MAX_SPLITS, (ws_bytes - ws_fixed(n_pairs)) / per_split);
-  const int S = choose_splits(n_pairs, a.n_tiles, std::max(1, ws_splits));
+  if (kern == K_TC) {
+    if ((long long)n_pairs * a.n_tiles >= (1LL << 31))
+      return fail(KVQ_ERR_UNSUPPORTED, "more than 2^31 tiles");
+    // stream-K: a.n_splits is the record stride per pair
+    a.n_splits = std::max(1, ws_splits);
+    a.n_cta = tc_grid(n_pairs, a.n_tiles, ws_splits);
+    if (tc_max_pieces(n_pairs, a.n_tiles, a.n_cta) > a.n_splits)
+      return fail(KVQ_ERR_UNSUPPORTED, "stream-K planning failed");
+  }
+  const int S = kern == K_TC ? 1 : choose_splits(n_pairs, a.n_tiles, std::max(1, ws_splits));
   // split boundaries with equal byte cost: split k ends at the first tile
   // whose cost midpoint passes k/S of the head's bytes
   std::vector<long long> prefix(a.n_tiles + 1, 0);
   for (int t = 0; t < a.n_tiles; ++t) prefix[t + 1] = prefix[t] + cost[t];
   const long long total = prefix[a.n_tiles];
-  a.n_splits = S;
+  if (kern != K_TC) a.n_splits = S;
   a.split_tile[0] = 0;
   for (int k = 1; k < S; ++k) {
     const long long target = total * k / S;
@@ -629,7 +663,7 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   a.part = reinterpret_cast<float*>(w + ws_fixed(n_pairs));
   st = verify_decode_plan(cache, a, n_pairs, kern);
   if (st != KVQ_OK) return st;
-  const cudaError_t e = kern == K_TC    ? kvq::launch_decode_tc(a, n_pairs, cache->seg[0].bits, s)
+  const cudaError_t e = kern == K_TC    ? kvq::launch_decode_tc(a, cache->seg[0].bits, s)
                         : kern == K_MHA ? kvq::launch_decode_mha(a, n_pairs, cache->seg[0].bits, s)
                                         : kvq::launch_decode(a, n_pairs, s);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "decode launch");

@@ -1,6 +1,6 @@
-// Decode attention for one query head per kv head (MHA), d_h = 128, one
-// packed segment plus the fp16 ring (the KIVI layout), with the contractions
-// on the tensor cores (mma.sync m16n8k16, f16 operands, f32 accumulation).
+// Decode attention for one query head per kv head (MHA) at d_h = 128 over one
+// packed segment plus the fp16 ring (the KIVI layout), with both contractions
+// on the tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation).
 //
 // What is computed (KIVI page, Algorithm 1 decoding branch):
 //   a_t = sm_scale * q . k_t, p = softmax(a), out = sum_t p_t v_t,
@@ -8,23 +8,28 @@
 // channel group).  The algebra that makes both contractions tensor-core
 // shaped:
 //   K:  q . k_t = sum_c (q_c s_gc) code_tc + sum_c q_c z_gc.  A = codes
-//       [token][channel], B = the scaled query (split into an fp16 high and
-//       low part, columns 0 and 1), plus a per-group bias.
+//       [token][channel]; B = the scaled query split into an fp16 high part
+//       (even columns) and low part (odd columns), so every lane ends up with
+//       the whole score of its rows; plus the per-group bias q . z_g.
 //   V:  sum_t p_t (code_tc s_tg(c) + z_tg(c)) = sum_t (p_t s_tg) code_tc +
-//       sum_t p_t z_tg.  A = codes [channel][token], B[t][n] = p_t s_tn for
-//       each channel group n: row c keeps only column g(c).
+//       sum_t p_t z_tg.  A = codes [channel][token]; B[t][n] = p_t s_tn for
+//       the channel groups n < 4 and p_t z_t(n-4) for n >= 4.  Row c keeps
+//       column g(c); one more MMA with an all-ones A yields the z sums.
 // Codes become fp16 operands without any conversion: a code field left at bit
-// p (2 <= p <= 8) of a 16-bit half, all other bits zero, is the fp16
+// p (0 <= p <= 8) of a 16-bit half, every other bit zero, is the fp16
 // subnormal code * 2^(p - 24) exactly; one 32-bit AND yields two of them.
 // The products are exact in the fp32 accumulators, so the factor 2^(24 - p)
-// is applied afterwards: folded into B for K (2^-p) with the scores scaled
-// by 2^24, divided out of each channel row for V.
+// is folded into B for K (2^-p, scores scaled by 2^24 afterwards) and divided
+// out of each channel row for V.
 //
-// CTA = 4 consumer warps + 1 producer warp, one (batch, kv head), a range of
-// its tiles; the producer stages tiles with bulk copies (TMA engine), builds
-// the K operand table of each tile's groups and signals "ready"; consumers
-// each take a slice of 16-token sub-tiles, keep their own online softmax and
-// release the stage.
+// Work split: a persistent grid of CTAs walks the concatenated tile list of
+// all (batch, kv head) pairs in equal contiguous ranges (stream-K); a range
+// that covers part of a pair leaves a partial (o, m, l) record and the last
+// CTA of that pair to finish merges the records.  CTA = 6 consumer warps
+// that take the 16-token sub-tiles of each staged tile in round-robin order,
+// each with its own online softmax; 1 warp that builds each tile's K operand
+// table once its bytes have landed; 1 warp that issues the bulk copies
+// (TMA engine) of up to 4 tiles ahead.
 #include <float.h>
 
 #include "kvq_device.cuh"
@@ -34,58 +39,81 @@ namespace kvq {
 namespace {
 
 constexpr int NCW = kTcConsumerWarps;
-constexpr int NTH = (NCW + 1) * 32;
+constexpr int NTH = (NCW + 2) * 32;  // + table warp + bulk-copy warp
 constexpr int D = 128;
+constexpr int NS = kTcStages;
+constexpr uint32_t kFull = 0xffffffffu;
 
-// ---- shared memory layout ---------------------------------------------------
+// What the producer records about the tile it staged in a stage.
+struct TcRec {
+  // read by the consumer warps
+  int n;       // tokens
+  int kq, vq;  // 1: K / V come from the packed segment, 0: from the ring
+  int kr0;     // first packed K row mod G
+  uint32_t k_off, v_off, vs_off, vz_off;
+  // read by the K table warp
+  int ng;      // K groups staged
+  uint32_t ks_off, kz_off;
+  int pad[5];
+};
+static_assert(sizeof(TcRec) == 64, "record size");
+
+constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
 struct TcSmem {
   static constexpr int stages = 0;
-  static constexpr int ktab = stages + kTcStages * kTcStageBytes;      // [stage][group][hi/lo][tig][kt][2] u32
-  static constexpr int kbias = ktab + kTcStages * kTcKtabBytes;        // [stage][group] f32
-  static constexpr int qnat = kbias + kTcStages * kTcMaxGroups * 4;    // [D] f16, natural order
-  static constexpr int merge = qnat + D * 2;                          // [NCW][D + 2] f32
-  static constexpr int bars = merge + NCW * (D + 2) * 4;
-  static constexpr int flags = bars + 3 * kTcStages * 8;
+  static constexpr int q = stages + NS * kTcStageBytes;               // [stage][D] f16
+  static constexpr int ktab = q + NS * D * 2;                         // [stage] K operand table
+  static constexpr int kbias = ktab + NS * kTcKtabBytes;              // [stage][group] f32
+  static constexpr int rec = kbias + NS * kTcMaxGroups * 4;           // [stage] TcRec
+  static constexpr int merge = rec + NS * 64;                         // [NCW][D + 2] f32
+  static constexpr int zero = align_up(merge + NCW * (D + 2) * 4, 16);  // 64 zero bytes
+  static constexpr int args = zero + 64;                             // DecodeArgs copy
+  static constexpr int bars = align_up(args + (int)sizeof(DecodeArgs), 16);
+  static constexpr int flags = bars + 3 * NS * 8;
   static constexpr int total = flags + 16;
 };
+static_assert(TcSmem::q % 16 == 0 && TcSmem::ktab % 16 == 0 && TcSmem::rec % 16 == 0, "align");
+static_assert(2 * (TcSmem::total + 1024) <= 228 * 1024, "two CTAs per SM");
+
+// Token of row r of a 16-token sub-tile.  Swapping neighbours in the upper
+// half of each 8-row block keeps both the K row loads (rows gid) and the V
+// row loads (rows 2 tig, 2 tig + 1, ...) free of shared-memory bank conflicts.
+__host__ __device__ constexpr int sigma(int r) { return r ^ ((r >> 2) & 1); }
 
 // ---- code fields ------------------------------------------------------------
-// A 32-bit word holds 32/B codes.  View it as two 16-bit halves; field j of a
-// half (0 <= j < 16/B) holds the code of the channel at bit j*B of that half.
-// x << 2 moves fields j < HALFJ to bit j*B + 2; x >> 6 moves the others to
-// bit j*B - 6; either way the field sits at bit p in [2, 8] of its half.
+// A 32-bit word holds 32/B codes: two 16-bit halves of 16/B fields each.
+// Fields inside bits 0..9 of a half are used in place (p = j B); the others
+// are taken from the word shifted right by 6 (p = j B - 6).  Either way the
+// field sits at bit p <= 8 with p + B <= 10, inside the fp16 mantissa.
 template <int B>
 struct Fields {
-  static constexpr int PER_HALF = 16 / B;  // fields per half
-  static constexpr int HALFJ = B == 8 ? 1 : (B == 4 ? 2 : 4);
-  __host__ __device__ static constexpr int pos(int j) { return j < HALFJ ? j * B + 2 : j * B - 6; }
-  // half2 (c_lo 2^(p-24), c_hi 2^(p-24)): field j of both halves, as subnormals
-  __device__ static __forceinline__ uint32_t get(uint32_t xl, uint32_t xr, int j) {
+  static constexpr int INPLACE = B == 2 ? 5 : (B == 4 ? 2 : 1);
+  __host__ __device__ static constexpr int pos(int j) { return j < INPLACE ? j * B : j * B - 6; }
+  // (code_lo 2^(p-24), code_hi 2^(p-24)) as a half2: field j of both halves
+  __device__ static __forceinline__ uint32_t get(uint32_t x, uint32_t x_shr6, int j) {
     const uint32_t m = ((1u << B) - 1u) << pos(j);
-    return (j < HALFJ ? xl : xr) & (m | (m << 16));
+    return (j < INPLACE ? x : x_shr6) & (m | (m << 16));
   }
 };
 
-// K operand layout.  Consumer thread (gid, tig) of a warp owns the 32
-// channels [32 tig, 32 tig + 32) of its tokens.  Its h-th half2 (h < 16)
-// holds two channels of one token: word w = h / (2 * PER_HALF), field j = h
-// % PER_HALF of the low or high half (h / PER_HALF odd = high half ... see
-// below); k-tile kt uses h = 2 kt (cols 2 tig, 2 tig + 1) and h = 2 kt + 1
-// (cols 2 tig + 8, 2 tig + 9).
+// K: thread tig owns channels [32 tig, 32 tig + 32) of its rows; its h-th
+// half2 (h = 2 kt + e, e = 0 for k columns 2 tig.., 1 for 2 tig + 8..) holds
+// field j = h % PER_HALF of word w = h / PER_HALF: channels c_lo (low half)
+// and c_hi (high half).
 template <int B>
 __host__ __device__ constexpr void k_half2_channels(int tig, int h, int* c_lo, int* c_hi, int* p) {
-  constexpr int PH = 16 / B;             // fields per half = channels per half
-  const int w = h / PH;                  // word index among the thread's words
-  const int j = h % PH;                  // field inside each half
+  constexpr int PH = 16 / B;
+  const int w = h / PH, j = h % PH;
   const int base = 32 * tig + w * (32 / B);
-  *c_lo = base + j;                      // low half: channels base .. base + PH - 1
-  *c_hi = base + PH + j;                 // high half: channels base + PH ..
+  *c_lo = base + j;
+  *c_hi = base + PH + j;
   *p = Fields<B>::pos(j);
 }
 
-// V operand layout: thread gid owns channels [16 gid, 16 gid + 16) of the 4
-// tokens it reads; m-tile mt = (word w, field j) with w = mt / PER_HALF,
-// j = mt % PER_HALF; row gid <- low-half channel, row gid + 8 <- high-half.
+// V: thread gid owns channels [16 gid, 16 gid + 16) of its tokens; m-tile mt
+// = (word w, field j), w = mt / PER_HALF, j = mt % PER_HALF; row gid <- the
+// low-half channel, row gid + 8 <- the high-half channel.
 template <int B>
 __host__ __device__ constexpr void v_rows(int gid, int mt, int* c_row0, int* c_row8, int* p) {
   constexpr int PH = 16 / B;
@@ -105,29 +133,51 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
+// 8x8 b16 transpose across the warp: lane (gid, tig) passes row gid, columns
+// 2 tig, 2 tig + 1 and receives row gid of the transpose.
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
-__device__ __forceinline__ void ldmatrix_x4_t(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-__device__ __forceinline__ float2 unpack_half2(uint32_t u) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t halves(uint16_t lo, uint16_t hi) {
+  return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// try_wait that may sleep up to `ns` nanoseconds for the phase to complete
+// (the thread resumes as soon as it does).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: about 2^31 SM clocks, then the abort flag is raised.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, 1000000u)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > (1ll << 31)) {
       *abort_flag = 1;
@@ -141,422 +191,622 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Per-thread state of one consumer warp (V: D fragments carry 2^(p - 24)).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
+}
+
+// CTA owning global tile g when T tiles are cut into N equal ranges
+// [floor(i T / N), floor((i + 1) T / N)).
+__device__ __forceinline__ int owner_cta(long long g, long long T, int N) {
+  return (int)(((g + 1) * N + T - 1) / T) - 1;
+}
+
+// Per-warp online-softmax state.  acc holds, for the channel rows of m-tile
+// mt, D = sum_t B[t][n] A[c][t] (packed V: carrying 2^(p - 24) until the first
+// ring-V sub-tile or the end); accz columns 4.. hold sum_t p_t z_t(n-4).
 struct WarpState {
-  float m;            // running max (log2 domain), warp-uniform
-  float l;            // sum of p over this thread's tokens (tig == 0 threads)
-  float zs;           // sum p z for column gid (packed V), this thread's tokens
-  float acc[8][4];    // packed V: D fragments of the 8 channel m-tiles
-  float accr[8][4];   // ring V: D fragments, natural channel rows
+  float m;  // running max (log2 domain), warp-uniform
+  float l;  // sum of p over the rows of this lane (tig-replicated)
+  float acc[8][4];
+  float accz[4];
+  bool vring;  // acc already unscaled (ring V reached)
 };
 
 template <int B>
-__device__ __forceinline__ void rescale(WarpState& S, float alpha) {
-  S.l *= alpha;
-  S.zs *= alpha;
+__device__ __forceinline__ void unscale_acc(WarpState& S) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int mt = 0; mt < 8; ++mt) {
+    const int p = Fields<B>::pos(mt % (16 / B));
+    const float us = __uint_as_float((uint32_t)(127 + 24 - p) << 23);  // 2^(24 - p)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      S.acc[i][e] *= alpha;
-      S.accr[i][e] *= alpha;
-    }
+    for (int e = 0; e < 4; ++e) S.acc[mt][e] *= us;
+  }
 }
 
-// One 16-token sub-tile [s0, s0 + 16) of a tile (tokens >= n are padding).
+// The dynamic shared memory block of the decode kernel.
+__device__ __forceinline__ uint8_t* tc_smem() {
+  extern __shared__ __align__(128) uint8_t smem_dyn[];
+  return smem_dyn;
+}
+
+// Scores (log2 domain) of the rows gid and gid + 8 of the 16-token half at
+// s0 + 16 h, packed K: the shared B operand bq of the unit's K group, the
+// thread's code words of its two rows, 8 MMAs in two chains.
 template <int B>
-__device__ __forceinline__ void sub_tile(const DecodeArgs& a, const TileInfo& ti, const uint8_t* stage,
-                                         const uint32_t* kt_hi_lo, const float* kbias,
-                                         const __half* qnat, int s0, int lane, WarpState& S) {
-  constexpr int RB = D * B / 8;        // packed row bytes
+__device__ __forceinline__ void k_scores_packed(const uint8_t* kc, int s0, int r0, int r1, const uint32_t (&bq)[16],
+                                                float bias, float& x0, float& x1) {
   constexpr int PH = 16 / B;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int n = ti.n;
-  // ------------------------------------------------------------- scores
-  float sc[4] = {0.f, 0.f, 0.f, 0.f};  // C fragment: rows gid, gid + 8; cols 2 tig, 2 tig + 1
-  if (ti.kseg >= 0) {
-    // B operand (scaled query) of this token group: threads with gid 0 (high
-    // part) and gid 1 (low part) hold it; the other columns are zero
-    const int gl = min(((ti.ku0 + s0) >> a.log2G) - ti.g0, ti.ng - 1);
-    uint32_t bq[16];
-    if (gid < 2) {
-      const uint4* src = reinterpret_cast<const uint4*>(kt_hi_lo + ((gl * 2 + gid) * 4 + tig) * 16);
+  constexpr int RB = D * B / 8;           // packed row bytes
+  constexpr int NW = B;                   // words of a row per thread (32 channels)
+  constexpr int WPC = NW < 4 ? NW : 4;    // words per load
+  constexpr int NCH = NW / WPC;           // loads per row
+  float sc[4] = {0.f, 0.f, 0.f, 0.f};
+  float sd[4] = {0.f, 0.f, 0.f, 0.f};  // odd k-tiles: two shorter MMA chains
 #pragma unroll
-      for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(&bq[4 * k]) = src[k];
+  for (int ch = 0; ch < NCH; ++ch) {
+    uint32_t w0[WPC], w1[WPC];
+    if constexpr (WPC == 2) {
+      const uint2 u0 = *reinterpret_cast<const uint2*>(kc + (s0 + r0) * RB);
+      const uint2 u1 = *reinterpret_cast<const uint2*>(kc + (s0 + r1) * RB);
+      w0[0] = u0.x; w0[1] = u0.y;
+      w1[0] = u1.x; w1[1] = u1.y;
     } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) bq[k] = 0u;
-    }
-    // A operand: the thread's words of tokens s0 + gid and s0 + gid + 8
-    constexpr int NW = B;  // 32-bit words per thread per token (32 channels)
-    const uint32_t* r0 = reinterpret_cast<const uint32_t*>(stage + ti.k_off + (size_t)(s0 + gid) * RB) + tig * NW;
-    const uint32_t* r1 = reinterpret_cast<const uint32_t*>(stage + ti.k_off + (size_t)(s0 + gid + 8) * RB) + tig * NW;
-    uint32_t w0[NW], w1[NW];
-#pragma unroll
-    for (int k = 0; k < NW; ++k) {
-      w0[k] = r0[k];
-      w1[k] = r1[k];
+      const uint4 u0 = *reinterpret_cast<const uint4*>(kc + (s0 + r0) * RB + 16 * ch);
+      const uint4 u1 = *reinterpret_cast<const uint4*>(kc + (s0 + r1) * RB + 16 * ch);
+      w0[0] = u0.x; w0[1] = u0.y; w0[2] = u0.z; w0[3] = u0.w;
+      w1[0] = u1.x; w1[1] = u1.y; w1[2] = u1.z; w1[3] = u1.w;
     }
 #pragma unroll
-    for (int kt = 0; kt < 8; ++kt) {
-      uint32_t a[4];
+    for (int kk = 0; kk < 8 / NCH; ++kk) {
+      const int kt = ch * (8 / NCH) + kk;
+      uint32_t av[4];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int h = 2 * kt + e;
-        const int w = h / PH, j = h % PH;
-        a[2 * e + 0] = Fields<B>::get(w0[w] << 2, w0[w] >> 6, j);
-        a[2 * e + 1] = Fields<B>::get(w1[w] << 2, w1[w] >> 6, j);
+        const int w = h / PH - ch * WPC, j = h % PH;
+        av[2 * e + 0] = Fields<B>::get(w0[w], w0[w] >> 6, j);
+        av[2 * e + 1] = Fields<B>::get(w1[w], w1[w] >> 6, j);
       }
-      // fragment order: a0 (row gid, cols 2tig..), a1 (row gid+8), a2 (row gid, cols 2tig+8..), a3
-      mma16816(sc, a[0], a[1], a[2], a[3], bq[2 * kt], bq[2 * kt + 1]);
+      mma16816((kt & 1) ? sd : sc, av[0], av[1], av[2], av[3], bq[2 * kt], bq[2 * kt + 1]);
     }
-    const float bias = kbias[gl];
-    constexpr float k2p24 = 16777216.0f;  // the A operands carry 2^-24
-    sc[0] = (sc[0] + sc[1]) * k2p24 + bias;  // token s0 + gid (valid in tig == 0 threads)
-    sc[2] = (sc[2] + sc[3]) * k2p24 + bias;  // token s0 + gid + 8
-  } else {
-    // fp16 ring K in natural channel order: ldmatrix for A, q (natural) for B
+  }
+  // the table carries sm_scale log2(e) and 2^-p, the codes 2^(p - 24)
+  x0 = fmaf((sc[0] + sd[0]) + (sc[1] + sd[1]), 16777216.0f, bias);  // row gid: high + low column
+  x1 = fmaf((sc[2] + sd[2]) + (sc[3] + sd[3]), 16777216.0f, bias);  // row gid + 8
+}
+
+// Same for fp16 ring K.  Thread tig reads its 32 channels as four 16-byte
+// chunks, chunk kc at position (kc + tig) & 3 of the block (spreads the
+// banks), and the query words in the same order: each chunk feeds 2 MMAs.
+__device__ __forceinline__ void k_scores_ring(const uint8_t* kr, const uint8_t* qt, int s0, int r0, int r1,
+                                              int tig, float scale_log2, float& x0, float& x1) {
+  float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int kt = 0; kt < 8; ++kt) {
-      uint32_t a[4];
-      const int row = s0 + (lane & 15);
-      const int col = kt * 16 + (lane >> 4) * 8;
-      ldmatrix_x4(a, stage + ti.k_off + ((size_t)row * D + col) * 2);
-      uint32_t b0 = 0u, b1 = 0u;
-      if (gid == 0) {
-        b0 = *reinterpret_cast<const uint32_t*>(qnat + kt * 16 + 2 * tig);
-        b1 = *reinterpret_cast<const uint32_t*>(qnat + kt * 16 + 2 * tig + 8);
-      }
-      // ldmatrix x4 order: [rows 0-7, cols 0-7], [rows 8-15, cols 0-7],
-      // [rows 0-7, cols 8-15], [rows 8-15, cols 8-15] = a0, a1, a2, a3
-      mma16816(sc, a[0], a[1], a[2], a[3], b0, b1);
-    }
-    sc[2] = sc[2];
+  for (int kc = 0; kc < 4; ++kc) {
+    const int off = ((kc + tig) & 3) * 16;
+    const uint4 u0 = *reinterpret_cast<const uint4*>(kr + (s0 + r0) * (D * 2) + off);
+    const uint4 u1 = *reinterpret_cast<const uint4*>(kr + (s0 + r1) * (D * 2) + off);
+    const uint4 qw = *reinterpret_cast<const uint4*>(qt + off);
+    mma16816(sc, u0.x, u1.x, u0.y, u1.y, qw.x, qw.y);
+    mma16816(sc, u0.z, u1.z, u0.w, u1.w, qw.z, qw.w);
+  }
+  x0 = sc[0] * scale_log2;  // B = q in every column
+  x1 = sc[2] * scale_log2;
+}
+
+// One 32-token unit [s0, s0 + 32) of the staged tile: two 16-token halves
+// (rows sigma(r) of half h are tokens s0 + 16 h + sigma(r)).  s0 is a
+// multiple of 32 and the unit lies inside one K group (G >= 32, packed runs
+// start on 32-token boundaries), so both halves share one K operand.
+template <int B, bool KQ, bool VQ, bool FULL>
+__device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRec& r, int s0, int lane, WarpState& S) {
+  constexpr int PH = 16 / B;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int r0 = sigma(gid), r1 = sigma(gid + 8);
+  uint8_t* const sm = tc_smem();
+  const uint8_t* const stage = sm + TcSmem::stages + st * kTcStageBytes;
+  const int nv = r.n - s0;  // valid tokens from s0 (>= 32 when FULL)
+  // ------------------------------------------------------------- scores
+  float x[2][2];  // [half][row gid, row gid + 8]
+  if constexpr (KQ) {
+    const int gl = (r.kr0 + s0) >> a.log2G;
+    const uint4* tb = reinterpret_cast<const uint4*>(sm + TcSmem::ktab + st * kTcKtabBytes) + gl * 32 + (gid & 1) * 4 + tig;
+    uint32_t bq[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(&bq[4 * k]) = tb[k * 8];
+    const float bias = reinterpret_cast<const float*>(sm + TcSmem::kbias)[st * kTcMaxGroups + gl];
+    const uint8_t* kc = stage + r.k_off + tig * (B * 4);
+    k_scores_packed<B>(kc, s0, r0, r1, bq, bias, x[0][0], x[0][1]);
+    if (FULL || nv > 16) k_scores_packed<B>(kc, s0 + 16, r0, r1, bq, bias, x[1][0], x[1][1]);
+    else x[1][0] = x[1][1] = -INFINITY;
+  } else {
+    const uint8_t* qt = sm + TcSmem::q + st * D * 2 + tig * 64;
+    const uint8_t* kr = stage + r.k_off + tig * 64;
+    k_scores_ring(kr, qt, s0, r0, r1, tig, a.scale_log2, x[0][0], x[0][1]);
+    if (FULL || nv > 16) k_scores_ring(kr, qt, s0 + 16, r0, r1, tig, a.scale_log2, x[1][0], x[1][1]);
+    else x[1][0] = x[1][1] = -INFINITY;
+  }
+  if constexpr (!FULL) {
+    if (r0 >= nv) x[0][0] = -INFINITY;
+    if (r1 >= nv) x[0][1] = -INFINITY;
+    if (16 + r0 >= nv) x[1][0] = -INFINITY;
+    if (16 + r1 >= nv) x[1][1] = -INFINITY;
   }
   // ------------------------------------------------------ online softmax
-  const bool v0 = s0 + gid < n, v1 = s0 + gid + 8 < n;
-  float x0 = (tig == 0 && v0) ? sc[0] * a.scale_log2 : -INFINITY;
-  float x1 = (tig == 0 && v1) ? sc[2] * a.scale_log2 : -INFINITY;
-  float mx = fmaxf(x0, x1);
+  float mloc = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+  if (__any_sync(kFull, mloc > S.m)) {
+    mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 4));
+    mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 8));
+    mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 16));
+    const float alpha = ex2(S.m - mloc);  // 0 while S.m is -inf
+    S.l *= alpha;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  const float m_new = fmaxf(S.m, mx);
-  if (m_new != S.m && S.m != -INFINITY) rescale<B>(S, exp2f(S.m - m_new));
-  S.m = m_new;
-  const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - m_new);
-  const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - m_new);
-  S.l += p0 + p1;
-  // p of tokens 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 of the sub-tile
-  const float pa = __shfl_sync(0xffffffffu, p0, 8 * tig);      // token 2 tig
-  const float pb = __shfl_sync(0xffffffffu, p0, 8 * tig + 4);  // token 2 tig + 1
-  const float pc = __shfl_sync(0xffffffffu, p1, 8 * tig);      // token 2 tig + 8
-  const float pd = __shfl_sync(0xffffffffu, p1, 8 * tig + 4);  // token 2 tig + 9
-  const int ta = s0 + 2 * tig, tb = ta + 1, tc = ta + 8, td = ta + 9;
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) S.acc[mt][e] *= alpha;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) S.accz[e] *= alpha;
+    S.m = mloc;
+  }
+  uint32_t pp[2][2];  // B rows k = 2 tig, 2 tig + 1 | 2 tig + 8, 2 tig + 9 of each half
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float p0 = ex2(x[h][0] - S.m), p1 = ex2(x[h][1] - S.m);
+    S.l += p0 + p1;
+    pp[h][0] = movm_trans(pack_half2(p0, p0));
+    pp[h][1] = movm_trans(pack_half2(p1, p1));
+  }
+  const int ta = sigma(2 * tig), tb = sigma(2 * tig + 1), tc = sigma(2 * tig + 8), td = sigma(2 * tig + 9);
   // ------------------------------------------------------------------ PV
-  if (ti.vseg >= 0) {
+  if constexpr (VQ) {
+    constexpr int RB = D * B / 8;
+    constexpr int NW = B / 2;  // words per token for the thread's 16 channels
+    // column n = gid: scale (n < 4) or zero (n >= 4) of group n & 3
     const int ngv = D >> a.log2G;
-    const __half* vs = reinterpret_cast<const __half*>(stage + ti.vs_off);
-    const __half* vz = reinterpret_cast<const __half*>(stage + ti.vz_off);
-    uint32_t b0 = 0u, b1 = 0u;
-    if (gid < ngv) {
-      // padding tokens carry p = 0 and must not read scales (may be NaN)
-      const float sa = ta < n ? __half2float(vs[ta * ngv + gid]) : 0.f;
-      const float sb = tb < n ? __half2float(vs[tb * ngv + gid]) : 0.f;
-      const float sc2 = tc < n ? __half2float(vs[tc * ngv + gid]) : 0.f;
-      const float sd = td < n ? __half2float(vs[td * ngv + gid]) : 0.f;
-      b0 = pack_half2(pa * sa, pb * sb);
-      b1 = pack_half2(pc * sc2, pd * sd);
-      S.zs += (ta < n ? pa * __half2float(vz[ta * ngv + gid]) : 0.f) +
-              (tb < n ? pb * __half2float(vz[tb * ngv + gid]) : 0.f) +
-              (tc < n ? pc * __half2float(vz[tc * ngv + gid]) : 0.f) +
-              (td < n ? pd * __half2float(vz[td * ngv + gid]) : 0.f);
+    const int g = gid & 3;
+    const uint16_t* sp;
+    int stride;
+    if (g < ngv) {
+      sp = reinterpret_cast<const uint16_t*>(stage + (gid < 4 ? r.vs_off : r.vz_off)) + (s0 * ngv + g);
+      stride = ngv;
+    } else {
+      sp = reinterpret_cast<const uint16_t*>(sm + TcSmem::zero);
+      stride = 0;
     }
-    // A: the thread's 16 channels of tokens (ta, tb) and (tc, td)
-    constexpr int NW = B / 2;  // words per token for 16 channels
-    const uint32_t* ra = reinterpret_cast<const uint32_t*>(stage + ti.v_off + (size_t)ta * RB) + gid * NW;
-    const uint32_t* rb = reinterpret_cast<const uint32_t*>(stage + ti.v_off + (size_t)tb * RB) + gid * NW;
-    const uint32_t* rc = reinterpret_cast<const uint32_t*>(stage + ti.v_off + (size_t)tc * RB) + gid * NW;
-    const uint32_t* rd = reinterpret_cast<const uint32_t*>(stage + ti.v_off + (size_t)td * RB) + gid * NW;
+    uint32_t bv[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int o = 16 * h;
+      uint16_t sa = sp[(o + ta) * stride], sb = sp[(o + tb) * stride];
+      uint16_t scc = sp[(o + tc) * stride], sd = sp[(o + td) * stride];
+      if constexpr (!FULL) {
+        // padding tokens: p = 0, and their stale scale bits must not make NaN
+        if (o + ta >= nv) sa = 0;
+        if (o + tb >= nv) sb = 0;
+        if (o + tc >= nv) scc = 0;
+        if (o + td >= nv) sd = 0;
+      }
+      bv[h][0] = hmul2u(pp[h][0], halves(sa, sb));
+      bv[h][1] = hmul2u(pp[h][1], halves(scc, sd));
+    }
+    const uint8_t* vc = stage + r.v_off + s0 * RB + gid * (NW * 4);
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const uint32_t wa = ra[w], wb = rb[w], wc = rc[w], wd = rd[w];
-      const uint32_t lo1 = __byte_perm(wa, wb, 0x5410), hi1 = __byte_perm(wa, wb, 0x7632);
-      const uint32_t lo2 = __byte_perm(wc, wd, 0x5410), hi2 = __byte_perm(wc, wd, 0x7632);
+      uint32_t lo1[2], hi1[2], lo2[2], hi2[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint8_t* vh = vc + 16 * h * RB + 4 * w;
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vh + ta * RB);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vh + tb * RB);
+        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vh + tc * RB);
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vh + td * RB);
+        lo1[h] = __byte_perm(wa, wb, 0x5410);
+        hi1[h] = __byte_perm(wa, wb, 0x7632);
+        lo2[h] = __byte_perm(wc, wd, 0x5410);
+        hi2[h] = __byte_perm(wc, wd, 0x7632);
+      }
 #pragma unroll
       for (int j = 0; j < PH; ++j) {
         const int mt = w * PH + j;
-        mma16816(S.acc[mt], Fields<B>::get(lo1 << 2, lo1 >> 6, j), Fields<B>::get(hi1 << 2, hi1 >> 6, j),
-                 Fields<B>::get(lo2 << 2, lo2 >> 6, j), Fields<B>::get(hi2 << 2, hi2 >> 6, j), b0, b1);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          mma16816(S.acc[mt], Fields<B>::get(lo1[h], lo1[h] >> 6, j), Fields<B>::get(hi1[h], hi1[h] >> 6, j),
+                   Fields<B>::get(lo2[h], lo2[h] >> 6, j), Fields<B>::get(hi2[h], hi2[h] >> 6, j), bv[h][0], bv[h][1]);
       }
     }
+    constexpr uint32_t ONES = 0x3C003C00u;  // (1.0, 1.0)
+    mma16816(S.accz, ONES, ONES, ONES, ONES, bv[0][0], bv[0][1]);
+    mma16816(S.accz, ONES, ONES, ONES, ONES, bv[1][0], bv[1][1]);
   } else {
-    // fp16 ring V, natural channel rows: A = V^T tiles by ldmatrix.trans;
-    // B column 0 = p; padding rows of the last sub-tile are zeroed
-    const uint32_t b0 = gid == 0 ? pack_half2(pa, pb) : 0u;
-    const uint32_t b1 = gid == 0 ? pack_half2(pc, pd) : 0u;
-    const bool full = s0 + 16 <= n;
+    // fp16 ring V: B = p in every column; A rows are the same channels as
+    // for packed V, gathered from the thread's 16 channels of each token
+    if (!S.vring) {
+      unscale_acc<B>(S);
+      S.vring = true;
+    }
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      uint32_t r[4];
-      // matrices: [tok 0-7, ch mt*16+0..7], [tok 0-7, ch +8..15], [tok 8-15, ch 0..7], [tok 8-15, ch 8..15]
-      const int tok = s0 + (lane & 7) + ((lane >> 4) << 3);
-      const int ch = mt * 16 + ((lane >> 3) & 1) * 8;
-      ldmatrix_x4_t(r, stage + ti.v_off + ((size_t)tok * D + ch) * 2);
-      if (!full) {
-        // element (row = channel, col = token): r0/r1 hold tokens 2tig, 2tig+1; r2/r3 tokens +8
-        if (ta >= n) { r[0] &= 0xffff0000u; r[1] &= 0xffff0000u; }
-        if (tb >= n) { r[0] &= 0x0000ffffu; r[1] &= 0x0000ffffu; }
-        if (tc >= n) { r[2] &= 0xffff0000u; r[3] &= 0xffff0000u; }
-        if (td >= n) { r[2] &= 0x0000ffffu; r[3] &= 0x0000ffffu; }
+    for (int h = 0; h < 2; ++h) {
+      const int o = 16 * h;
+      if (!FULL && o >= nv) break;
+      // thread gid's 16 channels of tokens ta, tb, tc, td: 32-bit words (channel
+      // pairs) read per m-tile to keep few registers live; padding tokens'
+      // stale bytes (possibly NaN) are replaced by zeros
+      const uint8_t* vr = stage + r.v_off + (s0 + o) * (D * 2) + gid * 32;
+      const uint32_t* va = reinterpret_cast<const uint32_t*>(vr + ta * (D * 2));
+      const uint32_t* vb = reinterpret_cast<const uint32_t*>(vr + tb * (D * 2));
+      const uint32_t* vcc = reinterpret_cast<const uint32_t*>(vr + tc * (D * 2));
+      const uint32_t* vd = reinterpret_cast<const uint32_t*>(vr + td * (D * 2));
+      const uint32_t ma = (FULL || o + ta < nv) ? 0xffffffffu : 0u, mb = (FULL || o + tb < nv) ? 0xffffffffu : 0u;
+      const uint32_t mc = (FULL || o + tc < nv) ? 0xffffffffu : 0u, md = (FULL || o + td < nv) ? 0xffffffffu : 0u;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        int c0, c8, p;
+        v_rows<B>(0, mt, &c0, &c8, &p);  // offsets inside the thread's 16 channels
+        const uint32_t s0sel = (c0 & 1) ? 0x7632u : 0x5410u;
+        const uint32_t s8sel = (c8 & 1) ? 0x7632u : 0x5410u;
+        mma16816(S.acc[mt], __byte_perm(va[c0 >> 1] & ma, vb[c0 >> 1] & mb, s0sel),
+                 __byte_perm(va[c8 >> 1] & ma, vb[c8 >> 1] & mb, s8sel),
+                 __byte_perm(vcc[c0 >> 1] & mc, vd[c0 >> 1] & md, s0sel),
+                 __byte_perm(vcc[c8 >> 1] & mc, vd[c8 >> 1] & md, s8sel), pp[h][0], pp[h][1]);
       }
-      mma16816(S.accr[mt], r[0], r[1], r[2], r[3], b0, b1);
     }
   }
+}
+
+// The 32-token units j, j + NCW, ... of one staged tile (only the last unit
+// of a tile can be partial).  Returns this warp's first unit of the next
+// tile: the units are dealt out round-robin across tiles.
+template <int B, bool KQ, bool VQ>
+__device__ __forceinline__ int run_tile(const DecodeArgs& a, int st, const TcRec& r, int j, int lane, WarpState& S) {
+  const int n_full = r.n >> 5, n_unit = (r.n + 31) >> 5;
+  for (; j < n_full; j += NCW) sub_unit<B, KQ, VQ, true>(a, st, r, j * 32, lane, S);
+  if (j < n_unit) {
+    sub_unit<B, KQ, VQ, false>(a, st, r, j * 32, lane, S);
+    j += NCW;
+  }
+  return j - n_unit;
+}
+
+// End of a warp's share of one pair inside this CTA's range: merge the warps,
+// then write the output (the pair lies in this range only) or a partial
+// record (merged by the pair's last CTA to finish).
+template <int B>
+__device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, long long T, int warp,
+                             int lane, WarpState& S, volatile int* flags) {
+  const int gid = lane >> 2, tig = lane & 3;
+  float* mg = reinterpret_cast<float*>(smem + TcSmem::merge) + warp * (D + 2);
+  if (!S.vring) unscale_acc<B>(S);
+  float l = S.l;  // rows are replicated over tig: sum over gid only
+  l += __shfl_xor_sync(kFull, l, 4);
+  l += __shfl_xor_sync(kFull, l, 8);
+  l += __shfl_xor_sync(kFull, l, 16);
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    int c0, c8, p;
+    v_rows<B>(gid, mt, &c0, &c8, &p);
+    const int g = c0 >> a.log2G;  // c0 and c8 share their group
+    // z sum of group g: column 4 + g, held by lanes with tig = 2 + g / 2
+    const float z0 = __shfl_sync(kFull, S.accz[0], 2 + (g >> 1));
+    const float z1 = __shfl_sync(kFull, S.accz[1], 2 + (g >> 1));
+    const float zg = (g & 1) ? z1 : z0;
+    if (tig == (g >> 1)) {
+      mg[c0] = ((g & 1) ? S.acc[mt][1] : S.acc[mt][0]) + zg;
+      mg[c8] = ((g & 1) ? S.acc[mt][3] : S.acc[mt][2]) + zg;
+    }
+  }
+  if (lane == 0) {
+    mg[D] = S.m;
+    mg[D + 1] = l;
+  }
+  const int tid = warp * 32 + lane;
+  if (tid == 0) flags[2] = flags[0];  // one abort verdict for every thread
+  consumer_sync();
+  const long long nt = a.n_tiles;
+  const int first = owner_cta((long long)pair * nt, T, a.n_cta);
+  const int last = owner_cta((long long)pair * nt + nt - 1, T, a.n_cta);
+  const int pieces = last - first + 1;
+  const size_t out_base = (size_t)pair * D;
+  float* rec = a.part + ((size_t)pair * a.n_splits + (blockIdx.x - first)) * (D + 2);
+  const bool ok = flags[2] == 0;
+  if (ok && tid < D) {
+    const float* m0 = reinterpret_cast<const float*>(smem + TcSmem::merge);
+    float M = -INFINITY;
+    for (int w = 0; w < NCW; ++w) M = fmaxf(M, m0[w * (D + 2) + D]);
+    float L = 0.f, O = 0.f;
+    for (int w = 0; w < NCW; ++w) {
+      const float* mw = m0 + w * (D + 2);
+      const float sw = (mw[D] == -INFINITY) ? 0.f : exp2f(mw[D] - M);
+      L += mw[D + 1] * sw;
+      O += mw[tid] * sw;
+    }
+    if (pieces == 1) {
+      a.out[out_base + tid] = __float2half_rn(O / L);
+    } else {
+      rec[tid] = O;
+      if (tid == 0) {
+        rec[D] = M;
+        rec[D + 1] = L;
+      }
+    }
+  }
+  if (!ok && tid == 0) atomicExch(a.err, 1);
+  consumer_sync();  // merge area free again; records written
+  if (pieces == 1 || !ok) return;
+  __threadfence();
+  consumer_sync();
+  if (tid == 0) flags[1] = (atomicAdd(&a.counters[pair], 1) == pieces - 1);
+  consumer_sync();
+  const bool merger = flags[1] != 0;
+  consumer_sync();  // flags[1] read by all before a later piece rewrites it
+  if (!merger) return;
+  __threadfence();
+  const float* recs = a.part + (size_t)pair * a.n_splits * (D + 2);
+  if (tid < D) {
+    float MM = -INFINITY;
+    for (int s = 0; s < pieces; ++s) MM = fmaxf(MM, __ldcg(recs + (size_t)s * (D + 2) + D));
+    float L = 0.f, O = 0.f;
+    for (int s = 0; s < pieces; ++s) {
+      const float* rr = recs + (size_t)s * (D + 2);
+      const float w = exp2f(__ldcg(rr + D) - MM);
+      L += __ldcg(rr + D + 1) * w;
+      O += __ldcg(rr + tid) * w;
+    }
+    a.out[out_base + tid] = __float2half_rn(O / L);
+  }
+  if (tid == 0) a.counters[pair] = 0;
 }
 
 template <int B>
 __global__ void __launch_bounds__(NTH, 2) decode_tc_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcSmem::bars);
-  uint64_t* ready = full + kTcStages;
-  uint64_t* empty = ready + kTcStages;
+  uint64_t* ready = full + NS;
+  uint64_t* empty = ready + NS;
   volatile int* flags = reinterpret_cast<volatile int*>(smem + TcSmem::flags);
-  __half* qnat = reinterpret_cast<__half*>(smem + TcSmem::qnat);
+  TcRec* recs = reinterpret_cast<TcRec*>(smem + TcSmem::rec);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pair = blockIdx.x / a.n_splits;
-  const int split = blockIdx.x % a.n_splits;
-  const int t_begin = a.split_tile[split], t_end = a.split_tile[split + 1];
-  const int ntiles = t_end - t_begin;
-  const int b = pair / a.h_kv, hk = pair % a.h_kv;
-  const __half* qg = a.q + ((size_t)b * a.h_kv + hk) * D;
+  const int T = a.batch * a.h_kv * a.n_tiles;  // below 2^31 (checked by the host)
+  const int g_begin = (int)((long long)blockIdx.x * T / a.n_cta);
+  const int g_end = (int)((long long)(blockIdx.x + 1) * T / a.n_cta);
+  const int ntiles = g_end - g_begin;
 
   if (tid == 0) {
     flags[0] = 0;
-    for (int s = 0; s < kTcStages; ++s) {
+    flags[1] = 0;
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&ready[s], 1);
       mbar_init(&empty[s], NCW);
     }
     mbar_fence_init();
   }
-  for (int c = tid; c < D; c += NTH) qnat[c] = qg[c];
+  if (tid < 16) reinterpret_cast<uint32_t*>(smem + TcSmem::zero)[tid] = 0u;
+  static_assert(sizeof(DecodeArgs) % 4 == 0, "word copy");
+  for (int i = tid; i < (int)(sizeof(DecodeArgs) / 4); i += NTH)
+    reinterpret_cast<uint32_t*>(smem + TcSmem::args)[i] = reinterpret_cast<const uint32_t*>(&a)[i];
+  const DecodeArgs* args_s = reinterpret_cast<const DecodeArgs*>(smem + TcSmem::args);
   __syncthreads();
 
-  if (warp == NCW) {
-    // ------------------------------------------------------------ producer
-    auto issue = [&](int j) {
-      const int st = j % kTcStages;
-      if (j >= kTcStages &&
-          !wait_or_abort(&empty[st], (uint32_t)(((j / kTcStages) & 1) ^ 1), flags))
-        return false;
-      if (lane == 0) {
-        uint8_t* stage = smem + TcSmem::stages + st * kTcStageBytes;
-        const TileInfo ti = tile_info(a, t_begin + j);
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&full[st], ti.bytes);
-        for_each_tile_copy(a, (size_t)pair, ti,
-                           [&](const void* src, uint32_t off, uint32_t bytes, int, int) {
-                             bulk_g2s(stage + off, src, bytes, &full[st]);
-                           });
+  if (warp == NCW + 1) {
+    // ------------------------------------------------- bulk-copy issue warp
+    // Lane l works out the record and the copies of tile j0 + l for 32 tiles
+    // at once (from the shared-memory copy of the launch arguments: indexing
+    // kernel parameters dynamically would go through the constant cache);
+    // lane j % 32 then issues tile j, so a tile costs its copy instructions
+    // only.  Copy slots: 0-2 K (codes, scales, zeros or the ring's one or two
+    // pieces), 3-5 V likewise.
+    const DecodeArgs& sa = *args_s;
+    TcRec rec;
+    int pair = 0;
+    uint32_t bytes = 0;
+    const void* src[6];
+    uint32_t dst[6], nb[6];
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % NS;
+      if ((j & 31) == 0) {
+        const int jl = j + lane;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+          src[k] = nullptr;
+          dst[k] = nb[k] = 0u;
+        }
+        if (jl < ntiles) {
+          const int g = g_begin + jl;
+          pair = g / sa.n_tiles;
+          const TileInfo ti = tile_info(sa, g - pair * sa.n_tiles);
+          rec.n = ti.n;
+          rec.kq = ti.kseg >= 0;
+          rec.vq = ti.vseg >= 0;
+          rec.kr0 = ti.ku0 & (sa.G - 1);
+          rec.ng = ti.ng;
+          rec.k_off = ti.k_off;
+          rec.ks_off = ti.ks_off;
+          rec.kz_off = ti.kz_off;
+          rec.v_off = ti.v_off;
+          rec.vs_off = ti.vs_off;
+          rec.vz_off = ti.vz_off;
+          bytes = ti.bytes + D * 2;
+          bool k2 = false, v2 = false;
+          for_each_tile_copy(sa, (size_t)pair, ti, [&](const void* s_, uint32_t off, uint32_t n_, int buf, int) {
+            const int slot = buf < 6 ? buf : (buf == 6 ? (k2 ? 1 : 0) : (v2 ? 4 : 3));
+            if (buf == 6) k2 = true;
+            if (buf == 7) v2 = true;
+            src[slot] = s_;
+            dst[slot] = off;
+            nb[slot] = n_;
+          });
+        }
       }
-      return true;
-    };
-    // lane = (tig, kt): the 4 channels of the K operand entry (tig, kt, b0/b1)
+      if (j >= NS && __any_sync(kFull, !wait_or_abort(&empty[st], (uint32_t)(((j / NS) & 1) ^ 1), flags)))
+        break;
+      if (lane == (j & 31)) {
+        recs[st] = rec;
+        uint8_t* stage = smem + TcSmem::stages + st * kTcStageBytes;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&full[st], bytes);
+#pragma unroll
+        for (int k = 0; k < 6; ++k)
+          if (nb[k]) bulk_g2s(stage + dst[k], src[k], nb[k], &full[st]);
+        bulk_g2s(smem + TcSmem::q + st * D * 2, sa.q + (size_t)pair * D, D * 2, &full[st]);
+      }
+      __syncwarp();
+    }
+    return;
+  }
+
+  if (warp == NCW) {
+    // ------------------------------------------------ K operand table warp
+    // lane = (tig, kt): the channels of K operand entries (tig, kt, e = 0/1)
     const int ptig = lane >> 3, pkt = lane & 7;
-    int ch[4], pw[4];
+    int ch[4];
+    float pscale[4];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       int clo, chi, p;
       k_half2_channels<B>(ptig, 2 * pkt + e, &clo, &chi, &p);
       ch[2 * e] = clo;
       ch[2 * e + 1] = chi;
-      pw[2 * e] = pw[2 * e + 1] = p;
+      pscale[2 * e] = pscale[2 * e + 1] = __uint_as_float((uint32_t)(127 - p) << 23);  // 2^-p
     }
-    float qv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      qv[e] = __half2float(qnat[ch[e]]) * __uint_as_float((uint32_t)(127 - pw[e]) << 23);
-    const float qz0 = __half2float(qnat[lane]), qz1 = __half2float(qnat[lane + 32]);
-    const float qz2 = __half2float(qnat[lane + 64]), qz3 = __half2float(qnat[lane + 96]);
-    bool ok = true;
-    for (int j = 0; j < kTcStages - 1 && j < ntiles && ok; ++j) ok = issue(j);
-    for (int it = 0; it < ntiles && ok; ++it) {
-      const int st = it % kTcStages;
-      const uint32_t ph = (uint32_t)((it / kTcStages) & 1);
-      const TileInfo ti = tile_info(a, t_begin + it);
-      if (ti.kseg >= 0) {
-        if (!wait_or_abort(&full[st], ph, flags)) break;
+    for (int it = 0; it < ntiles; ++it) {
+      const int st = it % NS;
+      const uint32_t ph = (uint32_t)((it / NS) & 1);
+      if (__any_sync(kFull, !wait_or_abort(&full[st], ph, flags))) break;
+      const TcRec& r = recs[st];
+      if (r.kq) {
         const uint8_t* stage = smem + TcSmem::stages + st * kTcStageBytes;
-        const __half* ks = reinterpret_cast<const __half*>(stage + ti.ks_off);
-        const __half* kz = reinterpret_cast<const __half*>(stage + ti.kz_off);
-        uint32_t* kt_tab = reinterpret_cast<uint32_t*>(smem + TcSmem::ktab + st * kTcKtabBytes);
+        const __half* qs = reinterpret_cast<const __half*>(smem + TcSmem::q + st * D * 2);
+        const __half* ks = reinterpret_cast<const __half*>(stage + r.ks_off);
+        const __half* kz = reinterpret_cast<const __half*>(stage + r.kz_off);
+        uint32_t* tab = reinterpret_cast<uint32_t*>(smem + TcSmem::ktab + st * kTcKtabBytes);
         float* kb = reinterpret_cast<float*>(smem + TcSmem::kbias) + st * kTcMaxGroups;
-        for (int gl = 0; gl < ti.ng; ++gl) {
+        float qv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qv[e] = __half2float(qs[ch[e]]) * pscale[e] * a.scale_log2;
+        float qz[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qz[i] = __half2float(qs[lane + 32 * i]);
+        // all kTcMaxGroups groups, without branches: groups past ng read other
+        // bytes of the stage (in bounds) and fill table slots nobody reads
+        float zs[kTcMaxGroups];  // this lane's part of q . z_g (channels lane + 32 i)
+#pragma unroll
+        for (int gl = 0; gl < kTcMaxGroups; ++gl) {
           const __half* sg = ks + gl * D;
-          float v[4], hi[4], lo[4];
+          float hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            v[e] = qv[e] * __half2float(sg[ch[e]]);
-            hi[e] = __half2float(__float2half_rn(v[e]));
-            lo[e] = v[e] - hi[e];
+            const float v = qv[e] * __half2float(sg[ch[e]]);
+            hi[e] = __half2float(__float2half_rn(v));
+            lo[e] = v - hi[e];
           }
-          // entry (gl, part, tig, kt) holds b0 (h = 2kt) and b1 (h = 2kt+1)
-          uint2* dh = reinterpret_cast<uint2*>(kt_tab + ((gl * 2 + 0) * 4 + ptig) * 16) + pkt;
-          uint2* dl = reinterpret_cast<uint2*>(kt_tab + ((gl * 2 + 1) * 4 + ptig) * 16) + pkt;
-          *dh = make_uint2(pack_half2(hi[0], hi[1]), pack_half2(hi[2], hi[3]));
-          *dl = make_uint2(pack_half2(lo[0], lo[1]), pack_half2(lo[2], lo[3]));
+          // entry (gl, k = kt / 2, part, tig): 4 words, kt even (b0, b1) then kt odd
+          uint32_t* eh = tab + ((gl * 4 + (pkt >> 1)) * 8 + 0 * 4 + ptig) * 4 + (pkt & 1) * 2;
+          uint32_t* el = tab + ((gl * 4 + (pkt >> 1)) * 8 + 1 * 4 + ptig) * 4 + (pkt & 1) * 2;
+          *reinterpret_cast<uint2*>(eh) = make_uint2(pack_half2(hi[0], hi[1]), pack_half2(hi[2], hi[3]));
+          *reinterpret_cast<uint2*>(el) = make_uint2(pack_half2(lo[0], lo[1]), pack_half2(lo[2], lo[3]));
           const __half* zg = kz + gl * D;
-          float zsum = qz0 * __half2float(zg[lane]) + qz1 * __half2float(zg[lane + 32]) +
-                       qz2 * __half2float(zg[lane + 64]) + qz3 * __half2float(zg[lane + 96]);
+          zs[gl] = 0.f;
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) zsum += __shfl_xor_sync(0xffffffffu, zsum, off);
-          if (lane == 0) kb[gl] = zsum;
+          for (int i = 0; i < 4; ++i) zs[gl] = fmaf(qz[i], __half2float(zg[lane + 32 * i]), zs[gl]);
         }
-        __syncwarp();
+        // sum the 8 per-lane vectors over the warp: each exchange halves the
+        // groups a lane keeps (xor 16: 4 left, xor 8: 2, xor 4: 1), then the 4
+        // lanes of one group add up; lane 4 g holds group g.
+        static_assert(kTcMaxGroups == 8, "bias reduction is written for 8 groups");
+        float y4[4], y2[2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const bool up = lane & 16;
+          y4[k] = (up ? zs[k + 4] : zs[k]) + __shfl_xor_sync(kFull, up ? zs[k] : zs[k + 4], 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const bool up = lane & 8;
+          y2[k] = (up ? y4[k + 2] : y4[k]) + __shfl_xor_sync(kFull, up ? y4[k] : y4[k + 2], 8);
+        }
+        const bool up = lane & 4;
+        float y = (up ? y2[1] : y2[0]) + __shfl_xor_sync(kFull, up ? y2[0] : y2[1], 4);
+        y += __shfl_xor_sync(kFull, y, 2);
+        y += __shfl_xor_sync(kFull, y, 1);
+        if ((lane & 3) == 0) kb[lane >> 2] = y * a.scale_log2;
       }
+      __syncwarp();
       if (lane == 0) mbar_arrive(&ready[st]);
-      if (it + kTcStages - 1 < ntiles) ok = issue(it + kTcStages - 1);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
   WarpState S;
-  S.m = -INFINITY;
-  S.l = S.zs = 0.f;
+  auto reset = [&]() {
+    S.m = -INFINITY;
+    S.l = 0.f;
+    S.vring = false;
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) S.acc[i][e] = S.accr[i][e] = 0.f;
-
+      for (int e = 0; e < 4; ++e) S.acc[i][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) S.accz[e] = 0.f;
+  };
+  reset();
+  int cur_pair = g_begin / a.n_tiles;
+  int t_in_pair = g_begin - cur_pair * a.n_tiles;
+  int jstart = warp;  // this warp's first sub-tile of the next tile (round-robin)
+  bool aborted = false;
   for (int it = 0; it < ntiles; ++it) {
-    const int st = it % kTcStages;
-    const uint32_t ph = (uint32_t)((it / kTcStages) & 1);
-    if (!wait_or_abort(&ready[st], ph, flags)) break;
-    if (!wait_or_abort(&full[st], ph, flags)) break;
-    const uint8_t* stage = smem + TcSmem::stages + st * kTcStageBytes;
-    const int t = t_begin + it;
-    const TileInfo ti = tile_info(a, t);
-    int ri = 0;
-    while (ri + 1 < a.n_runs && a.runs[ri + 1].tile0 <= t) ++ri;
-    const int wt = a.runs[ri].wt;  // tokens of a warp slice (multiple of 16)
-    const uint32_t* kt_tab = reinterpret_cast<const uint32_t*>(smem + TcSmem::ktab + st * kTcKtabBytes);
-    const float* kb = reinterpret_cast<const float*>(smem + TcSmem::kbias) + st * kTcMaxGroups;
-    for (int s0 = warp * wt; s0 < warp * wt + wt && s0 < ti.n; s0 += 16)
-      sub_tile<B>(a, ti, stage, kt_tab, kb, qnat, s0, lane, S);
+    const int st = it % NS;
+    const uint32_t ph = (uint32_t)((it / NS) & 1);
+    if (t_in_pair == a.n_tiles) {  // first tile of the next pair
+      finish_piece<B>(a, smem, cur_pair, T, warp, lane, S, flags);
+      reset();
+      ++cur_pair;
+      t_in_pair = 0;
+    }
+    ++t_in_pair;
+    if (!aborted && __any_sync(kFull, !wait_or_abort(&ready[st], ph, flags))) aborted = true;
+    if (!aborted) {
+      const int4 r0 = *reinterpret_cast<const int4*>(&recs[st].n);
+      const int4 r1 = *reinterpret_cast<const int4*>(&recs[st].k_off);
+      TcRec r;
+      r.n = r0.x;
+      r.kq = r0.y;
+      r.vq = r0.z;
+      r.kr0 = r0.w;
+      r.k_off = (uint32_t)r1.x;
+      r.v_off = (uint32_t)r1.y;
+      r.vs_off = (uint32_t)r1.z;
+      r.vz_off = (uint32_t)r1.w;
+      if (r.kq) {
+        jstart = r.vq ? run_tile<B, true, true>(a, st, r, jstart, lane, S) : run_tile<B, true, false>(a, st, r, jstart, lane, S);
+      } else {
+        jstart = r.vq ? run_tile<B, false, true>(a, st, r, jstart, lane, S) : run_tile<B, false, false>(a, st, r, jstart, lane, S);
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
   }
-
-  // ---- this warp's output row, o[c] for all channels, into shared memory
-  const int gid = lane >> 2, tig = lane & 3;
-  float* mg = reinterpret_cast<float*>(smem + TcSmem::merge) + warp * (D + 2);
-  // column sums over the 4 threads (tig) of each gid
-  float zs = S.zs, l = S.l;
-  zs += __shfl_xor_sync(0xffffffffu, zs, 1);
-  zs += __shfl_xor_sync(0xffffffffu, zs, 2);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-  // zs of column n now sits in the threads with gid == n
-  const int ngv = D >> a.log2G;
-  // ring V (natural rows): thread (gid, tig == 0) has rows gid, gid + 8 of col 0
-  // packed V: rows gid, gid + 8 of m-tile mt are channels v_rows(gid, mt);
-  // their column is the channels' group g; the owner thread has tig == g / 2
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    int c0, c8, p;
-    v_rows<B>(gid, mt, &c0, &c8, &p);
-    const int g = c0 >> a.log2G;  // c0 and c8 share the group (16-channel block)
-    const float zsg = __shfl_sync(0xffffffffu, zs, 4 * g);
-    const float unscale = __uint_as_float((uint32_t)(127 + 24 - p) << 23);  // 2^(24 - p)
-    if (tig == (g >> 1)) {
-      const float d0 = (g & 1) ? S.acc[mt][1] : S.acc[mt][0];
-      const float d8 = (g & 1) ? S.acc[mt][3] : S.acc[mt][2];
-      mg[c0] = d0 * unscale + zsg;
-      mg[c8] = d8 * unscale + zsg;
-    }
-  }
-  __syncwarp();
-  if (tig == 0) {
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      mg[mt * 16 + gid] += S.accr[mt][0];
-      mg[mt * 16 + gid + 8] += S.accr[mt][2];
-    }
-  }
-  (void)ngv;
-  if (lane == 0) {
-    mg[D] = S.m;
-    mg[D + 1] = l;
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
-  if (flags[0]) {
-    if (tid == 0) atomicExch(a.err, 1);
-    return;
-  }
-  // ---- merge the consumer warps
-  const float* m0 = reinterpret_cast<const float*>(smem + TcSmem::merge);
-  float M = -INFINITY;
-  for (int w = 0; w < NCW; ++w) M = fmaxf(M, m0[w * (D + 2) + D]);
-  const size_t out_base = ((size_t)b * a.h_kv + hk) * D;
-  float* rec = a.part + ((size_t)pair * a.n_splits + split) * (D + 2);
-  for (int c = tid; c < D; c += NCW * 32) {
-    float L = 0.f, O = 0.f;
-    for (int w = 0; w < NCW; ++w) {
-      const float* mw = m0 + w * (D + 2);
-      const float sw = (mw[D] == -INFINITY) ? 0.f : exp2f(mw[D] - M);
-      L += mw[D + 1] * sw;
-      O += mw[c] * sw;
-    }
-    if (a.n_splits == 1) {
-      a.out[out_base + c] = __float2half_rn(O / L);
-    } else {
-      rec[c] = O;
-      if (c == 0) {
-        rec[D] = M;
-        rec[D + 1] = L;
-      }
-    }
-  }
-  if (a.n_splits == 1) return;
-  __threadfence();
-  asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
-  if (tid == 0) flags[1] = (atomicAdd(&a.counters[pair], 1) == a.n_splits - 1);
-  asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
-  if (!flags[1]) return;
-  __threadfence();
-  const float* recs = a.part + (size_t)pair * a.n_splits * (D + 2);
-  for (int c = tid; c < D; c += NCW * 32) {
-    float MM = -INFINITY;
-    for (int s = 0; s < a.n_splits; ++s) MM = fmaxf(MM, __ldcg(recs + (size_t)s * (D + 2) + D));
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < a.n_splits; ++s) {
-      const float* rr = recs + (size_t)s * (D + 2);
-      const float w = exp2f(__ldcg(rr + D) - MM);
-      L += __ldcg(rr + D + 1) * w;
-      O += __ldcg(rr + c) * w;
-    }
-    a.out[out_base + c] = __float2half_rn(O / L);
-  }
-  if (tid == 0) a.counters[pair] = 0;
+  if (ntiles > 0) finish_piece<B>(a, smem, cur_pair, T, warp, lane, S, flags);
 }
 
 template <int B>
-cudaError_t launch_tc_b(const DecodeArgs& a, int n_pairs, cudaStream_t s) {
+cudaError_t launch_tc_b(const DecodeArgs& a, cudaStream_t s) {
   const int smem = TcSmem::total;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<B>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<B><<<n_pairs * a.n_splits, NTH, smem, s>>>(a);
+  decode_tc_kernel<B><<<a.n_cta, NTH, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode_tc(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s) {
-  if (bits == 2) return launch_tc_b<2>(a, n_pairs, s);
-  if (bits == 4) return launch_tc_b<4>(a, n_pairs, s);
-  return launch_tc_b<8>(a, n_pairs, s);
+int decode_tc_ctas_per_sm() { return 2; }
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, cudaStream_t s) {
+  if (bits == 2) return launch_tc_b<2>(a, s);
+  if (bits == 4) return launch_tc_b<4>(a, s);
+  return launch_tc_b<8>(a, s);
 }
 
 }  // namespace kvq

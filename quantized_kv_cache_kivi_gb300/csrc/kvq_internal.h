@@ -23,9 +23,10 @@ constexpr int kMhaConsumerWarps = 7;
 constexpr int kMhaStageBytes = 25600;   // staged tile data per pipeline stage
 constexpr int kMhaMaxGroups = 16;       // K scale groups one tile may touch
 constexpr int kMhaQtabBytes = kMhaMaxGroups * 4 * 36 * 4;  // scaled-query rows per stage
-// tensor-core one-query-head kernel (d_h = 128): 4 consumer warps + 1
-// producer, 4 stages, two CTAs per SM
-constexpr int kTcConsumerWarps = 4;
+// tensor-core one-query-head kernel (d_h = 128): 6 consumer warps, a K table
+// warp and a bulk-copy warp, 4 stages, two CTAs per SM (16 warps: 128
+// registers a thread)
+constexpr int kTcConsumerWarps = 6;
 constexpr int kTcStages = 4;
 constexpr int kTcStageBytes = 19456;
 constexpr int kTcMaxGroups = 8;                      // K groups one tile may touch
@@ -68,7 +69,8 @@ struct DecodeArgs {
   int n_runs;
   Run runs[kMaxRuns];
   int n_tiles;   // tiles per (batch, kv head)
-  int n_splits;  // CTAs per (batch, kv head)
+  int n_splits;  // CTAs per (batch, kv head); tensor-core kernel: records per pair
+  int n_cta;     // tensor-core kernel: CTAs of the persistent grid
   int split_tile[KVQ_MAX_SPLITS + 1];
   const __half* q;
   __half* out;
@@ -240,7 +242,8 @@ cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int n_pairs, cudaStream_t s);
 size_t decode_smem_bytes(int gq, int d);
 cudaError_t launch_decode_mha(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s);
-cudaError_t launch_decode_tc(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, cudaStream_t s);
+int decode_tc_ctas_per_sm();
 size_t decode_mha_smem_bytes();
 
 struct WindowArgs {
