@@ -124,6 +124,8 @@ __host__ __device__ constexpr void v_rows(int gid, int mt, int* c_row0, int* c_r
   *p = Fields<B>::pos(j);
 }
 
+// Volatile on purpose: the source order of the MMAs is their issue order,
+// which is arranged so that two MMAs on one accumulator are several apart.
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -137,7 +139,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // 2 tig, 2 tig + 1 and receives row gid of the transpose.
 __device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
   uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
 
@@ -159,29 +161,37 @@ __device__ __forceinline__ uint32_t halves(uint16_t lo, uint16_t hi) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// try_wait that may sleep up to `ns` nanoseconds for the phase to complete
-// (the thread resumes as soon as it does).
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+__device__ __forceinline__ bool try_wait_at(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait: about 2^31 SM clocks, then the abort flag is raised.
+// Bounded wait: about 2^31 SM clocks, then the abort flag is raised.  The
+// warps that run ahead (bulk copies, K table) back off with a growing sleep
+// between polls so their polling does not take issue slots from the
+// consumer warps; the consumers poll without sleeping.
+template <bool BACKOFF>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+  const uint32_t addr = smem_u32(bar);
+  if (try_wait_at(addr, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait_sleep(bar, parity, 1000000u)) {
+  uint32_t ns = 64;
+  while (!try_wait_at(addr, parity)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > (1ll << 31)) {
       *abort_flag = 1;
       return false;
+    }
+    if (BACKOFF) {
+      __nanosleep(ns);
+      ns = ns < 512 ? 2 * ns : ns;
     }
   }
   return true;
@@ -275,6 +285,43 @@ __device__ __forceinline__ void k_scores_packed(const uint8_t* kc, int s0, int r
   x1 = fmaf((sc[2] + sd[2]) + (sc[3] + sd[3]), 16777216.0f, bias);  // row gid + 8
 }
 
+// Both halves of a 32-token unit at 2 bits, their MMA chains interleaved
+// (four accumulators, an MMA's successor on the same accumulator comes four
+// MMAs later).
+__device__ __forceinline__ void k_scores_packed2_b2(const uint8_t* kc, int s0, int r0, int r1,
+                                                    const uint32_t (&bq)[16], float bias, float (&x)[2][2]) {
+  constexpr int RB = D * 2 / 8;
+  uint32_t w[2][2][2];  // [half][row][word]
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint2 u0 = *reinterpret_cast<const uint2*>(kc + (s0 + 16 * h + r0) * RB);
+    const uint2 u1 = *reinterpret_cast<const uint2*>(kc + (s0 + 16 * h + r1) * RB);
+    w[h][0][0] = u0.x; w[h][0][1] = u0.y;
+    w[h][1][0] = u1.x; w[h][1][1] = u1.y;
+  }
+  float acc[2][2][4] = {};  // [half][k-tile parity][fragment]
+#pragma unroll
+  for (int kt = 0; kt < 8; ++kt) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t av[4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int hh = 2 * kt + e;
+        const int wi = hh / 8, j = hh % 8;
+        av[2 * e + 0] = Fields<2>::get(w[h][0][wi], w[h][0][wi] >> 6, j);
+        av[2 * e + 1] = Fields<2>::get(w[h][1][wi], w[h][1][wi] >> 6, j);
+      }
+      mma16816(acc[h][kt & 1], av[0], av[1], av[2], av[3], bq[2 * kt], bq[2 * kt + 1]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    x[h][0] = fmaf((acc[h][0][0] + acc[h][1][0]) + (acc[h][0][1] + acc[h][1][1]), 16777216.0f, bias);
+    x[h][1] = fmaf((acc[h][0][2] + acc[h][1][2]) + (acc[h][0][3] + acc[h][1][3]), 16777216.0f, bias);
+  }
+}
+
 // Same for fp16 ring K.  Thread tig reads its 32 channels as four 16-byte
 // chunks, chunk kc at position (kc + tig) & 3 of the block (spreads the
 // banks), and the query words in the same order: each chunk feeds 2 MMAs.
@@ -316,9 +363,13 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
     for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(&bq[4 * k]) = tb[k * 8];
     const float bias = reinterpret_cast<const float*>(sm + TcSmem::kbias)[st * kTcMaxGroups + gl];
     const uint8_t* kc = stage + r.k_off + tig * (B * 4);
-    k_scores_packed<B>(kc, s0, r0, r1, bq, bias, x[0][0], x[0][1]);
-    if (FULL || nv > 16) k_scores_packed<B>(kc, s0 + 16, r0, r1, bq, bias, x[1][0], x[1][1]);
-    else x[1][0] = x[1][1] = -INFINITY;
+    if constexpr (B == 2) {
+      k_scores_packed2_b2(kc, s0, r0, r1, bq, bias, x);  // rows past the tile read stale bytes: masked below
+    } else {
+      k_scores_packed<B>(kc, s0, r0, r1, bq, bias, x[0][0], x[0][1]);
+      if (FULL || nv > 16) k_scores_packed<B>(kc, s0 + 16, r0, r1, bq, bias, x[1][0], x[1][1]);
+      else x[1][0] = x[1][1] = -INFINITY;
+    }
   } else {
     const uint8_t* qt = sm + TcSmem::q + st * D * 2 + tig * 64;
     const uint8_t* kr = stage + r.k_off + tig * 64;
@@ -406,13 +457,13 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
         hi2[h] = __byte_perm(wc, wd, 0x7632);
       }
 #pragma unroll
-      for (int j = 0; j < PH; ++j) {
-        const int mt = w * PH + j;
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int j = 0; j < PH; ++j) {
+          const int mt = w * PH + j;
           mma16816(S.acc[mt], Fields<B>::get(lo1[h], lo1[h] >> 6, j), Fields<B>::get(hi1[h], hi1[h] >> 6, j),
                    Fields<B>::get(lo2[h], lo2[h] >> 6, j), Fields<B>::get(hi2[h], hi2[h] >> 6, j), bv[h][0], bv[h][1]);
-      }
+        }
     }
     constexpr uint32_t ONES = 0x3C003C00u;  // (1.0, 1.0)
     mma16816(S.accz, ONES, ONES, ONES, ONES, bv[0][0], bv[0][1]);
@@ -638,7 +689,7 @@ __global__ void __launch_bounds__(NTH, 2) decode_tc_kernel(const DecodeArgs a) {
           });
         }
       }
-      if (j >= NS && __any_sync(kFull, !wait_or_abort(&empty[st], (uint32_t)(((j / NS) & 1) ^ 1), flags)))
+      if (j >= NS && __any_sync(kFull, !wait_or_abort<true>(&empty[st], (uint32_t)(((j / NS) & 1) ^ 1), flags)))
         break;
       if (lane == (j & 31)) {
         recs[st] = rec;
@@ -672,7 +723,7 @@ __global__ void __launch_bounds__(NTH, 2) decode_tc_kernel(const DecodeArgs a) {
     for (int it = 0; it < ntiles; ++it) {
       const int st = it % NS;
       const uint32_t ph = (uint32_t)((it / NS) & 1);
-      if (__any_sync(kFull, !wait_or_abort(&full[st], ph, flags))) break;
+      if (__any_sync(kFull, !wait_or_abort<true>(&full[st], ph, flags))) break;
       const TcRec& r = recs[st];
       if (r.kq) {
         const uint8_t* stage = smem + TcSmem::stages + st * kTcStageBytes;
@@ -765,7 +816,7 @@ __global__ void __launch_bounds__(NTH, 2) decode_tc_kernel(const DecodeArgs a) {
       t_in_pair = 0;
     }
     ++t_in_pair;
-    if (!aborted && __any_sync(kFull, !wait_or_abort(&ready[st], ph, flags))) aborted = true;
+    if (!aborted && __any_sync(kFull, !wait_or_abort<false>(&ready[st], ph, flags))) aborted = true;
     if (!aborted) {
       const int4 r0 = *reinterpret_cast<const int4*>(&recs[st].n);
       const int4 r1 = *reinterpret_cast<const int4*>(&recs[st].k_off);
