@@ -43,15 +43,17 @@ __device__ __forceinline__ uint32_t qcode(float x, const QParams& p, int bits) {
 // (x - z) * (1/s).  Both that product and the IEEE quotient lie within a few
 // fp32 ulps of the exact ratio (ulp <= 2^-16 for ratios below 256), so they
 // round to the same integer unless the product is within 1e-4 of a
-// half-integer; only then is the IEEE division done.  `rcp` = 1/s rounded.
-__device__ __forceinline__ uint32_t qcode_fast(float x, const QParams& p, float rcp, int bits) {
-  if (p.s == 0.0f) return 0u;
-  const float qmax = (float)((1 << bits) - 1);
-  const float d = __fsub_rn(x, p.z);
-  float t = __fmul_rn(d, rcp);
-  if (fabsf(t - floorf(t) - 0.5f) < 1e-4f) t = __fdiv_rn(d, p.s);
-  const float r = fminf(fmaxf(rintf(t), 0.0f), qmax);
-  return (uint32_t)r;
+// half-integer (|t - rint(t)| > 0.4999); only then is the IEEE division
+// done.  `rcp` = 1/s rounded, or 0 when s == 0 (then t = 0 and the code is
+// 0, as in qcode).  x >= z always (z is the group minimum), so the rounded
+// quotient is >= 0; it is clamped to 2^BITS - 1 from above.
+template <int BITS>
+__device__ __forceinline__ uint32_t qcode_fast(float x, float z, float s, float rcp) {
+  const float d = __fsub_rn(x, z);
+  const float t = __fmul_rn(d, rcp);
+  float r = rintf(t);
+  if (fabsf(t - r) > 0.4999f) r = rintf(__fdiv_rn(d, s));
+  return min(__float2uint_rn(r), (1u << BITS) - 1u);
 }
 
 // ---------------------------------------------------------------------------

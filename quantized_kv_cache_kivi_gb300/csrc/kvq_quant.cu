@@ -29,51 +29,144 @@ __device__ __forceinline__ const __half* src_row(const __half* ring, const __hal
   return p < s.n_old ? ring + (size_t)((s.start + p) % R) * D : in + (size_t)(p - s.n_old) * D;
 }
 
+// Shared memory of the quantize kernels: the staged K group (G rows of D
+// halves), the warps' partial channel minima/maxima and the channel
+// parameters (s, 1/s, z) of the group.
+struct QuantSmem {
+  __half* xs;    // [G][D]
+  float* red;    // [2][kQuantThreads / 32][D]
+  float* par;    // [3][D]
+};
+
+__host__ __device__ inline size_t quant_smem_bytes(int G, int d) {
+  return (size_t)G * d * 2 + (size_t)(2 * (kQuantThreads / 32) + 3) * d * 4;
+}
+
+__device__ __forceinline__ QuantSmem quant_smem_view(uint8_t* base, int G, int D) {
+  QuantSmem q;
+  q.xs = reinterpret_cast<__half*>(base);
+  q.red = reinterpret_cast<float*>(base + (size_t)G * D * 2);
+  q.par = q.red + 2 * (kQuantThreads / 32) * D;
+  return q;
+}
+
 // Quantize one K group (G pushed tokens starting at push index p0, all D
 // channels, one group per channel) into packed rows [row0, row0 + G) and
-// scale/zero row `grow` of the destination segment.  Whole block.  The G
-// source rows are first staged in shared memory with 16-byte loads (all in
-// flight at once), then each thread reduces and quantizes one channel.
-template <int D>
-__device__ void quant_k_group(const SegDev& dst, int bits, int G, int R, size_t pair,
+// scale/zero row `grow` of the destination segment.  Whole block of
+// kQuantThreads threads.  The G source rows are staged in shared memory with
+// 16-byte loads; thread t then owns the 8-channel chunk t % (D/8) of the
+// tokens t / (D/8) + k TL (TL = threads / (D/8)): exact half2 min/max over
+// its tokens, a warp and a block reduction give each channel's (min, max),
+// one thread per channel turns them into (s, z), and every thread writes
+// the codes of its chunk of its tokens (8 codes = `bits` bytes, one store).
+template <int D, int BITS>
+__device__ void quant_k_group(const SegDev& dst, int G, int R, size_t pair,
                               const __half* ring, const __half* in, const RowSrc& src, int p0,
-                              int row0, int grow, __half* xs, uint8_t* codes_s) {
-  const int tid = threadIdx.x;
-  constexpr int kVec = D * 2 / 16;  // 16-byte vectors per row
-  for (int idx = tid; idx < G * kVec; idx += blockDim.x) {
-    const int i = idx / kVec, v = idx % kVec;
-    reinterpret_cast<int4*>(xs + (size_t)i * D)[v] =
-        reinterpret_cast<const int4*>(src_row<D>(ring, in, R, src, p0 + i))[v];
+                              int row0, int grow, const QuantSmem& q) {
+  constexpr int CH = D / 8;                 // 8-channel chunks of a row
+  constexpr int TL = kQuantThreads / CH;    // token lanes
+  constexpr int NWARP = kQuantThreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cch = tid % CH, tl = tid / CH;
+  // up to 4 loads per thread in flight before their stores
+  for (int b0 = 0; b0 < G * CH; b0 += 4 * kQuantThreads) {
+    int4 v4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = b0 + k * kQuantThreads + tid;
+      if (idx < G * CH) v4[k] = reinterpret_cast<const int4*>(src_row<D>(ring, in, R, src, p0 + idx / CH))[idx % CH];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = b0 + k * kQuantThreads + tid;
+      if (idx < G * CH) reinterpret_cast<int4*>(q.xs + (size_t)(idx / CH) * D)[idx % CH] = v4[k];
+    }
   }
   __syncthreads();
-  for (int c = tid; c < D; c += blockDim.x) {
-    float mn = __half2float(xs[c]);
-    float mx = mn;
-    for (int i = 1; i < G; ++i) {
-      const float v = __half2float(xs[(size_t)i * D + c]);
-      mn = fminf(mn, v);
-      mx = fmaxf(mx, v);
+  // per-thread min/max of 8 channels over tokens tl, tl + TL, ...
+  __half2 mn[4], mx[4];
+  {
+    const uint4 u = reinterpret_cast<const uint4*>(q.xs + (size_t)tl * D)[cch];
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mn[e] = mx[e] = h[e];
+  }
+  for (int i = tl + TL; i < G; i += TL) {
+    const uint4 u = reinterpret_cast<const uint4*>(q.xs + (size_t)i * D)[cch];
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mn[e] = __hmin2(mn[e], h[e]);
+      mx[e] = __hmax2(mx[e], h[e]);
     }
-    const QParams qp = qparams(mn, mx, bits);
-    const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
-    const size_t gidx = (pair * (size_t)(dst.cap / G) + grow) * D + c;
+  }
+  // lanes of one warp that share the chunk: lane ^ CH, lane ^ 2 CH, ...
+#pragma unroll
+  for (int off = CH; off < 32; off <<= 1)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mn[e] = __hmin2(mn[e], __shfl_xor_sync(0xffffffffu, mn[e], off));
+      mx[e] = __hmax2(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], off));
+    }
+  if (lane < CH) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = __half22float2(mn[e]), b = __half22float2(mx[e]);
+      q.red[(0 * NWARP + warp) * D + cch * 8 + 2 * e] = a.x;
+      q.red[(0 * NWARP + warp) * D + cch * 8 + 2 * e + 1] = a.y;
+      q.red[(1 * NWARP + warp) * D + cch * 8 + 2 * e] = b.x;
+      q.red[(1 * NWARP + warp) * D + cch * 8 + 2 * e + 1] = b.y;
+    }
+  }
+  __syncthreads();
+  if (tid < D) {
+    float lo = q.red[tid], hi = q.red[NWARP * D + tid];
+    for (int w = 1; w < NWARP; ++w) {
+      lo = fminf(lo, q.red[w * D + tid]);
+      hi = fmaxf(hi, q.red[(NWARP + w) * D + tid]);
+    }
+    const QParams qp = qparams(lo, hi, BITS);
+    const size_t gidx = (pair * (size_t)(dst.cap / G) + grow) * D + tid;
     const_cast<__half*>(dst.ks)[gidx] = qp.sh;
     const_cast<__half*>(dst.kz)[gidx] = qp.zh;
-    for (int i = 0; i < G; ++i)
-      codes_s[(size_t)i * D + c] = (uint8_t)qcode_fast(__half2float(xs[(size_t)i * D + c]), qp, rcp, bits);
+    q.par[tid] = qp.s;
+    q.par[D + tid] = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
+    q.par[2 * D + tid] = qp.z;
   }
   __syncthreads();
-  const int per_word = 32 / bits;
-  const int words = D * bits / 32;
-  const int rb = D * bits / 8;
+  float cs[8], cr[8], cz[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    cs[e] = q.par[cch * 8 + e];
+    cr[e] = q.par[D + cch * 8 + e];
+    cz[e] = q.par[2 * D + cch * 8 + e];
+  }
+  constexpr int rb = D * BITS / 8;
   uint8_t* base = const_cast<uint8_t*>(dst.kc) + (pair * (size_t)dst.cap + row0) * rb;
-  for (int idx = tid; idx < G * words; idx += blockDim.x) {
-    const int i = idx / words, w = idx % words;
-    uint32_t word = 0;
-    for (int j = 0; j < per_word; ++j) word |= (uint32_t)codes_s[(size_t)i * D + w * per_word + j] << (j * bits);
-    reinterpret_cast<uint32_t*>(base + (size_t)i * rb)[w] = word;
+  for (int i = tl; i < G; i += TL) {
+    const uint4 u = reinterpret_cast<const uint4*>(q.xs + (size_t)i * D)[cch];
+    const __half* h = reinterpret_cast<const __half*>(&u);
+    uint32_t lo = 0, hi = 0;  // codes 0-3 and 4-7 (8 codes = BITS bytes)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      lo |= qcode_fast<BITS>(__half2float(h[e]), cz[e], cs[e], cr[e]) << (e * BITS);
+      hi |= qcode_fast<BITS>(__half2float(h[e + 4]), cz[e + 4], cs[e + 4], cr[e + 4]) << (e * BITS);
+    }
+    uint8_t* out = base + (size_t)i * rb + cch * BITS;
+    if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(out) = (uint16_t)(lo | (hi << 8));
+    else if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(out) = lo | (hi << 16);
+    else *reinterpret_cast<uint2*>(out) = make_uint2(lo, hi);
   }
   __syncthreads();
+}
+
+template <int D>
+__device__ __forceinline__ void quant_k_group_any(const SegDev& dst, int bits, int G, int R, size_t pair,
+                                                  const __half* ring, const __half* in, const RowSrc& src,
+                                                  int p0, int row0, int grow, const QuantSmem& q) {
+  if (bits == 2) quant_k_group<D, 2>(dst, G, R, pair, ring, in, src, p0, row0, grow, q);
+  else if (bits == 4) quant_k_group<D, 4>(dst, G, R, pair, ring, in, src, p0, row0, grow, q);
+  else quant_k_group<D, 8>(dst, G, R, pair, ring, in, src, p0, row0, grow, q);
 }
 
 // Quantize one V token (all D channels, one group per G channels) into packed
@@ -102,7 +195,12 @@ __device__ void quant_v_token(const SegDev& dst, int bits, int G, size_t pair, c
   const QParams qp = qparams(mn, mx, bits);
   const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
   uint32_t packed = 0;
-  for (int j = 0; j < 4; ++j) packed |= qcode_fast(v[j], qp, rcp, bits) << (j * bits);
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t c = bits == 2 ? qcode_fast<2>(v[j], qp.z, qp.s, rcp)
+                       : bits == 4 ? qcode_fast<4>(v[j], qp.z, qp.s, rcp)
+                                   : qcode_fast<8>(v[j], qp.z, qp.s, rcp);
+    packed |= c << (j * bits);
+  }
   const int rb = D * bits / 8;
   uint8_t* rowp = const_cast<uint8_t*>(dst.vc) + (pair * (size_t)dst.cap + row) * rb;
   if (bits == 2) rowp[lane] = (uint8_t)packed;
@@ -130,8 +228,7 @@ __device__ void copy_to_ring(__half* ring, int R, int slot0, const __half* src, 
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
-  __half* xs = reinterpret_cast<__half*>(qsm);
-  uint8_t* codes_s = qsm + (size_t)a.G * D * 2;
+  const QuantSmem qs = quant_smem_view(qsm, a.G, D);
   const size_t pair = blockIdx.x;
   const int chunk = blockIdx.y;
   const __half* in_k = a.k_new + pair * (size_t)a.T * D;
@@ -141,20 +238,39 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 
   if (chunk == 0) {
+    // A few new tokens (a decode step) are read into registers first, so
+    // their load latency overlaps the quantization below; they are written
+    // to the ring only after every read of old ring slots.
+    constexpr int kVec = D * 2 / 16;
+    const int nk_new = a.T - a.k_first_ring, nv_new = a.T - a.v_first_ring;
+    const bool few = nk_new * kVec <= (int)blockDim.x && nv_new * kVec <= (int)blockDim.x;
+    int4 pk = make_int4(0, 0, 0, 0), pv = make_int4(0, 0, 0, 0);
+    const int tid = threadIdx.x;
+    if (few) {
+      if (tid < nk_new * kVec) pk = reinterpret_cast<const int4*>(in_k + (size_t)a.k_first_ring * D)[tid];
+      if (tid < nv_new * kVec) pv = reinterpret_cast<const int4*>(in_v + (size_t)a.v_first_ring * D)[tid];
+    }
     // work that reads old ring slots, before any new token lands in the ring
     for (int gi = 0; gi < a.k_ring_groups; ++gi)
-      quant_k_group<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
-                       a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, xs, codes_s);
+      quant_k_group_any<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
+                       a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
     for (int p = warp; p < a.v_ring_tokens; p += nwarps)
       quant_v_token<D>(a.dst, a.bits, a.G, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
                        a.v_nv0 + p);
     __syncthreads();
-    if (a.k_first_ring < a.T)
-      copy_to_ring<D>(ring_k, a.R, a.k_slot0 + a.k_first_ring, in_k + (size_t)a.k_first_ring * D,
-                      a.T - a.k_first_ring);
-    if (a.v_first_ring < a.T)
-      copy_to_ring<D>(ring_v, a.R, a.v_slot0 + a.v_first_ring, in_v + (size_t)a.v_first_ring * D,
-                      a.T - a.v_first_ring);
+    if (few) {
+      if (tid < nk_new * kVec)
+        reinterpret_cast<int4*>(ring_k + (size_t)((a.k_slot0 + a.k_first_ring + tid / kVec) % a.R) * D)[tid % kVec] = pk;
+      if (tid < nv_new * kVec)
+        reinterpret_cast<int4*>(ring_v + (size_t)((a.v_slot0 + a.v_first_ring + tid / kVec) % a.R) * D)[tid % kVec] = pv;
+    } else {
+      if (a.k_first_ring < a.T)
+        copy_to_ring<D>(ring_k, a.R, a.k_slot0 + a.k_first_ring, in_k + (size_t)a.k_first_ring * D,
+                        a.T - a.k_first_ring);
+      if (a.v_first_ring < a.T)
+        copy_to_ring<D>(ring_v, a.R, a.v_slot0 + a.v_first_ring, in_v + (size_t)a.v_first_ring * D,
+                        a.T - a.v_first_ring);
+    }
   }
   // work that reads only the new tokens, spread over the chunks (chunk 0
   // takes part only when it is the only one)
@@ -162,8 +278,8 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
   const int me = a.chunks > 1 ? chunk - 1 : 0;
   if (a.chunks > 1 && chunk == 0) return;
   for (int gi = a.k_ring_groups + me; gi < a.k_groups; gi += workers)
-    quant_k_group<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
-                     a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, xs, codes_s);
+    quant_k_group_any<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
+                     a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
   for (int p = a.v_ring_tokens + me * nwarps + warp; p < a.v_evict; p += workers * nwarps)
     quant_v_token<D>(a.dst, a.bits, a.G, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
                      a.v_nv0 + p);
@@ -173,21 +289,19 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) flush_kernel(const AppendArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
-  __half* xs = reinterpret_cast<__half*>(qsm);
-  uint8_t* codes_s = qsm + (size_t)a.G * D * 2;
+  const QuantSmem qs = quant_smem_view(qsm, a.G, D);
   const size_t pair = blockIdx.x;
   const int gi = blockIdx.y;
   const __half* ring_k = a.kr + pair * (size_t)a.R * D;
-  quant_k_group<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, nullptr, a.ksrc, gi * a.G,
-                   a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, xs, codes_s);
+  quant_k_group_any<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, nullptr, a.ksrc, gi * a.G,
+                   a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
 }
 
 // WindowQuant ingest: block (pair, job); job n_jobs is the fp16 tail.
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
-  __half* xs = reinterpret_cast<__half*>(qsm);
-  uint8_t* codes_s = qsm + (size_t)a.G * D * 2;
+  const QuantSmem qs = quant_smem_view(qsm, a.G, D);
   const size_t pair = blockIdx.x;
   const int j = blockIdx.y;
   const __half* in_k = a.k_new + pair * (size_t)a.T * D;
@@ -211,8 +325,8 @@ __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs 
   const RowSrc src{0, 0};
   const __half* wk = in_k + (size_t)job.src_token * D;
   for (int gi = 0; gi < a.S / a.G; ++gi)
-    quant_k_group<D>(dst, dst.bits, a.G, a.R, pair, nullptr, wk, src, gi * a.G, job.dst + gi * a.G,
-                     job.dst / a.G + gi, xs, codes_s);
+    quant_k_group_any<D>(dst, dst.bits, a.G, a.R, pair, nullptr, wk, src, gi * a.G, job.dst + gi * a.G,
+                     job.dst / a.G + gi, qs);
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int p = warp; p < a.S; p += nwarps)
     quant_v_token<D>(dst, dst.bits, a.G, pair, in_v + (size_t)(job.src_token + p) * D, job.dst + p);
@@ -220,7 +334,7 @@ __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs 
 
 }  // namespace
 
-size_t quant_smem(int G, int d) { return (size_t)G * d * 3; }
+size_t quant_smem(int G, int d) { return quant_smem_bytes(G, d); }
 
 template <class K>
 cudaError_t set_smem(K kernel, size_t bytes) {
