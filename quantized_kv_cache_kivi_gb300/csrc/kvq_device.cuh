@@ -56,6 +56,21 @@ __device__ __forceinline__ uint32_t qcode_fast(float x, float z, float s, float 
   return min(__float2uint_rn(r), (1u << BITS) - 1u);
 }
 
+// The fast half of qcode_fast without its branch: the code from the product,
+// and whether the IEEE quotient has to decide instead (qcode_exact).
+template <int BITS>
+__device__ __forceinline__ uint32_t qcode_guess(float x, float z, float rcp, bool& near_tie) {
+  const float t = __fmul_rn(__fsub_rn(x, z), rcp);
+  const float r = rintf(t);
+  near_tie = fabsf(t - r) > 0.4999f;
+  return min(__float2uint_rn(r), (1u << BITS) - 1u);
+}
+template <int BITS>
+__device__ __forceinline__ uint32_t qcode_exact(float x, float z, float s) {
+  if (s == 0.0f) return 0u;  // constant group (or an underflowed scale): code 0
+  return min(__float2uint_rn(rintf(__fdiv_rn(__fsub_rn(x, z), s))), (1u << BITS) - 1u);
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory address, mbarrier and 1-D bulk copy (TMA engine, no tensor map)
 // ---------------------------------------------------------------------------

@@ -146,11 +146,23 @@ __device__ void quant_k_group(const SegDev& dst, int G, int R, size_t pair,
   for (int i = tl; i < G; i += TL) {
     const uint4 u = reinterpret_cast<const uint4*>(q.xs + (size_t)i * D)[cch];
     const __half* h = reinterpret_cast<const __half*>(&u);
+    uint32_t c[8];
+    bool tie = false;  // some code too close to a rounding tie for the product
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      bool t;
+      c[e] = qcode_guess<BITS>(__half2float(h[e]), cz[e], cr[e], t);
+      tie |= t;
+    }
+    if (tie) {  // rare: redo the chunk with IEEE quotients
+#pragma unroll
+      for (int e = 0; e < 8; ++e) c[e] = qcode_exact<BITS>(__half2float(h[e]), cz[e], cs[e]);
+    }
     uint32_t lo = 0, hi = 0;  // codes 0-3 and 4-7 (8 codes = BITS bytes)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      lo |= qcode_fast<BITS>(__half2float(h[e]), cz[e], cs[e], cr[e]) << (e * BITS);
-      hi |= qcode_fast<BITS>(__half2float(h[e + 4]), cz[e + 4], cs[e + 4], cr[e + 4]) << (e * BITS);
+      lo |= c[e] << (e * BITS);
+      hi |= c[e + 4] << (e * BITS);
     }
     uint8_t* out = base + (size_t)i * rb + cch * BITS;
     if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(out) = (uint16_t)(lo | (hi << 8));

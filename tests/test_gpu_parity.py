@@ -72,6 +72,31 @@ def test_deferred_flush_state_bit_exact():
     pair.assert_buffers_bit_exact()
 
 
+def test_ties_and_constant_groups_bit_exact():
+    """Rounding ties ((x - z) / s exactly k + 1/2) next to constant groups
+    (s = 0) in the same 8-channel chunk, for K groups and V tokens: the
+    quantizer's exact fallback must keep the constant groups' codes at 0."""
+    B, H, d, G, R = 1, 2, 128, 32, 32
+    l = 3 * R + 5
+    K, V = kv(14, B, H, l, d)
+    ties = np.array([0.0, 3.0, 0.5, 1.5, 2.5], np.float16)
+    for t in range(l):
+        K[:, :, t, 0] = ties[t % 5]          # 2-bit: s = 1, ties at .5
+        K[:, :, t, 1] = np.float16(1.25)     # constant channel: s = 0
+        K[:, :, t, 9] = ties[(t + 2) % 5]
+        K[:, :, t, 10] = np.float16(-0.75)
+    V[:, :, ::3, :32] = np.float16(0.5)      # constant V groups (s = 0) ...
+    V[:, :, ::3, 32:37] = ties               # ... beside tie groups
+    V[:, :, ::3, 37:64] = np.float16(0.0)
+    for bits in (2, 4, 8):
+        pair = KiviPair(B, H, H, d, G, R, bits, cap=256)
+        pair.prefill(K[:, :, :2 * R + 3], V[:, :, :2 * R + 3])
+        for t in range(2 * R + 3, l):
+            pair.append(K[:, :, t:t + 1], V[:, :, t:t + 1])
+        pair.flush()
+        pair.assert_buffers_bit_exact()
+
+
 # ---------------------------------------------------------------------------
 # attention parity
 # ---------------------------------------------------------------------------
