@@ -80,9 +80,10 @@ def profiled_traffic():
         return None
     vals = {}
     for line in txt.splitlines():
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_hash")):
+        line = line.strip().lstrip("-* ")
+        if ":" in line and line.startswith(("traffic_bytes_per_launch", "source_hash")):
             k, v = line.split(":", 1)
-            vals[k.strip().strip("-* `")] = v.strip().strip("`")
+            vals[k.strip().strip("`")] = v.strip().strip("`")
     if vals.get("source_hash") != kernel_source_hash():
         return None
     try:
