@@ -74,7 +74,7 @@ struct TcSmem {
   static constexpr int total = flags + 16;
 };
 static_assert(TcSmem::q % 16 == 0 && TcSmem::ktab % 16 == 0 && TcSmem::rec % 16 == 0, "align");
-static_assert(2 * (TcSmem::total + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(kTcCtasPerSm * (TcSmem::total + 1024) <= 228 * 1024, "CTAs per SM");
 
 // Token of row r of a 16-token sub-tile.  Swapping neighbours in the upper
 // half of each 8-row block keeps both the K row loads (rows gid) and the V
@@ -608,7 +608,7 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, long 
 }
 
 template <int B>
-__global__ void __launch_bounds__(NTH, 2) decode_tc_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcSmem::bars);
   uint64_t* ready = full + NS;
@@ -852,7 +852,7 @@ cudaError_t launch_tc_b(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-int decode_tc_ctas_per_sm() { return 2; }
+int decode_tc_ctas_per_sm() { return kTcCtasPerSm; }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, cudaStream_t s) {
   if (bits == 2) return launch_tc_b<2>(a, s);

@@ -28,6 +28,7 @@ constexpr int kMhaQtabBytes = kMhaMaxGroups * 4 * 36 * 4;  // scaled-query rows 
 // registers a thread)
 constexpr int kTcConsumerWarps = 6;
 constexpr int kTcStages = 4;
+constexpr int kTcCtasPerSm = 2;
 constexpr int kTcStageBytes = 19456;
 constexpr int kTcMaxGroups = 8;                      // K groups one tile may touch
 constexpr int kTcKtabBytes = kTcMaxGroups * 512;     // K operand table per stage
