@@ -66,8 +66,10 @@ struct TcSmem {
   static constexpr int ktab = q + NS * D * 2;                         // [stage] K operand table
   static constexpr int kbias = ktab + NS * kTcKtabBytes;              // [stage][group] f32
   static constexpr int rec = kbias + NS * kTcMaxGroups * 4;           // [stage] TcRec
-  static constexpr int merge = rec + NS * 64;                         // [NCW][D + 2] f32
-  static constexpr int zero = align_up(merge + NCW * (D + 2) * 4, 16);  // 64 zero bytes
+  static constexpr int merge = rec + NS * 64;                         // [slot][NCW][D + 2] f32
+  static constexpr int slot_owner = align_up(merge + kTcMergeSlots * NCW * (D + 2) * 4, 16);  // [slot] piece served
+  static constexpr int slot_count = slot_owner + 16;                  // [slot] warps arrived
+  static constexpr int zero = slot_count + 16;                        // 64 zero bytes
   static constexpr int args = zero + 64;                             // DecodeArgs copy
   static constexpr int bars = align_up(args + (int)sizeof(DecodeArgs), 16);
   static constexpr int flags = bars + 3 * NS * 8;
@@ -174,15 +176,15 @@ __device__ __forceinline__ bool try_wait_at(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: about 2^31 SM clocks, then the abort flag is raised.  The
-// warps that run ahead (bulk copies, K table) back off with a growing sleep
-// between polls so their polling does not take issue slots from the
-// consumer warps; the consumers poll without sleeping.
+// warps that run ahead (bulk copies, K table) sleep between polls, up to
+// 128 ns, so their polling leaves issue slots to the consumer warps without
+// adding much to the stage round trip; the consumers poll without sleeping.
 template <bool BACKOFF>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   const uint32_t addr = smem_u32(bar);
   if (try_wait_at(addr, parity)) return true;
   const long long t0 = clock64();
-  uint32_t ns = 64;
+  uint32_t ns = 32;
   while (!try_wait_at(addr, parity)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > (1ll << 31)) {
@@ -191,7 +193,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     }
     if (BACKOFF) {
       __nanosleep(ns);
-      ns = ns < 512 ? 2 * ns : ns;
+      ns = ns < 128 ? 2 * ns : ns;
     }
   }
   return true;
@@ -201,9 +203,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
-}
 
 // CTA owning global tile g when T tiles are cut into N equal ranges
 // [floor(i T / N), floor((i + 1) T / N)).
@@ -518,14 +517,36 @@ __device__ __forceinline__ int run_tile(const DecodeArgs& a, int st, const TcRec
   return j - n_unit;
 }
 
-// End of a warp's share of one pair inside this CTA's range: merge the warps,
-// then write the output (the pair lies in this range only) or a partial
-// record (merged by the pair's last CTA to finish).
+// End of a warp's share of one pair inside this CTA's range (the CTA's k-th
+// piece).  The warp leaves its partial (o, m, l) in merge slot k % NSLOT and
+// goes on; the last of the NCW warps to arrive combines them and writes the
+// output (the pair lies in this range only) or the CTA's record; for a split
+// pair the last record to arrive merges all records.  No CTA-wide barrier:
+// warps that have drifted apart by a few tiles do not wait for each other.
+// Slot reuse: warps are at most NS tiles apart (the stage ring), each piece
+// has at least one tile, and the merger of piece k is its last warp, so a
+// warp reaching piece k + NSLOT waits (bounded) only if fewer than NSLOT
+// slots separate it from a merge still running.
 template <int B>
-__device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, long long T, int warp,
+__device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int piece, long long T, int warp,
                              int lane, WarpState& S, volatile int* flags) {
   const int gid = lane >> 2, tig = lane & 3;
-  float* mg = reinterpret_cast<float*>(smem + TcSmem::merge) + warp * (D + 2);
+  const int slot = piece % kTcMergeSlots;
+  volatile int* owner = reinterpret_cast<volatile int*>(smem + TcSmem::slot_owner);
+  int* count = reinterpret_cast<int*>(smem + TcSmem::slot_count);
+  // wait until the slot serves this piece (its previous piece merged)
+  if (owner[slot] != piece) {
+    const long long t0 = clock64();
+    while (owner[slot] != piece) {
+      if (flags[0] || clock64() - t0 > (1ll << 31)) {
+        flags[0] = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  __syncwarp();
+  float* mg = reinterpret_cast<float*>(smem + TcSmem::merge) + (slot * NCW + warp) * (D + 2);
   if (!S.vring) unscale_acc<B>(S);
   float l = S.l;  // rows are replicated over tig: sum over gid only
   l += __shfl_xor_sync(kFull, l, 4);
@@ -549,62 +570,78 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, long 
     mg[D] = S.m;
     mg[D + 1] = l;
   }
-  const int tid = warp * 32 + lane;
-  if (tid == 0) flags[2] = flags[0];  // one abort verdict for every thread
-  consumer_sync();
+  __threadfence_block();
+  __syncwarp();
+  int last_warp = 0;
+  if (lane == 0) last_warp = atomicAdd(&count[slot], 1) == NCW - 1;
+  if (!__shfl_sync(kFull, last_warp, 0)) return;
+  __threadfence_block();
+  // this warp merges the slot: lane owns channels lane + 32 i
+  const float* m0 = reinterpret_cast<const float*>(smem + TcSmem::merge) + slot * NCW * (D + 2);
+  float M = -INFINITY;
+  for (int w = 0; w < NCW; ++w) M = fmaxf(M, m0[w * (D + 2) + D]);
+  float L = 0.f, O[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) O[i] = 0.f;
+  for (int w = 0; w < NCW; ++w) {
+    const float* mw = m0 + w * (D + 2);
+    const float sw = (mw[D] == -INFINITY) ? 0.f : exp2f(mw[D] - M);
+    L += mw[D + 1] * sw;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) O[i] += mw[lane + 32 * i] * sw;
+  }
+  // the slot is free for piece + NSLOT
+  __syncwarp();
+  if (lane == 0) {
+    count[slot] = 0;
+    __threadfence_block();
+    owner[slot] = piece + kTcMergeSlots;
+  }
+  const bool ok = flags[0] == 0;
+  if (!ok) {
+    if (lane == 0) atomicExch(a.err, 1);
+    return;
+  }
   const long long nt = a.n_tiles;
   const int first = owner_cta((long long)pair * nt, T, a.n_cta);
   const int last = owner_cta((long long)pair * nt + nt - 1, T, a.n_cta);
   const int pieces = last - first + 1;
   const size_t out_base = (size_t)pair * D;
-  float* rec = a.part + ((size_t)pair * a.n_splits + (blockIdx.x - first)) * (D + 2);
-  const bool ok = flags[2] == 0;
-  if (ok && tid < D) {
-    const float* m0 = reinterpret_cast<const float*>(smem + TcSmem::merge);
-    float M = -INFINITY;
-    for (int w = 0; w < NCW; ++w) M = fmaxf(M, m0[w * (D + 2) + D]);
-    float L = 0.f, O = 0.f;
-    for (int w = 0; w < NCW; ++w) {
-      const float* mw = m0 + w * (D + 2);
-      const float sw = (mw[D] == -INFINITY) ? 0.f : exp2f(mw[D] - M);
-      L += mw[D + 1] * sw;
-      O += mw[tid] * sw;
-    }
-    if (pieces == 1) {
-      a.out[out_base + tid] = __float2half_rn(O / L);
-    } else {
-      rec[tid] = O;
-      if (tid == 0) {
-        rec[D] = M;
-        rec[D + 1] = L;
-      }
-    }
+  if (pieces == 1) {
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) a.out[out_base + lane + 32 * i] = __float2half_rn(O[i] / L);
+    return;
   }
-  if (!ok && tid == 0) atomicExch(a.err, 1);
-  consumer_sync();  // merge area free again; records written
-  if (pieces == 1 || !ok) return;
+  float* rec = a.part + ((size_t)pair * a.n_splits + (blockIdx.x - first)) * (D + 2);
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) rec[lane + 32 * i] = O[i];
+  if (lane == 0) {
+    rec[D] = M;
+    rec[D + 1] = L;
+  }
   __threadfence();
-  consumer_sync();
-  if (tid == 0) flags[1] = (atomicAdd(&a.counters[pair], 1) == pieces - 1);
-  consumer_sync();
-  const bool merger = flags[1] != 0;
-  consumer_sync();  // flags[1] read by all before a later piece rewrites it
-  if (!merger) return;
+  __syncwarp();
+  // the last record of the pair to arrive merges them all
+  int last_in = 0;
+  if (lane == 0) last_in = atomicAdd(&a.counters[pair], 1) == pieces - 1;
+  if (!__shfl_sync(kFull, last_in, 0)) return;
   __threadfence();
   const float* recs = a.part + (size_t)pair * a.n_splits * (D + 2);
-  if (tid < D) {
-    float MM = -INFINITY;
-    for (int s = 0; s < pieces; ++s) MM = fmaxf(MM, __ldcg(recs + (size_t)s * (D + 2) + D));
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < pieces; ++s) {
-      const float* rr = recs + (size_t)s * (D + 2);
-      const float w = exp2f(__ldcg(rr + D) - MM);
-      L += __ldcg(rr + D + 1) * w;
-      O += __ldcg(rr + tid) * w;
-    }
-    a.out[out_base + tid] = __float2half_rn(O / L);
+  float MM = -INFINITY;
+  for (int s = 0; s < pieces; ++s) MM = fmaxf(MM, __ldcg(recs + (size_t)s * (D + 2) + D));
+  float LL = 0.f;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) O[i] = 0.f;
+  for (int s = 0; s < pieces; ++s) {
+    const float* rr = recs + (size_t)s * (D + 2);
+    const float w = exp2f(__ldcg(rr + D) - MM);
+    LL += __ldcg(rr + D + 1) * w;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) O[i] += __ldcg(rr + lane + 32 * i) * w;
   }
-  if (tid == 0) a.counters[pair] = 0;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) a.out[out_base + lane + 32 * i] = __float2half_rn(O[i] / LL);
+  if (lane == 0) a.counters[pair] = 0;
 }
 
 template <int B>
@@ -633,6 +670,10 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
     mbar_fence_init();
   }
   if (tid < 16) reinterpret_cast<uint32_t*>(smem + TcSmem::zero)[tid] = 0u;
+  if (tid < kTcMergeSlots) {
+    reinterpret_cast<int*>(smem + TcSmem::slot_owner)[tid] = tid;
+    reinterpret_cast<int*>(smem + TcSmem::slot_count)[tid] = 0;
+  }
   static_assert(sizeof(DecodeArgs) % 4 == 0, "word copy");
   for (int i = tid; i < (int)(sizeof(DecodeArgs) / 4); i += NTH)
     reinterpret_cast<uint32_t*>(smem + TcSmem::args)[i] = reinterpret_cast<const uint32_t*>(&a)[i];
@@ -804,13 +845,14 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
   reset();
   int cur_pair = g_begin / a.n_tiles;
   int t_in_pair = g_begin - cur_pair * a.n_tiles;
+  int piece = 0;  // pieces (pairs) of this CTA's range finished so far
   int jstart = warp;  // this warp's first sub-tile of the next tile (round-robin)
   bool aborted = false;
   for (int it = 0; it < ntiles; ++it) {
     const int st = it % NS;
     const uint32_t ph = (uint32_t)((it / NS) & 1);
     if (t_in_pair == a.n_tiles) {  // first tile of the next pair
-      finish_piece<B>(a, smem, cur_pair, T, warp, lane, S, flags);
+      finish_piece<B>(a, smem, cur_pair, piece++, T, warp, lane, S, flags);
       reset();
       ++cur_pair;
       t_in_pair = 0;
@@ -838,7 +880,7 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
   }
-  if (ntiles > 0) finish_piece<B>(a, smem, cur_pair, T, warp, lane, S, flags);
+  if (ntiles > 0) finish_piece<B>(a, smem, cur_pair, piece, T, warp, lane, S, flags);
 }
 
 template <int B>

@@ -29,6 +29,7 @@ constexpr int kMhaQtabBytes = kMhaMaxGroups * 4 * 36 * 4;  // scaled-query rows 
 constexpr int kTcConsumerWarps = 6;
 constexpr int kTcStages = 4;
 constexpr int kTcCtasPerSm = 2;
+constexpr int kTcMergeSlots = 3;                     // pieces whose warp partials can be in flight
 constexpr int kTcStageBytes = 19456;
 constexpr int kTcMaxGroups = 8;                      // K groups one tile may touch
 constexpr int kTcKtabBytes = kTcMaxGroups * 512;     // K operand table per stage
