@@ -25,11 +25,11 @@
 // Work split: a persistent grid of CTAs walks the concatenated tile list of
 // all (batch, kv head) pairs in equal contiguous ranges (stream-K); a range
 // that covers part of a pair leaves a partial (o, m, l) record and the last
-// CTA of that pair to finish merges the records.  CTA = 6 consumer warps
-// that take the 16-token sub-tiles of each staged tile in round-robin order,
-// each with its own online softmax; 1 warp that builds each tile's K operand
-// table once its bytes have landed; 1 warp that issues the bulk copies
-// (TMA engine) of up to 4 tiles ahead.
+// CTA of that pair to finish merges the records.  CTA = 7 consumer warps
+// that take the 32-token units of each staged tile in round-robin order, each
+// building the K operand of its unit's K group and keeping its own online
+// softmax, and 1 warp that issues the bulk copies (TMA engine) of up to 4
+// tiles ahead.
 #include <float.h>
 
 #include "kvq_device.cuh"
@@ -39,22 +39,19 @@ namespace kvq {
 namespace {
 
 constexpr int NCW = kTcConsumerWarps;
-constexpr int NTH = (NCW + 2) * 32;  // + table warp + bulk-copy warp
+constexpr int NTH = (NCW + 1) * 32;  // + bulk-copy warp
 constexpr int D = 128;
 constexpr int NS = kTcStages;
 constexpr uint32_t kFull = 0xffffffffu;
 
 // What the producer records about the tile it staged in a stage.
 struct TcRec {
-  // read by the consumer warps
   int n;       // tokens
   int kq, vq;  // 1: K / V come from the packed segment, 0: from the ring
   int kr0;     // first packed K row mod G
   uint32_t k_off, v_off, vs_off, vz_off;
-  // read by the K table warp
-  int ng;      // K groups staged
-  uint32_t ks_off, kz_off;
-  int pad[5];
+  uint32_t ks_off, kz_off;  // K scales / zeros of the staged groups
+  int pad[6];
 };
 static_assert(sizeof(TcRec) == 64, "record size");
 
@@ -63,16 +60,15 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 struct TcSmem {
   static constexpr int stages = 0;
   static constexpr int q = stages + NS * kTcStageBytes;               // [stage][D] f16
-  static constexpr int ktab = q + NS * D * 2;                         // [stage] K operand table
-  static constexpr int kbias = ktab + NS * kTcKtabBytes;              // [stage][group] f32
-  static constexpr int rec = kbias + NS * kTcMaxGroups * 4;           // [stage] TcRec
+  static constexpr int ktab = q + NS * D * 2;                         // [warp] K operand of its unit
+  static constexpr int rec = ktab + NCW * 512;                        // [stage] TcRec
   static constexpr int merge = rec + NS * 64;                         // [slot][NCW][D + 2] f32
   static constexpr int slot_owner = align_up(merge + kTcMergeSlots * NCW * (D + 2) * 4, 16);  // [slot] piece served
   static constexpr int slot_count = slot_owner + 16;                  // [slot] warps arrived
   static constexpr int zero = slot_count + 16;                        // 64 zero bytes
   static constexpr int args = zero + 64;                             // DecodeArgs copy
   static constexpr int bars = align_up(args + (int)sizeof(DecodeArgs), 16);
-  static constexpr int flags = bars + 3 * NS * 8;
+  static constexpr int flags = bars + 2 * NS * 8;
   static constexpr int total = flags + 16;
 };
 static_assert(TcSmem::q % 16 == 0 && TcSmem::ktab % 16 == 0 && TcSmem::rec % 16 == 0, "align");
@@ -340,6 +336,51 @@ __device__ __forceinline__ void k_scores_ring(const uint8_t* kr, const uint8_t* 
   x1 = sc[2] * scale_log2;
 }
 
+// The K operand of one K group, built by the consuming warp itself: lane
+// (tig, kt) computes q_c s_gc 2^-p sm_scale log2(e) for the 4 channels of
+// the operand entries (tig, kt, e = 0/1), splits each into an fp16 high and
+// low part and stores both; every lane then reads the 16 words of its own
+// (hi or lo, tig) row.  The bias q . z_g (log2 domain) comes from a warp sum.
+template <int B>
+__device__ __forceinline__ float build_k_operand(const DecodeArgs& a, const uint8_t* stage, const __half* qs,
+                                                 const TcRec& r, int gl, uint32_t* scratch, int lane,
+                                                 uint32_t (&bq)[16]) {
+  const int ptig = lane >> 3, pkt = lane & 7;
+  const __half* sg = reinterpret_cast<const __half*>(stage + r.ks_off) + gl * D;
+  const __half* zg = reinterpret_cast<const __half*>(stage + r.kz_off) + gl * D;
+  float hi[4], lo[4];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    int clo, chi, p;
+    k_half2_channels<B>(ptig, 2 * pkt + e, &clo, &chi, &p);
+    const float f = __uint_as_float((uint32_t)(127 - p) << 23) * a.scale_log2;  // 2^-p sm_scale log2(e)
+    const float v0 = __half2float(qs[clo]) * __half2float(sg[clo]) * f;
+    const float v1 = __half2float(qs[chi]) * __half2float(sg[chi]) * f;
+    hi[2 * e] = __half2float(__float2half_rn(v0));
+    lo[2 * e] = v0 - hi[2 * e];
+    hi[2 * e + 1] = __half2float(__float2half_rn(v1));
+    lo[2 * e + 1] = v1 - hi[2 * e + 1];
+  }
+  // scratch entry (k = kt / 2, part, tig): 4 words, kt even (b0, b1) then kt odd
+  *reinterpret_cast<uint2*>(scratch + ((pkt >> 1) * 8 + 0 * 4 + ptig) * 4 + (pkt & 1) * 2) =
+      make_uint2(pack_half2(hi[0], hi[1]), pack_half2(hi[2], hi[3]));
+  *reinterpret_cast<uint2*>(scratch + ((pkt >> 1) * 8 + 1 * 4 + ptig) * 4 + (pkt & 1) * 2) =
+      make_uint2(pack_half2(lo[0], lo[1]), pack_half2(lo[2], lo[3]));
+  float zsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    zsum = fmaf(__half2float(qs[lane + 32 * i]), __half2float(zg[lane + 32 * i]), zsum);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) zsum += __shfl_xor_sync(kFull, zsum, off);
+  __syncwarp();
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint4* tb = reinterpret_cast<const uint4*>(scratch) + (gid & 1) * 4 + tig;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(&bq[4 * k]) = tb[k * 8];
+  __syncwarp();  // scratch reads done before the next unit rewrites it
+  return zsum * a.scale_log2;
+}
+
 // One 32-token unit [s0, s0 + 32) of the staged tile: two 16-token halves
 // (rows sigma(r) of half h are tokens s0 + 16 h + sigma(r)).  s0 is a
 // multiple of 32 and the unit lies inside one K group (G >= 32, packed runs
@@ -356,11 +397,10 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
   float x[2][2];  // [half][row gid, row gid + 8]
   if constexpr (KQ) {
     const int gl = (r.kr0 + s0) >> a.log2G;
-    const uint4* tb = reinterpret_cast<const uint4*>(sm + TcSmem::ktab + st * kTcKtabBytes) + gl * 32 + (gid & 1) * 4 + tig;
     uint32_t bq[16];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(&bq[4 * k]) = tb[k * 8];
-    const float bias = reinterpret_cast<const float*>(sm + TcSmem::kbias)[st * kTcMaxGroups + gl];
+    const float bias = build_k_operand<B>(a, stage, reinterpret_cast<const __half*>(sm + TcSmem::q + st * D * 2), r,
+                                          gl, reinterpret_cast<uint32_t*>(sm + TcSmem::ktab) + (threadIdx.x >> 5) * 128,
+                                          lane, bq);
     const uint8_t* kc = stage + r.k_off + tig * (B * 4);
     if constexpr (B == 2) {
       k_scores_packed2_b2(kc, s0, r0, r1, bq, bias, x);  // rows past the tile read stale bytes: masked below
@@ -648,8 +688,7 @@ template <int B>
 __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcSmem::bars);
-  uint64_t* ready = full + NS;
-  uint64_t* empty = ready + NS;
+  uint64_t* empty = full + NS;
   volatile int* flags = reinterpret_cast<volatile int*>(smem + TcSmem::flags);
   TcRec* recs = reinterpret_cast<TcRec*>(smem + TcSmem::rec);
 
@@ -664,7 +703,6 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
     flags[1] = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&ready[s], 1);
       mbar_init(&empty[s], NCW);
     }
     mbar_fence_init();
@@ -680,7 +718,7 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
   const DecodeArgs* args_s = reinterpret_cast<const DecodeArgs*>(smem + TcSmem::args);
   __syncthreads();
 
-  if (warp == NCW + 1) {
+  if (warp == NCW) {
     // ------------------------------------------------- bulk-copy issue warp
     // Lane l works out the record and the copies of tile j0 + l for 32 tiles
     // at once (from the shared-memory copy of the launch arguments: indexing
@@ -711,7 +749,6 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
           rec.kq = ti.kseg >= 0;
           rec.vq = ti.vseg >= 0;
           rec.kr0 = ti.ku0 & (sa.G - 1);
-          rec.ng = ti.ng;
           rec.k_off = ti.k_off;
           rec.ks_off = ti.ks_off;
           rec.kz_off = ti.kz_off;
@@ -747,88 +784,6 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
     return;
   }
 
-  if (warp == NCW) {
-    // ------------------------------------------------ K operand table warp
-    // lane = (tig, kt): the channels of K operand entries (tig, kt, e = 0/1)
-    const int ptig = lane >> 3, pkt = lane & 7;
-    int ch[4];
-    float pscale[4];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      int clo, chi, p;
-      k_half2_channels<B>(ptig, 2 * pkt + e, &clo, &chi, &p);
-      ch[2 * e] = clo;
-      ch[2 * e + 1] = chi;
-      pscale[2 * e] = pscale[2 * e + 1] = __uint_as_float((uint32_t)(127 - p) << 23);  // 2^-p
-    }
-    for (int it = 0; it < ntiles; ++it) {
-      const int st = it % NS;
-      const uint32_t ph = (uint32_t)((it / NS) & 1);
-      if (__any_sync(kFull, !wait_or_abort<true>(&full[st], ph, flags))) break;
-      const TcRec& r = recs[st];
-      if (r.kq) {
-        const uint8_t* stage = smem + TcSmem::stages + st * kTcStageBytes;
-        const __half* qs = reinterpret_cast<const __half*>(smem + TcSmem::q + st * D * 2);
-        const __half* ks = reinterpret_cast<const __half*>(stage + r.ks_off);
-        const __half* kz = reinterpret_cast<const __half*>(stage + r.kz_off);
-        uint32_t* tab = reinterpret_cast<uint32_t*>(smem + TcSmem::ktab + st * kTcKtabBytes);
-        float* kb = reinterpret_cast<float*>(smem + TcSmem::kbias) + st * kTcMaxGroups;
-        float qv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qv[e] = __half2float(qs[ch[e]]) * pscale[e] * a.scale_log2;
-        float qz[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) qz[i] = __half2float(qs[lane + 32 * i]);
-        // all kTcMaxGroups groups, without branches: groups past ng read other
-        // bytes of the stage (in bounds) and fill table slots nobody reads
-        float zs[kTcMaxGroups];  // this lane's part of q . z_g (channels lane + 32 i)
-#pragma unroll
-        for (int gl = 0; gl < kTcMaxGroups; ++gl) {
-          const __half* sg = ks + gl * D;
-          float hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float v = qv[e] * __half2float(sg[ch[e]]);
-            hi[e] = __half2float(__float2half_rn(v));
-            lo[e] = v - hi[e];
-          }
-          // entry (gl, k = kt / 2, part, tig): 4 words, kt even (b0, b1) then kt odd
-          uint32_t* eh = tab + ((gl * 4 + (pkt >> 1)) * 8 + 0 * 4 + ptig) * 4 + (pkt & 1) * 2;
-          uint32_t* el = tab + ((gl * 4 + (pkt >> 1)) * 8 + 1 * 4 + ptig) * 4 + (pkt & 1) * 2;
-          *reinterpret_cast<uint2*>(eh) = make_uint2(pack_half2(hi[0], hi[1]), pack_half2(hi[2], hi[3]));
-          *reinterpret_cast<uint2*>(el) = make_uint2(pack_half2(lo[0], lo[1]), pack_half2(lo[2], lo[3]));
-          const __half* zg = kz + gl * D;
-          zs[gl] = 0.f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) zs[gl] = fmaf(qz[i], __half2float(zg[lane + 32 * i]), zs[gl]);
-        }
-        // sum the 8 per-lane vectors over the warp: each exchange halves the
-        // groups a lane keeps (xor 16: 4 left, xor 8: 2, xor 4: 1), then the 4
-        // lanes of one group add up; lane 4 g holds group g.
-        static_assert(kTcMaxGroups == 8, "bias reduction is written for 8 groups");
-        float y4[4], y2[2];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const bool up = lane & 16;
-          y4[k] = (up ? zs[k + 4] : zs[k]) + __shfl_xor_sync(kFull, up ? zs[k] : zs[k + 4], 16);
-        }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const bool up = lane & 8;
-          y2[k] = (up ? y4[k + 2] : y4[k]) + __shfl_xor_sync(kFull, up ? y4[k] : y4[k + 2], 8);
-        }
-        const bool up = lane & 4;
-        float y = (up ? y2[1] : y2[0]) + __shfl_xor_sync(kFull, up ? y2[0] : y2[1], 4);
-        y += __shfl_xor_sync(kFull, y, 2);
-        y += __shfl_xor_sync(kFull, y, 1);
-        if ((lane & 3) == 0) kb[lane >> 2] = y * a.scale_log2;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ready[st]);
-    }
-    return;
-  }
-
   // -------------------------------------------------------------- consumers
   WarpState S;
   auto reset = [&]() {
@@ -858,10 +813,11 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
       t_in_pair = 0;
     }
     ++t_in_pair;
-    if (!aborted && __any_sync(kFull, !wait_or_abort<false>(&ready[st], ph, flags))) aborted = true;
+    if (!aborted && __any_sync(kFull, !wait_or_abort<false>(&full[st], ph, flags))) aborted = true;
     if (!aborted) {
       const int4 r0 = *reinterpret_cast<const int4*>(&recs[st].n);
       const int4 r1 = *reinterpret_cast<const int4*>(&recs[st].k_off);
+      const int2 r2 = *reinterpret_cast<const int2*>(&recs[st].ks_off);
       TcRec r;
       r.n = r0.x;
       r.kq = r0.y;
@@ -871,6 +827,8 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
       r.v_off = (uint32_t)r1.y;
       r.vs_off = (uint32_t)r1.z;
       r.vz_off = (uint32_t)r1.w;
+      r.ks_off = (uint32_t)r2.x;
+      r.kz_off = (uint32_t)r2.y;
       if (r.kq) {
         jstart = r.vq ? run_tile<B, true, true>(a, st, r, jstart, lane, S) : run_tile<B, true, false>(a, st, r, jstart, lane, S);
       } else {
