@@ -160,6 +160,109 @@ def setup_workload(w, device):
     return cache
 
 
+def cache_bytes(cache):
+    """Bytes one decode attention must read from a cache's current state:
+    packed codes + fp16 scales/zeros of every segment + the fp16 rings."""
+    c = cache.c
+    P, d, G = c.batch * c.h_kv, c.d_h, c.group
+    per = (c.nkr + c.nvr) * d * 2
+    for i in range(c.n_seg):
+        s = c.seg[i]
+        per += s.nk * d * s.bits // 8 + (s.nk // G) * d * 4
+        per += s.nv * d * s.bits // 8 + s.nv * (d // G) * 4
+    return P * per
+
+
+def per_workload_attention(device, flush_l2, peak, reps=20):
+    """Decode attention alone on each workload the pages name besides the
+    timed step's, at the state the workload describes: mean CUDA-event time
+    over `reps` calls with L2 flushed before each.  Inputs are seeded
+    synthetic data of the workloads' shapes and distributions (K ~ N(0,1)
+    with 2% outlier channels x15, V, q ~ N(0,1)), drawn on the device."""
+    import torch
+    from quantized_kv_cache_kivi_gb300 import kvq, synth
+
+    def dev_kv(seed, B, H, n, d, n_out, factor):
+        g = torch.Generator(device=device).manual_seed(seed)
+        K = torch.randn(B, H, n, d, generator=g, device=device)
+        ch = torch.randperm(d, generator=torch.Generator().manual_seed(seed))[:n_out].to(device)
+        K[:, :, :, ch] *= factor
+        V = torch.randn(B, H, n, d, generator=g, device=device)
+        return K.half(), V.half()
+
+    def timed(cache, B, Hq, d, seed):
+        q = torch.randn(B, Hq, d, generator=torch.Generator(device=device).manual_seed(seed + 7),
+                        device=device).half()
+        out = torch.empty_like(q)
+        ws = torch.zeros(kvq.kvq_workspace_bytes(cache, kvq.KVQ_MAX_SPLITS), dtype=torch.uint8,
+                         device=device)
+        for _ in range(3):
+            kvq.kvq_decode_attention(cache, q, out, ws)
+        ts = []
+        for i in range(reps):
+            flush_l2(i)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            kvq.kvq_decode_attention(cache, q, out, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        if kvq.kvq_workspace_error(ws):
+            raise RuntimeError("decode kernel reported a timed-out wait")
+        us = float(np.mean(ts)) * 1e3
+        nb = cache_bytes(cache)
+        gbs = nb / (us * 1e-6) / 1e9
+        return {"us": us, "GB/s": gbs, "frac": gbs / peak, "bytes": nb,
+                "state": dict(nk=[cache.c.seg[i].nk for i in range(cache.c.n_seg)],
+                              nv=[cache.c.seg[i].nv for i in range(cache.c.n_seg)],
+                              nkr=cache.c.nkr, nvr=cache.c.nvr)}
+
+    res = {}
+    for name in ("tiny", "llama3_8b_gqa", "streaming"):
+        w = synth.WORKLOADS[name]
+        B, Hq, H, d, G, R, bits = w["batch"], w["h_q"], w["h_kv"], w["d"], w["G"], w["R"], w["bits"]
+        n = w["prompt"] + R // 2 if name == "streaming" else w["n_packed"] + w["n_resid"]
+        cache = kvq.alloc_cache(B, H, Hq, d, G, R, [(bits, n + R)], device=device)
+        if name == "streaming":
+            # prompt, then decode steps up to the average K residual (R/2)
+            K, V = dev_kv(w["seed"], B, H, w["prompt"], d, w["n_out"], w["factor"])
+            if kvq.kvq_quantize_append(cache, K, V) == kvq.KVQ_FLUSH_DUE:
+                kvq.kvq_flush_residual(cache)
+            del K, V
+            K, V = dev_kv(w["seed"] + 1, B, H, R // 2, d, w["n_out"], w["factor"])
+            for t in range(R // 2):
+                if kvq.kvq_quantize_append(cache, K[:, :, t:t + 1].contiguous(),
+                                           V[:, :, t:t + 1].contiguous()) == kvq.KVQ_FLUSH_DUE:
+                    kvq.kvq_flush_residual(cache)
+        else:
+            # the stated state: the flush a full K ring would trigger is left due
+            K, V = dev_kv(w["seed"], B, H, n, d, w["n_out"], w["factor"])
+            kvq.kvq_quantize_append(cache, K, V)
+        del K, V
+        torch.cuda.synchronize()
+        res[name] = timed(cache, B, Hq, d, w["seed"])
+        del cache
+        torch.cuda.empty_cache()
+    # WindowQuant: windows ranked and reordered into INT8/INT4/INT2 segments,
+    # 64 fp16 text tokens in the ring
+    w = synth.WORKLOADS["windowquant_llava_ov"]
+    B, Hq, H, d, G, S = w["batch"], w["h_q"], w["h_kv"], w["d"], w["G"], w["S"]
+    vis, txt = synth.window_keys(w["seed"], B, H, w["n_win"], S, w["n_text"], d)
+    vd, td = torch.from_numpy(vis).to(device), torch.from_numpy(txt).to(device)
+    bits, perm, _ = kvq.kvq_window_assign(vd, td, S, w["frac8"], w["frac4"])
+    caps = [(b, max(G, int((bits == b).sum()) * S)) for b in (8, 4, 2)]
+    cache = kvq.alloc_cache(B, H, Hq, d, G, 128, caps, policy=kvq.KVQ_POLICY_FP16_TAIL, device=device)
+    g = torch.Generator(device=device).manual_seed(w["seed"])
+    Vv = torch.randn(B, H, vis.shape[2], d, generator=g, device=device).half()
+    Vt = torch.randn(B, H, txt.shape[2], d, generator=g, device=device).half()
+    kvq.kvq_quantize_append(cache, vd, Vv, plan=kvq.make_plan(S, bits, perm))
+    kvq.kvq_quantize_append(cache, td, Vt)
+    torch.cuda.synchronize()
+    res["windowquant_llava_ov"] = timed(cache, B, Hq, d, w["seed"])
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -299,9 +402,10 @@ def run_ours(args, rank, world, local_rank):
     if err:
         raise RuntimeError("decode kernel reported a timed-out wait")
     e2e_step = float(np.mean(e2e_s))
+    others = per_workload_attention(device, flush_l2, measured_peak()[0]) if args.per_workload else {}
     return dict(w=w, attn_bytes=attn_bytes, total_ms=total_ms, step_ms=step_ms, attn_ms=attn_ms,
                 app_ms=app_ms, fl_ms=fl_ms, clocks=clocks, t_wall=t_wall, e2e_step=e2e_step,
-                attn_state=attn_state,
+                attn_state=attn_state, others=others,
                 h2d=(k_in.numel() + v_in.numel() + q_in.numel()) * 2,
                 d2h=oh.numel() * 2)
 
@@ -408,6 +512,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--per-workload", type=int, default=1,
+                    help="also time the attention alone on the other workloads (0: skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -455,6 +561,7 @@ def main():
         "e2e": {"value": r["attn_bytes"] / r["e2e_step"] / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "us_per_step": r["e2e_step"] * 1e6},
+        "per_workload_attention": r["others"],
         "gpu_launches": 3 * args.steps,
         "clocks": r["clocks"],
     }
