@@ -604,6 +604,10 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   int kern = K_GENERAL;
   if (gq == 1 && cache->n_seg == 1 && cache->group >= cache->d_h / 4)
     kern = cache->d_h == 128 ? K_TC : K_MHA;
+  // 2-4 query heads per kv head, at most two V groups per token: the
+  // tensor-core kernel's four-head form
+  else if (gq >= 2 && gq <= 4 && cache->n_seg == 1 && cache->d_h == 128 && cache->group >= 64)
+    kern = K_TC;
   st = plan_decode(cache, a, cost, kern);
   if (st != KVQ_OK) return st;
   if (a.n_tiles == 0) {

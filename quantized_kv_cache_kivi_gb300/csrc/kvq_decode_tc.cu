@@ -38,9 +38,17 @@
 namespace kvq {
 namespace {
 
-constexpr int NCW = kTcConsumerWarps;
-constexpr int NTH = (NCW + 1) * 32;  // + bulk-copy warp
 constexpr int D = 128;
+
+// HQ = query-head slots of a lane quad: 1 (one query head per kv head; every
+// column of the K operand carries it) or 4 (2-4 query heads per kv head; lane
+// tig of a quad owns head tig).
+template <int HQ>
+struct TcCfg {
+  static constexpr int NCW = HQ == 1 ? 7 : 6;      // consumer warps
+  static constexpr int NTH = (NCW + 1) * 32;       // + the bulk-copy warp
+  static constexpr int NSLOT = HQ == 1 ? 3 : 1;    // merge slots
+};
 constexpr int NS = kTcStages;
 constexpr uint32_t kFull = 0xffffffffu;
 
@@ -57,13 +65,16 @@ static_assert(sizeof(TcRec) == 64, "record size");
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
+template <int HQ>
 struct TcSmem {
+  static constexpr int NCW = TcCfg<HQ>::NCW;
   static constexpr int stages = 0;
-  static constexpr int q = stages + NS * kTcStageBytes;               // [stage][D] f16
-  static constexpr int ktab = q + NS * D * 2;                         // [warp] K operand of its unit
-  static constexpr int rec = ktab + NCW * 512;                        // [stage] TcRec
-  static constexpr int merge = rec + NS * 64;                         // [slot][NCW][D + 2] f32
-  static constexpr int slot_owner = align_up(merge + kTcMergeSlots * NCW * (D + 2) * 4, 16);  // [slot] piece served
+  static constexpr int q = stages + NS * kTcStageBytes;               // [stage][HQ][D] f16
+  static constexpr int ktab = q + NS * HQ * D * 2;                    // [warp] K operand of its unit
+  static constexpr int rec = ktab + NCW * HQ * 512;                   // [stage] TcRec
+  static constexpr int merge = rec + NS * 64;                         // [slot][NCW][HQ][D + 2] f32
+  static constexpr int slot_owner =
+      align_up(merge + TcCfg<HQ>::NSLOT * NCW * HQ * (D + 2) * 4, 16);  // [slot] piece served
   static constexpr int slot_count = slot_owner + 16;                  // [slot] warps arrived
   static constexpr int zero = slot_count + 16;                        // 64 zero bytes
   static constexpr int args = zero + 64;                             // DecodeArgs copy
@@ -71,8 +82,10 @@ struct TcSmem {
   static constexpr int flags = bars + 2 * NS * 8;
   static constexpr int total = flags + 16;
 };
-static_assert(TcSmem::q % 16 == 0 && TcSmem::ktab % 16 == 0 && TcSmem::rec % 16 == 0, "align");
-static_assert(kTcCtasPerSm * (TcSmem::total + 1024) <= 228 * 1024, "CTAs per SM");
+static_assert(TcSmem<1>::q % 16 == 0 && TcSmem<1>::ktab % 16 == 0 && TcSmem<1>::rec % 16 == 0, "align");
+static_assert(TcSmem<4>::q % 16 == 0 && TcSmem<4>::ktab % 16 == 0 && TcSmem<4>::rec % 16 == 0, "align");
+static_assert(kTcCtasPerSm * (TcSmem<1>::total + 1024) <= 228 * 1024, "CTAs per SM");
+static_assert(kTcCtasPerSm * (TcSmem<4>::total + 1024) <= 228 * 1024, "CTAs per SM");
 
 // Token of row r of a 16-token sub-tile.  Swapping neighbours in the upper
 // half of each 8-row block keeps both the K row loads (rows gid) and the V
@@ -155,8 +168,8 @@ __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
   const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
-__device__ __forceinline__ uint32_t halves(uint16_t lo, uint16_t hi) {
-  return (uint32_t)lo | ((uint32_t)hi << 16);
+__device__ __forceinline__ uint32_t halves(uint32_t lo, uint32_t hi) {
+  return (lo & 0xffffu) | (hi << 16);
 }
 
 __device__ __forceinline__ bool try_wait_at(uint32_t bar, uint32_t parity) {
@@ -320,8 +333,8 @@ __device__ __forceinline__ void k_scores_packed2_b2(const uint8_t* kc, int s0, i
 // Same for fp16 ring K.  Thread tig reads its 32 channels as four 16-byte
 // chunks, chunk kc at position (kc + tig) & 3 of the block (spreads the
 // banks), and the query words in the same order: each chunk feeds 2 MMAs.
-__device__ __forceinline__ void k_scores_ring(const uint8_t* kr, const uint8_t* qt, int s0, int r0, int r1,
-                                              int tig, float scale_log2, float& x0, float& x1) {
+__device__ __forceinline__ void k_scores_ring(const uint8_t* kr, const uint8_t* qt, uint32_t qmask, int s0, int r0,
+                                              int r1, int tig, float scale_log2, float& x0, float& x1) {
   float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int kc = 0; kc < 4; ++kc) {
@@ -329,78 +342,103 @@ __device__ __forceinline__ void k_scores_ring(const uint8_t* kr, const uint8_t* 
     const uint4 u0 = *reinterpret_cast<const uint4*>(kr + (s0 + r0) * (D * 2) + off);
     const uint4 u1 = *reinterpret_cast<const uint4*>(kr + (s0 + r1) * (D * 2) + off);
     const uint4 qw = *reinterpret_cast<const uint4*>(qt + off);
-    mma16816(sc, u0.x, u1.x, u0.y, u1.y, qw.x, qw.y);
-    mma16816(sc, u0.z, u1.z, u0.w, u1.w, qw.z, qw.w);
+    mma16816(sc, u0.x, u1.x, u0.y, u1.y, qw.x & qmask, qw.y & qmask);
+    mma16816(sc, u0.z, u1.z, u0.w, u1.w, qw.z & qmask, qw.w & qmask);
   }
-  x0 = sc[0] * scale_log2;  // B = q in every column
+  x0 = sc[0] * scale_log2;  // columns 2 tig and 2 tig + 1 carry the same query
   x1 = sc[2] * scale_log2;
 }
 
 // The K operand of one K group, built by the consuming warp itself: lane
 // (tig, kt) computes q_c s_gc 2^-p sm_scale log2(e) for the 4 channels of
-// the operand entries (tig, kt, e = 0/1), splits each into an fp16 high and
-// low part and stores both; every lane then reads the 16 words of its own
-// (hi or lo, tig) row.  The bias q . z_g (log2 domain) comes from a warp sum.
-template <int B>
+// the operand entries (tig, kt, e = 0/1) and every query head, splits each
+// into an fp16 high and low part and stores both; every lane then reads the
+// 16 words of its own column (head, hi or lo; tig) row.  Returns the bias
+// q_h . z_g (log2 domain) of the lane's head.  Query heads past `gq` (HQ = 4
+// with 2 or 3 heads) read as zero.
+template <int B, int HQ>
 __device__ __forceinline__ float build_k_operand(const DecodeArgs& a, const uint8_t* stage, const __half* qs,
                                                  const TcRec& r, int gl, uint32_t* scratch, int lane,
                                                  uint32_t (&bq)[16]) {
   const int ptig = lane >> 3, pkt = lane & 7;
   const __half* sg = reinterpret_cast<const __half*>(stage + r.ks_off) + gl * D;
   const __half* zg = reinterpret_cast<const __half*>(stage + r.kz_off) + gl * D;
-  float hi[4], lo[4];
+  int cs[4];
+  float f[4];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     int clo, chi, p;
     k_half2_channels<B>(ptig, 2 * pkt + e, &clo, &chi, &p);
-    const float f = __uint_as_float((uint32_t)(127 - p) << 23) * a.scale_log2;  // 2^-p sm_scale log2(e)
-    const float v0 = __half2float(qs[clo]) * __half2float(sg[clo]) * f;
-    const float v1 = __half2float(qs[chi]) * __half2float(sg[chi]) * f;
-    hi[2 * e] = __half2float(__float2half_rn(v0));
-    lo[2 * e] = v0 - hi[2 * e];
-    hi[2 * e + 1] = __half2float(__float2half_rn(v1));
-    lo[2 * e + 1] = v1 - hi[2 * e + 1];
+    cs[2 * e] = clo;
+    cs[2 * e + 1] = chi;
+    f[2 * e] = f[2 * e + 1] = __uint_as_float((uint32_t)(127 - p) << 23) * a.scale_log2;  // 2^-p sm_scale log2(e)
   }
-  // scratch entry (k = kt / 2, part, tig): 4 words, kt even (b0, b1) then kt odd
-  *reinterpret_cast<uint2*>(scratch + ((pkt >> 1) * 8 + 0 * 4 + ptig) * 4 + (pkt & 1) * 2) =
-      make_uint2(pack_half2(hi[0], hi[1]), pack_half2(hi[2], hi[3]));
-  *reinterpret_cast<uint2*>(scratch + ((pkt >> 1) * 8 + 1 * 4 + ptig) * 4 + (pkt & 1) * 2) =
-      make_uint2(pack_half2(lo[0], lo[1]), pack_half2(lo[2], lo[3]));
-  float zsum = 0.f;
+  float sv[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    zsum = fmaf(__half2float(qs[lane + 32 * i]), __half2float(zg[lane + 32 * i]), zsum);
+  for (int e = 0; e < 4; ++e) sv[e] = __half2float(sg[cs[e]]) * f[e];
+  float zsum[HQ];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) zsum += __shfl_xor_sync(kFull, zsum, off);
+  for (int h = 0; h < HQ; ++h) {
+    const bool live = HQ == 1 || h < a.gq;
+    const __half* qh = qs + h * D;
+    float hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float v = live ? __half2float(qh[cs[e]]) * sv[e] : 0.f;
+      hi[e] = __half2float(__float2half_rn(v));
+      lo[e] = v - hi[e];
+    }
+    // scratch entry (k = kt / 2, column hp = 2 h + part, tig): 4 words, kt even (b0, b1) then kt odd
+    *reinterpret_cast<uint2*>(scratch + (((pkt >> 1) * 2 * HQ + 2 * h) * 4 + ptig) * 4 + (pkt & 1) * 2) =
+        make_uint2(pack_half2(hi[0], hi[1]), pack_half2(hi[2], hi[3]));
+    *reinterpret_cast<uint2*>(scratch + (((pkt >> 1) * 2 * HQ + 2 * h + 1) * 4 + ptig) * 4 + (pkt & 1) * 2) =
+        make_uint2(pack_half2(lo[0], lo[1]), pack_half2(lo[2], lo[3]));
+    float z = 0.f;
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) z = fmaf(__half2float(qh[lane + 32 * i]), __half2float(zg[lane + 32 * i]), z);
+    }
+    zsum[h] = z;
+  }
+#pragma unroll
+  for (int h = 0; h < HQ; ++h)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) zsum[h] += __shfl_xor_sync(kFull, zsum[h], off);
   __syncwarp();
   const int gid = lane >> 2, tig = lane & 3;
-  const uint4* tb = reinterpret_cast<const uint4*>(scratch) + (gid & 1) * 4 + tig;
+  // column n = gid: HQ = 1 -> hi (even) / lo (odd); HQ = 4 -> head gid / 2, hi / lo
+  const int hp = HQ == 1 ? (gid & 1) : gid;
+  const uint4* tb = reinterpret_cast<const uint4*>(scratch) + hp * 4 + tig;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(&bq[4 * k]) = tb[k * 8];
+  for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(&bq[4 * k]) = tb[k * 8 * HQ];
   __syncwarp();  // scratch reads done before the next unit rewrites it
-  return zsum * a.scale_log2;
+  float bias = zsum[0];
+#pragma unroll
+  for (int h = 1; h < HQ; ++h) bias = tig == h ? zsum[h] : bias;
+  return bias * a.scale_log2;
 }
 
 // One 32-token unit [s0, s0 + 32) of the staged tile: two 16-token halves
 // (rows sigma(r) of half h are tokens s0 + 16 h + sigma(r)).  s0 is a
 // multiple of 32 and the unit lies inside one K group (G >= 32, packed runs
 // start on 32-token boundaries), so both halves share one K operand.
-template <int B, bool KQ, bool VQ, bool FULL>
+template <int B, int HQ, bool KQ, bool VQ, bool FULL>
 __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRec& r, int s0, int lane, WarpState& S) {
+  using SM = TcSmem<HQ>;
   constexpr int PH = 16 / B;
   const int gid = lane >> 2, tig = lane & 3;
   const int r0 = sigma(gid), r1 = sigma(gid + 8);
   uint8_t* const sm = tc_smem();
-  const uint8_t* const stage = sm + TcSmem::stages + st * kTcStageBytes;
+  const uint8_t* const stage = sm + SM::stages + st * kTcStageBytes;
   const int nv = r.n - s0;  // valid tokens from s0 (>= 32 when FULL)
   // ------------------------------------------------------------- scores
   float x[2][2];  // [half][row gid, row gid + 8]
   if constexpr (KQ) {
     const int gl = (r.kr0 + s0) >> a.log2G;
     uint32_t bq[16];
-    const float bias = build_k_operand<B>(a, stage, reinterpret_cast<const __half*>(sm + TcSmem::q + st * D * 2), r,
-                                          gl, reinterpret_cast<uint32_t*>(sm + TcSmem::ktab) + (threadIdx.x >> 5) * 128,
-                                          lane, bq);
+    const float bias = build_k_operand<B, HQ>(
+        a, stage, reinterpret_cast<const __half*>(sm + SM::q + st * HQ * D * 2), r, gl,
+        reinterpret_cast<uint32_t*>(sm + SM::ktab) + (threadIdx.x >> 5) * 128 * HQ, lane, bq);
     const uint8_t* kc = stage + r.k_off + tig * (B * 4);
     if constexpr (B == 2) {
       k_scores_packed2_b2(kc, s0, r0, r1, bq, bias, x);  // rows past the tile read stale bytes: masked below
@@ -410,10 +448,13 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
       else x[1][0] = x[1][1] = -INFINITY;
     }
   } else {
-    const uint8_t* qt = sm + TcSmem::q + st * D * 2 + tig * 64;
+    // column n = gid holds the query of head gid / 2 (HQ = 4) or of the one head
+    const int qh = HQ == 1 ? 0 : gid >> 1;
+    const uint8_t* qt = sm + SM::q + (st * HQ + qh) * D * 2 + tig * 64;
+    const uint32_t qmask = (HQ == 1 || qh < a.gq) ? 0xffffffffu : 0u;
     const uint8_t* kr = stage + r.k_off + tig * 64;
-    k_scores_ring(kr, qt, s0, r0, r1, tig, a.scale_log2, x[0][0], x[0][1]);
-    if (FULL || nv > 16) k_scores_ring(kr, qt, s0 + 16, r0, r1, tig, a.scale_log2, x[1][0], x[1][1]);
+    k_scores_ring(kr, qt, qmask, s0, r0, r1, tig, a.scale_log2, x[0][0], x[0][1]);
+    if (FULL || nv > 16) k_scores_ring(kr, qt, qmask, s0 + 16, r0, r1, tig, a.scale_log2, x[1][0], x[1][1]);
     else x[1][0] = x[1][1] = -INFINITY;
   }
   if constexpr (!FULL) {
@@ -451,33 +492,45 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
   if constexpr (VQ) {
     constexpr int RB = D * B / 8;
     constexpr int NW = B / 2;  // words per token for the thread's 16 channels
-    // column n = gid: scale (n < 4) or zero (n >= 4) of group n & 3
+    // HQ = 1: column n = gid is the scale (n < 4) or the zero (n >= 4) of
+    // group n & 3, and one all-ones MMA sums the zero columns.  HQ = 4:
+    // column n = gid is head n / 2 and group n & 1 (group 0 when d/G = 1);
+    // the scales go to the code MMAs and the zeros to the all-ones MMA.
     const int ngv = D >> a.log2G;
-    const int g = gid & 3;
     const uint16_t* sp;
+    const uint16_t* zp = nullptr;
     int stride;
-    if (g < ngv) {
-      sp = reinterpret_cast<const uint16_t*>(stage + (gid < 4 ? r.vs_off : r.vz_off)) + (s0 * ngv + g);
-      stride = ngv;
+    if constexpr (HQ == 1) {
+      const int g = gid & 3;
+      if (g < ngv) {
+        sp = reinterpret_cast<const uint16_t*>(stage + (gid < 4 ? r.vs_off : r.vz_off)) + (s0 * ngv + g);
+        stride = ngv;
+      } else {
+        sp = reinterpret_cast<const uint16_t*>(sm + SM::zero);
+        stride = 0;
+      }
     } else {
-      sp = reinterpret_cast<const uint16_t*>(sm + TcSmem::zero);
-      stride = 0;
+      const int g = ngv == 1 ? 0 : (gid & 1);
+      sp = reinterpret_cast<const uint16_t*>(stage + r.vs_off) + (s0 * ngv + g);
+      zp = reinterpret_cast<const uint16_t*>(stage + r.vz_off) + (s0 * ngv + g);
+      stride = ngv;
     }
-    uint32_t bv[2][2];
+    uint32_t bv[2][2], bz[2][2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int o = 16 * h;
-      uint16_t sa = sp[(o + ta) * stride], sb = sp[(o + tb) * stride];
-      uint16_t scc = sp[(o + tc) * stride], sd = sp[(o + td) * stride];
-      if constexpr (!FULL) {
-        // padding tokens: p = 0, and their stale scale bits must not make NaN
-        if (o + ta >= nv) sa = 0;
-        if (o + tb >= nv) sb = 0;
-        if (o + tc >= nv) scc = 0;
-        if (o + td >= nv) sd = 0;
+      const uint32_t ka = (FULL || o + ta < nv) ? 0xffffu : 0u, kb = (FULL || o + tb < nv) ? 0xffffu : 0u;
+      const uint32_t kc = (FULL || o + tc < nv) ? 0xffffu : 0u, kd = (FULL || o + td < nv) ? 0xffffu : 0u;
+      // padding tokens: p = 0, and their stale scale bits must not make NaN
+      bv[h][0] = hmul2u(pp[h][0], halves(sp[(o + ta) * stride] & ka, sp[(o + tb) * stride] & kb));
+      bv[h][1] = hmul2u(pp[h][1], halves(sp[(o + tc) * stride] & kc, sp[(o + td) * stride] & kd));
+      if constexpr (HQ != 1) {
+        bz[h][0] = hmul2u(pp[h][0], halves(zp[(o + ta) * stride] & ka, zp[(o + tb) * stride] & kb));
+        bz[h][1] = hmul2u(pp[h][1], halves(zp[(o + tc) * stride] & kc, zp[(o + td) * stride] & kd));
+      } else {
+        bz[h][0] = bv[h][0];
+        bz[h][1] = bv[h][1];
       }
-      bv[h][0] = hmul2u(pp[h][0], halves(sa, sb));
-      bv[h][1] = hmul2u(pp[h][1], halves(scc, sd));
     }
     const uint8_t* vc = stage + r.v_off + s0 * RB + gid * (NW * 4);
 #pragma unroll
@@ -505,8 +558,8 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
         }
     }
     constexpr uint32_t ONES = 0x3C003C00u;  // (1.0, 1.0)
-    mma16816(S.accz, ONES, ONES, ONES, ONES, bv[0][0], bv[0][1]);
-    mma16816(S.accz, ONES, ONES, ONES, ONES, bv[1][0], bv[1][1]);
+    mma16816(S.accz, ONES, ONES, ONES, ONES, bz[0][0], bz[0][1]);
+    mma16816(S.accz, ONES, ONES, ONES, ONES, bz[1][0], bz[1][1]);
   } else {
     // fp16 ring V: B = p in every column; A rows are the same channels as
     // for packed V, gathered from the thread's 16 channels of each token
@@ -546,12 +599,13 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
 // The 32-token units j, j + NCW, ... of one staged tile (only the last unit
 // of a tile can be partial).  Returns this warp's first unit of the next
 // tile: the units are dealt out round-robin across tiles.
-template <int B, bool KQ, bool VQ>
+template <int B, int HQ, bool KQ, bool VQ>
 __device__ __forceinline__ int run_tile(const DecodeArgs& a, int st, const TcRec& r, int j, int lane, WarpState& S) {
+  constexpr int NCW = TcCfg<HQ>::NCW;
   const int n_full = r.n >> 5, n_unit = (r.n + 31) >> 5;
-  for (; j < n_full; j += NCW) sub_unit<B, KQ, VQ, true>(a, st, r, j * 32, lane, S);
+  for (; j < n_full; j += NCW) sub_unit<B, HQ, KQ, VQ, true>(a, st, r, j * 32, lane, S);
   if (j < n_unit) {
-    sub_unit<B, KQ, VQ, false>(a, st, r, j * 32, lane, S);
+    sub_unit<B, HQ, KQ, VQ, false>(a, st, r, j * 32, lane, S);
     j += NCW;
   }
   return j - n_unit;
@@ -567,13 +621,16 @@ __device__ __forceinline__ int run_tile(const DecodeArgs& a, int st, const TcRec
 // has at least one tile, and the merger of piece k is its last warp, so a
 // warp reaching piece k + NSLOT waits (bounded) only if fewer than NSLOT
 // slots separate it from a merge still running.
-template <int B>
+template <int B, int HQ>
 __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int piece, long long T, int warp,
                              int lane, WarpState& S, volatile int* flags) {
+  using SM = TcSmem<HQ>;
+  constexpr int NCW = TcCfg<HQ>::NCW, NSLOT = TcCfg<HQ>::NSLOT;
+  constexpr int REC = D + 2;  // (o[D], m, l)
   const int gid = lane >> 2, tig = lane & 3;
-  const int slot = piece % kTcMergeSlots;
-  volatile int* owner = reinterpret_cast<volatile int*>(smem + TcSmem::slot_owner);
-  int* count = reinterpret_cast<int*>(smem + TcSmem::slot_count);
+  const int slot = piece % NSLOT;
+  volatile int* owner = reinterpret_cast<volatile int*>(smem + SM::slot_owner);
+  int* count = reinterpret_cast<int*>(smem + SM::slot_count);
   // wait until the slot serves this piece (its previous piece merged)
   if (owner[slot] != piece) {
     const long long t0 = clock64();
@@ -586,9 +643,10 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
     }
   }
   __syncwarp();
-  float* mg = reinterpret_cast<float*>(smem + TcSmem::merge) + (slot * NCW + warp) * (D + 2);
+  float* slot_base = reinterpret_cast<float*>(smem + SM::merge) + slot * NCW * HQ * REC;
+  float* mg = slot_base + (warp * HQ + (HQ == 1 ? 0 : tig)) * REC;  // this lane's head
   if (!S.vring) unscale_acc<B>(S);
-  float l = S.l;  // rows are replicated over tig: sum over gid only
+  float l = S.l;  // a lane's rows cover gid: sum over gid (lanes of one tig)
   l += __shfl_xor_sync(kFull, l, 4);
   l += __shfl_xor_sync(kFull, l, 8);
   l += __shfl_xor_sync(kFull, l, 16);
@@ -597,16 +655,23 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
     int c0, c8, p;
     v_rows<B>(gid, mt, &c0, &c8, &p);
     const int g = c0 >> a.log2G;  // c0 and c8 share their group
-    // z sum of group g: column 4 + g, held by lanes with tig = 2 + g / 2
-    const float z0 = __shfl_sync(kFull, S.accz[0], 2 + (g >> 1));
-    const float z1 = __shfl_sync(kFull, S.accz[1], 2 + (g >> 1));
-    const float zg = (g & 1) ? z1 : z0;
-    if (tig == (g >> 1)) {
+    if constexpr (HQ == 1) {
+      // z sum of group g: column 4 + g, held by lanes with tig = 2 + g / 2
+      const float z0 = __shfl_sync(kFull, S.accz[0], 2 + (g >> 1));
+      const float z1 = __shfl_sync(kFull, S.accz[1], 2 + (g >> 1));
+      const float zg = (g & 1) ? z1 : z0;
+      if (tig == (g >> 1)) {
+        mg[c0] = ((g & 1) ? S.acc[mt][1] : S.acc[mt][0]) + zg;
+        mg[c8] = ((g & 1) ? S.acc[mt][3] : S.acc[mt][2]) + zg;
+      }
+    } else {
+      // columns 2 tig + g: head tig, group g (d/G <= 2)
+      const float zg = (g & 1) ? S.accz[1] : S.accz[0];
       mg[c0] = ((g & 1) ? S.acc[mt][1] : S.acc[mt][0]) + zg;
       mg[c8] = ((g & 1) ? S.acc[mt][3] : S.acc[mt][2]) + zg;
     }
   }
-  if (lane == 0) {
+  if (gid == 0 && (HQ != 1 || tig == 0)) {
     mg[D] = S.m;
     mg[D + 1] = l;
   }
@@ -616,26 +681,31 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
   if (lane == 0) last_warp = atomicAdd(&count[slot], 1) == NCW - 1;
   if (!__shfl_sync(kFull, last_warp, 0)) return;
   __threadfence_block();
-  // this warp merges the slot: lane owns channels lane + 32 i
-  const float* m0 = reinterpret_cast<const float*>(smem + TcSmem::merge) + slot * NCW * (D + 2);
-  float M = -INFINITY;
-  for (int w = 0; w < NCW; ++w) M = fmaxf(M, m0[w * (D + 2) + D]);
-  float L = 0.f, O[D / 32];
+  // this warp merges the slot, head by head: lane owns channels lane + 32 i
+  const int nh = HQ == 1 ? 1 : a.gq;
+  float M[HQ], L[HQ], O[HQ][D / 32];
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) O[i] = 0.f;
-  for (int w = 0; w < NCW; ++w) {
-    const float* mw = m0 + w * (D + 2);
-    const float sw = (mw[D] == -INFINITY) ? 0.f : exp2f(mw[D] - M);
-    L += mw[D + 1] * sw;
+  for (int h = 0; h < HQ; ++h) {
+    M[h] = -INFINITY;
+    L[h] = 0.f;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) O[i] += mw[lane + 32 * i] * sw;
+    for (int i = 0; i < D / 32; ++i) O[h][i] = 0.f;
+    if (h >= nh) continue;
+    for (int w = 0; w < NCW; ++w) M[h] = fmaxf(M[h], slot_base[(w * HQ + h) * REC + D]);
+    for (int w = 0; w < NCW; ++w) {
+      const float* mw = slot_base + (w * HQ + h) * REC;
+      const float sw = (mw[D] == -INFINITY) ? 0.f : exp2f(mw[D] - M[h]);
+      L[h] += mw[D + 1] * sw;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) O[h][i] += mw[lane + 32 * i] * sw;
+    }
   }
   // the slot is free for piece + NSLOT
   __syncwarp();
   if (lane == 0) {
     count[slot] = 0;
     __threadfence_block();
-    owner[slot] = piece + kTcMergeSlots;
+    owner[slot] = piece + NSLOT;
   }
   const bool ok = flags[0] == 0;
   if (!ok) {
@@ -646,18 +716,26 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
   const int first = owner_cta((long long)pair * nt, T, a.n_cta);
   const int last = owner_cta((long long)pair * nt + nt - 1, T, a.n_cta);
   const int pieces = last - first + 1;
-  const size_t out_base = (size_t)pair * D;
+  const size_t out_base = (size_t)pair * nh * D;  // heads of a pair are consecutive query heads
   if (pieces == 1) {
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) a.out[out_base + lane + 32 * i] = __float2half_rn(O[i] / L);
+    for (int h = 0; h < HQ; ++h)
+      if (h < nh)
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) a.out[out_base + h * D + lane + 32 * i] = __float2half_rn(O[h][i] / L[h]);
     return;
   }
-  float* rec = a.part + ((size_t)pair * a.n_splits + (blockIdx.x - first)) * (D + 2);
+  // records [pair][piece][head][REC]
+  float* rec = a.part + ((size_t)pair * a.n_splits + (blockIdx.x - first)) * nh * REC;
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) rec[lane + 32 * i] = O[i];
-  if (lane == 0) {
-    rec[D] = M;
-    rec[D + 1] = L;
+  for (int h = 0; h < HQ; ++h) {
+    if (h >= nh) continue;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) rec[h * REC + lane + 32 * i] = O[h][i];
+    if (lane == 0) {
+      rec[h * REC + D] = M[h];
+      rec[h * REC + D + 1] = L[h];
+    }
   }
   __threadfence();
   __syncwarp();
@@ -666,31 +744,35 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
   if (lane == 0) last_in = atomicAdd(&a.counters[pair], 1) == pieces - 1;
   if (!__shfl_sync(kFull, last_in, 0)) return;
   __threadfence();
-  const float* recs = a.part + (size_t)pair * a.n_splits * (D + 2);
-  float MM = -INFINITY;
-  for (int s = 0; s < pieces; ++s) MM = fmaxf(MM, __ldcg(recs + (size_t)s * (D + 2) + D));
-  float LL = 0.f;
+  const float* recs = a.part + (size_t)pair * a.n_splits * nh * REC;
+  for (int h = 0; h < nh; ++h) {
+    float MM = -INFINITY;
+    for (int s = 0; s < pieces; ++s) MM = fmaxf(MM, __ldcg(recs + ((size_t)s * nh + h) * REC + D));
+    float LL = 0.f, OO[D / 32];
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) O[i] = 0.f;
-  for (int s = 0; s < pieces; ++s) {
-    const float* rr = recs + (size_t)s * (D + 2);
-    const float w = exp2f(__ldcg(rr + D) - MM);
-    LL += __ldcg(rr + D + 1) * w;
+    for (int i = 0; i < D / 32; ++i) OO[i] = 0.f;
+    for (int s = 0; s < pieces; ++s) {
+      const float* rr = recs + ((size_t)s * nh + h) * REC;
+      const float w = exp2f(__ldcg(rr + D) - MM);
+      LL += __ldcg(rr + D + 1) * w;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) O[i] += __ldcg(rr + lane + 32 * i) * w;
+      for (int i = 0; i < D / 32; ++i) OO[i] += __ldcg(rr + lane + 32 * i) * w;
+    }
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) a.out[out_base + h * D + lane + 32 * i] = __float2half_rn(OO[i] / LL);
   }
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) a.out[out_base + lane + 32 * i] = __float2half_rn(O[i] / LL);
   if (lane == 0) a.counters[pair] = 0;
 }
 
-template <int B>
-__global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const DecodeArgs a) {
+template <int B, int HQ>
+__global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel(const DecodeArgs a) {
+  using SM = TcSmem<HQ>;
+  constexpr int NCW = TcCfg<HQ>::NCW, NTH = TcCfg<HQ>::NTH, NSLOT = TcCfg<HQ>::NSLOT;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcSmem::bars);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::bars);
   uint64_t* empty = full + NS;
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + TcSmem::flags);
-  TcRec* recs = reinterpret_cast<TcRec*>(smem + TcSmem::rec);
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + SM::flags);
+  TcRec* recs = reinterpret_cast<TcRec*>(smem + SM::rec);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.batch * a.h_kv * a.n_tiles;  // below 2^31 (checked by the host)
@@ -707,15 +789,15 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
     }
     mbar_fence_init();
   }
-  if (tid < 16) reinterpret_cast<uint32_t*>(smem + TcSmem::zero)[tid] = 0u;
-  if (tid < kTcMergeSlots) {
-    reinterpret_cast<int*>(smem + TcSmem::slot_owner)[tid] = tid;
-    reinterpret_cast<int*>(smem + TcSmem::slot_count)[tid] = 0;
+  if (tid < 16) reinterpret_cast<uint32_t*>(smem + SM::zero)[tid] = 0u;
+  if (tid < NSLOT) {
+    reinterpret_cast<int*>(smem + SM::slot_owner)[tid] = tid;
+    reinterpret_cast<int*>(smem + SM::slot_count)[tid] = 0;
   }
   static_assert(sizeof(DecodeArgs) % 4 == 0, "word copy");
   for (int i = tid; i < (int)(sizeof(DecodeArgs) / 4); i += NTH)
-    reinterpret_cast<uint32_t*>(smem + TcSmem::args)[i] = reinterpret_cast<const uint32_t*>(&a)[i];
-  const DecodeArgs* args_s = reinterpret_cast<const DecodeArgs*>(smem + TcSmem::args);
+    reinterpret_cast<uint32_t*>(smem + SM::args)[i] = reinterpret_cast<const uint32_t*>(&a)[i];
+  const DecodeArgs* args_s = reinterpret_cast<const DecodeArgs*>(smem + SM::args);
   __syncthreads();
 
   if (warp == NCW) {
@@ -755,7 +837,7 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
           rec.v_off = ti.v_off;
           rec.vs_off = ti.vs_off;
           rec.vz_off = ti.vz_off;
-          bytes = ti.bytes + D * 2;
+          bytes = ti.bytes + (HQ == 1 ? 1 : sa.gq) * D * 2;
           bool k2 = false, v2 = false;
           for_each_tile_copy(sa, (size_t)pair, ti, [&](const void* s_, uint32_t off, uint32_t n_, int buf, int) {
             const int slot = buf < 6 ? buf : (buf == 6 ? (k2 ? 1 : 0) : (v2 ? 4 : 3));
@@ -771,13 +853,14 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
         break;
       if (lane == (j & 31)) {
         recs[st] = rec;
-        uint8_t* stage = smem + TcSmem::stages + st * kTcStageBytes;
+        uint8_t* stage = smem + SM::stages + st * kTcStageBytes;
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&full[st], bytes);
 #pragma unroll
         for (int k = 0; k < 6; ++k)
           if (nb[k]) bulk_g2s(stage + dst[k], src[k], nb[k], &full[st]);
-        bulk_g2s(smem + TcSmem::q + st * D * 2, sa.q + (size_t)pair * D, D * 2, &full[st]);
+        const int nq = HQ == 1 ? 1 : sa.gq;  // query heads of the pair (consecutive)
+        bulk_g2s(smem + SM::q + st * HQ * D * 2, sa.q + (size_t)pair * nq * D, nq * D * 2, &full[st]);
       }
       __syncwarp();
     }
@@ -807,7 +890,7 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
     const int st = it % NS;
     const uint32_t ph = (uint32_t)((it / NS) & 1);
     if (t_in_pair == a.n_tiles) {  // first tile of the next pair
-      finish_piece<B>(a, smem, cur_pair, piece++, T, warp, lane, S, flags);
+      finish_piece<B, HQ>(a, smem, cur_pair, piece++, T, warp, lane, S, flags);
       reset();
       ++cur_pair;
       t_in_pair = 0;
@@ -830,34 +913,41 @@ __global__ void __launch_bounds__(NTH, kTcCtasPerSm) decode_tc_kernel(const Deco
       r.ks_off = (uint32_t)r2.x;
       r.kz_off = (uint32_t)r2.y;
       if (r.kq) {
-        jstart = r.vq ? run_tile<B, true, true>(a, st, r, jstart, lane, S) : run_tile<B, true, false>(a, st, r, jstart, lane, S);
+        jstart = r.vq ? run_tile<B, HQ, true, true>(a, st, r, jstart, lane, S) : run_tile<B, HQ, true, false>(a, st, r, jstart, lane, S);
       } else {
-        jstart = r.vq ? run_tile<B, false, true>(a, st, r, jstart, lane, S) : run_tile<B, false, false>(a, st, r, jstart, lane, S);
+        jstart = r.vq ? run_tile<B, HQ, false, true>(a, st, r, jstart, lane, S) : run_tile<B, HQ, false, false>(a, st, r, jstart, lane, S);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
   }
-  if (ntiles > 0) finish_piece<B>(a, smem, cur_pair, piece, T, warp, lane, S, flags);
+  if (ntiles > 0) finish_piece<B, HQ>(a, smem, cur_pair, piece, T, warp, lane, S, flags);
 }
 
-template <int B>
+template <int B, int HQ>
 cudaError_t launch_tc_b(const DecodeArgs& a, cudaStream_t s) {
-  const int smem = TcSmem::total;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<B>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = TcSmem<HQ>::total;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<B, HQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<B><<<a.n_cta, NTH, smem, s>>>(a);
+  decode_tc_kernel<B, HQ><<<a.n_cta, TcCfg<HQ>::NTH, smem, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int HQ>
+cudaError_t launch_tc_hq(const DecodeArgs& a, int bits, cudaStream_t s) {
+  if (bits == 2) return launch_tc_b<2, HQ>(a, s);
+  if (bits == 4) return launch_tc_b<4, HQ>(a, s);
+  return launch_tc_b<8, HQ>(a, s);
 }
 
 }  // namespace
 
 int decode_tc_ctas_per_sm() { return kTcCtasPerSm; }
 
+// gq = 1: one query head per kv head; 2 <= gq <= 4 with d_h / G <= 2: the
+// four-head form.
 cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, cudaStream_t s) {
-  if (bits == 2) return launch_tc_b<2>(a, s);
-  if (bits == 4) return launch_tc_b<4>(a, s);
-  return launch_tc_b<8>(a, s);
+  return a.gq == 1 ? launch_tc_hq<1>(a, bits, s) : launch_tc_hq<4>(a, bits, s);
 }
 
 }  // namespace kvq

@@ -23,13 +23,10 @@ constexpr int kMhaConsumerWarps = 7;
 constexpr int kMhaStageBytes = 25600;   // staged tile data per pipeline stage
 constexpr int kMhaMaxGroups = 16;       // K scale groups one tile may touch
 constexpr int kMhaQtabBytes = kMhaMaxGroups * 4 * 36 * 4;  // scaled-query rows per stage
-// tensor-core one-query-head kernel (d_h = 128): 7 consumer warps and a
-// bulk-copy warp, 4 stages, two CTAs per SM (16 warps: 128 registers a
-// thread)
-constexpr int kTcConsumerWarps = 7;
+// tensor-core kernel (d_h = 128, one query head or 2-4 per kv head): a
+// bulk-copy warp and 6-7 consumer warps, 4 stages, two CTAs per SM
 constexpr int kTcStages = 4;
 constexpr int kTcCtasPerSm = 2;
-constexpr int kTcMergeSlots = 3;                     // pieces whose warp partials can be in flight
 constexpr int kTcStageBytes = 19456;
 constexpr int kTcMaxGroups = 8;                      // K groups one tile may touch
 
