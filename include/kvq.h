@@ -159,7 +159,7 @@ kvq_status kvq_flush_residual(kvq_cache* cache, void* stream);
 
 /* Bytes of device workspace kvq_decode_attention needs when it may split each
  * (batch, kv head) over at most max_splits CTAs (1..KVQ_MAX_SPLITS). */
-#define KVQ_MAX_SPLITS 64
+#define KVQ_MAX_SPLITS 128
 size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t max_splits);
 
 /* Zero-fill a workspace before its first use (cudaMemsetAsync).  Every later

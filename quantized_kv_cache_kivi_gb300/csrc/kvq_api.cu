@@ -223,11 +223,12 @@ kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>&
   return KVQ_OK;
 }
 
-// Splits per (batch, kv head): minimise the per-SM load model
-// ceil(pairs * s / SMs) * (1/s + f), f = fixed cost of one CTA relative to a
-// whole head's stream; ties go to fewer splits.
+// Splits per (batch, kv head): minimise the load model
+// ceil(pairs * s / slots) * (1/s + f), slots = SMs x the 2 CTAs an SM holds
+// at once (both split-K kernels fit two), f = fixed cost of one CTA relative
+// to a whole head's stream; ties go to fewer splits.
 int choose_splits(int n_pairs, int n_tiles, int max_splits) {
-  const int n_sm = sm_count();
+  const int n_sm = 2 * sm_count();
   const int cap = std::min(std::min(max_splits, n_tiles), KVQ_MAX_SPLITS);
   const double f = 0.02;
   int best = 1;

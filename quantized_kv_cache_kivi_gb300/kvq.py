@@ -24,7 +24,7 @@ KVQ_ERR_WORKSPACE = -5
 KVQ_POLICY_KIVI = 0
 KVQ_POLICY_FP16_TAIL = 1
 KVQ_MAX_SEGMENTS = 8
-KVQ_MAX_SPLITS = 64
+KVQ_MAX_SPLITS = 128
 
 
 class kvq_segment(ctypes.Structure):

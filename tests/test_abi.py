@@ -104,7 +104,12 @@ def test_workspace_size_arithmetic(L):
     fixed = 256 + 256  # header + counters rounded to 256 bytes
     assert L.kvq_workspace_bytes(ctypes.byref(c), 1) == fixed
     assert L.kvq_workspace_bytes(ctypes.byref(c), 8) == fixed + pairs * 8 * gq * (d + 2) * 4
-    assert L.kvq_workspace_bytes(ctypes.byref(c), 1000) == fixed + pairs * 64 * gq * (d + 2) * 4
+    # clamped to KVQ_MAX_SPLITS (read from the header)
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kvq.h")).read()
+    cap = int(re.search(r"#define KVQ_MAX_SPLITS (\d+)", hdr).group(1))
+    assert cap == kvq.KVQ_MAX_SPLITS
+    assert L.kvq_workspace_bytes(ctypes.byref(c), 1000) == fixed + pairs * cap * gq * (d + 2) * 4
 
 
 def test_status_strings(L):
