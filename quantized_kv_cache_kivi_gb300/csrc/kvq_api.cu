@@ -212,7 +212,13 @@ kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>&
     const int nt = (len + r.tile - 1) / r.tile;
     for (int t = 0; t < nt; ++t) {
       const int n = std::min(r.tile, len - t * r.tile);
-      tile_cost.push_back(tile_bytes(n, kb, vb, c->d_h, c->group));
+      // bytes streamed plus the CUDA-core work of the general kernel (every
+      // token costs gq dot products over d channels whatever its width), in
+      // byte equivalents: with several query heads the work dominates, and
+      // splitting by bytes alone would give the 2-bit splits three times the
+      // tokens of the 8-bit ones
+      const int work = kern == K_GENERAL ? n * gq * c->d_h / 2 : 0;
+      tile_cost.push_back(tile_bytes(n, kb, vb, c->d_h, c->group) + work);
     }
     a.n_tiles += nt;
     oi += len;
@@ -244,31 +250,39 @@ int choose_splits(int n_pairs, int n_tiles, int max_splits) {
   return best;
 }
 
-// CTA owning global tile g when T tiles are cut into N equal contiguous
-// ranges [floor(i T / N), floor((i + 1) T / N)) (the tensor-core kernel's
-// stream-K split; the kernel uses the same formula).
-long long tc_owner(long long g, long long T, long long N) { return ((g + 1) * N + T - 1) / T - 1; }
-
-// Bound on the ranges that cover one pair, for N ranges over n_pairs x
-// n_tiles tiles: every range holds at least floor(T / N) tiles.
-int tc_max_pieces(int n_pairs, int n_tiles, int N) {
+// Most partial records any pair gets from the stream-K ranges of N CTAs
+// with a first wave of nf (kvq::tc_begin): the ranges that meet the pair.
+int tc_max_pieces(int n_pairs, int n_tiles, int N, int nf) {
   const long long T = (long long)n_pairs * n_tiles;
-  const long long per = T / N;
-  if (T % N == 0 && per % n_tiles == 0) return 1;  // ranges are whole pairs
-  return (int)std::min<long long>(N, (n_tiles - 1 + per - 1) / per + 1);
+  std::vector<int> pieces(n_pairs, 0);
+  for (int i = 0; i < N; ++i) {
+    const long long b0 = kvq::tc_begin(i, N, nf, T), b1 = kvq::tc_begin(i + 1, N, nf, T);
+    if (b1 <= b0) continue;
+    // the kernel finds a pair's first and last range with tc_owner
+    if (kvq::tc_owner(b0, N, nf, T) != i || kvq::tc_owner(b1 - 1, N, nf, T) != i) return INT_MAX;
+    for (long long p = b0 / n_tiles; p <= (b1 - 1) / n_tiles; ++p) ++pieces[p];
+  }
+  return *std::max_element(pieces.begin(), pieces.end());
 }
 
 // Persistent grid of the tensor-core kernel: as many CTAs as fit on the GPU
 // at once (never more than tiles), fewer while some pair could be cut into
-// more partial records than the workspace holds; one CTA per pair needs none.
-int tc_grid(int n_pairs, int n_tiles, int records) {
+// more partial records than the workspace holds.  The first wave is one CTA
+// per SM; a grid that fits one wave has equal ranges, and so has the
+// fallback of one CTA per pair, which needs no records.
+int tc_grid(int n_pairs, int n_tiles, int records, int* n_first) {
   const long long T = (long long)n_pairs * n_tiles;
   const int cap = std::max(records, 1);
-  int N = (int)std::min<long long>(T, (long long)sm_count() * kvq::decode_tc_ctas_per_sm());
-  while (tc_max_pieces(n_pairs, n_tiles, N) > cap) {
-    if (N <= n_pairs) return n_pairs;
+  const int n_sm = sm_count();
+  int N = (int)std::min<long long>(T, (long long)n_sm * kvq::decode_tc_ctas_per_sm());
+  while (tc_max_pieces(n_pairs, n_tiles, N, std::min(N, n_sm)) > cap) {
+    if (N <= n_pairs) {
+      *n_first = n_pairs;
+      return n_pairs;
+    }
     N = std::max(n_pairs, N - std::max(1, N / 32));
   }
+  *n_first = std::min(N, n_sm);
   return N;
 }
 
@@ -623,8 +637,8 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
       return fail(KVQ_ERR_UNSUPPORTED, "more than 2^31 tiles");
     // stream-K: a.n_splits is the record stride per pair
     a.n_splits = std::max(1, ws_splits);
-    a.n_cta = tc_grid(n_pairs, a.n_tiles, ws_splits);
-    if (tc_max_pieces(n_pairs, a.n_tiles, a.n_cta) > a.n_splits)
+    a.n_cta = tc_grid(n_pairs, a.n_tiles, ws_splits, &a.n_first);
+    if (tc_max_pieces(n_pairs, a.n_tiles, a.n_cta, a.n_first) > a.n_splits)
       return fail(KVQ_ERR_UNSUPPORTED, "stream-K planning failed");
   }
   const int S = kern == K_TC ? 1 : choose_splits(n_pairs, a.n_tiles, std::max(1, ws_splits));

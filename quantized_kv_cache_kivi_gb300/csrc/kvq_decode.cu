@@ -401,20 +401,40 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
   __syncthreads();
   if (!flag_s[1]) return;
   __threadfence();
+  // Merge of the splits' records.  First the weight of each (split, head),
+  // 2^(m_s - M) / L with M the max and L the weighted sum of l over the
+  // splits, one warp per head; then every output element is a sum of
+  // independent loads (the records are cold in L2, so a chain of dependent
+  // loads per element would cost a round trip per split).
   const float* recs = a.part + (size_t)pair * a.n_splits * a.gq * (D + 2);
+  float* wts = o_s + kMaxGq * D;  // [n_splits][gq]
+  static_assert((NT / 32 + 2 * kMaxGq) * 128 + KVQ_MAX_SPLITS * kMaxGq <= kStages * kStageBytes / 4,
+                "merge scratch inside the drained stages");
+  for (int h = warp; h < a.gq; h += NT / 32) {
+    float M = -INFINITY;
+    for (int sp = lane; sp < a.n_splits; sp += 32)
+      M = fmaxf(M, __ldcg(recs + ((size_t)sp * a.gq + h) * (D + 2) + D));
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int sp = lane; sp < a.n_splits; sp += 32) {
+      const float* r = recs + ((size_t)sp * a.gq + h) * (D + 2);
+      const float w = exp2f(__ldcg(r + D) - M);
+      wts[sp * a.gq + h] = w;
+      L += __ldcg(r + D + 1) * w;
+    }
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    __syncwarp();
+    const float inv = 1.f / L;
+    for (int sp = lane; sp < a.n_splits; sp += 32) wts[sp * a.gq + h] *= inv;
+  }
+  __syncthreads();
   for (int i = tid; i < a.gq * D; i += NT) {
     const int h = i / D, c = i % D;
-    float M = -INFINITY;
-    for (int s = 0; s < a.n_splits; ++s)
-      M = fmaxf(M, __ldcg(recs + ((size_t)s * a.gq + h) * (D + 2) + D));
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < a.n_splits; ++s) {
-      const float* r = recs + ((size_t)s * a.gq + h) * (D + 2);
-      const float w = exp2f(__ldcg(r + D) - M);
-      L += __ldcg(r + D + 1) * w;
-      O += __ldcg(r + c) * w;
-    }
-    a.out[out_base + i] = __float2half_rn(O / L);
+    float O = 0.f;
+#pragma unroll 8
+    for (int sp = 0; sp < a.n_splits; ++sp)
+      O += __ldcg(recs + ((size_t)sp * a.gq + h) * (D + 2) + c) * wts[sp * a.gq + h];
+    a.out[out_base + i] = __float2half_rn(O);
   }
   if (tid == 0) a.counters[pair] = 0;
 }

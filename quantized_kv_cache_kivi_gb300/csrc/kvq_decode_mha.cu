@@ -331,11 +331,15 @@ __global__ void __launch_bounds__(NTH, 2) decode_mha_kernel(const DecodeArgs a) 
     // were issued kStages-1 steps earlier), release it to the consumers, then
     // issue the copies of tile it + kStages - 1 into the stage that tile
     // it - 1 used.  Loads stay kStages - 1 tiles ahead of the consumers.
+    int nissued = 0;
     auto issue = [&](int j) {
       const int st = j % kStages;
-      if (j >= kStages &&
-          !wait_or_abort(&empty[st], (uint32_t)(((j / kStages) & 1) ^ 1), abort_flag))
-        return false;
+      if (j >= kStages) {
+        if (!wait_or_abort(&empty[st], (uint32_t)(((j / kStages) & 1) ^ 1), abort_flag)) return false;
+        // consumers that gave up release a stage without waiting for it
+        mbar_drain_bounded(&full[st], (uint32_t)(((j / kStages) & 1) ^ 1));
+      }
+      nissued = j + 1;
       if (lane == 0) {
         uint8_t* stage = smem + MhaSmem::stages + st * kMhaStageBytes;
         const TileInfo ti = tile_info(a, t_begin + j);
@@ -410,6 +414,9 @@ __global__ void __launch_bounds__(NTH, 2) decode_mha_kernel(const DecodeArgs a) 
       if (lane == 0) mbar_arrive(&ready[st]);
       if (it + kStages - 1 < ntiles) ok = issue(it + kStages - 1);
     }
+    // no copy of this block may still be in flight when it exits
+    for (int j = nissued > kStages ? nissued - kStages : 0; j < nissued; ++j)
+      mbar_drain_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1));
     return;
   }
 
@@ -502,18 +509,34 @@ __global__ void __launch_bounds__(NTH, 2) decode_mha_kernel(const DecodeArgs a) 
   asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
   if (!abort_flag[1]) return;
   __threadfence();
+  // Merge of the splits' records: the weights 2^(m_s - M) / L of the splits
+  // first (one warp, into the merge area the warps no longer read), then each
+  // channel as a sum of independent loads.
   const float* recs = a.part + (size_t)pair * a.n_splits * (D + 2);
-  for (int c = tid; c < D; c += NCW * 32) {
+  float* wts = reinterpret_cast<float*>(smem + MhaSmem::merge);
+  static_assert(KVQ_MAX_SPLITS <= NCW * (128 + 4), "split weights fit the merge area");
+  if (warp == 0) {
     float MM = -INFINITY;
-    for (int s = 0; s < a.n_splits; ++s) MM = fmaxf(MM, __ldcg(recs + (size_t)s * (D + 2) + D));
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < a.n_splits; ++s) {
-      const float* rr = recs + (size_t)s * (D + 2);
+    for (int sp = lane; sp < a.n_splits; sp += 32) MM = fmaxf(MM, __ldcg(recs + (size_t)sp * (D + 2) + D));
+    for (int off = 16; off > 0; off >>= 1) MM = fmaxf(MM, __shfl_xor_sync(0xffffffffu, MM, off));
+    float L = 0.f;
+    for (int sp = lane; sp < a.n_splits; sp += 32) {
+      const float* rr = recs + (size_t)sp * (D + 2);
       const float w = exp2f(__ldcg(rr + D) - MM);
+      wts[sp] = w;
       L += __ldcg(rr + D + 1) * w;
-      O += __ldcg(rr + c) * w;
     }
-    a.out[out_base + c] = __float2half_rn(O / L);
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    __syncwarp();
+    const float inv = 1.f / L;
+    for (int sp = lane; sp < a.n_splits; sp += 32) wts[sp] *= inv;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
+  for (int c = tid; c < D; c += NCW * 32) {
+    float O = 0.f;
+#pragma unroll 8
+    for (int sp = 0; sp < a.n_splits; ++sp) O += __ldcg(recs + (size_t)sp * (D + 2) + c) * wts[sp];
+    a.out[out_base + c] = __float2half_rn(O);
   }
   if (tid == 0) a.counters[pair] = 0;
 }

@@ -213,12 +213,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 
-// CTA owning global tile g when T tiles are cut into N equal ranges
-// [floor(i T / N), floor((i + 1) T / N)).
-__device__ __forceinline__ int owner_cta(long long g, long long T, int N) {
-  return (int)(((g + 1) * N + T - 1) / T) - 1;
-}
-
 // Per-warp online-softmax state.  acc holds, for the channel rows of m-tile
 // mt, D = sum_t B[t][n] A[c][t] (packed V: carrying 2^(p - 24) until the first
 // ring-V sub-tile or the end); accz columns 4.. hold sum_t p_t z_t(n-4).
@@ -713,8 +707,8 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
     return;
   }
   const long long nt = a.n_tiles;
-  const int first = owner_cta((long long)pair * nt, T, a.n_cta);
-  const int last = owner_cta((long long)pair * nt + nt - 1, T, a.n_cta);
+  const int first = tc_owner((long long)pair * nt, a.n_cta, a.n_first, T);
+  const int last = tc_owner((long long)pair * nt + nt - 1, a.n_cta, a.n_first, T);
   const int pieces = last - first + 1;
   const size_t out_base = (size_t)pair * nh * D;  // heads of a pair are consecutive query heads
   if (pieces == 1) {
@@ -776,8 +770,8 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.batch * a.h_kv * a.n_tiles;  // below 2^31 (checked by the host)
-  const int g_begin = (int)((long long)blockIdx.x * T / a.n_cta);
-  const int g_end = (int)((long long)(blockIdx.x + 1) * T / a.n_cta);
+  const int g_begin = tc_begin(blockIdx.x, a.n_cta, a.n_first, T);
+  const int g_end = tc_begin(blockIdx.x + 1, a.n_cta, a.n_first, T);
   const int ntiles = g_end - g_begin;
 
   if (tid == 0) {
@@ -814,6 +808,7 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
     uint32_t bytes = 0;
     const void* src[6];
     uint32_t dst[6], nb[6];
+    int nissued = 0;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % NS;
       if ((j & 31) == 0) {
@@ -849,8 +844,12 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
           });
         }
       }
-      if (j >= NS && __any_sync(kFull, !wait_or_abort<true>(&empty[st], (uint32_t)(((j / NS) & 1) ^ 1), flags)))
-        break;
+      if (j >= NS) {
+        if (__any_sync(kFull, !wait_or_abort<true>(&empty[st], (uint32_t)(((j / NS) & 1) ^ 1), flags))) break;
+        // consumers that gave up release a stage without waiting for it
+        mbar_drain_bounded(&full[st], (uint32_t)(((j / NS) & 1) ^ 1));
+      }
+      nissued = j + 1;
       if (lane == (j & 31)) {
         recs[st] = rec;
         uint8_t* stage = smem + SM::stages + st * kTcStageBytes;
@@ -864,6 +863,8 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
       }
       __syncwarp();
     }
+    // no copy of this block may still be in flight when it exits
+    for (int j = nissued > NS ? nissued - NS : 0; j < nissued; ++j) mbar_drain_bounded(&full[j % NS], (uint32_t)((j / NS) & 1));
     return;
   }
 

@@ -69,6 +69,7 @@ struct DecodeArgs {
   int n_tiles;   // tiles per (batch, kv head)
   int n_splits;  // CTAs per (batch, kv head); tensor-core kernel: records per pair
   int n_cta;     // tensor-core kernel: CTAs of the persistent grid
+  int n_first;   // tensor-core kernel: CTAs of the first wave (one per SM)
   int split_tile[KVQ_MAX_SPLITS + 1];
   const __half* q;
   __half* out;
@@ -147,6 +148,29 @@ struct TileInfo {
 };
 
 __host__ __device__ inline uint32_t align16u(uint32_t x) { return (x + 15u) & ~15u; }
+
+// Stream-K ranges of the tensor-core kernel.  CTA i of N takes the tiles
+// [tc_begin(i), tc_begin(i + 1)) of the T tiles of all pairs.  Two CTAs share
+// an SM; the one placed first (blockIdx below n_first, one per SM) gets the
+// larger share of issue slots and finishes its range sooner, so its range
+// is weighted kTcWave1 against kTcWave2 for the others, which evens out the
+// finish times of the two.
+constexpr long long kTcWave1 = 8, kTcWave2 = 7;
+__host__ __device__ inline long long tc_weight(int i, int n_first) {
+  return i <= n_first ? kTcWave1 * i : kTcWave1 * n_first + kTcWave2 * (i - n_first);
+}
+__host__ __device__ inline int tc_begin(int i, int N, int n_first, long long T) {
+  return (int)(T * tc_weight(i, n_first) / tc_weight(N, n_first));
+}
+// The CTA whose range holds tile g (0 <= g < T): the last i with
+// tc_begin(i) <= g, i.e. T W(i) < (g + 1) W(N), so W(i) <= x below; empty
+// ranges never own a tile.
+__host__ __device__ inline int tc_owner(long long g, int N, int n_first, long long T) {
+  const long long x = ((g + 1) * tc_weight(N, n_first) - 1) / T;
+  const long long i =
+      x < kTcWave1 * n_first ? x / kTcWave1 : n_first + (x - kTcWave1 * n_first) / kTcWave2;
+  return (int)(i < N - 1 ? i : N - 1);
+}
 
 __host__ __device__ inline TileInfo tile_info(const DecodeArgs& a, int t) {
   int r = 0;
