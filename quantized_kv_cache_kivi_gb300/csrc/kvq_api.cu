@@ -257,7 +257,8 @@ int tc_max_pieces(int n_pairs, int n_tiles, int N, int nf) {
   std::vector<int> pieces(n_pairs, 0);
   for (int i = 0; i < N; ++i) {
     const long long b0 = kvq::tc_begin(i, N, nf, T), b1 = kvq::tc_begin(i + 1, N, nf, T);
-    if (b1 <= b0) continue;
+    // an empty range would count as a piece that never reports
+    if (b1 <= b0) return INT_MAX;
     // the kernel finds a pair's first and last range with tc_owner
     if (kvq::tc_owner(b0, N, nf, T) != i || kvq::tc_owner(b1 - 1, N, nf, T) != i) return INT_MAX;
     for (long long p = b0 / n_tiles; p <= (b1 - 1) / n_tiles; ++p) ++pieces[p];

@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(NTH, 2) decode_mha_kernel(const DecodeArgs a) 
       if (j >= kStages) {
         if (!wait_or_abort(&empty[st], (uint32_t)(((j / kStages) & 1) ^ 1), abort_flag)) return false;
         // consumers that gave up release a stage without waiting for it
-        mbar_drain_bounded(&full[st], (uint32_t)(((j / kStages) & 1) ^ 1));
+        if (!mbar_drain_bounded(&full[st], (uint32_t)(((j / kStages) & 1) ^ 1)) && lane == 0) atomicExch(a.err, 1);
       }
       nissued = j + 1;
       if (lane == 0) {
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(NTH, 2) decode_mha_kernel(const DecodeArgs a) 
     }
     // no copy of this block may still be in flight when it exits
     for (int j = nissued > kStages ? nissued - kStages : 0; j < nissued; ++j)
-      mbar_drain_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1));
+      if (!mbar_drain_bounded(&full[j % kStages], (uint32_t)((j / kStages) & 1)) && lane == 0) atomicExch(a.err, 1);
     return;
   }
 

@@ -847,7 +847,7 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
       if (j >= NS) {
         if (__any_sync(kFull, !wait_or_abort<true>(&empty[st], (uint32_t)(((j / NS) & 1) ^ 1), flags))) break;
         // consumers that gave up release a stage without waiting for it
-        mbar_drain_bounded(&full[st], (uint32_t)(((j / NS) & 1) ^ 1));
+        if (!mbar_drain_bounded(&full[st], (uint32_t)(((j / NS) & 1) ^ 1)) && lane == 0) atomicExch(sa.err, 1);
       }
       nissued = j + 1;
       if (lane == (j & 31)) {
@@ -864,7 +864,8 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
       __syncwarp();
     }
     // no copy of this block may still be in flight when it exits
-    for (int j = nissued > NS ? nissued - NS : 0; j < nissued; ++j) mbar_drain_bounded(&full[j % NS], (uint32_t)((j / NS) & 1));
+    for (int j = nissued > NS ? nissued - NS : 0; j < nissued; ++j)
+      if (!mbar_drain_bounded(&full[j % NS], (uint32_t)((j / NS) & 1)) && lane == 0) atomicExch(sa.err, 1);
     return;
   }
 

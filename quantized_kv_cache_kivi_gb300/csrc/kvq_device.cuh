@@ -123,9 +123,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // Bounded wait that ignores any abort flag (about 2^28 SM clocks): a warp
 // that issued bulk copies waits with it for them to land before their stage
 // is reused and before its block exits, aborted or not.
-__device__ __forceinline__ void mbar_drain_bounded(uint64_t* bar, uint32_t parity) {
+// Returns false if the phase did not complete in time.
+__device__ __forceinline__ bool mbar_drain_bounded(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity) && clock64() - t0 < (1ll << 28)) __nanosleep(128);
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 >= (1ll << 28)) return false;
+    __nanosleep(128);
+  }
+  return true;
 }
 
 // global -> shared bulk copy completing on an mbarrier (16-byte aligned

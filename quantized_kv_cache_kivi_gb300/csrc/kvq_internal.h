@@ -151,11 +151,13 @@ __host__ __device__ inline uint32_t align16u(uint32_t x) { return (x + 15u) & ~1
 
 // Stream-K ranges of the tensor-core kernel.  CTA i of N takes the tiles
 // [tc_begin(i), tc_begin(i + 1)) of the T tiles of all pairs.  Two CTAs share
-// an SM; the one placed first (blockIdx below n_first, one per SM) gets the
-// larger share of issue slots and finishes its range sooner, so its range
-// is weighted kTcWave1 against kTcWave2 for the others, which evens out the
-// finish times of the two.
-constexpr long long kTcWave1 = 8, kTcWave2 = 7;
+// an SM, and the one placed first (blockIdx below n_first, one per SM) gets
+// the larger share of issue slots; its range can be weighted kTcWave1
+// against kTcWave2 for the others.  Measured: 8:7 evened the two CTAs of an
+// SM at one query head per kv head but lost more with four, and a pool of
+// chunks claimed at run time lost everywhere (a piece per chunk costs a
+// merge), so the ranges stay equal.
+constexpr long long kTcWave1 = 1, kTcWave2 = 1;
 __host__ __device__ inline long long tc_weight(int i, int n_first) {
   return i <= n_first ? kTcWave1 * i : kTcWave1 * n_first + kTcWave2 * (i - n_first);
 }

@@ -130,16 +130,21 @@ class KiviPair:
             out[(b, h)] = oracle.attention_head(K, V, qh, self.gpu.c.sm_scale)
         return out
 
-    def gpu_attention(self, q, ws_splits=kvq.KVQ_MAX_SPLITS):
+    def gpu_attention(self, q, ws_splits=kvq.KVQ_MAX_SPLITS, ws=None):
         import torch
         qd = to_dev(q)
         out = torch.empty_like(qd)
-        ws = torch.zeros(kvq.kvq_workspace_bytes(self.gpu, ws_splits), dtype=torch.uint8,
-                         device="cuda")
+        if ws is None:
+            ws = self.workspace(ws_splits)
         kvq.kvq_decode_attention(self.gpu, qd, out, ws)
         torch.cuda.synchronize()
         assert kvq.kvq_workspace_error(ws) == 0
         return out.cpu().numpy()
+
+    def workspace(self, ws_splits=kvq.KVQ_MAX_SPLITS):
+        import torch
+        return torch.zeros(kvq.kvq_workspace_bytes(self.gpu, ws_splits), dtype=torch.uint8,
+                           device="cuda")
 
     def attention_error(self, q, **kw):
         gq = self.h_q // self.h_kv

@@ -116,6 +116,24 @@ def test_attention_parity(d, G, R, bits, gq):
         assert pair.attention_error(_q(6 + t, B, H * gq, d)) < TOL
 
 
+@pytest.mark.parametrize("G,bits,gq,ws_splits", [(32, 2, 1, None), (64, 4, 4, None), (32, 2, 1, 3)])
+def test_attention_many_pairs_repeatable(G, bits, gq, ws_splits):
+    """Many (batch, kv head) pairs cut into stream-K ranges, with the default
+    and a three-record workspace: every head matches the oracle, and repeated
+    calls on one workspace give identical outputs (the per-pair counters are
+    rewound by each launch's merges)."""
+    B, H, d, R = 4, 8, 128, 128
+    pair = KiviPair(B, H, H * gq, d, G, R, bits, cap=1024)
+    K, V = kv(41 + gq, B, H, 700, d)
+    pair.prefill(K, V)
+    q = _q(9, B, H * gq, d)
+    ws = pair.workspace() if ws_splits is None else pair.workspace(ws_splits)
+    assert pair.attention_error(q, ws=ws) < TOL
+    first = pair.gpu_attention(q, ws=ws)
+    for _ in range(3):
+        assert np.array_equal(pair.gpu_attention(q, ws=ws), first)
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 64])
 def test_attention_split_counts(splits):
     """The merge of split partials gives the same result for any split count."""
