@@ -250,41 +250,79 @@ int choose_splits(int n_pairs, int n_tiles, int max_splits) {
   return best;
 }
 
-// Most partial records any pair gets from the stream-K ranges of N CTAs
-// with a first wave of nf (kvq::tc_begin): the ranges that meet the pair.
-int tc_max_pieces(int n_pairs, int n_tiles, int N, int nf) {
-  const long long T = (long long)n_pairs * n_tiles;
-  std::vector<int> pieces(n_pairs, 0);
-  for (int i = 0; i < N; ++i) {
-    const long long b0 = kvq::tc_begin(i, N, nf, T), b1 = kvq::tc_begin(i + 1, N, nf, T);
-    // an empty range would count as a piece that never reports
-    if (b1 <= b0) return INT_MAX;
-    // the kernel finds a pair's first and last range with tc_owner
-    if (kvq::tc_owner(b0, N, nf, T) != i || kvq::tc_owner(b1 - 1, N, nf, T) != i) return INT_MAX;
-    for (long long p = b0 / n_tiles; p <= (b1 - 1) / n_tiles; ++p) ++pieces[p];
+// Stream-K ranges of the tensor-core kernel.  Tile t of a pair costs its
+// 32-token units plus a quarter unit of per-tile work, the same in every
+// pair; CTA i's range starts at the first tile whose cost prefix reaches
+// i / N of the total, kept non-empty.  Returns the most ranges that meet one
+// pair (its partial records).
+int tc_ranges(const kvq::DecodeArgs& a, int n_pairs, int N, int* bound) {
+  const int nt = a.n_tiles;
+  std::vector<long long> pre(nt + 1, 0);
+  for (int r = 0, t = 0; t < nt; ++t) {  // tokens of tile t from the runs alone
+    while (r + 1 < a.n_runs && a.runs[r + 1].tile0 <= t) ++r;
+    const kvq::Run& run = a.runs[r];
+    const int n = std::min(run.tile, run.len - (t - run.tile0) * run.tile);
+    pre[t + 1] = pre[t] + 4 * ((n + 31) / 32) + 1;
   }
-  return *std::max_element(pieces.begin(), pieces.end());
+  const long long per_pair = pre[nt], T = (long long)n_pairs * nt;
+  const long long total = per_pair * n_pairs;
+  auto prefix = [&](long long g) { return (g / nt) * per_pair + pre[g % nt]; };
+  bound[0] = 0;
+  for (int i = 1; i < N; ++i) {
+    const long long target = total * i / N;
+    long long lo = 0, hi = T;  // first g with prefix(g) >= target
+    while (lo < hi) {
+      const long long mid = (lo + hi) / 2;
+      if (prefix(mid) >= target) hi = mid;
+      else lo = mid + 1;
+    }
+    lo = std::max<long long>(lo, bound[i - 1] + 1);
+    lo = std::min<long long>(lo, T - (N - i));
+    bound[i] = (int)lo;
+  }
+  bound[N] = (int)T;
+  // ranges meeting pair p: 1 + the range starts strictly inside it
+  int most = 1, run = 1;
+  long long run_pair = -1;
+  for (int i = 1; i < N; ++i) {
+    if (bound[i] % nt == 0) continue;
+    const long long p = bound[i] / nt;
+    run = p == run_pair ? run + 1 : 2;
+    run_pair = p;
+    most = std::max(most, run);
+  }
+  return most;
 }
 
 // Persistent grid of the tensor-core kernel: as many CTAs as fit on the GPU
 // at once (never more than tiles), fewer while some pair could be cut into
-// more partial records than the workspace holds.  The first wave is one CTA
-// per SM; a grid that fits one wave has equal ranges, and so has the
-// fallback of one CTA per pair, which needs no records.
-int tc_grid(int n_pairs, int n_tiles, int records, int* n_first) {
-  const long long T = (long long)n_pairs * n_tiles;
+// more partial records than the workspace holds; one CTA per pair needs no
+// records.  Up to kTcMaxPieces records per pair, the last CTA of the pair
+// merges them (one warp); beyond, a launch of its own does.
+constexpr int kTcMaxPieces = 16;
+
+kvq_status tc_grid(kvq::DecodeArgs& a, int n_pairs, int records) {
+  const long long T = (long long)n_pairs * a.n_tiles;
   const int cap = std::max(records, 1);
-  const int n_sm = sm_count();
-  int N = (int)std::min<long long>(T, (long long)n_sm * kvq::decode_tc_ctas_per_sm());
-  while (tc_max_pieces(n_pairs, n_tiles, N, std::min(N, n_sm)) > cap) {
+  long long N = std::min<long long>(T, (long long)sm_count() * kvq::decode_tc_ctas_per_sm());
+  N = std::min<long long>(N, kvq::kTcMaxCtas);
+  N = std::min<long long>(N, std::max<long long>(n_pairs, (long long)n_pairs * (cap - 1)));
+  a.tc_defer = 0;
+  while (true) {
+    const int most = tc_ranges(a, n_pairs, (int)N, a.tc_bound);
+    a.tc_defer = most > kTcMaxPieces;
+    if (most <= cap) break;
     if (N <= n_pairs) {
-      *n_first = n_pairs;
-      return n_pairs;
+      a.n_cta = n_pairs;  // one pair per CTA
+      a.tc_whole = 1;
+      a.tc_defer = 0;
+      return KVQ_OK;
     }
-    N = std::max(n_pairs, N - std::max(1, N / 32));
+    N = std::max<long long>(n_pairs, N - std::max<long long>(1, N / 32));
   }
-  *n_first = std::min(N, n_sm);
-  return N;
+  a.n_cta = (int)N;
+  a.tc_whole = 0;
+  return KVQ_OK;
 }
 
 // Walk every tile of the first and the last (batch, kv head) through the same
@@ -617,15 +655,38 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   std::vector<int> cost;
   // one query head per kv head, one segment, each lane's channel quarter
   // inside one V group: the specialised kernel
-  int kern = K_GENERAL;
-  if (gq == 1 && cache->n_seg == 1 && cache->group >= cache->d_h / 4)
+  int kern = K_GENERAL, form = 0;
+  if (gq == 1 && cache->n_seg == 1 && cache->group >= cache->d_h / 4) {
     kern = cache->d_h == 128 ? K_TC : K_MHA;
-  // 2-4 query heads per kv head, at most two V groups per token: the
-  // tensor-core kernel's four-head form
-  else if (gq >= 2 && gq <= 4 && cache->n_seg == 1 && cache->d_h == 128 && cache->group >= 64)
+    form = 1;
+  } else if (gq >= 2 && gq <= 4 && cache->n_seg == 1 && cache->d_h == 128 && cache->group >= 64) {
+    // 2-4 query heads per kv head, at most two V groups per token: the
+    // tensor-core kernel's four-head form
     kern = K_TC;
+    form = 4;
+  } else if (gq <= kvq::kMaxGq && cache->d_h == 128 && cache->group >= 32) {
+    // up to 8 query heads, any segments: the eight-head form, if every tile
+    // is K and V packed at one width, packed K with ring V, or ring only
+    kern = K_TC;
+    form = 8;
+  }
   st = plan_decode(cache, a, cost, kern);
   if (st != KVQ_OK) return st;
+  if (form == 8) {
+    bool ok = true;
+    for (int i = 0; i < a.n_runs; ++i) {
+      const kvq::Run& r = a.runs[i];
+      if (r.seg_k < 0 ? r.seg_v >= 0
+                      : r.seg_v >= 0 && cache->seg[r.seg_k].bits != cache->seg[r.seg_v].bits)
+        ok = false;
+    }
+    if (!ok) {
+      kern = K_GENERAL;
+      form = 0;
+      st = plan_decode(cache, a, cost, kern);
+      if (st != KVQ_OK) return st;
+    }
+  }
   if (a.n_tiles == 0) {
     const size_t bytes = (size_t)cache->batch * cache->h_q * cache->d_h * 2;
     const cudaError_t e = cudaMemsetAsync(out, 0, bytes, s);
@@ -638,9 +699,8 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
       return fail(KVQ_ERR_UNSUPPORTED, "more than 2^31 tiles");
     // stream-K: a.n_splits is the record stride per pair
     a.n_splits = std::max(1, ws_splits);
-    a.n_cta = tc_grid(n_pairs, a.n_tiles, ws_splits, &a.n_first);
-    if (tc_max_pieces(n_pairs, a.n_tiles, a.n_cta, a.n_first) > a.n_splits)
-      return fail(KVQ_ERR_UNSUPPORTED, "stream-K planning failed");
+    st = tc_grid(a, n_pairs, ws_splits);
+    if (st != KVQ_OK) return st;
   }
   const int S = kern == K_TC ? 1 : choose_splits(n_pairs, a.n_tiles, std::max(1, ws_splits));
   // split boundaries with equal byte cost: split k ends at the first tile
@@ -683,9 +743,10 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   a.part = reinterpret_cast<float*>(w + ws_fixed(n_pairs));
   st = verify_decode_plan(cache, a, n_pairs, kern);
   if (st != KVQ_OK) return st;
-  const cudaError_t e = kern == K_TC    ? kvq::launch_decode_tc(a, cache->seg[0].bits, s)
-                        : kern == K_MHA ? kvq::launch_decode_mha(a, n_pairs, cache->seg[0].bits, s)
-                                        : kvq::launch_decode(a, n_pairs, s);
+  cudaError_t e = kern == K_TC    ? kvq::launch_decode_tc(a, cache->seg[0].bits, form, s)
+                  : kern == K_MHA ? kvq::launch_decode_mha(a, n_pairs, cache->seg[0].bits, s)
+                                  : kvq::launch_decode(a, n_pairs, s);
+  if (e == cudaSuccess && kern == K_TC && a.tc_defer) e = kvq::launch_decode_tc_merge(a, n_pairs, s);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "decode launch");
 }
 

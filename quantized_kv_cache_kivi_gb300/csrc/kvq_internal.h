@@ -11,6 +11,7 @@
 namespace kvq {
 
 constexpr int kMaxRuns = 20;        // token runs of uniform (K source, V source)
+constexpr int kTcMaxCtas = 512;      // tensor-core kernel: CTAs of the persistent grid, at most
 constexpr int kMaxGq = 8;           // query heads per kv head handled by one CTA
 constexpr int kDecodeThreads = 256; // threads of a decode CTA
 constexpr int kStageBytes = 20480;  // one pipeline stage of staged tile data
@@ -69,8 +70,10 @@ struct DecodeArgs {
   int n_tiles;   // tiles per (batch, kv head)
   int n_splits;  // CTAs per (batch, kv head); tensor-core kernel: records per pair
   int n_cta;     // tensor-core kernel: CTAs of the persistent grid
-  int n_first;   // tensor-core kernel: CTAs of the first wave (one per SM)
   int split_tile[KVQ_MAX_SPLITS + 1];
+  int tc_whole;                  // tensor-core kernel: 1 = CTA i takes pair i (tc_bound unused)
+  int tc_defer;                  // tensor-core kernel: 1 = records merged by launch_decode_tc_merge
+  int tc_bound[kTcMaxCtas + 1];  // tensor-core kernel: first tile of each CTA's range, then T
   const __half* q;
   __half* out;
   float* part;   // [pairs][splits][gq][d + 2]  (o..., m, l)
@@ -149,29 +152,17 @@ struct TileInfo {
 
 __host__ __device__ inline uint32_t align16u(uint32_t x) { return (x + 15u) & ~15u; }
 
-// Stream-K ranges of the tensor-core kernel.  CTA i of N takes the tiles
-// [tc_begin(i), tc_begin(i + 1)) of the T tiles of all pairs.  Two CTAs share
-// an SM, and the one placed first (blockIdx below n_first, one per SM) gets
-// the larger share of issue slots; its range can be weighted kTcWave1
-// against kTcWave2 for the others.  Measured: 8:7 evened the two CTAs of an
-// SM at one query head per kv head but lost more with four, and a pool of
-// chunks claimed at run time lost everywhere (a piece per chunk costs a
-// merge), so the ranges stay equal.
-constexpr long long kTcWave1 = 1, kTcWave2 = 1;
-__host__ __device__ inline long long tc_weight(int i, int n_first) {
-  return i <= n_first ? kTcWave1 * i : kTcWave1 * n_first + kTcWave2 * (i - n_first);
-}
-__host__ __device__ inline int tc_begin(int i, int N, int n_first, long long T) {
-  return (int)(T * tc_weight(i, n_first) / tc_weight(N, n_first));
-}
-// The CTA whose range holds tile g (0 <= g < T): the last i with
-// tc_begin(i) <= g, i.e. T W(i) < (g + 1) W(N), so W(i) <= x below; empty
-// ranges never own a tile.
-__host__ __device__ inline int tc_owner(long long g, int N, int n_first, long long T) {
-  const long long x = ((g + 1) * tc_weight(N, n_first) - 1) / T;
-  const long long i =
-      x < kTcWave1 * n_first ? x / kTcWave1 : n_first + (x - kTcWave1 * n_first) / kTcWave2;
-  return (int)(i < N - 1 ? i : N - 1);
+// Stream-K ranges of the tensor-core kernel: CTA i of n_cta takes the tiles
+// [tc_bound[i], tc_bound[i + 1]) of all pairs' tiles (pair-major), none
+// empty.  The owner of tile g is the last i with tc_bound[i] <= g.
+__host__ __device__ inline int tc_owner(const int* bound, int n_cta, long long g) {
+  int lo = 0, hi = n_cta - 1;  // (the caller maps whole-pair grids itself)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (bound[mid] <= g) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 __host__ __device__ inline TileInfo tile_info(const DecodeArgs& a, int t) {
@@ -266,7 +257,8 @@ cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int n_pairs, cudaStream_t s);
 size_t decode_smem_bytes(int gq, int d);
 cudaError_t launch_decode_mha(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s);
-cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, int form, cudaStream_t s);
+cudaError_t launch_decode_tc_merge(const DecodeArgs& a, int n_pairs, cudaStream_t s);
 int decode_tc_ctas_per_sm();
 size_t decode_mha_smem_bytes();
 

@@ -134,6 +134,21 @@ def test_attention_many_pairs_repeatable(G, bits, gq, ws_splits):
         assert np.array_equal(pair.gpu_attention(q, ws=ws), first)
 
 
+@pytest.mark.parametrize("gq,G,bits", [(1, 32, 2), (7, 32, 4), (4, 64, 4)])
+def test_attention_one_long_head(gq, G, bits):
+    """One kv head with a long context: its tiles spread over more CTAs than
+    one warp merges, so a separate launch merges the records."""
+    B, H, d, R = 1, 1, 128, 128
+    pair = KiviPair(B, H, H * gq, d, G, R, bits, cap=8192)
+    K, V = kv(51 + gq, B, H, 7000, d)
+    pair.prefill(K, V)
+    q = _q(10, B, H * gq, d)
+    assert pair.attention_error(q) < TOL
+    ws = pair.workspace()
+    first = pair.gpu_attention(q, ws=ws)
+    assert np.array_equal(pair.gpu_attention(q, ws=ws), first)
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 64])
 def test_attention_split_counts(splits):
     """The merge of split partials gives the same result for any split count."""
