@@ -218,7 +218,34 @@ def per_workload_attention(device, flush_l2, peak, reps=20):
                               nv=[cache.c.seg[i].nv for i in range(cache.c.n_seg)],
                               nkr=cache.c.nkr, nvr=cache.c.nvr)}
 
-    res = {}
+    def lengths(cache):
+        c = cache.c
+        return ([(c.seg[i].nk, c.seg[i].nv) for i in range(c.n_seg)], c.nkr, c.nvr,
+                c.k_ring_start, c.v_ring_start)
+
+    def set_lengths(cache, st):
+        c = cache.c
+        for i, (nk, nv) in enumerate(st[0]):
+            c.seg[i].nk, c.seg[i].nv = nk, nv
+        c.nkr, c.nvr, c.k_ring_start, c.v_ring_start = st[1:]
+
+    def timed_ingest(cache, fn, reps=5):
+        """Mean event time of fn() from the same starting state, L2 flushed."""
+        st0 = lengths(cache)
+        ts = []
+        for i in range(reps):
+            set_lengths(cache, st0)
+            flush_l2(i)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.mean(ts)) * 1e3
+
+    res, ing = {}, {}
     for name in ("tiny", "llama3_8b_gqa", "streaming"):
         w = synth.WORKLOADS[name]
         B, Hq, H, d, G, R, bits = w["batch"], w["h_q"], w["h_kv"], w["d"], w["G"], w["R"], w["bits"]
@@ -227,8 +254,18 @@ def per_workload_attention(device, flush_l2, peak, reps=20):
         if name == "streaming":
             # prompt, then decode steps up to the average K residual (R/2)
             K, V = dev_kv(w["seed"], B, H, w["prompt"], d, w["n_out"], w["factor"])
-            if kvq.kvq_quantize_append(cache, K, V) == kvq.KVQ_FLUSH_DUE:
-                kvq.kvq_flush_residual(cache)
+
+            def prefill():
+                if kvq.kvq_quantize_append(cache, K, V) == kvq.KVQ_FLUSH_DUE:
+                    kvq.kvq_flush_residual(cache)
+
+            # KIVI prefill of the prompt (bulk quantize-pack, rows a1-a3):
+            # fp16 K and V read, packed codes / scales / zeros and ring written
+            us = timed_ingest(cache, prefill)
+            nb = K.numel() * 2 * 2 + cache_bytes(cache)
+            ing["prefill_streaming"] = {"us": us, "GB/s": nb / (us * 1e-6) / 1e9,
+                                        "frac": nb / (us * 1e-6) / 1e9 / peak, "bytes": nb,
+                                        "tokens": int(B * H * w["prompt"])}
             del K, V
             K, V = dev_kv(w["seed"] + 1, B, H, R // 2, d, w["n_out"], w["factor"])
             for t in range(R // 2):
@@ -251,16 +288,27 @@ def per_workload_attention(device, flush_l2, peak, reps=20):
     vis, txt = synth.window_keys(w["seed"], B, H, w["n_win"], S, w["n_text"], d)
     vd, td = torch.from_numpy(vis).to(device), torch.from_numpy(txt).to(device)
     bits, perm, _ = kvq.kvq_window_assign(vd, td, S, w["frac8"], w["frac4"])
+    # row a7 timing: the assignment returns host arrays (synchronous call)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(5):
+        kvq.kvq_window_assign(vd, td, S, w["frac8"], w["frac4"])
+    ing["windowquant_assign"] = {"us": (time.perf_counter() - t0) / 5 * 1e6,
+                                 "note": "host-synchronous call (host arrays out)"}
     caps = [(b, max(G, int((bits == b).sum()) * S)) for b in (8, 4, 2)]
     cache = kvq.alloc_cache(B, H, Hq, d, G, 128, caps, policy=kvq.KVQ_POLICY_FP16_TAIL, device=device)
     g = torch.Generator(device=device).manual_seed(w["seed"])
     Vv = torch.randn(B, H, vis.shape[2], d, generator=g, device=device).half()
     Vt = torch.randn(B, H, txt.shape[2], d, generator=g, device=device).half()
-    kvq.kvq_quantize_append(cache, vd, Vv, plan=kvq.make_plan(S, bits, perm))
+    plan = kvq.make_plan(S, bits, perm)
+    us = timed_ingest(cache, lambda: kvq.kvq_quantize_append(cache, vd, Vv, plan=plan))  # leaves it ingested
+    nb = vd.numel() * 2 * 2 + cache_bytes(cache)
+    ing["windowquant_ingest"] = {"us": us, "GB/s": nb / (us * 1e-6) / 1e9, "frac": nb / (us * 1e-6) / 1e9 / peak,
+                                 "bytes": nb}
     kvq.kvq_quantize_append(cache, td, Vt)
     torch.cuda.synchronize()
     res["windowquant_llava_ov"] = timed(cache, B, Hq, d, w["seed"])
-    return res
+    return res, ing
 
 
 def run_ours(args, rank, world, local_rank):
@@ -402,10 +450,11 @@ def run_ours(args, rank, world, local_rank):
     if err:
         raise RuntimeError("decode kernel reported a timed-out wait")
     e2e_step = float(np.mean(e2e_s))
-    others = per_workload_attention(device, flush_l2, measured_peak()[0]) if args.per_workload else {}
+    others, ingest = (per_workload_attention(device, flush_l2, measured_peak()[0]) if args.per_workload
+                      else ({}, {}))
     return dict(w=w, attn_bytes=attn_bytes, total_ms=total_ms, step_ms=step_ms, attn_ms=attn_ms,
                 app_ms=app_ms, fl_ms=fl_ms, clocks=clocks, t_wall=t_wall, e2e_step=e2e_step,
-                attn_state=attn_state, others=others,
+                attn_state=attn_state, others=others, ingest=ingest,
                 h2d=(k_in.numel() + v_in.numel() + q_in.numel()) * 2,
                 d2h=oh.numel() * 2)
 
@@ -562,6 +611,7 @@ def main():
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "us_per_step": r["e2e_step"] * 1e6},
         "per_workload_attention": r["others"],
+        "per_workload_ingest": r["ingest"],
         "gpu_launches": 3 * args.steps,
         "clocks": r["clocks"],
     }

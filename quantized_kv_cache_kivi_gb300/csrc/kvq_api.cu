@@ -458,7 +458,10 @@ kvq_status append_kivi(kvq_cache* c, const void* k_new, const void* v_new, int T
   a.v_slot0 = c->v_ring_start + c->nvr;
   const int in_k = a.k_groups - a.k_ring_groups;
   const int in_v = a.v_evict - a.v_ring_tokens;
-  a.chunks = (in_k + in_v > 0) ? 1 + std::min(256, in_k + (in_v + 63) / 64) : 1;
+  // new-token work of a bulk append (a prompt) goes to grid-wide kernels;
+  // chunk 0 of the append kernel keeps the ring work
+  a.bulk = c->d_h == 128 && G >= 8 && G <= 128 && in_k + in_v > 0;
+  a.chunks = (!a.bulk && in_k + in_v > 0) ? 1 + std::min(256, in_k + (in_v + 63) / 64) : 1;
   if (a.chunks == 2 && a.k_ring_groups == 0 && a.v_ring_tokens == 0 && a.k_first_ring >= T &&
       a.v_first_ring >= T)
     a.chunks = 1;

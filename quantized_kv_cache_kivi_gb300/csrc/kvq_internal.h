@@ -113,6 +113,7 @@ struct AppendArgs {
   int k_first_ring, k_slot0;
   int v_first_ring, v_slot0;
   int chunks;           // CTAs per (batch, kv head); chunk 0 does ring work
+  int bulk;             // 1: the new-token work goes to the bulk kernels (d_h 128)
 };
 
 struct WindowJob {   // one window of the WindowQuant ingest plan

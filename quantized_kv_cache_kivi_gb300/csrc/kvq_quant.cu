@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
                         a.T - a.v_first_ring);
     }
   }
+  if (a.bulk) return;  // the bulk kernels quantize the new tokens
   // work that reads only the new tokens, spread over the chunks (chunk 0
   // takes part only when it is the only one)
   const int workers = a.chunks > 1 ? a.chunks - 1 : 1;
@@ -348,9 +349,171 @@ __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs 
 
 size_t quant_smem(int G, int d) { return quant_smem_bytes(G, d); }
 
+// ---- bulk quantize of new tokens (prefill-sized appends), d_h = 128 --------
+// Rows a1 / a2 for the groups and tokens that read only the appended input:
+// independent work items, so a grid of warps walks them with no block-wide
+// step.  Codes match quant_k_group / quant_v_token bit for bit (same qparams,
+// same product-then-quotient rounding, decided per element).
+
+constexpr int kBulkThreads = 256;
+
+template <int BITS>
+__device__ __forceinline__ uint32_t pack4(const float (&x)[4], const float (&s)[4], const float (&r)[4],
+                                          const float (&z)[4]) {
+  uint32_t p = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) p |= qcode_fast<BITS>(x[e], z[e], s[e], r[e]) << (e * BITS);
+  return p;
+}
+
+__device__ __forceinline__ uint32_t halves_u32(__half lo, __half hi) {
+  return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+// K: one warp per group of G new tokens; lane l owns channels 4l .. 4l + 3.
+// Pass 1 takes the channel minima / maxima over the G rows, pass 2 re-reads
+// the rows (now in L1/L2) and writes the codes.
+template <int BITS>
+__global__ void __launch_bounds__(kBulkThreads) bulk_k_kernel(const AppendArgs a) {
+  constexpr int D = 128;
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (kBulkThreads / 32);
+  const int per_pair = a.k_groups - a.k_ring_groups;
+  const long long items = (long long)a.batch * a.h_kv * per_pair;
+  for (long long it = blockIdx.x * (kBulkThreads / 32) + (threadIdx.x >> 5); it < items; it += warps) {
+    const size_t pair = (size_t)(it / per_pair);
+    const int gi = a.k_ring_groups + (int)(it % per_pair);
+    const int p0 = gi * a.G;  // push index of the group's first token
+    const __half* src = a.k_new + (pair * (size_t)a.T + (size_t)(p0 - a.ksrc.n_old)) * D + 4 * lane;
+    float mn[4], mx[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mn[e] = INFINITY;
+      mx[e] = -INFINITY;
+    }
+#pragma unroll 8
+    for (int j = 0; j < a.G; ++j) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)j * D));
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      const float f[4] = {f0.x, f0.y, f1.x, f1.y};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        mn[e] = fminf(mn[e], f[e]);
+        mx[e] = fmaxf(mx[e], f[e]);
+      }
+    }
+    float s[4], r[4], z[4];
+    __half sh[4], zh[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const QParams qp = qparams(mn[e], mx[e], BITS);
+      s[e] = qp.s;
+      r[e] = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
+      z[e] = qp.z;
+      sh[e] = qp.sh;
+      zh[e] = qp.zh;
+    }
+    const size_t gidx = (pair * (size_t)(a.dst.cap / a.G) + (size_t)(a.k_nk0 / a.G + gi)) * D + 4 * lane;
+    *reinterpret_cast<uint2*>(const_cast<__half*>(a.dst.ks) + gidx) =
+        make_uint2(halves_u32(sh[0], sh[1]), halves_u32(sh[2], sh[3]));
+    *reinterpret_cast<uint2*>(const_cast<__half*>(a.dst.kz) + gidx) =
+        make_uint2(halves_u32(zh[0], zh[1]), halves_u32(zh[2], zh[3]));
+    constexpr int rb = D * BITS / 8;
+    uint8_t* out = const_cast<uint8_t*>(a.dst.kc) + (pair * (size_t)a.dst.cap + (size_t)(a.k_nk0 + p0)) * rb;
+#pragma unroll 8
+    for (int j = 0; j < a.G; ++j) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)j * D));
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      const float f[4] = {f0.x, f0.y, f1.x, f1.y};
+      const uint32_t p = pack4<BITS>(f, s, r, z);
+      uint8_t* o = out + (size_t)j * rb + lane * (BITS / 2);
+      if constexpr (BITS == 2) *o = (uint8_t)p;
+      else if constexpr (BITS == 4) *reinterpret_cast<uint16_t*>(o) = (uint16_t)p;
+      else *reinterpret_cast<uint32_t*>(o) = p;
+    }
+  }
+}
+
+// V: one half-warp per new token; lane h of the half owns channels 8h .. 8h +
+// 7, so a channel group of G is G / 8 neighbouring lanes.
+template <int BITS>
+__global__ void __launch_bounds__(kBulkThreads) bulk_v_kernel(const AppendArgs a) {
+  constexpr int D = 128;
+  const int lane = threadIdx.x & 31, hl = lane & 15;
+  const int halves_n = gridDim.x * (kBulkThreads / 16);
+  const int per_pair = a.v_evict - a.v_ring_tokens;
+  const long long items = (long long)a.batch * a.h_kv * per_pair;
+  const int lpg = a.G / 8;  // lanes per channel group
+  // both halves of a warp run the same number of iterations (shuffles)
+  const long long first = (long long)blockIdx.x * (kBulkThreads / 16) + (threadIdx.x >> 4);
+  const long long rounds = (items + halves_n - 1) / halves_n;
+  for (long long k = 0; k < rounds; ++k) {
+    const long long it = first + k * halves_n;
+    const bool live = it < items;
+    const size_t pair = live ? (size_t)(it / per_pair) : 0;
+    const int p = live ? a.v_ring_tokens + (int)(it % per_pair) : 0;
+    float f[8];
+    if (live) {
+      const uint4 u =
+          __ldg(reinterpret_cast<const uint4*>(a.v_new + (pair * (size_t)a.T + (size_t)(p - a.vsrc.n_old)) * D) + hl);
+      const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 t = __half22float2(h2[e]);
+        f[2 * e] = t.x;
+        f[2 * e + 1] = t.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = 0.f;
+    }
+    float mn = f[0], mx = f[0];
+#pragma unroll
+    for (int e = 1; e < 8; ++e) {
+      mn = fminf(mn, f[e]);
+      mx = fmaxf(mx, f[e]);
+    }
+    for (int off = 1; off < lpg; off <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    if (!live) continue;
+    const QParams qp = qparams(mn, mx, BITS);
+    const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      lo |= qcode_fast<BITS>(f[e], qp.z, qp.s, rcp) << (e * BITS);
+      hi |= qcode_fast<BITS>(f[e + 4], qp.z, qp.s, rcp) << (e * BITS);
+    }
+    const size_t row = pair * (size_t)a.dst.cap + (size_t)(a.v_nv0 + p);
+    uint8_t* o = const_cast<uint8_t*>(a.dst.vc) + row * (D * BITS / 8) + hl * BITS;
+    if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(o) = (uint16_t)(lo | (hi << 8));
+    else if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(o) = lo | (hi << 16);
+    else *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
+    if ((hl & (lpg - 1)) == 0) {
+      const size_t sidx = row * (D / a.G) + (size_t)(8 * hl / a.G);
+      const_cast<__half*>(a.dst.vs)[sidx] = qp.sh;
+      const_cast<__half*>(a.dst.vz)[sidx] = qp.zh;
+    }
+  }
+}
+
 template <class K>
 cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int BITS>
+cudaError_t launch_bulk_b(const AppendArgs& a, cudaStream_t s) {
+  const long long P = (long long)a.batch * a.h_kv;
+  const long long nk = P * (a.k_groups - a.k_ring_groups), nv = P * (a.v_evict - a.v_ring_tokens);
+  const long long cap = 4096;  // blocks: enough to fill any GPU, then the warps loop
+  if (nk > 0) bulk_k_kernel<BITS><<<(int)std::min(cap, (nk + 7) / 8), kBulkThreads, 0, s>>>(a);
+  if (nv > 0) bulk_v_kernel<BITS><<<(int)std::min(cap, (nv + 15) / 16), kBulkThreads, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
@@ -360,6 +523,12 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   if (a.d == 128) {
     if ((e = set_smem(append_kernel<128>, sm)) != cudaSuccess) return e;
     append_kernel<128><<<grid, kQuantThreads, sm, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.bulk) {
+      if (a.bits == 2) return launch_bulk_b<2>(a, s);
+      if (a.bits == 4) return launch_bulk_b<4>(a, s);
+      return launch_bulk_b<8>(a, s);
+    }
   } else {
     if ((e = set_smem(append_kernel<64>, sm)) != cudaSuccess) return e;
     append_kernel<64><<<grid, kQuantThreads, sm, s>>>(a);
