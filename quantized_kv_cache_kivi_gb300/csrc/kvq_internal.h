@@ -134,6 +134,7 @@ struct IngestArgs {
   int krs_push, vrs_push;  // ring slot of push index 0 (start + count)
   int n_jobs;              // windows; tail handled as job n_jobs
   int tail_src, tail_len, tail_dst;
+  int ring_only;           // 1: ingest_kernel leaves quantized windows to the bulk kernels
   WindowJob jobs[kMaxWindowJobs];
 };
 

@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs 
     return;
   }
   const WindowJob job = a.jobs[j];
+  if (a.ring_only && job.seg >= 0) return;  // quantized by the bulk ingest kernels
   if (job.seg < 0) {
     copy_to_ring<D>(ring_k, a.R, a.krs_push + job.dst, in_k + (size_t)job.src_token * D, a.S);
     copy_to_ring<D>(ring_v, a.R, a.vrs_push + job.dst, in_v + (size_t)job.src_token * D, a.S);
@@ -370,9 +371,117 @@ __device__ __forceinline__ uint32_t halves_u32(__half lo, __half hi) {
   return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
-// K: one warp per group of G new tokens; lane l owns channels 4l .. 4l + 3.
+// One K group of G rows (src, row stride D) into packed rows row0.. of dst
+// and scale / zero group grow, by one warp; lane l owns channels 4l .. 4l + 3.
 // Pass 1 takes the channel minima / maxima over the G rows, pass 2 re-reads
 // the rows (now in L1/L2) and writes the codes.
+template <int BITS>
+__device__ __forceinline__ void quant_group_warp(const __half* src, const SegDev& dst, int G, size_t pair, int row0,
+                                                 int grow, int lane) {
+  constexpr int D = 128;
+  src += 4 * lane;
+  float mn[4], mx[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    mn[e] = INFINITY;
+    mx[e] = -INFINITY;
+  }
+#pragma unroll 8
+  for (int j = 0; j < G; ++j) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)j * D));
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    const float f[4] = {f0.x, f0.y, f1.x, f1.y};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mn[e] = fminf(mn[e], f[e]);
+      mx[e] = fmaxf(mx[e], f[e]);
+    }
+  }
+  float s[4], r[4], z[4];
+  __half sh[4], zh[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const QParams qp = qparams(mn[e], mx[e], BITS);
+    s[e] = qp.s;
+    r[e] = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
+    z[e] = qp.z;
+    sh[e] = qp.sh;
+    zh[e] = qp.zh;
+  }
+  const size_t gidx = (pair * (size_t)(dst.cap / G) + (size_t)grow) * D + 4 * lane;
+  *reinterpret_cast<uint2*>(const_cast<__half*>(dst.ks) + gidx) =
+      make_uint2(halves_u32(sh[0], sh[1]), halves_u32(sh[2], sh[3]));
+  *reinterpret_cast<uint2*>(const_cast<__half*>(dst.kz) + gidx) =
+      make_uint2(halves_u32(zh[0], zh[1]), halves_u32(zh[2], zh[3]));
+  constexpr int rb = D * BITS / 8;
+  uint8_t* out = const_cast<uint8_t*>(dst.kc) + (pair * (size_t)dst.cap + (size_t)row0) * rb;
+#pragma unroll 8
+  for (int j = 0; j < G; ++j) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)j * D));
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    const float f[4] = {f0.x, f0.y, f1.x, f1.y};
+    const uint32_t p = pack4<BITS>(f, s, r, z);
+    uint8_t* o = out + (size_t)j * rb + lane * (BITS / 2);
+    if constexpr (BITS == 2) *o = (uint8_t)p;
+    else if constexpr (BITS == 4) *reinterpret_cast<uint16_t*>(o) = (uint16_t)p;
+    else *reinterpret_cast<uint32_t*>(o) = p;
+  }
+}
+
+// One V token (8 channels f of half-lane hl, values already loaded) into
+// packed row `row` of dst; the min / max shuffles run on the whole warp, so
+// both halves call this together (live = this half has a token).
+template <int BITS>
+__device__ __forceinline__ void quant_token_half(const float (&f)[8], bool live, const SegDev& dst, int G,
+                                                 size_t pair, int row_in_pair, int hl) {
+  constexpr int D = 128;
+  const int lpg = G / 8;  // lanes per channel group
+  float mn = f[0], mx = f[0];
+#pragma unroll
+  for (int e = 1; e < 8; ++e) {
+    mn = fminf(mn, f[e]);
+    mx = fmaxf(mx, f[e]);
+  }
+  for (int off = 1; off < lpg; off <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  if (!live) return;
+  const QParams qp = qparams(mn, mx, BITS);
+  const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    lo |= qcode_fast<BITS>(f[e], qp.z, qp.s, rcp) << (e * BITS);
+    hi |= qcode_fast<BITS>(f[e + 4], qp.z, qp.s, rcp) << (e * BITS);
+  }
+  const size_t row = pair * (size_t)dst.cap + (size_t)row_in_pair;
+  uint8_t* o = const_cast<uint8_t*>(dst.vc) + row * (D * BITS / 8) + hl * BITS;
+  if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(o) = (uint16_t)(lo | (hi << 8));
+  else if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(o) = lo | (hi << 16);
+  else *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
+  if ((hl & (lpg - 1)) == 0) {
+    const size_t sidx = row * (D / G) + (size_t)(8 * hl / G);
+    const_cast<__half*>(dst.vs)[sidx] = qp.sh;
+    const_cast<__half*>(dst.vz)[sidx] = qp.zh;
+  }
+}
+
+__device__ __forceinline__ void load8(const __half* p, bool live, float (&f)[8]) {
+  uint4 u = make_uint4(0u, 0u, 0u, 0u);
+  if (live) u = __ldg(reinterpret_cast<const uint4*>(p));
+  const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 t = __half22float2(h2[e]);
+    f[2 * e] = t.x;
+    f[2 * e + 1] = t.y;
+  }
+}
+
+// K groups of a bulk append that read only new tokens: one warp per group.
 template <int BITS>
 __global__ void __launch_bounds__(kBulkThreads) bulk_k_kernel(const AppendArgs a) {
   constexpr int D = 128;
@@ -384,69 +493,20 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_k_kernel(const AppendArgs a
     const size_t pair = (size_t)(it / per_pair);
     const int gi = a.k_ring_groups + (int)(it % per_pair);
     const int p0 = gi * a.G;  // push index of the group's first token
-    const __half* src = a.k_new + (pair * (size_t)a.T + (size_t)(p0 - a.ksrc.n_old)) * D + 4 * lane;
-    float mn[4], mx[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      mn[e] = INFINITY;
-      mx[e] = -INFINITY;
-    }
-#pragma unroll 8
-    for (int j = 0; j < a.G; ++j) {
-      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)j * D));
-      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-      const float f[4] = {f0.x, f0.y, f1.x, f1.y};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        mn[e] = fminf(mn[e], f[e]);
-        mx[e] = fmaxf(mx[e], f[e]);
-      }
-    }
-    float s[4], r[4], z[4];
-    __half sh[4], zh[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const QParams qp = qparams(mn[e], mx[e], BITS);
-      s[e] = qp.s;
-      r[e] = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
-      z[e] = qp.z;
-      sh[e] = qp.sh;
-      zh[e] = qp.zh;
-    }
-    const size_t gidx = (pair * (size_t)(a.dst.cap / a.G) + (size_t)(a.k_nk0 / a.G + gi)) * D + 4 * lane;
-    *reinterpret_cast<uint2*>(const_cast<__half*>(a.dst.ks) + gidx) =
-        make_uint2(halves_u32(sh[0], sh[1]), halves_u32(sh[2], sh[3]));
-    *reinterpret_cast<uint2*>(const_cast<__half*>(a.dst.kz) + gidx) =
-        make_uint2(halves_u32(zh[0], zh[1]), halves_u32(zh[2], zh[3]));
-    constexpr int rb = D * BITS / 8;
-    uint8_t* out = const_cast<uint8_t*>(a.dst.kc) + (pair * (size_t)a.dst.cap + (size_t)(a.k_nk0 + p0)) * rb;
-#pragma unroll 8
-    for (int j = 0; j < a.G; ++j) {
-      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)j * D));
-      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-      const float f[4] = {f0.x, f0.y, f1.x, f1.y};
-      const uint32_t p = pack4<BITS>(f, s, r, z);
-      uint8_t* o = out + (size_t)j * rb + lane * (BITS / 2);
-      if constexpr (BITS == 2) *o = (uint8_t)p;
-      else if constexpr (BITS == 4) *reinterpret_cast<uint16_t*>(o) = (uint16_t)p;
-      else *reinterpret_cast<uint32_t*>(o) = p;
-    }
+    const __half* src = a.k_new + (pair * (size_t)a.T + (size_t)(p0 - a.ksrc.n_old)) * D;
+    quant_group_warp<BITS>(src, a.dst, a.G, pair, a.k_nk0 + p0, a.k_nk0 / a.G + gi, lane);
   }
 }
 
-// V: one half-warp per new token; lane h of the half owns channels 8h .. 8h +
-// 7, so a channel group of G is G / 8 neighbouring lanes.
+// V tokens of a bulk append that read only new tokens: one half-warp each.
 template <int BITS>
 __global__ void __launch_bounds__(kBulkThreads) bulk_v_kernel(const AppendArgs a) {
   constexpr int D = 128;
-  const int lane = threadIdx.x & 31, hl = lane & 15;
-  const int halves_n = gridDim.x * (kBulkThreads / 16);
+  const int hl = threadIdx.x & 15;
+  const long long halves_n = (long long)gridDim.x * (kBulkThreads / 16);
   const int per_pair = a.v_evict - a.v_ring_tokens;
   const long long items = (long long)a.batch * a.h_kv * per_pair;
-  const int lpg = a.G / 8;  // lanes per channel group
-  // both halves of a warp run the same number of iterations (shuffles)
+  // both halves of a warp run the same number of rounds (shuffles)
   const long long first = (long long)blockIdx.x * (kBulkThreads / 16) + (threadIdx.x >> 4);
   const long long rounds = (items + halves_n - 1) / halves_n;
   for (long long k = 0; k < rounds; ++k) {
@@ -455,49 +515,62 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_v_kernel(const AppendArgs a
     const size_t pair = live ? (size_t)(it / per_pair) : 0;
     const int p = live ? a.v_ring_tokens + (int)(it % per_pair) : 0;
     float f[8];
-    if (live) {
-      const uint4 u =
-          __ldg(reinterpret_cast<const uint4*>(a.v_new + (pair * (size_t)a.T + (size_t)(p - a.vsrc.n_old)) * D) + hl);
-      const __half2* h2 = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 t = __half22float2(h2[e]);
-        f[2 * e] = t.x;
-        f[2 * e + 1] = t.y;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = 0.f;
-    }
-    float mn = f[0], mx = f[0];
-#pragma unroll
-    for (int e = 1; e < 8; ++e) {
-      mn = fminf(mn, f[e]);
-      mx = fmaxf(mx, f[e]);
-    }
-    for (int off = 1; off < lpg; off <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    }
-    if (!live) continue;
-    const QParams qp = qparams(mn, mx, BITS);
-    const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      lo |= qcode_fast<BITS>(f[e], qp.z, qp.s, rcp) << (e * BITS);
-      hi |= qcode_fast<BITS>(f[e + 4], qp.z, qp.s, rcp) << (e * BITS);
-    }
-    const size_t row = pair * (size_t)a.dst.cap + (size_t)(a.v_nv0 + p);
-    uint8_t* o = const_cast<uint8_t*>(a.dst.vc) + row * (D * BITS / 8) + hl * BITS;
-    if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(o) = (uint16_t)(lo | (hi << 8));
-    else if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(o) = lo | (hi << 16);
-    else *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
-    if ((hl & (lpg - 1)) == 0) {
-      const size_t sidx = row * (D / a.G) + (size_t)(8 * hl / a.G);
-      const_cast<__half*>(a.dst.vs)[sidx] = qp.sh;
-      const_cast<__half*>(a.dst.vz)[sidx] = qp.zh;
-    }
+    load8(a.v_new + (pair * (size_t)a.T + (size_t)(p - a.vsrc.n_old)) * D + 8 * hl, live, f);
+    quant_token_half<BITS>(f, live, a.dst, a.G, pair, a.v_nv0 + p, hl);
+  }
+}
+
+// WindowQuant reordered ingest: the K groups and V tokens of every quantized
+// window go to the rows its job names, in the segment of its width (rings
+// and the fp16 tail: ingest_kernel).  Work items are (pair, window, group)
+// for K and (pair, window, token) for V.
+__global__ void __launch_bounds__(kBulkThreads) ingest_bulk_k_kernel(const IngestArgs a) {
+  constexpr int D = 128;
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (kBulkThreads / 32);
+  const int gpw = a.S / a.G;  // K groups per window
+  const long long items = (long long)a.batch * a.h_kv * a.n_jobs * gpw;
+  for (long long it = blockIdx.x * (kBulkThreads / 32) + (threadIdx.x >> 5); it < items; it += warps) {
+    const size_t pair = (size_t)(it / ((long long)a.n_jobs * gpw));
+    const int rest = (int)(it % ((long long)a.n_jobs * gpw));
+    const WindowJob job = a.jobs[rest / gpw];
+    if (job.seg < 0) continue;
+    const int g = rest % gpw;
+    const SegDev& dst = a.seg[job.seg];
+    const __half* src = a.k_new + (pair * (size_t)a.T + (size_t)(job.src_token + g * a.G)) * D;
+    const int row0 = job.dst + g * a.G, grow = job.dst / a.G + g;
+    if (dst.bits == 2) quant_group_warp<2>(src, dst, a.G, pair, row0, grow, lane);
+    else if (dst.bits == 4) quant_group_warp<4>(src, dst, a.G, pair, row0, grow, lane);
+    else quant_group_warp<8>(src, dst, a.G, pair, row0, grow, lane);
+  }
+}
+
+__global__ void __launch_bounds__(kBulkThreads) ingest_bulk_v_kernel(const IngestArgs a) {
+  constexpr int D = 128;
+  const int hl = threadIdx.x & 15;
+  const long long halves_n = (long long)gridDim.x * (kBulkThreads / 16);
+  const long long per_pair = (long long)a.n_jobs * a.S;
+  const long long items = (long long)a.batch * a.h_kv * per_pair;
+  const long long first = (long long)blockIdx.x * (kBulkThreads / 16) + (threadIdx.x >> 4);
+  const long long rounds = (items + halves_n - 1) / halves_n;
+  for (long long k = 0; k < rounds; ++k) {
+    const long long it = first + k * halves_n;
+    bool live = it < items;
+    const size_t pair = live ? (size_t)(it / per_pair) : 0;
+    const int rest = live ? (int)(it % per_pair) : 0;
+    const WindowJob job = a.jobs[rest / a.S];
+    const int t = rest % a.S;
+    live = live && job.seg >= 0;
+    // a warp's two halves may hold windows of different widths: the group
+    // reduction is the same for all widths, so one call site per width with
+    // the other half idle keeps the shuffles converged
+    const int bits = live ? a.seg[job.seg].bits : 0;
+    float f[8];
+    load8(a.v_new + (pair * (size_t)a.T + (size_t)(job.src_token + t)) * D + 8 * hl, live, f);
+    const SegDev& dst = a.seg[live ? job.seg : 0];
+    quant_token_half<2>(f, live && bits == 2, dst, a.G, pair, job.dst + t, hl);
+    quant_token_half<4>(f, live && bits == 4, dst, a.G, pair, job.dst + t, hl);
+    quant_token_half<8>(f, live && bits == 8, dst, a.G, pair, job.dst + t, hl);
   }
 }
 
@@ -555,7 +628,19 @@ cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s) {
   dim3 grid(a.batch * a.h_kv, a.n_jobs + 1);
   const size_t sm = quant_smem(a.G, a.d);
   cudaError_t e;
-  if (a.d == 128) {
+  if (a.d == 128 && a.G >= 8 && a.G <= 128) {
+    // ring windows and the tail by the block kernel, quantized windows by
+    // the grid-wide ones
+    IngestArgs r = a;
+    r.ring_only = 1;
+    if ((e = set_smem(ingest_kernel<128>, sm)) != cudaSuccess) return e;
+    ingest_kernel<128><<<grid, kQuantThreads, sm, s>>>(r);
+    const long long P = (long long)a.batch * a.h_kv;
+    const long long nk = P * a.n_jobs * (a.S / a.G), nv = P * a.n_jobs * a.S;
+    const long long cap = 4096;
+    if (nk > 0) ingest_bulk_k_kernel<<<(int)std::min(cap, (nk + 7) / 8), kBulkThreads, 0, s>>>(a);
+    if (nv > 0) ingest_bulk_v_kernel<<<(int)std::min(cap, (nv + 15) / 16), kBulkThreads, 0, s>>>(a);
+  } else if (a.d == 128) {
     if ((e = set_smem(ingest_kernel<128>, sm)) != cudaSuccess) return e;
     ingest_kernel<128><<<grid, kQuantThreads, sm, s>>>(a);
   } else {
