@@ -173,7 +173,7 @@ def cache_bytes(cache):
     return P * per
 
 
-def per_workload_attention(device, flush_l2, peak, reps=20):
+def per_workload_attention(device, flush_l2, peak, reps=20, only=None):
     """Decode attention alone on each workload the pages name besides the
     timed step's, at the state the workload describes: mean CUDA-event time
     over `reps` calls with L2 flushed before each.  Inputs are seeded
@@ -247,6 +247,8 @@ def per_workload_attention(device, flush_l2, peak, reps=20):
 
     res, ing = {}, {}
     for name in ("tiny", "llama3_8b_gqa", "streaming"):
+        if only is not None and name != only and not (name == "streaming" and only == "prefill_streaming"):
+            continue
         w = synth.WORKLOADS[name]
         B, Hq, H, d, G, R, bits = w["batch"], w["h_q"], w["h_kv"], w["d"], w["G"], w["R"], w["bits"]
         n = w["prompt"] + R // 2 if name == "streaming" else w["n_packed"] + w["n_resid"]
@@ -261,7 +263,7 @@ def per_workload_attention(device, flush_l2, peak, reps=20):
 
             # KIVI prefill of the prompt (bulk quantize-pack, rows a1-a3):
             # fp16 K and V read, packed codes / scales / zeros and ring written
-            us = timed_ingest(cache, prefill)
+            us = timed_ingest(cache, prefill, reps=reps if only else 5)
             nb = K.numel() * 2 * 2 + cache_bytes(cache)
             ing["prefill_streaming"] = {"us": us, "GB/s": nb / (us * 1e-6) / 1e9,
                                         "frac": nb / (us * 1e-6) / 1e9 / peak, "bytes": nb,
@@ -278,9 +280,12 @@ def per_workload_attention(device, flush_l2, peak, reps=20):
             kvq.kvq_quantize_append(cache, K, V)
         del K, V
         torch.cuda.synchronize()
-        res[name] = timed(cache, B, Hq, d, w["seed"])
+        if only != "prefill_streaming":
+            res[name] = timed(cache, B, Hq, d, w["seed"])
         del cache
         torch.cuda.empty_cache()
+    if only is not None and only != "windowquant_llava_ov":
+        return res, ing
     # WindowQuant: windows ranked and reordered into INT8/INT4/INT2 segments,
     # 64 fp16 text tokens in the ring
     w = synth.WORKLOADS["windowquant_llava_ov"]
@@ -561,6 +566,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile-workload", default=None,
+                    choices=["tiny", "llama3_8b_gqa", "streaming", "prefill_streaming", "windowquant_llava_ov"],
+                    help="run one workload's calls a few times (for an ncu capture) and exit")
     ap.add_argument("--per-workload", type=int, default=1,
                     help="also time the attention alone on the other workloads (0: skip)")
     args = ap.parse_args()
@@ -568,6 +576,16 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.profile_workload:
+        import torch
+        device = torch.device("cuda", 0)
+        torch.cuda.set_device(device)
+        l2 = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        per_workload_attention(device, lambda i: l2.fill_(i & 255), measured_peak()[0], reps=3,
+                               only=args.profile_workload)
+        torch.cuda.synchronize()
+        print(json.dumps({"profiled": args.profile_workload}))
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
