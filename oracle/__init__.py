@@ -396,3 +396,71 @@ def window_assign(sim, frac8, frac4, first_window_fp16=False):
         bits[w] = 8 if r < n8 else (4 if r < n8 + n4 else 2)
     perm = np.array(sorted(range(n), key=lambda w: (-int(bits[w]), w)), np.int32)
     return bits, perm
+
+
+# ---------------------------------------------------------------------------
+# WindowQuant paper-exact assignment (§3.2.1 Eq.8 with thresholds, §3.2.2
+# first window, §3.2.3 Eq.10-11 thresholds and the batch vote)
+# ---------------------------------------------------------------------------
+def eq8_sims(vision, text, S):
+    """Eq.8 for every window of every batch element.
+
+    vision fp16 [B][M][D] (vision tokens), text fp16 [B][N][D] (text tokens);
+    window i holds vision tokens [i*S, i*S + S).  sim(T, W_i) = 1/(S N) *
+    sum_j sum_k t_j . w_k / (|t_j| |w_k|), written out as the mean of the
+    matrix of pairwise cosines (fp64).  A zero-norm token contributes 0.
+    Returns [B][M // S] float64."""
+    V = np.asarray(vision, np.float16).astype(np.float64)
+    T = np.asarray(text, np.float16).astype(np.float64)
+    B, M, D = V.shape
+    nw = M // S
+    out = np.zeros((B, nw), np.float64)
+    for b in range(B):
+        tn = np.linalg.norm(T[b], axis=1)
+        Tu = np.where(tn[:, None] > 0, T[b] / np.where(tn > 0, tn, 1.0)[:, None], 0.0)
+        for i in range(nw):
+            W = V[b, i * S:(i + 1) * S]
+            wn = np.linalg.norm(W, axis=1)
+            Wu = np.where(wn[:, None] > 0, W / np.where(wn > 0, wn, 1.0)[:, None], 0.0)
+            cos = Tu @ Wu.T  # [N][S] pairwise cosines
+            out[b, i] = cos.sum() / (S * T.shape[1])
+    return out
+
+
+def eq10_11_thresholds(layer_sim, alpha):
+    """T_low = f1(s) = (e^(alpha s) - 1) / (e^alpha - 1),
+    T_high = f2(s) = (e^(-alpha s) - 1) / (e^(-alpha) - 1)   (fp64)."""
+    s, a = float(layer_sim), float(alpha)
+    t_low = math.expm1(a * s) / math.expm1(a)
+    t_high = math.expm1(-a * s) / math.expm1(-a)
+    return t_low, t_high
+
+
+def eq8_configs(sims, t_low, t_high):
+    """Width per (batch element, window): above T_high FP16, below T_low
+    INT2, otherwise INT4 (§3.2.1)."""
+    sims = np.asarray(sims, np.float64)
+    return np.where(sims > t_high, 16, np.where(sims < t_low, 2, 4)).astype(np.int8)
+
+
+def window_assign_eq8(sims, layer_sim, alpha, first_window_fp16=False):
+    """Paper-exact window widths for a batch and the ingest permutation.
+
+    Per window the configuration each request picks (eq8_configs) is voted
+    over the batch and the most frequent one wins (§3.2.3); a tie goes to
+    the wider of the tied widths (this library's reading: the pages leave
+    ties open, and the wider width loses no accuracy).  first_window_fp16
+    pins window 0 to FP16 (§3.2.2).  The permutation lists windows by width
+    descending, index ascending, as window_assign's."""
+    t_low, t_high = eq10_11_thresholds(layer_sim, alpha)
+    cfg = eq8_configs(sims, t_low, t_high)
+    B, nw = cfg.shape
+    bits = np.zeros(nw, np.int8)
+    for w in range(nw):
+        counts = {b: int((cfg[:, w] == b).sum()) for b in (16, 4, 2)}
+        best = max(counts.values())
+        bits[w] = max(b for b in (16, 4, 2) if counts[b] == best)
+    if first_window_fp16 and nw > 0:
+        bits[0] = 16
+    perm = np.array(sorted(range(nw), key=lambda w: (-int(bits[w]), w)), np.int32)
+    return bits, perm

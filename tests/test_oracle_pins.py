@@ -4,6 +4,7 @@ None of these compare the oracle with a retyped copy of itself: each checks a
 closed form, an invariant, a brute-force or exact-rational result, or a
 hand-derived trace of the pages' Algorithm 1 (fixtures in tests/golden/).
 """
+import math
 import os
 from fractions import Fraction
 
@@ -416,3 +417,85 @@ def test_window_ingest_reorder_invariance(orc):
     Vo.append(XV[nw * S:].astype(np.float64))
     ref = orc.attention_dense(np.concatenate(Ko), np.concatenate(Vo), q, 0.125)
     assert np.allclose(out, ref, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# WindowQuant paper-exact assignment (§3.2.1 Eq.8, §3.2.2, §3.2.3 Eq.10-11)
+# ---------------------------------------------------------------------------
+def test_eq10_11_threshold_closed_forms(orc):
+    """f1, f2 at the endpoints are 0 and 1; f1 <= f2 on [0, 1]; the two are
+    mirror images, f1(s) = 1 - f2(1 - s); and f1(1/2) = 1 / (e^(a/2) + 1)."""
+    for alpha in (0.5, 2.0, 5.0):
+        assert orc.eq10_11_thresholds(0.0, alpha) == (0.0, 0.0)
+        lo, hi = orc.eq10_11_thresholds(1.0, alpha)
+        assert abs(lo - 1.0) < 1e-15 and abs(hi - 1.0) < 1e-15
+        for s in np.linspace(0.0, 1.0, 41):
+            lo, hi = orc.eq10_11_thresholds(s, alpha)
+            assert lo <= hi + 1e-15
+            assert abs(lo - (1.0 - orc.eq10_11_thresholds(1.0 - s, alpha)[1])) < 1e-14
+        lo, hi = orc.eq10_11_thresholds(0.5, alpha)
+        assert abs(lo - 1.0 / (math.exp(alpha / 2) + 1.0)) < 1e-15
+        assert abs(hi - (1.0 - lo)) < 1e-15
+
+
+def test_eq8_hand_built_windows(orc):
+    """Text tokens along one direction u (positive multiples): a window of
+    multiples of u scores 1, of -u scores -1, of vectors orthogonal to u
+    scores 0; positive rescaling of any token changes nothing."""
+    D, S, N = 16, 4, 3
+    u = np.zeros(D); u[3] = 1.0
+    v = np.zeros(D); v[7] = 1.0
+    text = np.stack([u * c for c in (0.5, 1.0, 2.0)])[None].astype(np.float16)
+    wins = [np.stack([u * c for c in (1, 2, 3, 4)]), np.stack([-u * c for c in (1, 2, 3, 4)]),
+            np.stack([v * c for c in (1, 0.5, 2, 3)])]
+    vision = np.concatenate(wins)[None].astype(np.float16)
+    sims = orc.eq8_sims(vision, text, S)
+    assert np.allclose(sims[0], [1.0, -1.0, 0.0], atol=1e-12)
+    rng = np.random.default_rng(4)
+    vis2 = rng.standard_normal((2, 6 * S, D)).astype(np.float16)
+    txt2 = rng.standard_normal((2, N, D)).astype(np.float16)
+    s1 = orc.eq8_sims(vis2, txt2, S)
+    scale_v = np.float16(2.0) ** rng.integers(-2, 3, size=(2, 6 * S, 1))
+    scale_t = np.float16(2.0) ** rng.integers(-2, 3, size=(2, N, 1))
+    s2 = orc.eq8_sims((vis2 * scale_v).astype(np.float16), (txt2 * scale_t).astype(np.float16), S)
+    assert np.allclose(s1, s2, atol=1e-12)
+
+
+def test_eq8_double_loop(orc):
+    """Eq.8 as the literal double sum of cosines, in plain Python loops."""
+    rng = np.random.default_rng(5)
+    B, S, nw, N, D = 2, 3, 4, 5, 6
+    vis = rng.standard_normal((B, S * nw, D)).astype(np.float16)
+    txt = rng.standard_normal((B, N, D)).astype(np.float16)
+    got = orc.eq8_sims(vis, txt, S)
+    for b in range(B):
+        for i in range(nw):
+            acc = 0.0
+            for j in range(N):
+                t = [float(x) for x in txt[b, j]]
+                tn = math.sqrt(sum(x * x for x in t))
+                for k in range(S):
+                    w = [float(x) for x in vis[b, i * S + k]]
+                    wn = math.sqrt(sum(x * x for x in w))
+                    acc += sum(x * y for x, y in zip(t, w)) / (tn * wn)
+            assert abs(got[b, i] - acc / (S * N)) < 1e-12
+
+
+def test_eq8_vote_and_first_window(orc):
+    """Thresholds at s = 1/2, alpha = 2: T_low = 1/(e + 1), T_high = e/(e + 1).
+    Per window the batch votes; a three-way tie goes to FP16, a tie between
+    INT4 and INT2 to INT4; a score equal to T_high is not above it (INT4)."""
+    lo, hi = orc.eq10_11_thresholds(0.5, 2.0)
+    sims = np.array([[0.9, 0.1, 0.5, hi, 0.1],
+                     [0.1, 0.2, 0.6, hi, 0.5],
+                     [0.5, 0.9, 0.1, 0.1, 0.6]])
+    cfg = orc.eq8_configs(sims, lo, hi)
+    assert cfg.tolist() == [[16, 2, 4, 4, 2], [2, 2, 4, 4, 4], [4, 16, 2, 2, 4]]
+    bits, perm = orc.window_assign_eq8(sims, 0.5, 2.0)
+    assert bits.tolist() == [16, 2, 4, 4, 4]
+    assert perm.tolist() == [0, 2, 3, 4, 1]
+    two = np.array([[0.5, 0.2], [0.1, 0.2]])  # window 0: INT4 / INT2 tie
+    bits, perm = orc.window_assign_eq8(two, 0.5, 2.0)
+    assert bits.tolist() == [4, 2] and perm.tolist() == [0, 1]
+    bits, perm = orc.window_assign_eq8(two, 0.5, 2.0, first_window_fp16=True)
+    assert bits.tolist() == [16, 2] and perm.tolist() == [0, 1]
