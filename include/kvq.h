@@ -15,7 +15,8 @@
  *   device pointer must be 16-byte aligned.
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   Every call that launches work is asynchronous on that stream, except
- *   kvq_window_assign, which returns host arrays and therefore synchronizes it.
+ *   kvq_window_assign and kvq_window_assign_eq8, which return host arrays and
+ *   therefore synchronize it.
  * - Arguments are validated on the host before anything is launched; a
  *   rejected call returns a negative kvq_status, launches nothing and leaves
  *   the cache struct untouched.  After a launch, a CUDA launch error maps to
@@ -211,6 +212,34 @@ kvq_status kvq_window_assign(const void* keys, const void* text_keys,
                              float frac4, int32_t first_window_fp16,
                              void* workspace, size_t ws_bytes, int8_t* bits_out,
                              int32_t* perm_out, double* sim_out, void* stream);
+
+/* WindowQuant window bit widths as the page defines them (WindowQuant §3.2.1
+ * Eq.8, §3.2.2, §3.2.3 Eq.10-11), and the reorder of §3.3.1:
+ *   vision fp16 [batch][M][dim] (vision-token embeddings, device)
+ *   text   fp16 [batch][N][dim] (text-token embeddings, device)
+ * Window w holds vision tokens [w*S, w*S+S) for w < n_windows = M / S (a tail
+ * M mod S stays FP16 at ingest).  Per request b and window w, Eq.8:
+ *   sim = 1/(S N) sum_j sum_k t_j . w_k / (|t_j| |w_k|)   (a zero token adds 0)
+ * computed in fp64.  Thresholds from the layer similarity s (Eq.9, given by
+ * the caller) and alpha (nonzero): T_low = (e^(alpha s) - 1) / (e^alpha - 1),
+ * T_high = (e^(-alpha s) - 1) / (e^(-alpha) - 1).  A request puts window w at
+ * 16 bits if sim > T_high, 2 bits if sim < T_low, else 4 bits; the batch takes
+ * the most frequent choice, a tie going to the wider width; first_window_fp16
+ * != 0 pins window 0 to 16 bits.  perm_out lists windows by width descending,
+ * index ascending (the ingest order of kvq_window_plan; 16-bit windows go to
+ * the fp16 ring).  bits_out int8 [n_windows], perm_out int32 [n_windows],
+ * sim_out double [batch][n_windows] or NULL: host memory.  workspace: device,
+ * at least kvq_window_assign_eq8_workspace_bytes(...) bytes, no
+ * initialization needed.  Synchronizes `stream`. */
+size_t kvq_window_assign_eq8_workspace_bytes(int32_t batch, int32_t dim,
+                                             int32_t M, int32_t S, int32_t N);
+kvq_status kvq_window_assign_eq8(const void* vision, const void* text,
+                                 int32_t batch, int32_t dim, int32_t M,
+                                 int32_t S, int32_t N, double layer_sim,
+                                 double alpha, int32_t first_window_fp16,
+                                 void* workspace, size_t ws_bytes,
+                                 int8_t* bits_out, int32_t* perm_out,
+                                 double* sim_out, void* stream);
 
 /* Decode attention without a caller workspace (no counterpart in the pages).
  *

@@ -816,4 +816,66 @@ kvq_status kvq_window_assign(const void* keys, const void* text_keys, int32_t ba
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "window assign copy-back");
 }
 
+static int eq8_chunks(int batch, int M, int S, int N) {
+  const int nw = M / S;
+  const int maxlen = std::max(S, N);
+  int z = std::max(1, (2 * sm_count() + batch * (nw + 1) - 1) / (batch * (nw + 1)));
+  z = std::max(z, (maxlen + 4095) / 4096);  // shared inverse norms of a chunk: at most 32 KB
+  return std::min(z, maxlen);
+}
+
+size_t kvq_window_assign_eq8_workspace_bytes(int32_t batch, int32_t dim, int32_t M, int32_t S, int32_t N) {
+  if (batch < 1 || dim < 1 || S < 1 || M < S || N < 1) return 0;
+  const size_t nw = (size_t)M / S;
+  const size_t z = (size_t)eq8_chunks(batch, M, S, N);
+  auto a256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  return a256((size_t)batch * (nw + 1) * z * dim * 8) + a256((size_t)batch * nw * 8) + a256(nw) + a256(nw * 4);
+}
+
+kvq_status kvq_window_assign_eq8(const void* vision, const void* text, int32_t batch, int32_t dim, int32_t M,
+                                 int32_t S, int32_t N, double layer_sim, double alpha, int32_t first_window_fp16,
+                                 void* ws, size_t ws_bytes, int8_t* bits_out, int32_t* perm_out, double* sim_out,
+                                 void* stream) {
+  if (!vision || !text || !bits_out || !perm_out) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
+  if (batch < 1 || dim < 1 || S < 1 || M < S || N < 1) return fail(KVQ_ERR_INVALID_ARG, "bad sizes");
+  if (!(alpha != 0.0 && std::isfinite(alpha) && std::isfinite(layer_sim)))
+    return fail(KVQ_ERR_INVALID_ARG, "alpha must be finite and nonzero, layer_sim finite");
+  const size_t need = kvq_window_assign_eq8_workspace_bytes(batch, dim, M, S, N);
+  if (!ws || !aligned16(ws) || ws_bytes < need)
+    return fail(KVQ_ERR_WORKSPACE, "window workspace needs %zu bytes", need);
+  const int nw = M / S;
+  kvq::Eq8Args a{};
+  a.vision = static_cast<const __half*>(vision);
+  a.text = static_cast<const __half*>(text);
+  a.batch = batch;
+  a.dim = dim;
+  a.M = M;
+  a.S = S;
+  a.N = N;
+  a.chunks = eq8_chunks(batch, M, S, N);
+  // Eq.10 and Eq.11
+  a.t_low = std::expm1(alpha * layer_sim) / std::expm1(alpha);
+  a.t_high = std::expm1(-alpha * layer_sim) / std::expm1(-alpha);
+  a.first_fp16 = first_window_fp16 ? 1 : 0;
+  auto a256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  size_t off = 0;
+  a.part = reinterpret_cast<double*>(w + off);
+  off += a256((size_t)batch * (nw + 1) * a.chunks * dim * 8);
+  a.sims = reinterpret_cast<double*>(w + off);
+  off += a256((size_t)batch * nw * 8);
+  a.bits = reinterpret_cast<int8_t*>(w + off);
+  off += a256((size_t)nw);
+  a.perm = reinterpret_cast<int32_t*>(w + off);
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = kvq::launch_window_assign_eq8(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "window assign launch");
+  e = cudaMemcpyAsync(bits_out, a.bits, nw, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(perm_out, a.perm, (size_t)nw * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && sim_out)
+    e = cudaMemcpyAsync(sim_out, a.sims, (size_t)batch * nw * 8, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "window assign copy-back");
+}
+
 }  // extern "C"

@@ -277,4 +277,19 @@ struct WindowArgs {
 };
 cudaError_t launch_window_assign(const WindowArgs& a, cudaStream_t s);
 
+// WindowQuant paper-exact assignment (Eq.8 scores, Eq.10-11 thresholds).
+struct Eq8Args {
+  const __half* vision;  // [B][M][dim]
+  const __half* text;    // [B][N][dim]
+  int batch, dim, M, S, N;
+  int chunks;            // token chunks per window / text (partial sums)
+  double t_low, t_high;
+  int first_fp16;
+  double* part;          // [B][n_win + 1][chunks][dim]: sums of unit vectors
+  double* sims;          // [B][n_win]
+  int8_t* bits;          // [n_win]
+  int32_t* perm;         // [n_win]
+};
+cudaError_t launch_window_assign_eq8(const Eq8Args& a, cudaStream_t s);
+
 }  // namespace kvq

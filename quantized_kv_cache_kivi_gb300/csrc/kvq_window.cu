@@ -112,7 +112,105 @@ __global__ void window_rank_kernel(WindowArgs a) {
   }
 }
 
+// ---- paper-exact assignment (WindowQuant §3.2.1 Eq.8, §3.2.3 Eq.10-11) -----
+// Eq.8 averages the cosines of every (text token, window token) pair:
+// sim = (1 / S N) (sum_j t_j / |t_j|) . (sum_k w_k / |w_k|), so each window and
+// the text reduce to one sum of unit vectors (fp64), split over `chunks`
+// token chunks (partial sums in a fixed order, no atomics).
+
+// Block (b, unit u, chunk z): unit u < n_win is window u, u = n_win the text.
+// Phase 1: one warp per token, its inverse norm; phase 2: one thread per
+// channel, the sum of x / |x| over the chunk's tokens.
+__global__ void eq8_unit_sum_kernel(Eq8Args a) {
+  extern __shared__ double inv[];  // [tokens of the chunk]
+  const int b = blockIdx.x, u = blockIdx.y, z = blockIdx.z;
+  const int nw = a.M / a.S;
+  const bool text = u == nw;
+  const int len = text ? a.N : a.S;
+  const int per = (len + a.chunks - 1) / a.chunks;
+  const int k0 = z * per, k1 = min(len, k0 + per);
+  const __half* base = text ? a.text + (size_t)b * a.N * a.dim
+                            : a.vision + ((size_t)b * a.M + (size_t)u * a.S) * a.dim;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
+  for (int k = k0 + warp; k < k1; k += nwarp) {
+    const __half* x = base + (size_t)k * a.dim;
+    double ss = 0.0;
+    for (int c = lane; c < a.dim; c += 32) {
+      const double v = (double)__half2float(x[c]);
+      ss += v * v;
+    }
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) inv[k - k0] = ss > 0.0 ? 1.0 / sqrt(ss) : 0.0;  // a zero token adds nothing
+  }
+  __syncthreads();
+  double* out = a.part + (((size_t)b * (nw + 1) + u) * a.chunks + z) * a.dim;
+  for (int c = threadIdx.x; c < a.dim; c += blockDim.x) {
+    double acc = 0.0;
+    for (int k = k0; k < k1; ++k) acc += (double)__half2float(base[(size_t)k * a.dim + c]) * inv[k - k0];
+    out[c] = acc;
+  }
+}
+
+// sims[b][w] = (window sum . text sum) / (S N), chunk partials added in order.
+__global__ void eq8_sim_kernel(Eq8Args a) {
+  __shared__ double red[kThreads / 32];
+  const int b = blockIdx.x, w = blockIdx.y;
+  const int nw = a.M / a.S;
+  const double* pw = a.part + ((size_t)b * (nw + 1) + w) * a.chunks * a.dim;
+  const double* pt = a.part + ((size_t)b * (nw + 1) + nw) * a.chunks * a.dim;
+  double dot = 0.0;
+  for (int c = threadIdx.x; c < a.dim; c += blockDim.x) {
+    double sw = 0.0, st = 0.0;
+    for (int z = 0; z < a.chunks; ++z) {
+      sw += pw[(size_t)z * a.dim + c];
+      st += pt[(size_t)z * a.dim + c];
+    }
+    dot += sw * st;
+  }
+  const double d = block_sum(dot, red);
+  if (threadIdx.x == 0) a.sims[(size_t)b * nw + w] = d / ((double)a.S * (double)a.N);
+}
+
+// One block: per window the configuration of every request (above T_high
+// FP16, below T_low INT2, else INT4), the batch's most frequent one (ties to
+// the wider), window 0 pinned to FP16 on request; then the ingest order.
+__global__ void eq8_decide_kernel(Eq8Args a) {
+  const int nw = a.M / a.S;
+  for (int w = threadIdx.x; w < nw; w += blockDim.x) {
+    int c16 = 0, c4 = 0, c2 = 0;
+    for (int b = 0; b < a.batch; ++b) {
+      const double v = a.sims[(size_t)b * nw + w];
+      if (v > a.t_high) ++c16;
+      else if (v < a.t_low) ++c2;
+      else ++c4;
+    }
+    int bits = (c16 >= c4 && c16 >= c2) ? 16 : (c4 >= c2 ? 4 : 2);
+    if (a.first_fp16 && w == 0) bits = 16;
+    a.bits[w] = (int8_t)bits;
+  }
+  __syncthreads();
+  for (int w = threadIdx.x; w < nw; w += blockDim.x) {
+    const int bw = a.bits[w];
+    int pos = 0;
+    for (int v = 0; v < nw; ++v) {
+      const int bv = a.bits[v];
+      pos += (bv > bw) || (bv == bw && v < w);
+    }
+    a.perm[pos] = w;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_window_assign_eq8(const Eq8Args& a, cudaStream_t s) {
+  const int nw = a.M / a.S;
+  const int maxlen = a.S > a.N ? a.S : a.N;
+  const size_t sm = (size_t)((maxlen + a.chunks - 1) / a.chunks) * sizeof(double);
+  eq8_unit_sum_kernel<<<dim3(a.batch, nw + 1, a.chunks), kThreads, sm, s>>>(a);
+  eq8_sim_kernel<<<dim3(a.batch, nw), kThreads, 0, s>>>(a);
+  eq8_decide_kernel<<<1, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_window_assign(const WindowArgs& a, cudaStream_t s) {
   text_sum_kernel<<<a.batch, kThreads, 0, s>>>(a);

@@ -79,12 +79,19 @@ def lib():
             [ctypes.c_float, ctypes.c_float, ctypes.c_int32, _P, ctypes.c_size_t,
              ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(ctypes.c_int32),
              ctypes.POINTER(ctypes.c_double), _P]
+        L.kvq_window_assign_eq8_workspace_bytes.argtypes = [ctypes.c_int32] * 5
+        L.kvq_window_assign_eq8_workspace_bytes.restype = ctypes.c_size_t
+        L.kvq_window_assign_eq8.argtypes = [_P, _P] + [ctypes.c_int32] * 5 + \
+            [ctypes.c_double, ctypes.c_double, ctypes.c_int32, _P, ctypes.c_size_t,
+             ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(ctypes.c_int32),
+             ctypes.POINTER(ctypes.c_double), _P]
         L.kvq_status_string.argtypes = [ctypes.c_int]
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_last_error_string.argtypes = []
         L.kvq_last_error_string.restype = ctypes.c_char_p
         for name in ("kvq_quantize_append", "kvq_flush_residual", "kvq_workspace_init",
-                     "kvq_decode_attention", "kvq_workspace_error", "kvq_window_assign"):
+                     "kvq_decode_attention", "kvq_workspace_error", "kvq_window_assign",
+                     "kvq_window_assign_eq8"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -186,6 +193,34 @@ def kvq_window_assign(keys, text_keys, S, frac8, frac4, first_window_fp16=False,
                                  sim.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                                  _stream(stream))
     _check(st, "kvq_window_assign")
+    return bits, perm, sim
+
+
+def kvq_window_assign_eq8_workspace_bytes(batch, dim, M, S, N):
+    return int(lib().kvq_window_assign_eq8_workspace_bytes(batch, dim, M, S, N))
+
+
+def kvq_window_assign_eq8(vision, text, S, layer_sim, alpha, first_window_fp16=False, ws=None,
+                          stream=None):
+    """vision fp16 [B][M][dim], text fp16 [B][N][dim] -> (bits, perm, sim [B][n_windows])."""
+    import numpy as np
+    import torch
+    B, M, dim = vision.shape
+    N = text.shape[1]
+    nw = M // S
+    need = kvq_window_assign_eq8_workspace_bytes(B, dim, M, S, N)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=vision.device)
+    bits = np.zeros(nw, np.int8)
+    perm = np.zeros(nw, np.int32)
+    sim = np.zeros((B, nw), np.float64)
+    st = lib().kvq_window_assign_eq8(_ptr(vision), _ptr(text), B, dim, M, S, N, float(layer_sim),
+                                     float(alpha), int(bool(first_window_fp16)), _ptr(ws), ws.numel(),
+                                     bits.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)),
+                                     perm.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                     sim.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                     _stream(stream))
+    _check(st, "kvq_window_assign_eq8")
     return bits, perm, sim
 
 

@@ -307,16 +307,17 @@ def test_window_assign_matches_oracle():
     assert np.array_equal(bits16, ob16) and np.array_equal(perm16, op16)
 
 
-def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False):
+def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, perm=None):
     vis, txt = synth.window_keys(seed, B, H, n_win, S, n_text, d)
     M = n_win * S
     Vv = np.stack([np.stack([synth.values(seed, b, h, M, d) for h in range(H)]) for b in range(B)])
     Vt = np.stack([np.stack([synth.values(seed + 1, b, h, n_text, d) for h in range(H)])
                    for b in range(B)])
-    sim = oracle.window_sims(vis, txt, S)
-    bits, perm = oracle.window_assign(sim, 0.1, 0.3, first_window_fp16=first16)
+    if bits is None:
+        sim = oracle.window_sims(vis, txt, S)
+        bits, perm = oracle.window_assign(sim, 0.1, 0.3, first_window_fp16=first16)
     caps = [(b, int(((bits == b).sum() * S + G - 1) // G * G) or G) for b in (8, 4, 2)]
-    R = 128 if not first16 else S + 128
+    R = 128 + int((bits == 16).sum()) * S
     c = kvq.alloc_cache(B, H, H * gq, d, G, R, caps, policy=kvq.KVQ_POLICY_FP16_TAIL)
     plan = kvq.make_plan(S, bits, perm)
     tail = 5  # vision tokens past the last whole window stay fp16
@@ -334,10 +335,59 @@ def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False):
     return c, heads, caps, R
 
 
+def _eq8_inputs(seed, B, n_win, S, N, dim):
+    """Vision / text embeddings whose windows lean towards the text by
+    seeded angles (so Eq.8 scores spread over [-0.4, 0.4])."""
+    rng = np.random.default_rng(seed)
+    amp = 0.75 * np.sqrt(dim)  # direction against noise of norm ~sqrt(dim)
+    t = rng.standard_normal(dim)
+    t /= np.linalg.norm(t)
+    vis = np.empty((B, n_win * S, dim))
+    for w, th in enumerate(rng.permutation(np.linspace(0.0, np.pi, n_win))):
+        v = rng.standard_normal(dim)
+        v -= (v @ t) * t
+        v /= np.linalg.norm(v)
+        vis[:, w * S:(w + 1) * S] = amp * (np.cos(th) * t + np.sin(th) * v) + rng.standard_normal((B, S, dim))
+    txt = amp * t + rng.standard_normal((B, N, dim))
+    return vis.astype(np.float16), txt.astype(np.float16)
+
+
+@pytest.mark.parametrize("B,n_win,S,N,dim,first16", [(3, 12, 32, 20, 64, False), (2, 64, 256, 64, 1152, True),
+                                                     (4, 7, 16, 5, 96, False)])
+def test_window_assign_eq8_matches_oracle(B, n_win, S, N, dim, first16):
+    layer_sim, alpha = 0.1, 2.0  # T_low ~ 0.035, T_high ~ 0.21
+    vis, txt = _eq8_inputs(11 + n_win, B, n_win, S, N, dim)
+    extra = 3  # vision tokens past the last window: not scored
+    vis_all = np.concatenate([vis, vis[:, :extra]], axis=1)
+    bits, perm, sim = kvq.kvq_window_assign_eq8(to_dev(vis_all), to_dev(txt), S, layer_sim, alpha, first16)
+    osim = oracle.eq8_sims(vis, txt, S)
+    assert np.allclose(sim, osim, rtol=0, atol=1e-12)
+    lo, hi = oracle.eq10_11_thresholds(layer_sim, alpha)
+    assert np.min(np.abs(osim - lo)) > 1e-9 and np.min(np.abs(osim - hi)) > 1e-9
+    obits, operm = oracle.window_assign_eq8(osim, layer_sim, alpha, first_window_fp16=first16)
+    assert np.array_equal(bits, obits) and np.array_equal(perm, operm)
+    assert len(set(bits.tolist())) == 3  # all three widths occur
+
+
+def test_windowquant_eq8_ingest_and_attention():
+    """Widths from the paper-exact assignment (FP16 windows into the ring),
+    reordered ingest and mixed-width attention against the oracle."""
+    n_win, S, n_text, B, H, gq, d, G = 12, 64, 24, 2, 2, 7, 128, 32
+    vis, txt = _eq8_inputs(5, B, n_win, S, 16, 96)
+    bits, perm, _ = kvq.kvq_window_assign_eq8(to_dev(vis), to_dev(txt), S, 0.1, 2.0, True)
+    assert (bits == 16).sum() >= 2
+    _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, 3, False, bits, perm)
+
+
 @pytest.mark.parametrize("first16", [False, True])
 def test_windowquant_ingest_and_attention(first16):
     n_win, S, n_text, B, H, gq, d, G = 16, 64, 24, 2, 2, 7, 128, 32
-    c, heads, caps, R = _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed=3, first16=first16)
+    _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, 3, first16, None, None)
+
+
+def _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, seed, first16, bits, perm):
+    c, heads, caps, R = _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed=seed, first16=first16,
+                                  bits=bits, perm=perm)
     torch.cuda.synchronize()
     P = B * H
     q = synth.q_block(9, B, H * gq, d)
