@@ -300,6 +300,23 @@ def per_workload_attention(device, flush_l2, peak, reps=20, only=None):
         kvq.kvq_window_assign(vd, td, S, w["frac8"], w["frac4"])
     ing["windowquant_assign"] = {"us": (time.perf_counter() - t0) / 5 * 1e6,
                                  "note": "host-synchronous call (host arrays out)"}
+    # paper-exact assignment (Eq.8 over embeddings of the LLM width, 3584 for
+    # the Qwen2-7B of LLaVA-OneVision): device time of its three kernels
+    dim = 3584
+    g8 = torch.Generator(device=device).manual_seed(w["seed"] + 5)
+    emb_v = torch.randn(B, vis.shape[2], dim, generator=g8, device=device).half()
+    emb_t = torch.randn(B, txt.shape[2], dim, generator=g8, device=device).half()
+    ws8 = torch.empty(kvq.kvq_window_assign_eq8_workspace_bytes(B, dim, emb_v.shape[1], S, emb_t.shape[1]),
+                      dtype=torch.uint8, device=device)
+    kvq.kvq_window_assign_eq8(emb_v, emb_t, S, 0.1, 2.0, ws=ws8)
+    t0 = time.perf_counter()
+    for _ in range(5):
+        kvq.kvq_window_assign_eq8(emb_v, emb_t, S, 0.1, 2.0, ws=ws8)
+    us8 = (time.perf_counter() - t0) / 5 * 1e6
+    nb8 = (emb_v.numel() + emb_t.numel()) * 2 * 2  # two passes over the embeddings
+    ing["windowquant_assign_eq8"] = {"us": us8, "bytes": nb8, "GB/s": nb8 / (us8 * 1e-6) / 1e9,
+                                     "note": "host-synchronous call; embeddings read twice (norms, sums)"}
+    del emb_v, emb_t, ws8
     caps = [(b, max(G, int((bits == b).sum()) * S)) for b in (8, 4, 2)]
     cache = kvq.alloc_cache(B, H, Hq, d, G, 128, caps, policy=kvq.KVQ_POLICY_FP16_TAIL, device=device)
     g = torch.Generator(device=device).manual_seed(w["seed"])

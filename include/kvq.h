@@ -220,7 +220,10 @@ kvq_status kvq_window_assign(const void* keys, const void* text_keys,
  * Window w holds vision tokens [w*S, w*S+S) for w < n_windows = M / S (a tail
  * M mod S stays FP16 at ingest).  Per request b and window w, Eq.8:
  *   sim = 1/(S N) sum_j sum_k t_j . w_k / (|t_j| |w_k|)   (a zero token adds 0)
- * computed in fp64.  Thresholds from the layer similarity s (Eq.9, given by
+ * as (sum_j t_j / |t_j|) . (sum_k w_k / |w_k|) / (S N): products in fp32 (exact
+ * for fp16 squares), sums of at most 16 terms in fp32 inside fp64 sums, so a
+ * score carries a relative error of about 1e-7 (a window within that of a
+ * threshold can fall either side).  dim must be a multiple of 8.  Thresholds from the layer similarity s (Eq.9, given by
  * the caller) and alpha (nonzero): T_low = (e^(alpha s) - 1) / (e^alpha - 1),
  * T_high = (e^(-alpha s) - 1) / (e^(-alpha) - 1).  A request puts window w at
  * 16 bits if sim > T_high, 2 bits if sim < T_low, else 4 bits; the batch takes

@@ -838,6 +838,8 @@ kvq_status kvq_window_assign_eq8(const void* vision, const void* text, int32_t b
                                  void* stream) {
   if (!vision || !text || !bits_out || !perm_out) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
   if (batch < 1 || dim < 1 || S < 1 || M < S || N < 1) return fail(KVQ_ERR_INVALID_ARG, "bad sizes");
+  if (dim % 8 != 0 || !aligned16(vision) || !aligned16(text))
+    return fail(KVQ_ERR_INVALID_ARG, "dim must be a multiple of 8 and the inputs 16-byte aligned");
   if (!(alpha != 0.0 && std::isfinite(alpha) && std::isfinite(layer_sim)))
     return fail(KVQ_ERR_INVALID_ARG, "alpha must be finite and nonzero, layer_sim finite");
   const size_t need = kvq_window_assign_eq8_workspace_bytes(batch, dim, M, S, N);

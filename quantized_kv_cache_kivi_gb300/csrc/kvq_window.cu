@@ -120,9 +120,11 @@ __global__ void window_rank_kernel(WindowArgs a) {
 
 // Block (b, unit u, chunk z): unit u < n_win is window u, u = n_win the text.
 // Phase 1: one warp per token, its inverse norm; phase 2: one thread per
-// channel, the sum of x / |x| over the chunk's tokens.
+// 8-channel slice, the sum of x / |x| over the chunk's tokens.  Products of
+// fp16 values are exact in fp32; sums run in fp32 over at most 16 terms and
+// then in fp64 (GB300's fp64 rate is a small fraction of its fp32 rate).
 __global__ void eq8_unit_sum_kernel(Eq8Args a) {
-  extern __shared__ double inv[];  // [tokens of the chunk]
+  extern __shared__ float inv[];  // [tokens of the chunk]
   const int b = blockIdx.x, u = blockIdx.y, z = blockIdx.z;
   const int nw = a.M / a.S;
   const bool text = u == nw;
@@ -132,22 +134,58 @@ __global__ void eq8_unit_sum_kernel(Eq8Args a) {
   const __half* base = text ? a.text + (size_t)b * a.N * a.dim
                             : a.vision + ((size_t)b * a.M + (size_t)u * a.S) * a.dim;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
+  const int n8 = a.dim / 8;  // 8-channel slices (dim % 8 == 0, checked by the host)
   for (int k = k0 + warp; k < k1; k += nwarp) {
-    const __half* x = base + (size_t)k * a.dim;
+    const uint4* x = reinterpret_cast<const uint4*>(base + (size_t)k * a.dim);
     double ss = 0.0;
-    for (int c = lane; c < a.dim; c += 32) {
-      const double v = (double)__half2float(x[c]);
-      ss += v * v;
+    for (int c0 = 0; c0 < n8; c0 += 32 * 2) {
+      float f = 0.f;  // at most 16 exact squares
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int c = c0 + 32 * r + lane;
+        if (c < n8) {
+          const uint4 v = __ldg(x + c);
+          const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 t = __half22float2(h[e]);
+            f = fmaf(t.x, t.x, f);
+            f = fmaf(t.y, t.y, f);
+          }
+        }
+      }
+      ss += (double)f;
     }
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if (lane == 0) inv[k - k0] = ss > 0.0 ? 1.0 / sqrt(ss) : 0.0;  // a zero token adds nothing
+    if (lane == 0) inv[k - k0] = ss > 0.0 ? (float)(1.0 / sqrt(ss)) : 0.f;  // a zero token adds nothing
   }
   __syncthreads();
   double* out = a.part + (((size_t)b * (nw + 1) + u) * a.chunks + z) * a.dim;
-  for (int c = threadIdx.x; c < a.dim; c += blockDim.x) {
-    double acc = 0.0;
-    for (int k = k0; k < k1; ++k) acc += (double)__half2float(base[(size_t)k * a.dim + c]) * inv[k - k0];
-    out[c] = acc;
+  for (int c = threadIdx.x; c < n8; c += blockDim.x) {
+    double acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0;
+    for (int k = k0; k < k1; k += 16) {
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = 0.f;
+      const int kk1 = min(k1, k + 16);
+      for (int q = k; q < kk1; ++q) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (size_t)q * a.dim) + c);
+        const __half2* h = reinterpret_cast<const __half2*>(&v);
+        const float w = inv[q - k0];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 t = __half22float2(h[e]);
+          f[2 * e] = fmaf(t.x, w, f[2 * e]);
+          f[2 * e + 1] = fmaf(t.y, w, f[2 * e + 1]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += (double)f[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) out[8 * c + e] = acc[e];
   }
 }
 
@@ -205,7 +243,7 @@ __global__ void eq8_decide_kernel(Eq8Args a) {
 cudaError_t launch_window_assign_eq8(const Eq8Args& a, cudaStream_t s) {
   const int nw = a.M / a.S;
   const int maxlen = a.S > a.N ? a.S : a.N;
-  const size_t sm = (size_t)((maxlen + a.chunks - 1) / a.chunks) * sizeof(double);
+  const size_t sm = (size_t)((maxlen + a.chunks - 1) / a.chunks) * sizeof(float);
   eq8_unit_sum_kernel<<<dim3(a.batch, nw + 1, a.chunks), kThreads, sm, s>>>(a);
   eq8_sim_kernel<<<dim3(a.batch, nw), kThreads, 0, s>>>(a);
   eq8_decide_kernel<<<1, kThreads, 0, s>>>(a);

@@ -361,9 +361,10 @@ def test_window_assign_eq8_matches_oracle(B, n_win, S, N, dim, first16):
     vis_all = np.concatenate([vis, vis[:, :extra]], axis=1)
     bits, perm, sim = kvq.kvq_window_assign_eq8(to_dev(vis_all), to_dev(txt), S, layer_sim, alpha, first16)
     osim = oracle.eq8_sims(vis, txt, S)
-    assert np.allclose(sim, osim, rtol=0, atol=1e-12)
+    # fp32 products and short fp32 sums inside fp64 accumulation: ~1e-7
+    assert np.allclose(sim, osim, rtol=0, atol=2e-6)
     lo, hi = oracle.eq10_11_thresholds(layer_sim, alpha)
-    assert np.min(np.abs(osim - lo)) > 1e-9 and np.min(np.abs(osim - hi)) > 1e-9
+    assert np.min(np.abs(osim - lo)) > 1e-4 and np.min(np.abs(osim - hi)) > 1e-4
     obits, operm = oracle.window_assign_eq8(osim, layer_sim, alpha, first_window_fp16=first16)
     assert np.array_equal(bits, obits) and np.array_equal(perm, operm)
     assert len(set(bits.tolist())) == 3  # all three widths occur
