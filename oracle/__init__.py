@@ -41,10 +41,11 @@ def lib():
         L = ctypes.CDLL(path)
         L.orc_quantize_group.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          _u8p, ctypes.c_int, _u16p, _u16p]
+        L.orc_quantize_group_intz.argtypes = L.orc_quantize_group.argtypes
         L.orc_quantize_k_block.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                           _u8p, _u16p, _u16p]
+                                           _u8p, _u16p, _u16p, ctypes.c_int]
         L.orc_quantize_v_token.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                           _u8p, _u16p, _u16p]
+                                           _u8p, _u16p, _u16p, ctypes.c_int]
         L.orc_pack_row.argtypes = [_u8p, ctypes.c_int, ctypes.c_int, _u8p]
         L.orc_unpack_row.argtypes = [_u8p, ctypes.c_int, ctypes.c_int, _u8p]
         L.orc_attention_dense.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p, _f64p,
@@ -78,38 +79,40 @@ def _as_u16(x):
 # ---------------------------------------------------------------------------
 # codec (KIVI "方法细节" first formula; WindowQuant §3.3.3 Eq.14, Eq.16)
 # ---------------------------------------------------------------------------
-def quantize_group(x, bits):
-    """One group of fp16 values -> (codes uint8 [n], s fp16-bits, z fp16-bits)."""
+def quantize_group(x, bits, intz=False):
+    """One group of fp16 values -> (codes uint8 [n], s fp16-bits, z fp16-bits).
+    intz: the integer-zero-point quantizer (WindowQuant Eq.14-16), z then
+    holds fp16(-s * z_int)."""
     x = _as_u16(x).ravel()
     codes = np.zeros(x.size, np.uint8)
     s = np.zeros(1, np.uint16)
     z = np.zeros(1, np.uint16)
-    lib().orc_quantize_group(_p(x, _u16p), x.size, 1, bits, _p(codes, _u8p), 1,
-                             _p(s, _u16p), _p(z, _u16p))
+    fn = lib().orc_quantize_group_intz if intz else lib().orc_quantize_group
+    fn(_p(x, _u16p), x.size, 1, bits, _p(codes, _u8p), 1, _p(s, _u16p), _p(z, _u16p))
     return codes, s[0], z[0]
 
 
-def quantize_k_block(x, bits):
-    """K block [G][D] fp16 -> codes [G][D], s [D], z [D] (per channel, KIVI)."""
+def quantize_k_block(x, bits, intz=False):
+    """K block [G][D] fp16 -> codes [G][D], s [D], z [D] (per channel)."""
     x = _as_u16(x)
     G, D = x.shape
     codes = np.zeros((G, D), np.uint8)
     s = np.zeros(D, np.uint16)
     z = np.zeros(D, np.uint16)
     lib().orc_quantize_k_block(_p(x, _u16p), G, D, bits, _p(codes, _u8p), _p(s, _u16p),
-                               _p(z, _u16p))
+                               _p(z, _u16p), int(bool(intz)))
     return codes, s, z
 
 
-def quantize_v_token(x, G, bits):
-    """V token [D] fp16 -> codes [D], s [D/G], z [D/G] (per token, KIVI)."""
+def quantize_v_token(x, G, bits, intz=False):
+    """V token [D] fp16 -> codes [D], s [D/G], z [D/G] (per token)."""
     x = _as_u16(x).ravel()
     D = x.size
     codes = np.zeros(D, np.uint8)
     s = np.zeros(D // G, np.uint16)
     z = np.zeros(D // G, np.uint16)
     lib().orc_quantize_v_token(_p(x, _u16p), D, G, bits, _p(codes, _u8p), _p(s, _u16p),
-                               _p(z, _u16p))
+                               _p(z, _u16p), int(bool(intz)))
     return codes, s, z
 
 
@@ -172,9 +175,10 @@ class KiviHead:
     slots: they advance by the number of tokens leaving each ring, mod R.
     """
 
-    def __init__(self, D, G, R, bits):
+    def __init__(self, D, G, R, bits, intz=False):
         assert R % G == 0
         self.D, self.G, self.R, self.bits = D, G, R, bits
+        self.intz = bool(intz)  # integer zero point (WindowQuant Eq.14-16)
         self.kg, self.kr, self.vg, self.vr = [], [], [], []
         self.krs = 0
         self.vrs = 0
@@ -184,7 +188,7 @@ class KiviHead:
     # count when the caller flushes.
     def _key_quant(self, X):
         for g0 in range(0, len(X), self.G):
-            self.kg.append(quantize_k_block(np.stack(X[g0:g0 + self.G]), self.bits))
+            self.kg.append(quantize_k_block(np.stack(X[g0:g0 + self.G]), self.bits, self.intz))
 
     def prefill(self, XK, XV):
         """Algorithm 1 Prefill: V first l-R tokens per token, last R fp16;
@@ -193,7 +197,7 @@ class KiviHead:
         l = XK.shape[0]
         nvq = max(l - self.R, 0)
         for t in range(nvq):
-            self.vg.append(quantize_v_token(XV[t], self.G, self.bits))
+            self.vg.append(quantize_v_token(XV[t], self.G, self.bits, self.intz))
         self.vr = [XV[t].copy() for t in range(nvq, l)]
         self.vrs = nvq % self.R
         r = l % self.R
@@ -219,7 +223,7 @@ class KiviHead:
         if flush_k and len(self.kr) == self.R:
             self.flush_k()
         if len(self.vr) > self.R:
-            self.vg.append(quantize_v_token(self.vr[0], self.G, self.bits))
+            self.vg.append(quantize_v_token(self.vr[0], self.G, self.bits, self.intz))
             self.vr = self.vr[1:]
             self.vrs = (self.vrs + 1) % self.R
 
@@ -238,8 +242,9 @@ class Segmented:
     §3.3.1): ``segs`` maps a segment position to its bit width and lists of
     quantized K groups / V tokens; ``kr``/``vr`` hold the fp16 tokens."""
 
-    def __init__(self, D, G, R, seg_bits):
+    def __init__(self, D, G, R, seg_bits, intz=False):
         self.D, self.G, self.R = D, G, R
+        self.intz = bool(intz)
         self.seg_bits = list(seg_bits)
         self.kg = [[] for _ in seg_bits]
         self.vg = [[] for _ in seg_bits]
@@ -261,9 +266,9 @@ class Segmented:
                 continue
             s = self.seg_bits.index(bits[w])
             for g0 in range(lo, lo + S, self.G):
-                self.kg[s].append(quantize_k_block(XK[g0:g0 + self.G], bits[w]))
+                self.kg[s].append(quantize_k_block(XK[g0:g0 + self.G], bits[w], self.intz))
             for t in range(lo, lo + S):
-                self.vg[s].append(quantize_v_token(XV[t], self.G, bits[w]))
+                self.vg[s].append(quantize_v_token(XV[t], self.G, bits[w], self.intz))
         for t in range(nw * S, XK.shape[0]):
             self.kr.append(XK[t].copy())
             self.vr.append(XV[t].copy())

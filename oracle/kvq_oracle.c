@@ -76,18 +76,61 @@ void orc_quantize_group(const uint16_t* x, int n, int stride, int bits,
   *z_out = z_h;
 }
 
-/* K block of G tokens x D channels (row-major [G][D]): one group per channel. */
+/* ---- the integer-zero-point quantizer (WindowQuant page §3.3.3): Eq.16
+ * s = (max - min) / (qmax - qmin), z = qmin - round(min / s); Eq.14
+ * Q = clamp(round(x / s) + z, qmin, qmax); Eq.15 X' = s (Q - z); unsigned
+ * range, qmin = 0.  s is stored as fp16 and used rounded, as in the KIVI
+ * quantizer; the zero point is stored as the fp16 of -s z, so that
+ * X' = Q s + stored zero as for the KIVI quantizer.  A constant group (s = 0)
+ * keeps codes 0 and stores its value as the zero (exact reconstruction). */
+void orc_quantize_group_intz(const uint16_t* x, int n, int stride, int bits,
+                             uint8_t* code, int code_stride, uint16_t* s_out,
+                             uint16_t* z_out) {
+  const int qmax = (1 << bits) - 1;
+  float mn = h2f(x[0]);
+  float mx = mn;
+  for (int i = 1; i < n; ++i) {
+    float v = h2f(x[(long)i * stride]);
+    if (v < mn) mn = v;
+    if (v > mx) mx = v;
+  }
+  float s32 = (mx - mn) / (float)qmax;
+  uint16_t s_h = f2h(s32);
+  float s = h2f(s_h);
+  if (s == 0.0f) {
+    for (int i = 0; i < n; ++i) code[(long)i * code_stride] = 0;
+    *s_out = s_h;
+    *z_out = f2h(mn);
+    return;
+  }
+  float zi = 0.0f - rintf(mn / s); /* an integer */
+  for (int i = 0; i < n; ++i) {
+    float r = rintf(h2f(x[(long)i * stride]) / s) + zi;
+    if (r < 0.0f) r = 0.0f;
+    if (r > (float)qmax) r = (float)qmax;
+    code[(long)i * code_stride] = (uint8_t)(int)r;
+  }
+  *s_out = s_h;
+  *z_out = f2h(-(s * zi));
+}
+
+/* K block of G tokens x D channels (row-major [G][D]): one group per channel;
+ * intz selects the integer-zero-point quantizer. */
 void orc_quantize_k_block(const uint16_t* x, int G, int D, int bits,
-                          uint8_t* codes, uint16_t* s, uint16_t* z) {
-  for (int c = 0; c < D; ++c)
-    orc_quantize_group(x + c, G, D, bits, codes + c, D, s + c, z + c);
+                          uint8_t* codes, uint16_t* s, uint16_t* z, int intz) {
+  for (int c = 0; c < D; ++c) {
+    if (intz) orc_quantize_group_intz(x + c, G, D, bits, codes + c, D, s + c, z + c);
+    else orc_quantize_group(x + c, G, D, bits, codes + c, D, s + c, z + c);
+  }
 }
 
 /* One V token of D channels: one group per G consecutive channels. */
 void orc_quantize_v_token(const uint16_t* x, int D, int G, int bits,
-                          uint8_t* codes, uint16_t* s, uint16_t* z) {
-  for (int g = 0; g < D / G; ++g)
-    orc_quantize_group(x + g * G, G, 1, bits, codes + g * G, 1, s + g, z + g);
+                          uint8_t* codes, uint16_t* s, uint16_t* z, int intz) {
+  for (int g = 0; g < D / G; ++g) {
+    if (intz) orc_quantize_group_intz(x + g * G, G, 1, bits, codes + g * G, 1, s + g, z + g);
+    else orc_quantize_group(x + g * G, G, 1, bits, codes + g * G, 1, s + g, z + g);
+  }
 }
 
 /* ---- packed rows: channel c at bit offset c*bits, LSB first ---------------- */

@@ -499,3 +499,78 @@ def test_eq8_vote_and_first_window(orc):
     assert bits.tolist() == [4, 2] and perm.tolist() == [0, 1]
     bits, perm = orc.window_assign_eq8(two, 0.5, 2.0, first_window_fp16=True)
     assert bits.tolist() == [16, 2] and perm.tolist() == [0, 1]
+
+
+# ---------------------------------------------------------------------------
+# integer-zero-point quantizer (WindowQuant §3.3.3 Eq.14-16)
+# ---------------------------------------------------------------------------
+def _h(v):
+    return float(np.float16(v))
+
+
+def test_intz_hand_worked_group(orc):
+    """x = (0.5, 1, 1.75, 2), 2 bits: s = 0.5, z = -round(0.5 / 0.5) = -1,
+    Q = round(x / s) + z = (0, 1, round(3.5) - 1 = 3, 4 - 1 -> clamp 3); the
+    stored zero is -s z = 0.5.  The KIVI quantizer rounds (x - min) / s
+    instead and puts 1.75 at code 2 (2.5 rounds to even)."""
+    x = np.array([0.5, 1.0, 1.75, 2.0], np.float16)
+    codes, s, z = orc.quantize_group(x, 2, intz=True)
+    assert codes.tolist() == [0, 1, 3, 3]
+    assert orc.h2f(s) == 0.5 and orc.h2f(z) == 0.5
+    kcodes, _, kz = orc.quantize_group(x, 2)
+    assert kcodes.tolist() == [0, 1, 2, 3] and orc.h2f(kz) == 0.5
+
+
+def test_intz_grid_and_error_bounds(orc):
+    """Dequantized values s (Q - z_int) lie on the grid s Z; an unclamped code
+    is within s/2 of its input, the top code within 3s/2 (the rounded scale
+    and the two roundings can leave the range one step short), each plus the
+    rounding of the fp32 quotient x / s."""
+    rng = np.random.default_rng(17)
+    for bits in (2, 4, 8):
+        qmax = (1 << bits) - 1
+        for _ in range(200):
+            x = (rng.standard_normal(32) * rng.choice([0.01, 1.0, 30.0]) + rng.normal() * 5).astype(np.float16)
+            codes, sh, zh = orc.quantize_group(x, bits, intz=True)
+            s = Fraction(orc.h2f(sh))
+            if s == 0:
+                continue
+            zs = Fraction(orc.h2f(zh))  # fp16(-s z_int)
+            zi = -Fraction(round(Fraction(float(x.min())) / s))  # only to bound the stored zero
+            assert abs(zs - (-s * zi)) <= abs(s * zi) * Fraction(1, 2048)
+            for xi, q in zip(x, codes):
+                assert 0 <= q <= qmax
+                xq = Fraction(float(xi))
+                deq = s * (int(q) - zi)
+                assert (deq / s).denominator == 1
+                # plus the rounding of the fp32 quotient x / s (|x| 2^-24 of a step)
+                bound = (s / 2 if q < qmax else 3 * s / 2) + abs(xq) * Fraction(1, 1 << 22)
+                assert abs(xq - deq) <= bound
+
+
+def test_intz_exact_grid_and_constant(orc):
+    """8 bits, inputs on the grid k s with s a power of two: exact; a constant
+    group stores its value as the zero with codes 0."""
+    s = 0.25
+    x = (np.arange(-40, 216, 1.0) * s).astype(np.float16)  # 256 points, range 255 s
+    codes, sh, zh = orc.quantize_group(x, 8, intz=True)
+    assert orc.h2f(sh) == s
+    zi = 40  # -round(-10 / 0.25)
+    assert orc.h2f(zh) == -s * zi
+    assert np.array_equal(codes.astype(np.float64) * s - s * zi, x.astype(np.float64))
+    c, sh, zh = orc.quantize_group(np.full(8, -3.5, np.float16), 4, intz=True)
+    assert c.tolist() == [0] * 8 and orc.h2f(sh) == 0.0 and orc.h2f(zh) == -3.5
+
+
+def test_intz_block_and_token_use_the_group_quantizer(orc):
+    rng = np.random.default_rng(3)
+    X = rng.standard_normal((32, 16)).astype(np.float16)
+    codes, s, z = orc.quantize_k_block(X, 4, intz=True)
+    for c in range(16):
+        cc, sc, zc = orc.quantize_group(X[:, c], 4, intz=True)
+        assert np.array_equal(codes[:, c], cc) and s[c] == sc and z[c] == zc
+    v = rng.standard_normal(64).astype(np.float16)
+    codes, s, z = orc.quantize_v_token(v, 16, 2, intz=True)
+    for g in range(4):
+        cc, sc, zc = orc.quantize_group(v[g * 16:(g + 1) * 16], 2, intz=True)
+        assert np.array_equal(codes[g * 16:(g + 1) * 16], cc) and s[g] == sc and z[g] == zc
