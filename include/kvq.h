@@ -33,6 +33,14 @@
  *   code_i = 0 if s == 0, else clamp(rint((x_i - z) / s), 0, qmax)
  *            (fp32 subtract and IEEE divide, rint = round half to even)
  *   dequantized value = code * s + z
+ * With zero_point = KVQ_ZERO_INT (WindowQuant §3.3.3 Eq.14-16, integer zero
+ * point, qmin = 0), for s != 0:
+ *   zi = -rint(mn / s)                              (IEEE fp32 divide)
+ *   code_i = clamp(rint(x_i / s) + zi, 0, qmax)     (IEEE fp32 divide)
+ *   stored zero z = fp16_round_nearest_even(-(s * zi))   (fp32 product)
+ * so that the dequantized value s (code - zi) is read as code * s + z, the
+ * same form as above (z carries fp16 rounding of s * zi); for s == 0 the codes
+ * are 0 and z = mn, as above.
  * K is quantized per channel over groups of `group` consecutive tokens; V is
  * quantized per token over groups of `group` consecutive channels.
  *
@@ -75,6 +83,12 @@ enum {
   KVQ_POLICY_FP16_TAIL = 1
 };
 
+/* Zero points of the quantizer (see "Quantizer" above). */
+enum {
+  KVQ_ZERO_MIN = 0, /* KIVI: z = min of the group, a float */
+  KVQ_ZERO_INT = 1  /* WindowQuant Eq.16: integer zero point */
+};
+
 #define KVQ_MAX_SEGMENTS 8
 
 /* One packed segment: a run of tokens quantized at one bit width.  KIVI uses
@@ -114,6 +128,7 @@ typedef struct kvq_cache {
   void* v_resid;     /* fp16 [batch][h_kv][resid_cap][d_h] */
   int32_t nkr, nvr;  /* residual K / V tokens */
   int32_t k_ring_start, v_ring_start; /* ring slot of the oldest residual token */
+  int32_t zero_point; /* KVQ_ZERO_MIN (0, the default) or KVQ_ZERO_INT */
 } kvq_cache;
 
 /* WindowQuant ingest plan (WindowQuant §3.1 Eq.7 windows, §3.3.1 reorder).

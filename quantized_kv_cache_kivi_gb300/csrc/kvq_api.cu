@@ -54,6 +54,8 @@ kvq_status validate_cache(const kvq_cache* c) {
     return fail(KVQ_ERR_INVALID_ARG, "resid_cap must be a positive multiple of group");
   if (c->policy != KVQ_POLICY_KIVI && c->policy != KVQ_POLICY_FP16_TAIL)
     return fail(KVQ_ERR_INVALID_ARG, "unknown policy %d", c->policy);
+  if (c->zero_point != KVQ_ZERO_MIN && c->zero_point != KVQ_ZERO_INT)
+    return fail(KVQ_ERR_INVALID_ARG, "unknown zero_point %d", c->zero_point);
   if (!std::isfinite(c->sm_scale)) return fail(KVQ_ERR_INVALID_ARG, "sm_scale is not finite");
   if (c->n_seg < 1 || c->n_seg > KVQ_MAX_SEGMENTS)
     return fail(KVQ_ERR_INVALID_ARG, "n_seg must be in 1..%d", KVQ_MAX_SEGMENTS);
@@ -87,8 +89,9 @@ kvq_status validate_cache(const kvq_cache* c) {
   return KVQ_OK;
 }
 
-kvq::SegDev seg_dev(const kvq_segment& g) {
+kvq::SegDev seg_dev(const kvq_segment& g, int zero_point = KVQ_ZERO_MIN) {
   kvq::SegDev d;
+  d.intz = zero_point == KVQ_ZERO_INT;
   d.kc = static_cast<const uint8_t*>(g.k_codes);
   d.ks = static_cast<const __half*>(g.k_scale);
   d.kz = static_cast<const __half*>(g.k_zero);
@@ -420,7 +423,7 @@ kvq_status append_kivi(kvq_cache* c, const void* k_new, const void* v_new, int T
   a.v_new = static_cast<const __half*>(v_new);
   a.kr = static_cast<__half*>(c->k_resid);
   a.vr = static_cast<__half*>(c->v_resid);
-  a.dst = seg_dev(last);
+  a.dst = seg_dev(last, c->zero_point);
   a.bits = last.bits;
   int fb = 0, evict = 0;
   bool flush_due = false;
@@ -509,7 +512,7 @@ kvq_status append_plan(kvq_cache* c, const void* k_new, const void* v_new, int T
   a.v_new = static_cast<const __half*>(v_new);
   a.kr = static_cast<__half*>(c->k_resid);
   a.vr = static_cast<__half*>(c->v_resid);
-  for (int s = 0; s < c->n_seg; ++s) a.seg[s] = seg_dev(c->seg[s]);
+  for (int s = 0; s < c->n_seg; ++s) a.seg[s] = seg_dev(c->seg[s], c->zero_point);
   a.krs_push = c->k_ring_start + c->nkr;
   a.vrs_push = c->v_ring_start + c->nvr;
   std::vector<int> add(c->n_seg, 0);
@@ -606,7 +609,7 @@ kvq_status kvq_flush_residual(kvq_cache* cache, void* stream) {
   a.G = G;
   a.R = R;
   a.kr = static_cast<__half*>(cache->k_resid);
-  a.dst = seg_dev(last);
+  a.dst = seg_dev(last, cache->zero_point);
   a.bits = last.bits;
   a.k_groups = n / G;
   a.k_nk0 = last.nk;
@@ -733,7 +736,7 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   a.R = cache->resid_cap;
   a.scale_log2 = cache->sm_scale * 1.4426950408889634f;
   a.n_seg = cache->n_seg;
-  for (int i = 0; i < cache->n_seg; ++i) a.seg[i] = seg_dev(cache->seg[i]);
+  for (int i = 0; i < cache->n_seg; ++i) a.seg[i] = seg_dev(cache->seg[i], cache->zero_point);
   a.kr = static_cast<const __half*>(cache->k_resid);
   a.vr = static_cast<const __half*>(cache->v_resid);
   a.krs = cache->k_ring_start;

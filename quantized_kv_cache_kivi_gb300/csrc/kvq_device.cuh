@@ -71,6 +71,55 @@ __device__ __forceinline__ uint32_t qcode_exact(float x, float z, float s) {
   return min(__float2uint_rn(rintf(__fdiv_rn(__fsub_rn(x, z), s))), (1u << BITS) - 1u);
 }
 
+// Integer zero point (WindowQuant §3.3.3 Eq.14-16, qmin = 0): p.z is the
+// integer zi = -rint(mn / s) as fp32, p.zh the stored zero fp16(-s zi); a
+// constant group (s = 0) stores mn and codes 0, as the KIVI quantizer.
+__device__ __forceinline__ QParams qparams_intz(float mn, float mx, int bits) {
+  const float qmax = (float)((1 << bits) - 1);
+  QParams p;
+  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+  p.sh = __float2half_rn(s32);
+  p.s = __half2float(p.sh);
+  if (p.s == 0.0f) {
+    p.z = 0.0f;
+    p.zh = __float2half_rn(mn);
+  } else {
+    p.z = __fsub_rn(0.0f, rintf(__fdiv_rn(mn, p.s)));
+    p.zh = __float2half_rn(-__fmul_rn(p.s, p.z));
+  }
+  return p;
+}
+
+// clamp(rint(x / s) + zi, 0, qmax): the product x * (1/s) decides unless it
+// lies within 1e-4 of a rounding tie, then the IEEE quotient does.
+template <int BITS>
+__device__ __forceinline__ uint32_t qcode_intz_guess(float x, float zi, float rcp, bool& near_tie) {
+  const float t = __fmul_rn(x, rcp);
+  const float r = rintf(t);
+  near_tie = fabsf(t - r) > 0.4999f;
+  return (uint32_t)min(max(__float2int_rn(r + zi), 0), (1 << BITS) - 1);
+}
+template <int BITS>
+__device__ __forceinline__ uint32_t qcode_intz_exact(float x, float zi, float s) {
+  if (s == 0.0f) return 0u;
+  return (uint32_t)min(max(__float2int_rn(rintf(__fdiv_rn(x, s)) + zi), 0), (1 << BITS) - 1);
+}
+template <int BITS>
+__device__ __forceinline__ uint32_t qcode_intz_fast(float x, float zi, float s, float rcp) {
+  bool tie;
+  const uint32_t c = qcode_intz_guess<BITS>(x, zi, rcp, tie);
+  return tie ? qcode_intz_exact<BITS>(x, zi, s) : c;
+}
+
+// Either quantizer, by the destination's zero point.
+__device__ __forceinline__ QParams qparams_any(float mn, float mx, int bits, int intz) {
+  return intz ? qparams_intz(mn, mx, bits) : qparams(mn, mx, bits);
+}
+template <int BITS>
+__device__ __forceinline__ uint32_t qcode_any(float x, float z, float s, float rcp, int intz) {
+  return intz ? qcode_intz_fast<BITS>(x, z, s, rcp) : qcode_fast<BITS>(x, z, s, rcp);
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory address, mbarrier and 1-D bulk copy (TMA engine, no tensor map)
 // ---------------------------------------------------------------------------

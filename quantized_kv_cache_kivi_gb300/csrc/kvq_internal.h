@@ -41,6 +41,7 @@ struct SegDev {
   const __half* vz;
   int bits;
   int cap;
+  int intz;  // quantize with the integer zero point (WindowQuant Eq.14-16)
 };
 
 // A run of consecutive attention positions whose K comes from one source and

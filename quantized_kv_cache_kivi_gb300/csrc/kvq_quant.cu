@@ -125,7 +125,7 @@ __device__ void quant_k_group(const SegDev& dst, int G, int R, size_t pair,
       lo = fminf(lo, q.red[w * D + tid]);
       hi = fmaxf(hi, q.red[(NWARP + w) * D + tid]);
     }
-    const QParams qp = qparams(lo, hi, BITS);
+    const QParams qp = qparams_any(lo, hi, BITS, dst.intz);
     const size_t gidx = (pair * (size_t)(dst.cap / G) + grow) * D + tid;
     const_cast<__half*>(dst.ks)[gidx] = qp.sh;
     const_cast<__half*>(dst.kz)[gidx] = qp.zh;
@@ -151,12 +151,15 @@ __device__ void quant_k_group(const SegDev& dst, int G, int R, size_t pair,
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       bool t;
-      c[e] = qcode_guess<BITS>(__half2float(h[e]), cz[e], cr[e], t);
+      c[e] = dst.intz ? qcode_intz_guess<BITS>(__half2float(h[e]), cz[e], cr[e], t)
+                      : qcode_guess<BITS>(__half2float(h[e]), cz[e], cr[e], t);
       tie |= t;
     }
     if (tie) {  // rare: redo the chunk with IEEE quotients
 #pragma unroll
-      for (int e = 0; e < 8; ++e) c[e] = qcode_exact<BITS>(__half2float(h[e]), cz[e], cs[e]);
+      for (int e = 0; e < 8; ++e)
+        c[e] = dst.intz ? qcode_intz_exact<BITS>(__half2float(h[e]), cz[e], cs[e])
+                        : qcode_exact<BITS>(__half2float(h[e]), cz[e], cs[e]);
     }
     uint32_t lo = 0, hi = 0;  // codes 0-3 and 4-7 (8 codes = BITS bytes)
 #pragma unroll
@@ -204,13 +207,13 @@ __device__ void quant_v_token(const SegDev& dst, int bits, int G, size_t pair, c
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
   if (!active) return;
-  const QParams qp = qparams(mn, mx, bits);
+  const QParams qp = qparams_any(mn, mx, bits, dst.intz);
   const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
   uint32_t packed = 0;
   for (int j = 0; j < 4; ++j) {
-    const uint32_t c = bits == 2 ? qcode_fast<2>(v[j], qp.z, qp.s, rcp)
-                       : bits == 4 ? qcode_fast<4>(v[j], qp.z, qp.s, rcp)
-                                   : qcode_fast<8>(v[j], qp.z, qp.s, rcp);
+    const uint32_t c = bits == 2 ? qcode_any<2>(v[j], qp.z, qp.s, rcp, dst.intz)
+                       : bits == 4 ? qcode_any<4>(v[j], qp.z, qp.s, rcp, dst.intz)
+                                   : qcode_any<8>(v[j], qp.z, qp.s, rcp, dst.intz);
     packed |= c << (j * bits);
   }
   const int rb = D * bits / 8;
@@ -360,10 +363,10 @@ constexpr int kBulkThreads = 256;
 
 template <int BITS>
 __device__ __forceinline__ uint32_t pack4(const float (&x)[4], const float (&s)[4], const float (&r)[4],
-                                          const float (&z)[4]) {
+                                          const float (&z)[4], int intz) {
   uint32_t p = 0;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) p |= qcode_fast<BITS>(x[e], z[e], s[e], r[e]) << (e * BITS);
+  for (int e = 0; e < 4; ++e) p |= qcode_any<BITS>(x[e], z[e], s[e], r[e], intz) << (e * BITS);
   return p;
 }
 
@@ -402,7 +405,7 @@ __device__ __forceinline__ void quant_group_warp(const __half* src, const SegDev
   __half sh[4], zh[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const QParams qp = qparams(mn[e], mx[e], BITS);
+    const QParams qp = qparams_any(mn[e], mx[e], BITS, dst.intz);
     s[e] = qp.s;
     r[e] = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
     z[e] = qp.z;
@@ -422,7 +425,7 @@ __device__ __forceinline__ void quant_group_warp(const __half* src, const SegDev
     const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
     const float f[4] = {f0.x, f0.y, f1.x, f1.y};
-    const uint32_t p = pack4<BITS>(f, s, r, z);
+    const uint32_t p = pack4<BITS>(f, s, r, z, dst.intz);
     uint8_t* o = out + (size_t)j * rb + lane * (BITS / 2);
     if constexpr (BITS == 2) *o = (uint8_t)p;
     else if constexpr (BITS == 4) *reinterpret_cast<uint16_t*>(o) = (uint16_t)p;
@@ -449,13 +452,13 @@ __device__ __forceinline__ void quant_token_half(const float (&f)[8], bool live,
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
   if (!live) return;
-  const QParams qp = qparams(mn, mx, BITS);
+  const QParams qp = qparams_any(mn, mx, BITS, dst.intz);
   const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
   uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    lo |= qcode_fast<BITS>(f[e], qp.z, qp.s, rcp) << (e * BITS);
-    hi |= qcode_fast<BITS>(f[e + 4], qp.z, qp.s, rcp) << (e * BITS);
+    lo |= qcode_any<BITS>(f[e], qp.z, qp.s, rcp, dst.intz) << (e * BITS);
+    hi |= qcode_any<BITS>(f[e + 4], qp.z, qp.s, rcp, dst.intz) << (e * BITS);
   }
   const size_t row = pair * (size_t)dst.cap + (size_t)row_in_pair;
   uint8_t* o = const_cast<uint8_t*>(dst.vc) + row * (D * BITS / 8) + hl * BITS;

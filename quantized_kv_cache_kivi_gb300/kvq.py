@@ -23,6 +23,7 @@ KVQ_ERR_CUDA = -4
 KVQ_ERR_WORKSPACE = -5
 KVQ_POLICY_KIVI = 0
 KVQ_POLICY_FP16_TAIL = 1
+KVQ_ZERO_MIN, KVQ_ZERO_INT = 0, 1
 KVQ_MAX_SEGMENTS = 8
 KVQ_MAX_SPLITS = 128
 
@@ -43,7 +44,8 @@ class kvq_cache(ctypes.Structure):
                 ("seg", kvq_segment * KVQ_MAX_SEGMENTS),
                 ("k_resid", ctypes.c_void_p), ("v_resid", ctypes.c_void_p),
                 ("nkr", ctypes.c_int32), ("nvr", ctypes.c_int32),
-                ("k_ring_start", ctypes.c_int32), ("v_ring_start", ctypes.c_int32)]
+                ("k_ring_start", ctypes.c_int32), ("v_ring_start", ctypes.c_int32),
+                ("zero_point", ctypes.c_int32)]
 
 
 class kvq_window_plan(ctypes.Structure):
@@ -251,13 +253,14 @@ class Cache:
 
 
 def alloc_cache(batch, h_kv, h_q, d_h, group, resid_cap, segments, policy=KVQ_POLICY_KIVI,
-                sm_scale=None, device="cuda"):
+                sm_scale=None, device="cuda", zero_point=0):
     """segments: list of (bits, capacity); each capacity is rounded up to a
     multiple of ``group`` (the layout kvq.h requires).  Buffers are zero-filled."""
     import torch
     c = kvq_cache()
     c.batch, c.h_kv, c.h_q, c.d_h, c.group = batch, h_kv, h_q, d_h, group
     c.resid_cap, c.policy = resid_cap, policy
+    c.zero_point = zero_point
     c.sm_scale = float(sm_scale if sm_scale is not None else 1.0 / math.sqrt(d_h))
     c.n_seg = len(segments)
     tensors = {}

@@ -30,15 +30,17 @@ class KiviPair:
     """A GPU cache and per-head oracle caches fed with the same tokens."""
 
     def __init__(self, batch, h_kv, h_q, d, G, R, bits, cap, policy=kvq.KVQ_POLICY_KIVI,
-                 heads=None):
+                 heads=None, zero_point=0):
         self.batch, self.h_kv, self.h_q, self.d, self.G, self.R, self.bits = \
             batch, h_kv, h_q, d, G, R, bits
-        self.gpu = kvq.alloc_cache(batch, h_kv, h_q, d, G, R, [(bits, cap)], policy=policy)
+        self.gpu = kvq.alloc_cache(batch, h_kv, h_q, d, G, R, [(bits, cap)], policy=policy,
+                                   zero_point=zero_point)
         self.cap = self.gpu.c.seg[0].capacity
         # oracle heads (optionally only a sample of (b, h) pairs)
         self.heads = heads if heads is not None else [(b, h) for b in range(batch)
                                                       for h in range(h_kv)]
-        self.orc = {bh: oracle.KiviHead(d, G, R, bits) for bh in self.heads}
+        self.orc = {bh: oracle.KiviHead(d, G, R, bits, intz=zero_point == kvq.KVQ_ZERO_INT)
+                    for bh in self.heads}
         self.started = False
 
     # -- stepping ---------------------------------------------------------

@@ -116,6 +116,26 @@ def test_attention_parity(d, G, R, bits, gq):
         assert pair.attention_error(_q(6 + t, B, H * gq, d)) < TOL
 
 
+@pytest.mark.parametrize("d,G,R,bits,gq", [(128, 32, 64, 2, 1), (128, 64, 128, 4, 4), (128, 32, 32, 8, 7),
+                                           (64, 16, 32, 4, 1)])
+def test_integer_zero_point_bit_exact_and_attention(d, G, R, bits, gq):
+    """WindowQuant's integer zero point (Eq.14-16): codes, scales and stored
+    zeros bit-exact through prefill (bulk kernels), decode steps (ring
+    evictions, flushes) and a bulk append; attention within tolerance."""
+    B, H = 2, 2
+    pair = KiviPair(B, H, H * gq, d, G, R, bits, cap=2048, zero_point=kvq.KVQ_ZERO_INT)
+    l = 6 * R + 9
+    K, V = kv(61 + bits, B, H, l + 2 * R + 40, d)
+    pair.prefill(K[:, :, :l], V[:, :, :l])
+    pair.assert_buffers_bit_exact()
+    for t in range(l, l + R + 3):
+        pair.append(K[:, :, t:t + 1], V[:, :, t:t + 1])
+    pair.assert_buffers_bit_exact()
+    pair.append(K[:, :, l + R + 3:], V[:, :, l + R + 3:])
+    pair.assert_buffers_bit_exact()
+    assert pair.attention_error(_q(8, B, H * gq, d)) < TOL
+
+
 @pytest.mark.parametrize("G,bits,gq,ws_splits", [(32, 2, 1, None), (64, 4, 4, None), (32, 2, 1, 3)])
 def test_attention_many_pairs_repeatable(G, bits, gq, ws_splits):
     """Many (batch, kv head) pairs cut into stream-K ranges, with the default
@@ -307,7 +327,7 @@ def test_window_assign_matches_oracle():
     assert np.array_equal(bits16, ob16) and np.array_equal(perm16, op16)
 
 
-def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, perm=None):
+def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, perm=None, zero_point=0):
     vis, txt = synth.window_keys(seed, B, H, n_win, S, n_text, d)
     M = n_win * S
     Vv = np.stack([np.stack([synth.values(seed, b, h, M, d) for h in range(H)]) for b in range(B)])
@@ -318,7 +338,7 @@ def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, 
         bits, perm = oracle.window_assign(sim, 0.1, 0.3, first_window_fp16=first16)
     caps = [(b, int(((bits == b).sum() * S + G - 1) // G * G) or G) for b in (8, 4, 2)]
     R = 128 + int((bits == 16).sum()) * S
-    c = kvq.alloc_cache(B, H, H * gq, d, G, R, caps, policy=kvq.KVQ_POLICY_FP16_TAIL)
+    c = kvq.alloc_cache(B, H, H * gq, d, G, R, caps, policy=kvq.KVQ_POLICY_FP16_TAIL, zero_point=zero_point)
     plan = kvq.make_plan(S, bits, perm)
     tail = 5  # vision tokens past the last whole window stay fp16
     extra_k = np.concatenate([vis, vis[:, :, :tail]], axis=2)
@@ -328,7 +348,7 @@ def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, 
     heads = {}
     for b in range(B):
         for h in range(H):
-            o = oracle.Segmented(d, G, R, [8, 4, 2])
+            o = oracle.Segmented(d, G, R, [8, 4, 2], intz=zero_point == kvq.KVQ_ZERO_INT)
             o.ingest_windows(extra_k[b, h], extra_v[b, h], S, bits, perm)
             o.append_fp16(txt[b, h], Vt[b, h])
             heads[(b, h)] = o
@@ -380,15 +400,15 @@ def test_windowquant_eq8_ingest_and_attention():
     _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, 3, False, bits, perm)
 
 
-@pytest.mark.parametrize("first16", [False, True])
-def test_windowquant_ingest_and_attention(first16):
+@pytest.mark.parametrize("first16,zero_point", [(False, 0), (True, 0), (False, 1)])
+def test_windowquant_ingest_and_attention(first16, zero_point):
     n_win, S, n_text, B, H, gq, d, G = 16, 64, 24, 2, 2, 7, 128, 32
-    _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, 3, first16, None, None)
+    _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, 3, first16, None, None, zero_point)
 
 
-def _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, seed, first16, bits, perm):
+def _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, seed, first16, bits, perm, zero_point=0):
     c, heads, caps, R = _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed=seed, first16=first16,
-                                  bits=bits, perm=perm)
+                                  bits=bits, perm=perm, zero_point=zero_point)
     torch.cuda.synchronize()
     P = B * H
     q = synth.q_block(9, B, H * gq, d)
