@@ -197,25 +197,34 @@ __device__ __forceinline__ bool try_wait_at(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: about 2^31 SM clocks, then the abort flag is raised.  The
-// warps that run ahead (bulk copies, K table) sleep between polls, up to
-// 128 ns, so their polling leaves issue slots to the consumer warps without
-// adding much to the stage round trip; the consumers poll without sleeping.
+// The same with a suspend-time hint: the waiting thread may sleep in the
+// barrier unit until the phase completes (or about `ns` nanoseconds pass)
+// instead of spinning through issue slots the working warps need.
+__device__ __forceinline__ bool try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: about 2^31 SM clocks, then the abort flag is raised.  Every
+// warp waits inside the barrier unit (suspend-time hint) rather than
+// spinning, so a waiting warp leaves its issue slots to the working ones.
 template <bool BACKOFF>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   const uint32_t addr = smem_u32(bar);
   if (try_wait_at(addr, parity)) return true;
   const long long t0 = clock64();
-  uint32_t ns = 32;
-  while (!try_wait_at(addr, parity)) {
+  while (!try_wait_sleep(addr, parity, 20000u)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > (1ll << 31)) {
       *abort_flag = 1;
       return false;
-    }
-    if (BACKOFF) {
-      __nanosleep(ns);
-      ns = ns < 128 ? 2 * ns : ns;
     }
   }
   return true;
