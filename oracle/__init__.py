@@ -51,7 +51,7 @@ def lib():
         L.orc_attention_dense.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p, _f64p,
                                           ctypes.c_double, _f64p, _f64p]
         pp = ctypes.POINTER(ctypes.c_void_p)
-        L.orc_dequant_head.argtypes = [ctypes.c_int] * 4 + [_i32p] * 3 + [pp] * 6 + \
+        L.orc_dequant_head.argtypes = [ctypes.c_int] * 5 + [_i32p] * 3 + [pp] * 6 + \
             [_u16p, _u16p] + [ctypes.c_int] * 4 + [_f64p, _f64p]
         L.orc_dequant_head.restype = ctypes.c_int
         L.orc_window_sims.argtypes = [_u16p, _u16p] + [ctypes.c_int] * 6 + [_f64p]
@@ -175,9 +175,10 @@ class KiviHead:
     slots: they advance by the number of tokens leaving each ring, mod R.
     """
 
-    def __init__(self, D, G, R, bits, intz=False):
+    def __init__(self, D, G, R, bits, intz=False, Gv=None):
         assert R % G == 0
         self.D, self.G, self.R, self.bits = D, G, R, bits
+        self.Gv = Gv or G  # V channel group (default: the K token group)
         self.intz = bool(intz)  # integer zero point (WindowQuant Eq.14-16)
         self.kg, self.kr, self.vg, self.vr = [], [], [], []
         self.krs = 0
@@ -197,7 +198,7 @@ class KiviHead:
         l = XK.shape[0]
         nvq = max(l - self.R, 0)
         for t in range(nvq):
-            self.vg.append(quantize_v_token(XV[t], self.G, self.bits, self.intz))
+            self.vg.append(quantize_v_token(XV[t], self.Gv, self.bits, self.intz))
         self.vr = [XV[t].copy() for t in range(nvq, l)]
         self.vrs = nvq % self.R
         r = l % self.R
@@ -223,7 +224,7 @@ class KiviHead:
         if flush_k and len(self.kr) == self.R:
             self.flush_k()
         if len(self.vr) > self.R:
-            self.vg.append(quantize_v_token(self.vr[0], self.G, self.bits, self.intz))
+            self.vg.append(quantize_v_token(self.vr[0], self.Gv, self.bits, self.intz))
             self.vr = self.vr[1:]
             self.vrs = (self.vrs + 1) % self.R
 
@@ -242,8 +243,9 @@ class Segmented:
     §3.3.1): ``segs`` maps a segment position to its bit width and lists of
     quantized K groups / V tokens; ``kr``/``vr`` hold the fp16 tokens."""
 
-    def __init__(self, D, G, R, seg_bits, intz=False):
+    def __init__(self, D, G, R, seg_bits, intz=False, Gv=None):
         self.D, self.G, self.R = D, G, R
+        self.Gv = Gv or G
         self.intz = bool(intz)
         self.seg_bits = list(seg_bits)
         self.kg = [[] for _ in seg_bits]
@@ -268,7 +270,7 @@ class Segmented:
             for g0 in range(lo, lo + S, self.G):
                 self.kg[s].append(quantize_k_block(XK[g0:g0 + self.G], bits[w], self.intz))
             for t in range(lo, lo + S):
-                self.vg[s].append(quantize_v_token(XV[t], self.G, bits[w], self.intz))
+                self.vg[s].append(quantize_v_token(XV[t], self.Gv, bits[w], self.intz))
         for t in range(nw * S, XK.shape[0]):
             self.kr.append(XK[t].copy())
             self.vr.append(XV[t].copy())
@@ -282,9 +284,9 @@ class Segmented:
 
 def _head_buffers(head, seg_bits, seg_caps, kg_lists, vg_lists):
     """Serialize one head's state into the library's buffer layout (kvq.h):
-    codes [cap][D*bits/8], k scale/zero [cap/G][D], v scale/zero [cap][D/G],
+    codes [cap][D*bits/8], k scale/zero [cap/G][D], v scale/zero [cap][D/Gv],
     ring [R][D] with residual token i at slot (start + i) % R."""
-    D, G, R = head.D, head.G, head.R
+    D, G, R, Gv = head.D, head.G, head.R, head.Gv
     out = []
     for s, (b, cap) in enumerate(zip(seg_bits, seg_caps)):
         rb = D * b // 8
@@ -292,8 +294,8 @@ def _head_buffers(head, seg_bits, seg_caps, kg_lists, vg_lists):
         ks = np.zeros((cap // G, D), np.uint16)
         kz = np.zeros((cap // G, D), np.uint16)
         vc = np.zeros((cap, rb), np.uint8)
-        vs = np.zeros((cap, D // G), np.uint16)
-        vz = np.zeros((cap, D // G), np.uint16)
+        vs = np.zeros((cap, D // Gv), np.uint16)
+        vz = np.zeros((cap, D // Gv), np.uint16)
         for gi, (codes, sc, zc) in enumerate(kg_lists[s]):
             for j in range(G):
                 kc[gi * G + j] = pack_row(codes[j], b)
@@ -321,7 +323,7 @@ def head_buffers(head, caps):
     return _head_buffers(head, head.seg_bits, caps, head.kg, head.vg)
 
 
-def dequant_head(segs, kr, vr, nkr, nvr, krs, vrs, D, G, R):
+def dequant_head(segs, kr, vr, nkr, nvr, krs, vrs, D, G, R, Gv=None):
     """Dense fp64 K, V [L][D] of one head from its serialized buffers, in the
     attention token order: segments, then the ring from its start slot."""
     n = len(segs)
@@ -345,7 +347,7 @@ def dequant_head(segs, kr, vr, nkr, nvr, krs, vrs, D, G, R):
     vc, vs, vz = arr("v_codes", _u8p), arr("v_scale", _u16p), arr("v_zero", _u16p)
     kr = _as_u16(kr)
     vr = _as_u16(vr)
-    got = lib().orc_dequant_head(D, G, R, n, _p(bits, _i32p), _p(nk, _i32p), _p(nv, _i32p),
+    got = lib().orc_dequant_head(D, G, Gv or G, R, n, _p(bits, _i32p), _p(nk, _i32p), _p(nv, _i32p),
                                  kc, ks, kz, vc, vs, vz, _p(kr, _u16p), _p(vr, _u16p),
                                  nkr, nvr, krs, vrs, _p(K, _f64p), _p(V, _f64p))
     if got < 0:

@@ -181,11 +181,12 @@ void orc_attention_dense(int L, int D, const double* K, const double* V,
 /* ---- dequantize one (batch, kv-head) cache into dense fp64 K and V --------
  * Per segment s: codes/scales/zeros point at this head's slice
  * (k_codes [cap][D*bits/8], k_scale/k_zero [cap/G][D], v_codes likewise,
- * v_scale/v_zero [cap][D/G]).  The ring slices are [R][D] fp16.
+ * v_scale/v_zero [cap][D/Gv]: K groups of G tokens, V groups of Gv
+ * channels).  The ring slices are [R][D] fp16.
  * Token order: segment 0 .. n_seg-1 packed tokens, then the ring from its
  * start slot.  Returns the token count L (same for K and V) or -1 if the
  * K and V counts differ. */
-int orc_dequant_head(int D, int G, int R, int n_seg, const int* bits,
+int orc_dequant_head(int D, int G, int Gv, int R, int n_seg, const int* bits,
                      const int* nk, const int* nv, const uint8_t* const* kc,
                      const uint16_t* const* ks, const uint16_t* const* kz,
                      const uint8_t* const* vc, const uint16_t* const* vs,
@@ -220,9 +221,9 @@ int orc_dequant_head(int D, int G, int R, int n_seg, const int* bits,
     for (int u = 0; u < nv[s]; ++u, ++t) {
       orc_unpack_row(vc[s] + (long)u * rb, D, bits[s], codes);
       for (int c = 0; c < D; ++c) {
-        const int g = c / G;
-        V[(long)t * D + c] = (double)codes[c] * (double)h2f(vs[s][(long)u * (D / G) + g]) +
-                             (double)h2f(vz[s][(long)u * (D / G) + g]);
+        const int g = c / Gv;
+        V[(long)t * D + c] = (double)codes[c] * (double)h2f(vs[s][(long)u * (D / Gv) + g]) +
+                             (double)h2f(vz[s][(long)u * (D / Gv) + g]);
       }
     }
   }

@@ -574,3 +574,27 @@ def test_intz_block_and_token_use_the_group_quantizer(orc):
     for g in range(4):
         cc, sc, zc = orc.quantize_group(v[g * 16:(g + 1) * 16], 2, intz=True)
         assert np.array_equal(codes[g * 16:(g + 1) * 16], cc) and s[g] == sc and z[g] == zc
+
+
+def test_separate_v_group(orc):
+    """K groups of G tokens, V groups of Gv channels (G = 8, Gv = 4 here):
+    the serialized buffers carry D / Gv V scales per token, and the dequantized
+    V of every token is its per-group codes * scale + zero."""
+    D, G, Gv, R = 16, 8, 4, 16
+    rng = np.random.default_rng(12)
+    XK = rng.standard_normal((40, D)).astype(np.float16)
+    XV = rng.standard_normal((40, D)).astype(np.float16)
+    head = orc.KiviHead(D, G, R, 4, Gv=Gv)
+    head.prefill(XK, XV)
+    segs, kr, vr = orc.head_buffers(head, [64])
+    assert segs[0]["v_scale"].shape == (64, D // Gv)
+    K, V = orc.dequant_head(segs, kr, vr, len(head.kr), len(head.vr), head.krs, head.vrs, D, G, R, Gv)
+    for t in range(head.nv):
+        codes, s, z = orc.quantize_v_token(XV[t], Gv, 4)
+        want = [codes[c] * orc.h2f(s[c // Gv]) + orc.h2f(z[c // Gv]) for c in range(D)]
+        assert np.array_equal(V[t], np.array(want))
+    for gi in range(head.nk // G):
+        codes, s, z = orc.quantize_k_block(XK[gi * G:(gi + 1) * G], 4)
+        for j in range(G):
+            want = [codes[j, c] * orc.h2f(s[c]) + orc.h2f(z[c]) for c in range(D)]
+            assert np.array_equal(K[gi * G + j], np.array(want))
