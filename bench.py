@@ -165,11 +165,12 @@ def cache_bytes(cache):
     packed codes + fp16 scales/zeros of every segment + the fp16 rings."""
     c = cache.c
     P, d, G = c.batch * c.h_kv, c.d_h, c.group
+    Gv = c.group_v or G
     per = (c.nkr + c.nvr) * d * 2
     for i in range(c.n_seg):
         s = c.seg[i]
         per += s.nk * d * s.bits // 8 + (s.nk // G) * d * 4
-        per += s.nv * d * s.bits // 8 + s.nv * (d // G) * 4
+        per += s.nv * d * s.bits // 8 + s.nv * (d // Gv) * 4
     return P * per
 
 

@@ -42,7 +42,8 @@
  * same form as above (z carries fp16 rounding of s * zi); for s == 0 the codes
  * are 0 and z = mn, as above.
  * K is quantized per channel over groups of `group` consecutive tokens; V is
- * quantized per token over groups of `group` consecutive channels.
+ * quantized per token over groups of `group_v` consecutive channels (group_v
+ * = 0 means group_v = group).
  *
  * Packed code layout (identical for K and V)
  * ------------------------------------------
@@ -103,8 +104,8 @@ typedef struct kvq_segment {
   void* k_scale;    /* fp16 [batch][h_kv][capacity/group][d_h] */
   void* k_zero;     /* fp16 [batch][h_kv][capacity/group][d_h] */
   void* v_codes;    /* u8   [batch][h_kv][capacity][d_h*bits/8] */
-  void* v_scale;    /* fp16 [batch][h_kv][capacity][d_h/group] */
-  void* v_zero;     /* fp16 [batch][h_kv][capacity][d_h/group] */
+  void* v_scale;    /* fp16 [batch][h_kv][capacity][d_h/group_v] */
+  void* v_zero;     /* fp16 [batch][h_kv][capacity][d_h/group_v] */
 } kvq_segment;
 
 /* The cache: packed segments plus one fp16 residual ring for K and one for V.
@@ -118,7 +119,7 @@ typedef struct kvq_cache {
   int32_t h_kv;      /* kv heads */
   int32_t h_q;       /* query heads; a multiple of h_kv (GQA when larger) */
   int32_t d_h;       /* head dim: 64 or 128 */
-  int32_t group;     /* G: quantization group (tokens for K, channels for V) */
+  int32_t group;     /* G: K quantization group in tokens (also V's, see group_v) */
   int32_t resid_cap; /* R: ring capacity in tokens, a multiple of group */
   int32_t policy;    /* KVQ_POLICY_* */
   float sm_scale;    /* softmax scale applied to q.k (1/sqrt(d_h) typical) */
@@ -129,6 +130,10 @@ typedef struct kvq_cache {
   int32_t nkr, nvr;  /* residual K / V tokens */
   int32_t k_ring_start, v_ring_start; /* ring slot of the oldest residual token */
   int32_t zero_point; /* KVQ_ZERO_MIN (0, the default) or KVQ_ZERO_INT */
+  int32_t group_v;    /* V quantization group in channels, a power of two
+                         dividing d_h, at least 8; 0 = group (WindowQuant
+                         §3.3.3: K groups of one window, S tokens, beside
+                         per-token V groups) */
 } kvq_cache;
 
 /* WindowQuant ingest plan (WindowQuant §3.1 Eq.7 windows, §3.3.1 reorder).

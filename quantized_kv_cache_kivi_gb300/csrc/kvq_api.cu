@@ -38,6 +38,9 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 // ---------------------------------------------------------------------------
 // cache validation
 // ---------------------------------------------------------------------------
+// V quantization group in channels (group_v, or group when 0).
+int group_v(const kvq_cache* c) { return c->group_v ? c->group_v : c->group; }
+
 kvq_status validate_cache(const kvq_cache* c) {
   if (!c) return fail(KVQ_ERR_INVALID_ARG, "cache is NULL");
   if (c->batch < 1 || c->h_kv < 1 || c->h_q < 1)
@@ -46,10 +49,12 @@ kvq_status validate_cache(const kvq_cache* c) {
   if (c->h_q / c->h_kv > kvq::kMaxGq)
     return fail(KVQ_ERR_UNSUPPORTED, "more than %d query heads per kv head", kvq::kMaxGq);
   if (c->d_h != 64 && c->d_h != 128) return fail(KVQ_ERR_UNSUPPORTED, "d_h must be 64 or 128");
-  const int G = c->group;
-  if (G != 16 && G != 32 && G != 64 && G != 128)
-    return fail(KVQ_ERR_UNSUPPORTED, "group must be 16, 32, 64 or 128");
-  if (c->d_h % G != 0) return fail(KVQ_ERR_INVALID_ARG, "d_h must be a multiple of group");
+  const int G = c->group, Gv = group_v(c);
+  if (G != 16 && G != 32 && G != 64 && G != 128 && G != 256)
+    return fail(KVQ_ERR_UNSUPPORTED, "group must be 16, 32, 64, 128 or 256");
+  if (Gv != 8 && Gv != 16 && Gv != 32 && Gv != 64 && Gv != 128)
+    return fail(KVQ_ERR_UNSUPPORTED, "the V group (group_v, or group) must be 8 .. 128, a power of two");
+  if (c->d_h % Gv != 0) return fail(KVQ_ERR_INVALID_ARG, "d_h must be a multiple of the V group");
   if (c->resid_cap < G || c->resid_cap % G != 0)
     return fail(KVQ_ERR_INVALID_ARG, "resid_cap must be a positive multiple of group");
   if (c->policy != KVQ_POLICY_KIVI && c->policy != KVQ_POLICY_FP16_TAIL)
@@ -119,24 +124,24 @@ struct Piece {
   int len;
 };
 
-int tile_bytes(int tile, int kbits, int vbits, int d, int G) {
+int tile_bytes(int tile, int kbits, int vbits, int d, int G, int Gv) {
   auto a16 = [](int x) { return (x + 15) & ~15; };
   int b = a16(tile * d * kbits / 8) + a16(tile * d * vbits / 8);
   if (kbits != 16) b += 2 * ((tile + G - 1) / G + 1) * d * 2;
-  if (vbits != 16) b += 2 * a16(tile * (d / G) * 2);
+  if (vbits != 16) b += 2 * a16(tile * (d / Gv) * 2);
   return b;
 }
 
 // Tile of the one-query-head kernel: nw consumer warps x wt tokens each,
 // the largest that fits one stage and the scaled-query table.
 // Among equal token counts, more warps (a smaller slice) wins.
-void choose_tile_mha(int kbits, int vbits, int d, int G, int* tile, int* wt) {
+void choose_tile_mha(int kbits, int vbits, int d, int G, int Gv, int* tile, int* wt) {
   *tile = *wt = 0;
   int best_nw = 0;
   for (int w = 32; w >= 8; w >>= 1) {
     for (int nw = kvq::kMhaConsumerWarps; nw >= 1; --nw) {
       const int t = w * nw;
-      if (tile_bytes(t, kbits, vbits, d, G) > kvq::kMhaStageBytes) continue;
+      if (tile_bytes(t, kbits, vbits, d, G, Gv) > kvq::kMhaStageBytes) continue;
       if (kbits != 16 && (t + G - 1) / G + 1 > kvq::kMhaMaxGroups) continue;
       if (t > *tile || (t == *tile && nw > best_nw)) {
         *tile = t;
@@ -148,15 +153,12 @@ void choose_tile_mha(int kbits, int vbits, int d, int G, int* tile, int* wt) {
   }
 }
 
-// Tile of the tensor-core kernel: nw <= 4 consumer warps x wt tokens each
-// (wt a multiple of 16), the largest that fits one stage and the K operand
-// table; among equal token counts, more warps win.
 // Tile of the tensor-core kernel: the most tokens (a multiple of the 32-token
 // unit) that fit one stage and the K operand table.
-void choose_tile_tc(int kbits, int vbits, int d, int G, int* tile, int* wt) {
+void choose_tile_tc(int kbits, int vbits, int d, int G, int Gv, int* tile, int* wt) {
   *tile = *wt = 0;
   for (int t = 256; t >= 32; t -= 32) {
-    if (tile_bytes(t, kbits, vbits, d, G) > kvq::kTcStageBytes) continue;
+    if (tile_bytes(t, kbits, vbits, d, G, Gv) > kvq::kTcStageBytes) continue;
     if (kbits != 16 && (t + G - 1) / G + 1 > kvq::kTcMaxGroups) continue;
     *tile = t;
     *wt = 32;
@@ -164,9 +166,9 @@ void choose_tile_tc(int kbits, int vbits, int d, int G, int* tile, int* wt) {
   }
 }
 
-int choose_tile(int kbits, int vbits, int d, int G, int gq) {
+int choose_tile(int kbits, int vbits, int d, int G, int Gv, int gq) {
   for (int tile = 128; tile >= 32; tile >>= 1) {
-    if (tile_bytes(tile, kbits, vbits, d, G) > kvq::kStageBytes) continue;
+    if (tile_bytes(tile, kbits, vbits, d, G, Gv) > kvq::kStageBytes) continue;
     if (kbits != 16 && ((tile + G - 1) / G + 1) * gq * d * 4 > kvq::kQsBytes) continue;
     return tile;
   }
@@ -206,9 +208,9 @@ kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>&
     const int kb = r.seg_k >= 0 ? c->seg[r.seg_k].bits : 16;
     const int vb = r.seg_v >= 0 ? c->seg[r.seg_v].bits : 16;
     r.wt = 0;
-    if (kern == K_TC) choose_tile_tc(kb, vb, c->d_h, c->group, &r.tile, &r.wt);
-    else if (kern == K_MHA) choose_tile_mha(kb, vb, c->d_h, c->group, &r.tile, &r.wt);
-    else r.tile = choose_tile(kb, vb, c->d_h, c->group, gq);
+    if (kern == K_TC) choose_tile_tc(kb, vb, c->d_h, c->group, group_v(c), &r.tile, &r.wt);
+    else if (kern == K_MHA) choose_tile_mha(kb, vb, c->d_h, c->group, group_v(c), &r.tile, &r.wt);
+    else r.tile = choose_tile(kb, vb, c->d_h, c->group, group_v(c), gq);
     if (r.tile == 0) return fail(KVQ_ERR_UNSUPPORTED, "no tile size fits shared memory");
     r.groups = (r.tile + c->group - 1) / c->group + 1;
     r.tile0 = a.n_tiles;
@@ -221,7 +223,7 @@ kvq_status plan_decode(const kvq_cache* c, kvq::DecodeArgs& a, std::vector<int>&
       // splitting by bytes alone would give the 2-bit splits three times the
       // tokens of the 8-bit ones
       const int work = kern == K_GENERAL ? n * gq * c->d_h / 2 : 0;
-      tile_cost.push_back(tile_bytes(n, kb, vb, c->d_h, c->group) + work);
+      tile_cost.push_back(tile_bytes(n, kb, vb, c->d_h, c->group, group_v(c)) + work);
     }
     a.n_tiles += nt;
     oi += len;
@@ -379,8 +381,9 @@ kvq_status verify_decode_plan(const kvq_cache* c, const kvq::DecodeArgs& a, int 
           const kvq_segment& g = c->seg[k.seg];
           const size_t cap = (size_t)g.capacity, rb = D * g.bits / 8;
           const void* ptrs[6] = {g.k_codes, g.k_scale, g.k_zero, g.v_codes, g.v_scale, g.v_zero};
+          const size_t Dv = (size_t)(D / group_v(c));
           const size_t sizes[6] = {P * cap * rb, P * (cap / G) * D * 2, P * (cap / G) * D * 2,
-                                   P * cap * rb, P * cap * (D / G) * 2, P * cap * (D / G) * 2};
+                                   P * cap * rb, P * cap * Dv * 2, P * cap * Dv * 2};
           base = static_cast<const uint8_t*>(ptrs[k.buf]);
           size = sizes[k.buf];
         }
@@ -417,6 +420,7 @@ kvq_status append_kivi(kvq_cache* c, const void* k_new, const void* v_new, int T
   a.h_kv = c->h_kv;
   a.d = c->d_h;
   a.G = G;
+  a.Gv = group_v(c);
   a.R = R;
   a.T = T;
   a.k_new = static_cast<const __half*>(k_new);
@@ -463,7 +467,7 @@ kvq_status append_kivi(kvq_cache* c, const void* k_new, const void* v_new, int T
   const int in_v = a.v_evict - a.v_ring_tokens;
   // new-token work of a bulk append (a prompt) goes to grid-wide kernels;
   // chunk 0 of the append kernel keeps the ring work
-  a.bulk = c->d_h == 128 && G >= 8 && G <= 128 && in_k + in_v > 0;
+  a.bulk = c->d_h == 128 && in_k + in_v > 0;  // V group 8..128 (validated)
   a.chunks = (!a.bulk && in_k + in_v > 0) ? 1 + std::min(256, in_k + (in_v + 63) / 64) : 1;
   if (a.chunks == 2 && a.k_ring_groups == 0 && a.v_ring_tokens == 0 && a.k_first_ring >= T &&
       a.v_first_ring >= T)
@@ -505,6 +509,7 @@ kvq_status append_plan(kvq_cache* c, const void* k_new, const void* v_new, int T
   a.h_kv = c->h_kv;
   a.d = c->d_h;
   a.G = G;
+  a.Gv = group_v(c);
   a.R = R;
   a.T = T;
   a.S = p->window;
@@ -607,6 +612,7 @@ kvq_status kvq_flush_residual(kvq_cache* cache, void* stream) {
   a.h_kv = cache->h_kv;
   a.d = cache->d_h;
   a.G = G;
+  a.Gv = group_v(cache);
   a.R = R;
   a.kr = static_cast<__half*>(cache->k_resid);
   a.dst = seg_dev(last, cache->zero_point);
@@ -662,15 +668,16 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   // one query head per kv head, one segment, each lane's channel quarter
   // inside one V group: the specialised kernel
   int kern = K_GENERAL, form = 0;
-  if (gq == 1 && cache->n_seg == 1 && cache->group >= cache->d_h / 4) {
+  const int Gk = cache->group, Gv = group_v(cache);
+  if (gq == 1 && cache->n_seg == 1 && Gv >= cache->d_h / 4 && (cache->d_h != 128 || Gk >= 32)) {
     kern = cache->d_h == 128 ? K_TC : K_MHA;
     form = 1;
-  } else if (gq >= 2 && gq <= 4 && cache->n_seg == 1 && cache->d_h == 128 && cache->group >= 64) {
+  } else if (gq >= 2 && gq <= 4 && cache->n_seg == 1 && cache->d_h == 128 && Gk >= 32 && Gv >= 64) {
     // 2-4 query heads per kv head, at most two V groups per token: the
     // tensor-core kernel's four-head form
     kern = K_TC;
     form = 4;
-  } else if (gq <= kvq::kMaxGq && cache->d_h == 128 && cache->group >= 32) {
+  } else if (gq <= kvq::kMaxGq && cache->d_h == 128 && Gk >= 32 && Gv >= 16) {
     // up to 8 query heads, any segments: the eight-head form, if every tile
     // is K and V packed at one width, packed K with ring V, or ring only
     kern = K_TC;
@@ -733,6 +740,9 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   a.G = cache->group;
   a.log2G = 0;
   while ((1 << a.log2G) < a.G) ++a.log2G;
+  a.Gv = group_v(cache);
+  a.log2Gv = 0;
+  while ((1 << a.log2Gv) < a.Gv) ++a.log2Gv;
   a.R = cache->resid_cap;
   a.scale_log2 = cache->sm_scale * 1.4426950408889634f;
   a.n_seg = cache->n_seg;

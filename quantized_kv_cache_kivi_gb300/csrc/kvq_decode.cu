@@ -153,8 +153,8 @@ __device__ void pv_packed(const DecodeArgs& a, const TileInfo& ti, const uint8_t
                           const float* sc, float (&acc)[GQ][8], float (&zsum)[GQ]) {
   constexpr int CHUNKS = D / 8, SLOTS = NT / CHUNKS, RB = D * B / 8;
   const int k = threadIdx.x % CHUNKS, slot = threadIdx.x / CHUNKS;
-  const int ngrp = D / a.G;
-  const int g = (8 * k) / a.G;
+  const int ngrp = D / a.Gv;
+  const int g = (8 * k) / a.Gv;
   const __half* vs = reinterpret_cast<const __half*>(stage + ti.vs_off);
   const __half* vz = reinterpret_cast<const __half*>(stage + ti.vz_off);
   for (int tok = slot; tok < ti.n; tok += SLOTS) {

@@ -239,8 +239,8 @@ __device__ __forceinline__ void consume_slice(const DecodeArgs& a, const TileInf
     for (int k = 0; k < CPL / 2; ++k) S.acc[k] = make_float2(S.acc[k].x * a2.x, S.acc[k].y * a2.y);
   }
   // ---- PV over this lane's tokens r + 8 i
-  const int ngv = D >> a.log2G;
-  const int gv = (cq * CPL) >> a.log2G;
+  const int ngv = D >> a.log2Gv;
+  const int gv = (cq * CPL) >> a.log2Gv;
 #pragma unroll 1
   for (int i = 0; i < TPL; ++i) {
     const int src = TPL == 4 ? (r * 4 + i) : (TPL == 2 ? (r * 4 + 2 * i) : lane);

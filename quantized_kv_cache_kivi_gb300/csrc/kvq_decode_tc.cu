@@ -524,7 +524,7 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
     // group n & 3, and one all-ones MMA sums the zero columns.  HQ = 4:
     // column n = gid is head n / 2 and group n & 1 (group 0 when d/G = 1);
     // the scales go to the code MMAs and the zeros to the all-ones MMA.
-    const int ngv = D >> a.log2G;
+    const int ngv = D >> a.log2Gv;
     const uint16_t* sp;
     const uint16_t* zp = nullptr;
     int stride;
@@ -950,8 +950,8 @@ __device__ __forceinline__ void sub_unit8(const DecodeArgs& a, int st, const TcR
     constexpr int RB = D * BV / 8;
     constexpr int NW = BV / 2;  // words per token for the thread's 16 channels
     constexpr int PH = 16 / BV;
-    const int ngv = D >> a.log2G;
-    const int g = (16 * gid) >> a.log2G;  // the lane's V group
+    const int ngv = D >> a.log2Gv;
+    const int g = (16 * gid) >> a.log2Gv;  // the lane's V group
     const uint16_t* sp = reinterpret_cast<const uint16_t*>(stage + r.vs_off) + s0 * ngv + g;
     const uint16_t* zp = reinterpret_cast<const uint16_t*>(stage + r.vz_off) + s0 * ngv + g;
     uint32_t sv[2][2], zv[2][2];  // [half][tokens (ta, tb) | (tc, td)]
@@ -1134,7 +1134,7 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
     for (int mt = 0; mt < 8; ++mt) {
       int c0, c8, p;
       v_rows<B>(gid, mt, &c0, &c8, &p);
-      const int g = c0 >> a.log2G;  // c0 and c8 share their group
+      const int g = c0 >> a.log2Gv;  // c0 and c8 share their group
       if constexpr (HQ == 1) {
         // z sum of group g: column 4 + g, held by lanes with tig = 2 + g / 2
         const float z0 = __shfl_sync(kFull, S.accz[0], 2 + (g >> 1));

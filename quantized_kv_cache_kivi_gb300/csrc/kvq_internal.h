@@ -60,6 +60,7 @@ struct Run {
 struct DecodeArgs {
   int batch, h_kv, gq, d, G, R;
   int log2G;         // G is a power of two
+  int Gv, log2Gv;    // V channel group and its log2
   float scale_log2;  // sm_scale * log2(e)
   int n_seg;
   SegDev seg[KVQ_MAX_SEGMENTS];
@@ -114,6 +115,7 @@ struct AppendArgs {
   int k_first_ring, k_slot0;
   int v_first_ring, v_slot0;
   int chunks;           // CTAs per (batch, kv head); chunk 0 does ring work
+  int Gv;               // V channel group
   int bulk;             // 1: the new-token work goes to the bulk kernels (d_h 128)
 };
 
@@ -136,6 +138,7 @@ struct IngestArgs {
   int n_jobs;              // windows; tail handled as job n_jobs
   int tail_src, tail_len, tail_dst;
   int ring_only;           // 1: ingest_kernel leaves quantized windows to the bulk kernels
+  int Gv;                  // V channel group
   WindowJob jobs[kMaxWindowJobs];
 };
 
@@ -199,7 +202,7 @@ __host__ __device__ inline TileInfo tile_info(const DecodeArgs& a, int t) {
   ti.v_off = off;
   off += align16u((uint32_t)ti.n * (uint32_t)(D * ti.vbits / 8));
   if (ti.vseg >= 0) {
-    const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.G) * 2u);
+    const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.Gv) * 2u);
     ti.vs_off = off;
     off += sb;
     ti.vz_off = off;
@@ -236,8 +239,8 @@ __host__ __device__ inline void for_each_tile_copy(const DecodeArgs& a, size_t p
     const SegDev& s = a.seg[ti.vseg];
     const int rb = D * s.bits / 8;
     f(s.vc + (pair * s.cap + ti.vu0) * rb, ti.v_off, (uint32_t)(ti.n * rb), 3, ti.vseg);
-    const size_t sbase = (pair * (size_t)s.cap + ti.vu0) * (D / a.G);
-    const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.G) * 2u);
+    const size_t sbase = (pair * (size_t)s.cap + ti.vu0) * (D / a.Gv);
+    const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.Gv) * 2u);
     f(s.vs + sbase, ti.vs_off, sb, 4, ti.vseg);
     f(s.vz + sbase, ti.vz_off, sb, 5, ti.vseg);
   } else {

@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
       quant_k_group_any<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
                        a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
     for (int p = warp; p < a.v_ring_tokens; p += nwarps)
-      quant_v_token<D>(a.dst, a.bits, a.G, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
+      quant_v_token<D>(a.dst, a.bits, a.Gv, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
                        a.v_nv0 + p);
     __syncthreads();
     if (few) {
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
     quant_k_group_any<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
                      a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
   for (int p = a.v_ring_tokens + me * nwarps + warp; p < a.v_evict; p += workers * nwarps)
-    quant_v_token<D>(a.dst, a.bits, a.G, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
+    quant_v_token<D>(a.dst, a.bits, a.Gv, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
                      a.v_nv0 + p);
 }
 
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs 
                      job.dst / a.G + gi, qs);
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int p = warp; p < a.S; p += nwarps)
-    quant_v_token<D>(dst, dst.bits, a.G, pair, in_v + (size_t)(job.src_token + p) * D, job.dst + p);
+    quant_v_token<D>(dst, dst.bits, a.Gv, pair, in_v + (size_t)(job.src_token + p) * D, job.dst + p);
 }
 
 }  // namespace
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_v_kernel(const AppendArgs a
     const int p = live ? a.v_ring_tokens + (int)(it % per_pair) : 0;
     float f[8];
     load8(a.v_new + (pair * (size_t)a.T + (size_t)(p - a.vsrc.n_old)) * D + 8 * hl, live, f);
-    quant_token_half<BITS>(f, live, a.dst, a.G, pair, a.v_nv0 + p, hl);
+    quant_token_half<BITS>(f, live, a.dst, a.Gv, pair, a.v_nv0 + p, hl);
   }
 }
 
@@ -571,9 +571,9 @@ __global__ void __launch_bounds__(kBulkThreads) ingest_bulk_v_kernel(const Inges
     float f[8];
     load8(a.v_new + (pair * (size_t)a.T + (size_t)(job.src_token + t)) * D + 8 * hl, live, f);
     const SegDev& dst = a.seg[live ? job.seg : 0];
-    quant_token_half<2>(f, live && bits == 2, dst, a.G, pair, job.dst + t, hl);
-    quant_token_half<4>(f, live && bits == 4, dst, a.G, pair, job.dst + t, hl);
-    quant_token_half<8>(f, live && bits == 8, dst, a.G, pair, job.dst + t, hl);
+    quant_token_half<2>(f, live && bits == 2, dst, a.Gv, pair, job.dst + t, hl);
+    quant_token_half<4>(f, live && bits == 4, dst, a.Gv, pair, job.dst + t, hl);
+    quant_token_half<8>(f, live && bits == 8, dst, a.Gv, pair, job.dst + t, hl);
   }
 }
 
@@ -631,7 +631,7 @@ cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s) {
   dim3 grid(a.batch * a.h_kv, a.n_jobs + 1);
   const size_t sm = quant_smem(a.G, a.d);
   cudaError_t e;
-  if (a.d == 128 && a.G >= 8 && a.G <= 128) {
+  if (a.d == 128 && a.Gv >= 8 && a.Gv <= 128) {
     // ring windows and the tail by the block kernel, quantized windows by
     // the grid-wide ones
     IngestArgs r = a;

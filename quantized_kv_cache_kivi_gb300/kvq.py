@@ -45,7 +45,7 @@ class kvq_cache(ctypes.Structure):
                 ("k_resid", ctypes.c_void_p), ("v_resid", ctypes.c_void_p),
                 ("nkr", ctypes.c_int32), ("nvr", ctypes.c_int32),
                 ("k_ring_start", ctypes.c_int32), ("v_ring_start", ctypes.c_int32),
-                ("zero_point", ctypes.c_int32)]
+                ("zero_point", ctypes.c_int32), ("group_v", ctypes.c_int32)]
 
 
 class kvq_window_plan(ctypes.Structure):
@@ -253,7 +253,7 @@ class Cache:
 
 
 def alloc_cache(batch, h_kv, h_q, d_h, group, resid_cap, segments, policy=KVQ_POLICY_KIVI,
-                sm_scale=None, device="cuda", zero_point=0):
+                sm_scale=None, device="cuda", zero_point=0, group_v=0):
     """segments: list of (bits, capacity); each capacity is rounded up to a
     multiple of ``group`` (the layout kvq.h requires).  Buffers are zero-filled."""
     import torch
@@ -261,6 +261,8 @@ def alloc_cache(batch, h_kv, h_q, d_h, group, resid_cap, segments, policy=KVQ_PO
     c.batch, c.h_kv, c.h_q, c.d_h, c.group = batch, h_kv, h_q, d_h, group
     c.resid_cap, c.policy = resid_cap, policy
     c.zero_point = zero_point
+    c.group_v = group_v
+    gv = group_v or group
     c.sm_scale = float(sm_scale if sm_scale is not None else 1.0 / math.sqrt(d_h))
     c.n_seg = len(segments)
     tensors = {}
@@ -273,8 +275,8 @@ def alloc_cache(batch, h_kv, h_q, d_h, group, resid_cap, segments, policy=KVQ_PO
             k_scale=torch.zeros(P * (cap // group) * d_h, dtype=torch.float16, device=device),
             k_zero=torch.zeros(P * (cap // group) * d_h, dtype=torch.float16, device=device),
             v_codes=torch.zeros(P * cap * rb, dtype=torch.uint8, device=device),
-            v_scale=torch.zeros(P * cap * (d_h // group), dtype=torch.float16, device=device),
-            v_zero=torch.zeros(P * cap * (d_h // group), dtype=torch.float16, device=device))
+            v_scale=torch.zeros(P * cap * (d_h // gv), dtype=torch.float16, device=device),
+            v_zero=torch.zeros(P * cap * (d_h // gv), dtype=torch.float16, device=device))
         tensors["seg%d" % i] = t
         s = c.seg[i]
         s.bits, s.capacity, s.nk, s.nv = bits, cap, 0, 0

@@ -30,16 +30,18 @@ class KiviPair:
     """A GPU cache and per-head oracle caches fed with the same tokens."""
 
     def __init__(self, batch, h_kv, h_q, d, G, R, bits, cap, policy=kvq.KVQ_POLICY_KIVI,
-                 heads=None, zero_point=0):
+                 heads=None, zero_point=0, group_v=0):
         self.batch, self.h_kv, self.h_q, self.d, self.G, self.R, self.bits = \
             batch, h_kv, h_q, d, G, R, bits
+        self.Gv = group_v or G
         self.gpu = kvq.alloc_cache(batch, h_kv, h_q, d, G, R, [(bits, cap)], policy=policy,
-                                   zero_point=zero_point)
+                                   zero_point=zero_point, group_v=group_v)
         self.cap = self.gpu.c.seg[0].capacity
         # oracle heads (optionally only a sample of (b, h) pairs)
         self.heads = heads if heads is not None else [(b, h) for b in range(batch)
                                                       for h in range(h_kv)]
-        self.orc = {bh: oracle.KiviHead(d, G, R, bits, intz=zero_point == kvq.KVQ_ZERO_INT)
+        self.orc = {bh: oracle.KiviHead(d, G, R, bits, intz=zero_point == kvq.KVQ_ZERO_INT,
+                                        Gv=self.Gv)
                     for bh in self.heads}
         self.started = False
 
@@ -92,8 +94,8 @@ class KiviPair:
             k_scale=t["k_scale"].cpu().numpy().view(np.uint16).reshape(P, cap // G, d),
             k_zero=t["k_zero"].cpu().numpy().view(np.uint16).reshape(P, cap // G, d),
             v_codes=t["v_codes"].cpu().numpy().reshape(P, cap, rb),
-            v_scale=t["v_scale"].cpu().numpy().view(np.uint16).reshape(P, cap, d // G),
-            v_zero=t["v_zero"].cpu().numpy().view(np.uint16).reshape(P, cap, d // G),
+            v_scale=t["v_scale"].cpu().numpy().view(np.uint16).reshape(P, cap, d // self.Gv),
+            v_zero=t["v_zero"].cpu().numpy().view(np.uint16).reshape(P, cap, d // self.Gv),
             k_resid=self.gpu.t["k_resid"].cpu().numpy().view(np.uint16).reshape(P, self.R, d),
             v_resid=self.gpu.t["v_resid"].cpu().numpy().view(np.uint16).reshape(P, self.R, d))
 
@@ -127,7 +129,7 @@ class KiviPair:
         for (b, h), head in self.orc.items():
             segs, kr, vr = oracle.head_buffers(head, [self.cap])
             K, V = oracle.dequant_head(segs, kr, vr, len(head.kr), len(head.vr), head.krs,
-                                       head.vrs, self.d, self.G, self.R)
+                                       head.vrs, self.d, self.G, self.R, self.Gv)
             qh = q[b, h * gq:(h + 1) * gq].astype(np.float64)
             out[(b, h)] = oracle.attention_head(K, V, qh, self.gpu.c.sm_scale)
         return out

@@ -136,6 +136,25 @@ def test_integer_zero_point_bit_exact_and_attention(d, G, R, bits, gq):
     assert pair.attention_error(_q(8, B, H * gq, d)) < TOL
 
 
+@pytest.mark.parametrize("d,G,Gv,R,bits,gq", [(128, 64, 32, 128, 2, 1), (128, 256, 128, 256, 4, 4),
+                                              (128, 32, 16, 64, 4, 7), (64, 32, 16, 64, 2, 1),
+                                              (128, 16, 64, 32, 8, 2), (128, 32, 8, 64, 2, 3)])
+def test_separate_v_group(d, G, Gv, R, bits, gq):
+    """K groups of G tokens beside V groups of Gv channels (G = 256: one
+    WindowQuant window per K group): buffers bit-exact, attention within
+    tolerance, for each kernel form the shapes select."""
+    B, H = 2, 2
+    pair = KiviPair(B, H, H * gq, d, G, R, bits, cap=4096, group_v=Gv)
+    l = 5 * R + 37
+    K, V = kv(71 + G, B, H, l + R + 9, d)
+    pair.prefill(K[:, :, :l], V[:, :, :l])
+    pair.assert_buffers_bit_exact()
+    for t in range(l, l + R + 9, 3):
+        pair.append(K[:, :, t:t + 3], V[:, :, t:t + 3])
+    pair.assert_buffers_bit_exact()
+    assert pair.attention_error(_q(12, B, H * gq, d)) < TOL
+
+
 @pytest.mark.parametrize("G,bits,gq,ws_splits", [(32, 2, 1, None), (64, 4, 4, None), (32, 2, 1, 3)])
 def test_attention_many_pairs_repeatable(G, bits, gq, ws_splits):
     """Many (batch, kv head) pairs cut into stream-K ranges, with the default
@@ -327,7 +346,8 @@ def test_window_assign_matches_oracle():
     assert np.array_equal(bits16, ob16) and np.array_equal(perm16, op16)
 
 
-def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, perm=None, zero_point=0):
+def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, perm=None, zero_point=0,
+              group_v=0):
     vis, txt = synth.window_keys(seed, B, H, n_win, S, n_text, d)
     M = n_win * S
     Vv = np.stack([np.stack([synth.values(seed, b, h, M, d) for h in range(H)]) for b in range(B)])
@@ -337,8 +357,9 @@ def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, 
         sim = oracle.window_sims(vis, txt, S)
         bits, perm = oracle.window_assign(sim, 0.1, 0.3, first_window_fp16=first16)
     caps = [(b, int(((bits == b).sum() * S + G - 1) // G * G) or G) for b in (8, 4, 2)]
-    R = 128 + int((bits == 16).sum()) * S
-    c = kvq.alloc_cache(B, H, H * gq, d, G, R, caps, policy=kvq.KVQ_POLICY_FP16_TAIL, zero_point=zero_point)
+    R = -(-(128 + int((bits == 16).sum()) * S) // G) * G
+    c = kvq.alloc_cache(B, H, H * gq, d, G, R, caps, policy=kvq.KVQ_POLICY_FP16_TAIL, zero_point=zero_point,
+                        group_v=group_v)
     plan = kvq.make_plan(S, bits, perm)
     tail = 5  # vision tokens past the last whole window stay fp16
     extra_k = np.concatenate([vis, vis[:, :, :tail]], axis=2)
@@ -348,7 +369,7 @@ def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, 
     heads = {}
     for b in range(B):
         for h in range(H):
-            o = oracle.Segmented(d, G, R, [8, 4, 2], intz=zero_point == kvq.KVQ_ZERO_INT)
+            o = oracle.Segmented(d, G, R, [8, 4, 2], intz=zero_point == kvq.KVQ_ZERO_INT, Gv=group_v or G)
             o.ingest_windows(extra_k[b, h], extra_v[b, h], S, bits, perm)
             o.append_fp16(txt[b, h], Vt[b, h])
             heads[(b, h)] = o
@@ -406,9 +427,19 @@ def test_windowquant_ingest_and_attention(first16, zero_point):
     _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, 3, first16, None, None, zero_point)
 
 
-def _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, seed, first16, bits, perm, zero_point=0):
+@pytest.mark.parametrize("zero_point", [0, 1])
+def test_windowquant_window_groups(zero_point):
+    """K groups of one window (G = S = 256, WindowQuant §3.3.3) with V groups
+    of 32 channels, integer or float zero point."""
+    n_win, S, n_text, B, H, gq, d = 10, 256, 24, 1, 2, 7, 128
+    _wq_attention_check(n_win, S, n_text, B, H, gq, d, S, 4, False, None, None, zero_point, group_v=32)
+
+
+def _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, seed, first16, bits, perm, zero_point=0,
+                        group_v=0):
+    Gv = group_v or G
     c, heads, caps, R = _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed=seed, first16=first16,
-                                  bits=bits, perm=perm, zero_point=zero_point)
+                                  bits=bits, perm=perm, zero_point=zero_point, group_v=group_v)
     torch.cuda.synchronize()
     P = B * H
     q = synth.q_block(9, B, H * gq, d)
@@ -433,10 +464,10 @@ def _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, seed, first16, bits, p
             assert np.array_equal(ks, seg["k_scale"][:n // G])
             vc = t["v_codes"].cpu().numpy().reshape(P, cap, rb)[p, :n]
             assert np.array_equal(vc, seg["v_codes"][:n])
-            vz = t["v_zero"].cpu().numpy().view(np.uint16).reshape(P, cap, d // G)[p, :n]
+            vz = t["v_zero"].cpu().numpy().view(np.uint16).reshape(P, cap, d // Gv)[p, :n]
             assert np.array_equal(vz, seg["v_zero"][:n])
         assert c.c.nkr == len(o.kr) and c.c.nvr == len(o.vr)
-        K, V = oracle.dequant_head(segs, kr, vr, len(o.kr), len(o.vr), 0, 0, d, G, R)
+        K, V = oracle.dequant_head(segs, kr, vr, len(o.kr), len(o.vr), 0, 0, d, G, R, Gv)
         ref = oracle.attention_head(K, V, q[b, h * gq:(h + 1) * gq].astype(np.float64), c.c.sm_scale)
         errs.append(max_abs_rel(got[b, h * gq:(h + 1) * gq], ref))
     assert max(errs) < TOL
