@@ -258,9 +258,12 @@ int choose_splits(int n_pairs, int n_tiles, int max_splits) {
 // Stream-K ranges of the tensor-core kernel.  Tile t of a pair costs its
 // 32-token units plus a quarter unit of per-tile work, the same in every
 // pair; CTA i's range starts at the first tile whose cost prefix reaches
-// i / N of the total, kept non-empty.  Returns the most ranges that meet one
-// pair (its partial records).
-int tc_ranges(const kvq::DecodeArgs& a, int n_pairs, int N, int* bound) {
+// W(i) / W(N) of the total, kept non-empty, where CTA i weighs w1 if it is
+// one of the first nf (the first wave, one per SM) and w2 otherwise (equal
+// weights by default: first-wave weights of 8:7 gained 1-2% with one query
+// head per kv head on some runs and lost 5% on others and with more heads).
+// Returns the most ranges that meet one pair (its partial records).
+int tc_ranges(const kvq::DecodeArgs& a, int n_pairs, int N, int* bound, int nf = 0, int w1 = 1, int w2 = 1) {
   const int nt = a.n_tiles;
   std::vector<long long> pre(nt + 1, 0);
   for (int r = 0, t = 0; t < nt; ++t) {  // tokens of tile t from the runs alone
@@ -272,9 +275,11 @@ int tc_ranges(const kvq::DecodeArgs& a, int n_pairs, int N, int* bound) {
   const long long per_pair = pre[nt], T = (long long)n_pairs * nt;
   const long long total = per_pair * n_pairs;
   auto prefix = [&](long long g) { return (g / nt) * per_pair + pre[g % nt]; };
+  auto weight = [&](long long i) { return i <= nf ? w1 * i : w1 * (long long)nf + w2 * (i - nf); };
+  const long long wn = weight(N);
   bound[0] = 0;
   for (int i = 1; i < N; ++i) {
-    const long long target = total * i / N;
+    const long long target = total * weight(i) / wn;
     long long lo = 0, hi = T;  // first g with prefix(g) >= target
     while (lo < hi) {
       const long long mid = (lo + hi) / 2;

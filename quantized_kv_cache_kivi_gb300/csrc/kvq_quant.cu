@@ -59,7 +59,7 @@ __device__ __forceinline__ QuantSmem quant_smem_view(uint8_t* base, int G, int D
 // its tokens, a warp and a block reduction give each channel's (min, max),
 // one thread per channel turns them into (s, z), and every thread writes
 // the codes of its chunk of its tokens (8 codes = `bits` bytes, one store).
-template <int D, int BITS>
+template <int D, int BITS, int Z>
 __device__ void quant_k_group(const SegDev& dst, int G, int R, size_t pair,
                               const __half* ring, const __half* in, const RowSrc& src, int p0,
                               int row0, int grow, const QuantSmem& q) {
@@ -125,7 +125,7 @@ __device__ void quant_k_group(const SegDev& dst, int G, int R, size_t pair,
       lo = fminf(lo, q.red[w * D + tid]);
       hi = fmaxf(hi, q.red[(NWARP + w) * D + tid]);
     }
-    const QParams qp = qparams_any(lo, hi, BITS, dst.intz);
+    const QParams qp = qparams_any(lo, hi, BITS, Z);
     const size_t gidx = (pair * (size_t)(dst.cap / G) + grow) * D + tid;
     const_cast<__half*>(dst.ks)[gidx] = qp.sh;
     const_cast<__half*>(dst.kz)[gidx] = qp.zh;
@@ -151,14 +151,14 @@ __device__ void quant_k_group(const SegDev& dst, int G, int R, size_t pair,
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       bool t;
-      c[e] = dst.intz ? qcode_intz_guess<BITS>(__half2float(h[e]), cz[e], cr[e], t)
+      c[e] = Z ? qcode_intz_guess<BITS>(__half2float(h[e]), cz[e], cr[e], t)
                       : qcode_guess<BITS>(__half2float(h[e]), cz[e], cr[e], t);
       tie |= t;
     }
     if (tie) {  // rare: redo the chunk with IEEE quotients
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        c[e] = dst.intz ? qcode_intz_exact<BITS>(__half2float(h[e]), cz[e], cs[e])
+        c[e] = Z ? qcode_intz_exact<BITS>(__half2float(h[e]), cz[e], cs[e])
                         : qcode_exact<BITS>(__half2float(h[e]), cz[e], cs[e]);
     }
     uint32_t lo = 0, hi = 0;  // codes 0-3 and 4-7 (8 codes = BITS bytes)
@@ -175,19 +175,19 @@ __device__ void quant_k_group(const SegDev& dst, int G, int R, size_t pair,
   __syncthreads();
 }
 
-template <int D>
+template <int D, int Z>
 __device__ __forceinline__ void quant_k_group_any(const SegDev& dst, int bits, int G, int R, size_t pair,
                                                   const __half* ring, const __half* in, const RowSrc& src,
                                                   int p0, int row0, int grow, const QuantSmem& q) {
-  if (bits == 2) quant_k_group<D, 2>(dst, G, R, pair, ring, in, src, p0, row0, grow, q);
-  else if (bits == 4) quant_k_group<D, 4>(dst, G, R, pair, ring, in, src, p0, row0, grow, q);
-  else quant_k_group<D, 8>(dst, G, R, pair, ring, in, src, p0, row0, grow, q);
+  if (bits == 2) quant_k_group<D, 2, Z>(dst, G, R, pair, ring, in, src, p0, row0, grow, q);
+  else if (bits == 4) quant_k_group<D, 4, Z>(dst, G, R, pair, ring, in, src, p0, row0, grow, q);
+  else quant_k_group<D, 8, Z>(dst, G, R, pair, ring, in, src, p0, row0, grow, q);
 }
 
 // Quantize one V token (all D channels, one group per G channels) into packed
 // row `row` of the destination segment.  One warp; lane l owns channels
 // 4l..4l+3 (lanes >= D/4 idle).
-template <int D>
+template <int D, int Z>
 __device__ void quant_v_token(const SegDev& dst, int bits, int G, size_t pair, const __half* x,
                               int row) {
   const int lane = threadIdx.x & 31;
@@ -207,13 +207,13 @@ __device__ void quant_v_token(const SegDev& dst, int bits, int G, size_t pair, c
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
   if (!active) return;
-  const QParams qp = qparams_any(mn, mx, bits, dst.intz);
+  const QParams qp = qparams_any(mn, mx, bits, Z);
   const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
   uint32_t packed = 0;
   for (int j = 0; j < 4; ++j) {
-    const uint32_t c = bits == 2 ? qcode_any<2>(v[j], qp.z, qp.s, rcp, dst.intz)
-                       : bits == 4 ? qcode_any<4>(v[j], qp.z, qp.s, rcp, dst.intz)
-                                   : qcode_any<8>(v[j], qp.z, qp.s, rcp, dst.intz);
+    const uint32_t c = bits == 2 ? qcode_any<2>(v[j], qp.z, qp.s, rcp, Z)
+                       : bits == 4 ? qcode_any<4>(v[j], qp.z, qp.s, rcp, Z)
+                                   : qcode_any<8>(v[j], qp.z, qp.s, rcp, Z);
     packed |= c << (j * bits);
   }
   const int rb = D * bits / 8;
@@ -240,7 +240,7 @@ __device__ void copy_to_ring(__half* ring, int R, int slot0, const __half* src, 
   }
 }
 
-template <int D>
+template <int D, int Z>
 __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
   const QuantSmem qs = quant_smem_view(qsm, a.G, D);
@@ -267,10 +267,10 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
     }
     // work that reads old ring slots, before any new token lands in the ring
     for (int gi = 0; gi < a.k_ring_groups; ++gi)
-      quant_k_group_any<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
+      quant_k_group_any<D, Z>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
                        a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
     for (int p = warp; p < a.v_ring_tokens; p += nwarps)
-      quant_v_token<D>(a.dst, a.bits, a.Gv, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
+      quant_v_token<D, Z>(a.dst, a.bits, a.Gv, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
                        a.v_nv0 + p);
     __syncthreads();
     if (few) {
@@ -294,27 +294,27 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
   const int me = a.chunks > 1 ? chunk - 1 : 0;
   if (a.chunks > 1 && chunk == 0) return;
   for (int gi = a.k_ring_groups + me; gi < a.k_groups; gi += workers)
-    quant_k_group_any<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
+    quant_k_group_any<D, Z>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
                      a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
   for (int p = a.v_ring_tokens + me * nwarps + warp; p < a.v_evict; p += workers * nwarps)
-    quant_v_token<D>(a.dst, a.bits, a.Gv, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
+    quant_v_token<D, Z>(a.dst, a.bits, a.Gv, pair, src_row<D>(ring_v, in_v, a.R, a.vsrc, p),
                      a.v_nv0 + p);
 }
 
 // K flush: group blockIdx.y of the ring's oldest tokens.
-template <int D>
+template <int D, int Z>
 __global__ void __launch_bounds__(kQuantThreads) flush_kernel(const AppendArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
   const QuantSmem qs = quant_smem_view(qsm, a.G, D);
   const size_t pair = blockIdx.x;
   const int gi = blockIdx.y;
   const __half* ring_k = a.kr + pair * (size_t)a.R * D;
-  quant_k_group_any<D>(a.dst, a.bits, a.G, a.R, pair, ring_k, nullptr, a.ksrc, gi * a.G,
+  quant_k_group_any<D, Z>(a.dst, a.bits, a.G, a.R, pair, ring_k, nullptr, a.ksrc, gi * a.G,
                    a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
 }
 
 // WindowQuant ingest: block (pair, job); job n_jobs is the fp16 tail.
-template <int D>
+template <int D, int Z>
 __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs a) {
   extern __shared__ __align__(16) uint8_t qsm[];
   const QuantSmem qs = quant_smem_view(qsm, a.G, D);
@@ -342,11 +342,11 @@ __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs 
   const RowSrc src{0, 0};
   const __half* wk = in_k + (size_t)job.src_token * D;
   for (int gi = 0; gi < a.S / a.G; ++gi)
-    quant_k_group_any<D>(dst, dst.bits, a.G, a.R, pair, nullptr, wk, src, gi * a.G, job.dst + gi * a.G,
+    quant_k_group_any<D, Z>(dst, dst.bits, a.G, a.R, pair, nullptr, wk, src, gi * a.G, job.dst + gi * a.G,
                      job.dst / a.G + gi, qs);
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int p = warp; p < a.S; p += nwarps)
-    quant_v_token<D>(dst, dst.bits, a.Gv, pair, in_v + (size_t)(job.src_token + p) * D, job.dst + p);
+    quant_v_token<D, Z>(dst, dst.bits, a.Gv, pair, in_v + (size_t)(job.src_token + p) * D, job.dst + p);
 }
 
 }  // namespace
@@ -361,12 +361,12 @@ size_t quant_smem(int G, int d) { return quant_smem_bytes(G, d); }
 
 constexpr int kBulkThreads = 256;
 
-template <int BITS>
+template <int BITS, int Z>
 __device__ __forceinline__ uint32_t pack4(const float (&x)[4], const float (&s)[4], const float (&r)[4],
-                                          const float (&z)[4], int intz) {
+                                          const float (&z)[4]) {
   uint32_t p = 0;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) p |= qcode_any<BITS>(x[e], z[e], s[e], r[e], intz) << (e * BITS);
+  for (int e = 0; e < 4; ++e) p |= qcode_any<BITS>(x[e], z[e], s[e], r[e], Z) << (e * BITS);
   return p;
 }
 
@@ -378,7 +378,7 @@ __device__ __forceinline__ uint32_t halves_u32(__half lo, __half hi) {
 // and scale / zero group grow, by one warp; lane l owns channels 4l .. 4l + 3.
 // Pass 1 takes the channel minima / maxima over the G rows, pass 2 re-reads
 // the rows (now in L1/L2) and writes the codes.
-template <int BITS>
+template <int BITS, int Z>
 __device__ __forceinline__ void quant_group_warp(const __half* src, const SegDev& dst, int G, size_t pair, int row0,
                                                  int grow, int lane) {
   constexpr int D = 128;
@@ -405,7 +405,7 @@ __device__ __forceinline__ void quant_group_warp(const __half* src, const SegDev
   __half sh[4], zh[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const QParams qp = qparams_any(mn[e], mx[e], BITS, dst.intz);
+    const QParams qp = qparams_any(mn[e], mx[e], BITS, Z);
     s[e] = qp.s;
     r[e] = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
     z[e] = qp.z;
@@ -425,7 +425,7 @@ __device__ __forceinline__ void quant_group_warp(const __half* src, const SegDev
     const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
     const float f[4] = {f0.x, f0.y, f1.x, f1.y};
-    const uint32_t p = pack4<BITS>(f, s, r, z, dst.intz);
+    const uint32_t p = pack4<BITS, Z>(f, s, r, z);
     uint8_t* o = out + (size_t)j * rb + lane * (BITS / 2);
     if constexpr (BITS == 2) *o = (uint8_t)p;
     else if constexpr (BITS == 4) *reinterpret_cast<uint16_t*>(o) = (uint16_t)p;
@@ -436,7 +436,7 @@ __device__ __forceinline__ void quant_group_warp(const __half* src, const SegDev
 // One V token (8 channels f of half-lane hl, values already loaded) into
 // packed row `row` of dst; the min / max shuffles run on the whole warp, so
 // both halves call this together (live = this half has a token).
-template <int BITS>
+template <int BITS, int Z>
 __device__ __forceinline__ void quant_token_half(const float (&f)[8], bool live, const SegDev& dst, int G,
                                                  size_t pair, int row_in_pair, int hl) {
   constexpr int D = 128;
@@ -452,13 +452,13 @@ __device__ __forceinline__ void quant_token_half(const float (&f)[8], bool live,
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   }
   if (!live) return;
-  const QParams qp = qparams_any(mn, mx, BITS, dst.intz);
+  const QParams qp = qparams_any(mn, mx, BITS, Z);
   const float rcp = qp.s != 0.0f ? __frcp_rn(qp.s) : 0.0f;
   uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    lo |= qcode_any<BITS>(f[e], qp.z, qp.s, rcp, dst.intz) << (e * BITS);
-    hi |= qcode_any<BITS>(f[e + 4], qp.z, qp.s, rcp, dst.intz) << (e * BITS);
+    lo |= qcode_any<BITS>(f[e], qp.z, qp.s, rcp, Z) << (e * BITS);
+    hi |= qcode_any<BITS>(f[e + 4], qp.z, qp.s, rcp, Z) << (e * BITS);
   }
   const size_t row = pair * (size_t)dst.cap + (size_t)row_in_pair;
   uint8_t* o = const_cast<uint8_t*>(dst.vc) + row * (D * BITS / 8) + hl * BITS;
@@ -485,7 +485,7 @@ __device__ __forceinline__ void load8(const __half* p, bool live, float (&f)[8])
 }
 
 // K groups of a bulk append that read only new tokens: one warp per group.
-template <int BITS>
+template <int BITS, int Z>
 __global__ void __launch_bounds__(kBulkThreads) bulk_k_kernel(const AppendArgs a) {
   constexpr int D = 128;
   const int lane = threadIdx.x & 31;
@@ -497,12 +497,12 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_k_kernel(const AppendArgs a
     const int gi = a.k_ring_groups + (int)(it % per_pair);
     const int p0 = gi * a.G;  // push index of the group's first token
     const __half* src = a.k_new + (pair * (size_t)a.T + (size_t)(p0 - a.ksrc.n_old)) * D;
-    quant_group_warp<BITS>(src, a.dst, a.G, pair, a.k_nk0 + p0, a.k_nk0 / a.G + gi, lane);
+    quant_group_warp<BITS, Z>(src, a.dst, a.G, pair, a.k_nk0 + p0, a.k_nk0 / a.G + gi, lane);
   }
 }
 
 // V tokens of a bulk append that read only new tokens: one half-warp each.
-template <int BITS>
+template <int BITS, int Z>
 __global__ void __launch_bounds__(kBulkThreads) bulk_v_kernel(const AppendArgs a) {
   constexpr int D = 128;
   const int hl = threadIdx.x & 15;
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_v_kernel(const AppendArgs a
     const int p = live ? a.v_ring_tokens + (int)(it % per_pair) : 0;
     float f[8];
     load8(a.v_new + (pair * (size_t)a.T + (size_t)(p - a.vsrc.n_old)) * D + 8 * hl, live, f);
-    quant_token_half<BITS>(f, live, a.dst, a.Gv, pair, a.v_nv0 + p, hl);
+    quant_token_half<BITS, Z>(f, live, a.dst, a.Gv, pair, a.v_nv0 + p, hl);
   }
 }
 
@@ -527,6 +527,7 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_v_kernel(const AppendArgs a
 // window go to the rows its job names, in the segment of its width (rings
 // and the fp16 tail: ingest_kernel).  Work items are (pair, window, group)
 // for K and (pair, window, token) for V.
+template <int Z>
 __global__ void __launch_bounds__(kBulkThreads) ingest_bulk_k_kernel(const IngestArgs a) {
   constexpr int D = 128;
   const int lane = threadIdx.x & 31;
@@ -542,12 +543,13 @@ __global__ void __launch_bounds__(kBulkThreads) ingest_bulk_k_kernel(const Inges
     const SegDev& dst = a.seg[job.seg];
     const __half* src = a.k_new + (pair * (size_t)a.T + (size_t)(job.src_token + g * a.G)) * D;
     const int row0 = job.dst + g * a.G, grow = job.dst / a.G + g;
-    if (dst.bits == 2) quant_group_warp<2>(src, dst, a.G, pair, row0, grow, lane);
-    else if (dst.bits == 4) quant_group_warp<4>(src, dst, a.G, pair, row0, grow, lane);
-    else quant_group_warp<8>(src, dst, a.G, pair, row0, grow, lane);
+    if (dst.bits == 2) quant_group_warp<2, Z>(src, dst, a.G, pair, row0, grow, lane);
+    else if (dst.bits == 4) quant_group_warp<4, Z>(src, dst, a.G, pair, row0, grow, lane);
+    else quant_group_warp<8, Z>(src, dst, a.G, pair, row0, grow, lane);
   }
 }
 
+template <int Z>
 __global__ void __launch_bounds__(kBulkThreads) ingest_bulk_v_kernel(const IngestArgs a) {
   constexpr int D = 128;
   const int hl = threadIdx.x & 15;
@@ -571,9 +573,9 @@ __global__ void __launch_bounds__(kBulkThreads) ingest_bulk_v_kernel(const Inges
     float f[8];
     load8(a.v_new + (pair * (size_t)a.T + (size_t)(job.src_token + t)) * D + 8 * hl, live, f);
     const SegDev& dst = a.seg[live ? job.seg : 0];
-    quant_token_half<2>(f, live && bits == 2, dst, a.Gv, pair, job.dst + t, hl);
-    quant_token_half<4>(f, live && bits == 4, dst, a.Gv, pair, job.dst + t, hl);
-    quant_token_half<8>(f, live && bits == 8, dst, a.Gv, pair, job.dst + t, hl);
+    quant_token_half<2, Z>(f, live && bits == 2, dst, a.Gv, pair, job.dst + t, hl);
+    quant_token_half<4, Z>(f, live && bits == 4, dst, a.Gv, pair, job.dst + t, hl);
+    quant_token_half<8, Z>(f, live && bits == 8, dst, a.Gv, pair, job.dst + t, hl);
   }
 }
 
@@ -582,75 +584,80 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <int BITS>
+template <int BITS, int Z>
 cudaError_t launch_bulk_b(const AppendArgs& a, cudaStream_t s) {
   const long long P = (long long)a.batch * a.h_kv;
   const long long nk = P * (a.k_groups - a.k_ring_groups), nv = P * (a.v_evict - a.v_ring_tokens);
   const long long cap = 4096;  // blocks: enough to fill any GPU, then the warps loop
-  if (nk > 0) bulk_k_kernel<BITS><<<(int)std::min(cap, (nk + 7) / 8), kBulkThreads, 0, s>>>(a);
-  if (nv > 0) bulk_v_kernel<BITS><<<(int)std::min(cap, (nv + 15) / 16), kBulkThreads, 0, s>>>(a);
+  if (nk > 0) bulk_k_kernel<BITS, Z><<<(int)std::min(cap, (nk + 7) / 8), kBulkThreads, 0, s>>>(a);
+  if (nv > 0) bulk_v_kernel<BITS, Z><<<(int)std::min(cap, (nv + 15) / 16), kBulkThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
+template <int D, int Z>
+cudaError_t launch_append_dz(const AppendArgs& a, cudaStream_t s) {
   dim3 grid(a.batch * a.h_kv, a.chunks);
   const size_t sm = quant_smem(a.G, a.d);
   cudaError_t e;
-  if (a.d == 128) {
-    if ((e = set_smem(append_kernel<128>, sm)) != cudaSuccess) return e;
-    append_kernel<128><<<grid, kQuantThreads, sm, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (a.bulk) {
-      if (a.bits == 2) return launch_bulk_b<2>(a, s);
-      if (a.bits == 4) return launch_bulk_b<4>(a, s);
-      return launch_bulk_b<8>(a, s);
-    }
-  } else {
-    if ((e = set_smem(append_kernel<64>, sm)) != cudaSuccess) return e;
-    append_kernel<64><<<grid, kQuantThreads, sm, s>>>(a);
+  if ((e = set_smem(append_kernel<D, Z>, sm)) != cudaSuccess) return e;
+  append_kernel<D, Z><<<grid, kQuantThreads, sm, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (D == 128 && a.bulk) {
+    if (a.bits == 2) return launch_bulk_b<2, Z>(a, s);
+    if (a.bits == 4) return launch_bulk_b<4, Z>(a, s);
+    return launch_bulk_b<8, Z>(a, s);
   }
+  return cudaSuccess;
+}
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
+  if (a.d == 128) return a.dst.intz ? launch_append_dz<128, 1>(a, s) : launch_append_dz<128, 0>(a, s);
+  return a.dst.intz ? launch_append_dz<64, 1>(a, s) : launch_append_dz<64, 0>(a, s);
+}
+
+template <int D, int Z>
+cudaError_t launch_flush_dz(const AppendArgs& a, cudaStream_t s) {
+  dim3 grid(a.batch * a.h_kv, a.k_groups);
+  const size_t sm = quant_smem(a.G, a.d);
+  cudaError_t e;
+  if ((e = set_smem(flush_kernel<D, Z>, sm)) != cudaSuccess) return e;
+  flush_kernel<D, Z><<<grid, kQuantThreads, sm, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_flush(const AppendArgs& a, cudaStream_t s) {
   if (a.k_groups <= 0) return cudaSuccess;
-  dim3 grid(a.batch * a.h_kv, a.k_groups);
+  if (a.d == 128) return a.dst.intz ? launch_flush_dz<128, 1>(a, s) : launch_flush_dz<128, 0>(a, s);
+  return a.dst.intz ? launch_flush_dz<64, 1>(a, s) : launch_flush_dz<64, 0>(a, s);
+}
+
+template <int D, int Z>
+cudaError_t launch_ingest_dz(const IngestArgs& a, cudaStream_t s) {
+  dim3 grid(a.batch * a.h_kv, a.n_jobs + 1);
   const size_t sm = quant_smem(a.G, a.d);
   cudaError_t e;
-  if (a.d == 128) {
-    if ((e = set_smem(flush_kernel<128>, sm)) != cudaSuccess) return e;
-    flush_kernel<128><<<grid, kQuantThreads, sm, s>>>(a);
+  if ((e = set_smem(ingest_kernel<D, Z>, sm)) != cudaSuccess) return e;
+  if (D == 128 && a.Gv >= 8 && a.Gv <= 128) {
+    // ring windows and the tail by the block kernel, quantized windows by
+    // the grid-wide ones
+    IngestArgs r = a;
+    r.ring_only = 1;
+    ingest_kernel<D, Z><<<grid, kQuantThreads, sm, s>>>(r);
+    const long long P = (long long)a.batch * a.h_kv;
+    const long long nk = P * a.n_jobs * (a.S / a.G), nv = P * a.n_jobs * a.S;
+    const long long cap = 4096;
+    if (nk > 0) ingest_bulk_k_kernel<Z><<<(int)std::min(cap, (nk + 7) / 8), kBulkThreads, 0, s>>>(a);
+    if (nv > 0) ingest_bulk_v_kernel<Z><<<(int)std::min(cap, (nv + 15) / 16), kBulkThreads, 0, s>>>(a);
   } else {
-    if ((e = set_smem(flush_kernel<64>, sm)) != cudaSuccess) return e;
-    flush_kernel<64><<<grid, kQuantThreads, sm, s>>>(a);
+    ingest_kernel<D, Z><<<grid, kQuantThreads, sm, s>>>(a);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s) {
-  dim3 grid(a.batch * a.h_kv, a.n_jobs + 1);
-  const size_t sm = quant_smem(a.G, a.d);
-  cudaError_t e;
-  if (a.d == 128 && a.Gv >= 8 && a.Gv <= 128) {
-    // ring windows and the tail by the block kernel, quantized windows by
-    // the grid-wide ones
-    IngestArgs r = a;
-    r.ring_only = 1;
-    if ((e = set_smem(ingest_kernel<128>, sm)) != cudaSuccess) return e;
-    ingest_kernel<128><<<grid, kQuantThreads, sm, s>>>(r);
-    const long long P = (long long)a.batch * a.h_kv;
-    const long long nk = P * a.n_jobs * (a.S / a.G), nv = P * a.n_jobs * a.S;
-    const long long cap = 4096;
-    if (nk > 0) ingest_bulk_k_kernel<<<(int)std::min(cap, (nk + 7) / 8), kBulkThreads, 0, s>>>(a);
-    if (nv > 0) ingest_bulk_v_kernel<<<(int)std::min(cap, (nv + 15) / 16), kBulkThreads, 0, s>>>(a);
-  } else if (a.d == 128) {
-    if ((e = set_smem(ingest_kernel<128>, sm)) != cudaSuccess) return e;
-    ingest_kernel<128><<<grid, kQuantThreads, sm, s>>>(a);
-  } else {
-    if ((e = set_smem(ingest_kernel<64>, sm)) != cudaSuccess) return e;
-    ingest_kernel<64><<<grid, kQuantThreads, sm, s>>>(a);
-  }
-  return cudaGetLastError();
+  const int z = a.seg[0].intz;  // one zero-point mode per cache
+  if (a.d == 128) return z ? launch_ingest_dz<128, 1>(a, s) : launch_ingest_dz<128, 0>(a, s);
+  return z ? launch_ingest_dz<64, 1>(a, s) : launch_ingest_dz<64, 0>(a, s);
 }
 
 }  // namespace kvq
