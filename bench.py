@@ -334,6 +334,25 @@ def per_workload_attention(device, flush_l2, peak, reps=20, only=None):
     return res, ing
 
 
+def max_over_ranks(x, device):
+    """The largest x over the ranks of the default process group (x itself
+    when there is none or it has one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replicas_value(bytes_per_step, steps, world, total_ms):
+    """Whole-job effective GB/s of `world` independent replicas (the pairs
+    need no exchange): the bytes all ranks processed over the slowest rank's
+    time."""
+    return bytes_per_step * steps * world / (total_ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -440,11 +459,7 @@ def run_ours(args, rank, world, local_rank):
     app_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
     attn_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
     fl_ms = np.array([e[2].elapsed_time(e[3]) for e in ev])
-    total_ms = float(step_ms.sum())
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(step_ms.sum()), device)
 
     # end to end through the plain API: pinned host inputs in, output back
     kh_pool = kn.unsqueeze(3).cpu().pin_memory()  # [pool][B][H][1][d]
@@ -616,8 +631,7 @@ def main():
     kvq.lib()
     r = run_ours(args, rank, world, local_rank)
     w = r["w"]
-    total_bytes = r["attn_bytes"] * args.steps * world
-    value = total_bytes / (r["total_ms"] * 1e-3) / 1e9
+    value = replicas_value(r["attn_bytes"], args.steps, world, r["total_ms"])
     peak, peak_kind = measured_peak()
     attn_mean_ms = float(np.mean(r["attn_ms"]))
     achieved = r["attn_bytes"] / (attn_mean_ms * 1e-3) / 1e9
