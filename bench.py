@@ -174,6 +174,21 @@ def cache_bytes(cache):
     return P * per
 
 
+def paged_bytes(cache):
+    """Bytes one decode attention must read from a paged cache: every
+    sequence's packed codes, scales/zeros and fp16 ring tokens."""
+    c = cache.c
+    d, G = c.d_h, c.group
+    Gv = c.group_v or G
+    rb = d * c.bits // 8
+    tot = 0
+    for b in range(c.batch):
+        s = c.seq[b]
+        tot += s.nk * rb + (s.nk // G) * d * 4 + s.nv * rb + s.nv * (d // Gv) * 4
+        tot += (s.nkr + s.nvr) * d * 2
+    return tot * c.h_kv
+
+
 def per_workload_attention(device, flush_l2, peak, reps=20, only=None):
     """Decode attention alone on each workload the pages name besides the
     timed step's, at the state the workload describes: mean CUDA-event time
@@ -209,17 +224,16 @@ def per_workload_attention(device, flush_l2, peak, reps=20, only=None):
             e1.record()
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1))
-        # warm: the same call again right after itself (what fits in L2 stays)
-        warm = []
+        # warm: calls enqueued back to back with events between them, so the
+        # cache stays in L2 where it fits and no host launch gap is timed
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        torch.cuda.synchronize()
+        ev[0].record()
         for i in range(reps):
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
             kvq.kvq_decode_attention(cache, q, out, ws)
-            e1.record()
-            torch.cuda.synchronize()
-            warm.append(e0.elapsed_time(e1))
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        warm = [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
         if kvq.kvq_workspace_error(ws):
             raise RuntimeError("decode kernel reported a timed-out wait")
         us = float(np.mean(ts)) * 1e3
@@ -295,6 +309,73 @@ def per_workload_attention(device, flush_l2, peak, reps=20, only=None):
         torch.cuda.synchronize()
         if only != "prefill_streaming":
             res[name] = timed(cache, B, Hq, d, w["seed"])
+        del cache
+        torch.cuda.empty_cache()
+    if only is None or only == "ragged_paged":
+        # per-sequence lengths in one paged cache: pages handed out in a
+        # shuffled order, prompts of ragged lengths ingested by one call
+        w = synth.WORKLOADS["ragged_paged"]
+        B, Hq, H, d, G, R, bits, Pg = (w[k] for k in ("batch", "h_q", "h_kv", "d", "G", "R", "bits", "page"))
+        lens = synth.ragged_lengths(w)
+        need = [-(-int(n) // Pg) + 1 for n in lens]
+        max_pages, n_pages = max(need), sum(need)
+        order = np.random.default_rng(w["seed"]).permutation(n_pages).astype(np.int32)
+        table = np.full((B, max_pages), -1, np.int32)
+        k = 0
+        for b in range(B):
+            table[b, :need[b]] = order[k:k + need[b]]
+            k += need[b]
+        cache = kvq.alloc_paged_cache(B, H, Hq, d, G, R, bits, Pg, n_pages, max_pages,
+                                      block_table=table, device=device)
+        K, V = dev_kv(w["seed"], B, H, int(lens.max()), d, w["n_out"], w["factor"])
+        seqs = cache.c.seq
+
+        def prefill():
+            if kvq.kvq_paged_append(cache, K, V, lens) == kvq.KVQ_FLUSH_DUE:
+                kvq.kvq_paged_flush_residual(cache)
+
+        ts = []
+        for i in range((reps if only else 5) + 1):  # the first call warms up
+            for b in range(B):
+                seqs[b].nk = seqs[b].nv = seqs[b].nkr = seqs[b].nvr = 0
+                seqs[b].k_ring_start = seqs[b].v_ring_start = 0
+            flush_l2(i)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            prefill()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        us = float(np.mean(ts[1:])) * 1e3
+        nb = int(lens.sum()) * H * d * 2 * 2 + paged_bytes(cache)
+        ing["prefill_ragged_paged"] = {"us": us, "GB/s": nb / (us * 1e-6) / 1e9,
+                                       "frac": nb / (us * 1e-6) / 1e9 / peak, "bytes": nb,
+                                       "tokens": int(lens.sum()) * H}
+        del K, V
+        q = torch.randn(B, Hq, d, generator=torch.Generator(device=device).manual_seed(w["seed"] + 7),
+                        device=device).half()
+        out = torch.empty_like(q)
+        ws = torch.zeros(kvq.kvq_paged_workspace_bytes(cache), dtype=torch.uint8, device=device)
+        for _ in range(3):
+            kvq.kvq_paged_decode_attention(cache, q, out, ws)
+        ts = []
+        for i in range(reps):
+            flush_l2(i)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            kvq.kvq_paged_decode_attention(cache, q, out, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        if kvq.kvq_workspace_error(ws) or kvq.kvq_workspace_error(cache.t["err"]):
+            raise RuntimeError("paged decode reported an error")
+        us = float(np.mean(ts)) * 1e3
+        nb = paged_bytes(cache)
+        res["ragged_paged"] = {"us": us, "GB/s": nb / (us * 1e-6) / 1e9, "frac": nb / (us * 1e-6) / 1e9 / peak,
+                               "bytes": nb, "lengths": "%d sequences, %d..%d tokens, %d in all" % (
+                                   B, int(lens.min()), int(lens.max()), int(lens.sum()))}
         del cache
         torch.cuda.empty_cache()
     if only is not None and only != "windowquant_llava_ov":
@@ -623,7 +704,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile-workload", default=None,
-                    choices=["tiny", "llama3_8b_gqa", "streaming", "prefill_streaming", "windowquant_llava_ov"],
+                    choices=["tiny", "llama3_8b_gqa", "streaming", "prefill_streaming", "windowquant_llava_ov",
+                             "ragged_paged"],
                     help="run one workload's calls a few times (for an ncu capture) and exit")
     ap.add_argument("--per-workload", type=int, default=1,
                     help="also time the attention alone on the other workloads (0: skip)")

@@ -264,6 +264,91 @@ kvq_status kvq_window_assign_eq8(const void* vision, const void* text,
                                  int8_t* bits_out, int32_t* perm_out,
                                  double* sim_out, void* stream);
 
+/* Paged cache with per-sequence lengths (no counterpart in the pages: the
+ * KIVI page names a combination with PagedAttention-style memory management
+ * as future work, "局限性与未来工作").
+ *
+ * Each sequence of the batch runs KIVI Algorithm 1 on its own: its lengths
+ * (packed K/V tokens, ring tokens, ring starts) are kept per sequence in the
+ * host struct, so sequences of different lengths share one launch.  Packed
+ * tokens live in a pool of pages of `page_tokens` tokens; page j of
+ * sequence b holds its packed tokens [j*P, j*P+P) (P = page_tokens) and is
+ * the pool page block_table[b*max_pages + j].  One pool page holds every kv
+ * head:
+ *   k_codes u8   [n_pages][h_kv][P][d_h*bits/8]
+ *   k_scale fp16 [n_pages][h_kv][P/group][d_h]     (k_zero alike)
+ *   v_codes u8   [n_pages][h_kv][P][d_h*bits/8]
+ *   v_scale fp16 [n_pages][h_kv][P][d_h/group_v]   (v_zero alike)
+ * The codec, the packed row format and the policy are those of kvq_cache
+ * with one segment and policy KVQ_POLICY_KIVI.  The fp16 rings are per
+ * sequence: k_resid/v_resid fp16 [batch][h_kv][resid_cap][d_h].
+ *
+ * The block table is device memory, owned and filled by the caller, who
+ * maps a sequence's pages before its packed tokens reach them (the host
+ * checks that the mapped extent, max_pages*P tokens, is not exceeded).
+ * The kernels read the table and check every entry: an entry outside
+ * 0..n_pages-1 is not followed (pool page 0 is read instead and nothing
+ * is written), and the device word `err` is set to 2; read it with
+ * kvq_workspace_error(err, ...).  A sequence with no tokens gets a zero
+ * output. */
+#define KVQ_MAX_SEQS 256
+
+typedef struct kvq_seq_state {
+  int32_t nk, nv;                      /* packed K / V tokens */
+  int32_t nkr, nvr;                    /* fp16 ring K / V tokens */
+  int32_t k_ring_start, v_ring_start;  /* ring slot of the oldest ring token */
+} kvq_seq_state;
+
+typedef struct kvq_paged_cache {
+  int32_t batch;       /* sequences, 1..KVQ_MAX_SEQS */
+  int32_t h_kv, h_q, d_h;
+  int32_t group;       /* G (K groups, tokens), a power of two 16..256 */
+  int32_t group_v;     /* V groups (channels); 0 = group */
+  int32_t resid_cap;   /* R, a multiple of group */
+  int32_t bits;        /* 2, 4 or 8 */
+  int32_t zero_point;  /* KVQ_ZERO_MIN or KVQ_ZERO_INT */
+  int32_t page_tokens; /* P, a multiple of 128 and of group */
+  int32_t n_pages;     /* pages in the pool */
+  int32_t max_pages;   /* columns of the block table */
+  float sm_scale;
+  void *k_codes, *k_scale, *k_zero, *v_codes, *v_scale, *v_zero; /* pool */
+  const int32_t* block_table; /* device int32 [batch][max_pages] */
+  void* k_resid;       /* fp16 [batch][h_kv][resid_cap][d_h] */
+  void* v_resid;
+  int32_t* err;        /* device int32 error word, zeroed by the caller */
+  kvq_seq_state seq[KVQ_MAX_SEQS];
+} kvq_paged_cache;
+
+/* Append new tokens per sequence (KIVI Algorithm 1, as kvq_quantize_append
+ * with plan == NULL and policy KIVI, each sequence on its own): k_new, v_new
+ * fp16 [batch][h_kv][T][d_h] (device); sequence b takes its first t_seq[b]
+ * rows (host int32 [batch], each 0..T; NULL = T for every sequence).
+ * Returns KVQ_FLUSH_DUE when some sequence's K ring is full after its last
+ * token (call kvq_paged_flush_residual), KVQ_ERR_CAPACITY (nothing launched)
+ * when some sequence would pass max_pages*P packed tokens. */
+kvq_status kvq_paged_append(kvq_paged_cache* cache, const void* k_new,
+                            const void* v_new, int32_t T,
+                            const int32_t* t_seq, void* stream);
+
+/* For every sequence whose K ring holds resid_cap tokens (the sequences
+ * that made kvq_paged_append return KVQ_FLUSH_DUE), quantize the block per
+ * channel into its pages (KIVI Algorithm 1: "len(X_Kr) == R"); the other
+ * sequences are left as they are. */
+kvq_status kvq_paged_flush_residual(kvq_paged_cache* cache, void* stream);
+
+/* Workspace of kvq_paged_decode_attention with at most max_splits CTAs per
+ * (sequence, kv head); zero it once with kvq_workspace_init. */
+size_t kvq_paged_workspace_bytes(const kvq_paged_cache* cache,
+                                 int32_t max_splits);
+
+/* Decode attention (as kvq_decode_attention) over each sequence's own
+ * tokens: q, out fp16 [batch][h_q][d_h] (device).  The host splits each
+ * sequence over a number of CTAs that grows with its length. */
+kvq_status kvq_paged_decode_attention(const kvq_paged_cache* cache,
+                                      const void* q, void* out,
+                                      void* workspace, size_t ws_bytes,
+                                      void* stream);
+
 /* Decode attention without a caller workspace (no counterpart in the pages).
  *
  * Same computation, arguments and result as kvq_decode_attention, for callers

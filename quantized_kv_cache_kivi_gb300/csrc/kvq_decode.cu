@@ -67,8 +67,8 @@ __device__ __forceinline__ float code8(uint32_t lo, uint32_t hi, int j) {
 // Scores of the tile's tokens for packed K of B bits: thread-per-token with
 // TPT threads sharing a token (channels split), partial sums reduced by
 // shuffles.  sc[h][tok] receives the log2-domain score.
-template <int D, int GQ, int B>
-__device__ void scores_packed(const DecodeArgs& a, const TileInfo& ti, const uint8_t* stage,
+template <int D, int GQ, int B, class A>
+__device__ void scores_packed(const A& a, const TileInfo& ti, const uint8_t* stage,
                               const float* qs, const float* bias, float* sc) {
   constexpr int RB = D * B / 8;
   const int tpt = NT / max(ti.n <= 32 ? 32 : (ti.n <= 64 ? 64 : 128), 1);
@@ -109,8 +109,8 @@ __device__ void scores_packed(const DecodeArgs& a, const TileInfo& ti, const uin
 }
 
 // Scores for fp16 ring K.
-template <int D, int GQ>
-__device__ void scores_ring(const DecodeArgs& a, const TileInfo& ti, const uint8_t* stage,
+template <int D, int GQ, class A>
+__device__ void scores_ring(const A& a, const TileInfo& ti, const uint8_t* stage,
                             const float* q_s, float* sc) {
   const int tpt = NT / (ti.n <= 32 ? 32 : (ti.n <= 64 ? 64 : 128));
   const int tid = threadIdx.x;
@@ -148,8 +148,8 @@ __device__ void scores_ring(const DecodeArgs& a, const TileInfo& ti, const uint8
 }
 
 // PV for packed V of B bits: thread owns an 8-channel chunk and a token slot.
-template <int D, int GQ, int B>
-__device__ void pv_packed(const DecodeArgs& a, const TileInfo& ti, const uint8_t* stage,
+template <int D, int GQ, int B, class A>
+__device__ void pv_packed(const A& a, const TileInfo& ti, const uint8_t* stage,
                           const float* sc, float (&acc)[GQ][8], float (&zsum)[GQ]) {
   constexpr int CHUNKS = D / 8, SLOTS = NT / CHUNKS, RB = D * B / 8;
   const int k = threadIdx.x % CHUNKS, slot = threadIdx.x / CHUNKS;
@@ -177,8 +177,8 @@ __device__ void pv_packed(const DecodeArgs& a, const TileInfo& ti, const uint8_t
   }
 }
 
-template <int D, int GQ>
-__device__ void pv_ring(const DecodeArgs& a, const TileInfo& ti, const uint8_t* stage,
+template <int D, int GQ, class A>
+__device__ void pv_ring(const A& a, const TileInfo& ti, const uint8_t* stage,
                         const float* sc, float (&acc)[GQ][8]) {
   constexpr int CHUNKS = D / 8, SLOTS = NT / CHUNKS;
   const int k = threadIdx.x % CHUNKS, slot = threadIdx.x / CHUNKS;
@@ -203,8 +203,75 @@ __device__ void pv_ring(const DecodeArgs& a, const TileInfo& ti, const uint8_t* 
   }
 }
 
-template <int D, int GQ>
-__global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
+// What one CTA does: (batch or sequence, kv head), its split and tile range.
+struct CtaWork {
+  int b, hk, pair, split, nsplit, t_begin, t_end;
+};
+
+__device__ inline CtaWork cta_work(const DecodeArgs& a) {
+  CtaWork w;
+  w.pair = blockIdx.x / a.n_splits;
+  w.split = blockIdx.x % a.n_splits;
+  w.nsplit = a.n_splits;
+  w.t_begin = a.split_tile[w.split];
+  w.t_end = a.split_tile[w.split + 1];
+  w.b = w.pair / a.h_kv;
+  w.hk = w.pair % a.h_kv;
+  return w;
+}
+__device__ inline TileInfo cta_tile(const DecodeArgs& a, const CtaWork&, int t) { return tile_info(a, t); }
+__device__ inline void cta_issue(const DecodeArgs& a, const CtaWork& w, int t, uint8_t* stage, uint64_t* bar) {
+  issue_tile(a, w.pair, t, stage, bar);
+}
+
+// Paged cache: grid column x belongs to the last sequence whose first
+// column is <= x; blockIdx.y is the kv head.  The sequence's tiles are dealt
+// to its CTAs in equal contiguous ranges.
+__device__ inline CtaWork cta_work(const PagedArgs& a) {
+  int lo = 0, hi = a.n_seq - 1;
+  const int x = blockIdx.x;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.seq[mid].split0 <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  const PagedSeq& s = a.seq[lo];
+  CtaWork w;
+  w.b = lo;
+  w.hk = blockIdx.y;
+  w.pair = lo * a.h_kv + w.hk;
+  w.split = x - s.split0;
+  w.nsplit = s.n_split;
+  w.t_begin = (int)((long long)s.n_tiles * w.split / s.n_split);
+  w.t_end = (int)((long long)s.n_tiles * (w.split + 1) / s.n_split);
+  return w;
+}
+__device__ inline TileInfo cta_tile(const PagedArgs& a, const CtaWork& w, int t) {
+  return paged_tile(a, a.seq[w.b], t);
+}
+// A block-table entry outside the pool is not followed: page 0 is read
+// instead (the copy stays inside the pool and its byte count unchanged) and
+// the cache's error word records it.
+__device__ inline void cta_issue(const PagedArgs& a, const CtaWork& w, int t, uint8_t* stage, uint64_t* bar) {
+  const PagedSeq& s = a.seq[w.b];
+  const TileInfo ti = paged_tile(a, s, t);
+  mbar_arrive_expect_tx(bar, ti.bytes);
+  auto page = [&](int row) {
+    const int j = row / a.P;
+    const int pg = j < a.max_pages ? a.table[(size_t)w.b * a.max_pages + j] : -1;
+    if (pg < 0 || pg >= a.n_pages) {
+      atomicExch(a.page_err, 2);
+      return 0;
+    }
+    return pg;
+  };
+  for_each_paged_copy(a, w.b, w.hk, s, ti, page, [&](const void* src, uint32_t off, uint32_t bytes) {
+    bulk_g2s(stage + off, src, bytes, bar);
+  });
+}
+
+template <int D, int GQ, class A>
+__device__ __forceinline__ void decode_cta(const A& a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
   float* qs = reinterpret_cast<float*>(smem + kStages * kStageBytes);
@@ -218,11 +285,11 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(flag_s + 4);
 
   const int tid = threadIdx.x;
-  const int pair = blockIdx.x / a.n_splits;
-  const int split = blockIdx.x % a.n_splits;
-  const int t_begin = a.split_tile[split], t_end = a.split_tile[split + 1];
-  const int ntiles = t_end - t_begin;
-  const int b = pair / a.h_kv, hk = pair % a.h_kv;
+  const CtaWork cw = cta_work(a);
+  const int pair = cw.pair, split = cw.split, nsplit = cw.nsplit;
+  const int t_begin = cw.t_begin;
+  const int ntiles = cw.t_end - cw.t_begin;
+  const int b = cw.b, hk = cw.hk;
 
   for (int i = tid; i < a.gq * D; i += NT) {
     const int h = i / D, c = i % D;
@@ -241,7 +308,7 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
   __syncthreads();
   if (tid == 0) {
     for (int i = 0; i < kStages && i < ntiles; ++i)
-      issue_tile(a, pair, t_begin + i, stages + i * kStageBytes, &bars[i]);
+      cta_issue(a, cw, t_begin + i, stages + i * kStageBytes, &bars[i]);
   }
 
   float acc[GQ][8];
@@ -268,7 +335,7 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
       }
       return;
     }
-    const TileInfo ti = tile_info(a, t);
+    const TileInfo ti = cta_tile(a, cw, t);
 
     // scaled query and bias per K group of the tile
     if (ti.kseg >= 0) {
@@ -343,7 +410,7 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
     __syncthreads();
     if (tid == 0 && it + kStages < ntiles) {
       fence_proxy_async_smem();
-      issue_tile(a, pair, t + kStages, stage, &bars[st]);
+      cta_issue(a, cw, t + kStages, stage, &bars[st]);
     }
   }
 
@@ -376,10 +443,11 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
   }
 
   const size_t out_base = ((size_t)b * a.h_kv * a.gq + (size_t)hk * a.gq) * D;
-  if (a.n_splits == 1) {
+  if (nsplit == 1) {
+    // (l = 0 only for a sequence with no tokens: its output is zero)
     for (int i = tid; i < a.gq * D; i += NT) {
       const int h = i / D;
-      a.out[out_base + i] = __float2half_rn(o_s[i] / l_s[h]);
+      a.out[out_base + i] = __float2half_rn(l_s[h] > 0.f ? o_s[i] / l_s[h] : 0.f);
     }
     return;
   }
@@ -396,7 +464,7 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
   __syncthreads();
   if (tid == 0) {
     const int ticket = atomicAdd(&a.counters[pair], 1);
-    flag_s[1] = (ticket == a.n_splits - 1);
+    flag_s[1] = (ticket == nsplit - 1);
   }
   __syncthreads();
   if (!flag_s[1]) return;
@@ -406,17 +474,17 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
   // splits, one warp per head; then every output element is a sum of
   // independent loads (the records are cold in L2, so a chain of dependent
   // loads per element would cost a round trip per split).
-  const float* recs = a.part + (size_t)pair * a.n_splits * a.gq * (D + 2);
+  const float* recs = a.part + (size_t)pair * a.n_splits * a.gq * (D + 2);  // n_splits records a pair
   float* wts = o_s + kMaxGq * D;  // [n_splits][gq]
   static_assert((NT / 32 + 2 * kMaxGq) * 128 + KVQ_MAX_SPLITS * kMaxGq <= kStages * kStageBytes / 4,
                 "merge scratch inside the drained stages");
   for (int h = warp; h < a.gq; h += NT / 32) {
     float M = -INFINITY;
-    for (int sp = lane; sp < a.n_splits; sp += 32)
+    for (int sp = lane; sp < nsplit; sp += 32)
       M = fmaxf(M, __ldcg(recs + ((size_t)sp * a.gq + h) * (D + 2) + D));
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
-    for (int sp = lane; sp < a.n_splits; sp += 32) {
+    for (int sp = lane; sp < nsplit; sp += 32) {
       const float* r = recs + ((size_t)sp * a.gq + h) * (D + 2);
       const float w = exp2f(__ldcg(r + D) - M);
       wts[sp * a.gq + h] = w;
@@ -425,18 +493,28 @@ __global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     __syncwarp();
     const float inv = 1.f / L;
-    for (int sp = lane; sp < a.n_splits; sp += 32) wts[sp * a.gq + h] *= inv;
+    for (int sp = lane; sp < nsplit; sp += 32) wts[sp * a.gq + h] *= inv;
   }
   __syncthreads();
   for (int i = tid; i < a.gq * D; i += NT) {
     const int h = i / D, c = i % D;
     float O = 0.f;
 #pragma unroll 8
-    for (int sp = 0; sp < a.n_splits; ++sp)
+    for (int sp = 0; sp < nsplit; ++sp)
       O += __ldcg(recs + ((size_t)sp * a.gq + h) * (D + 2) + c) * wts[sp * a.gq + h];
     a.out[out_base + i] = __float2half_rn(O);
   }
   if (tid == 0) a.counters[pair] = 0;
+}
+
+template <int D, int GQ>
+__global__ void __launch_bounds__(NT, 2) decode_kernel(const DecodeArgs a) {
+  decode_cta<D, GQ>(a);
+}
+
+template <int D, int GQ>
+__global__ void __launch_bounds__(NT, 2) decode_paged_kernel(const PagedArgs a) {
+  decode_cta<D, GQ>(a);
 }
 
 template <int D>
@@ -468,6 +546,30 @@ size_t decode_smem_bytes(int /*gq*/, int d) {
 
 cudaError_t launch_decode(const DecodeArgs& a, int n_pairs, cudaStream_t s) {
   return a.d == 128 ? launch_d<128>(a, n_pairs, s) : launch_d<64>(a, n_pairs, s);
+}
+
+namespace {
+template <int D>
+cudaError_t launch_paged_d(const PagedArgs& a, cudaStream_t s) {
+  const size_t smem = decode_smem_bytes(a.gq, D);
+  const dim3 grid(a.n_cols, a.h_kv);
+  cudaError_t e;
+#define KVQ_LAUNCH(GQV)                                                                          \
+  e = cudaFuncSetAttribute(decode_paged_kernel<D, GQV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           (int)smem);                                                           \
+  if (e != cudaSuccess) return e;                                                                \
+  decode_paged_kernel<D, GQV><<<grid, NT, smem, s>>>(a);
+  if (a.gq == 1) { KVQ_LAUNCH(1) }
+  else if (a.gq == 2) { KVQ_LAUNCH(2) }
+  else if (a.gq <= 4) { KVQ_LAUNCH(4) }
+  else { KVQ_LAUNCH(8) }
+#undef KVQ_LAUNCH
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_decode_paged(const PagedArgs& a, cudaStream_t s) {
+  return a.d == 128 ? launch_paged_d<128>(a, s) : launch_paged_d<64>(a, s);
 }
 
 }  // namespace kvq

@@ -252,6 +252,184 @@ __host__ __device__ inline void for_each_tile_copy(const DecodeArgs& a, size_t p
   }
 }
 
+// ---------------------------------------------------------------------------
+// Paged cache with per-sequence lengths.  A sequence's token axis is cut into
+// three runs -- both packed [0, min(nk, nv)), one side packed [min, max),
+// both ring [max, L) -- and each run into tiles aligned to multiples of the
+// tile size in the token index, so a packed tile never crosses a page
+// (the tile sizes divide the page).
+// ---------------------------------------------------------------------------
+struct PagedSeq {
+  int nk, nv, nkr, nvr, krs, vrs;
+  int n_tiles;  // tiles of the sequence (the same for each kv head)
+  int split0;   // first grid column of the sequence
+  int n_split;  // CTAs per kv head of the sequence
+};
+
+struct PagedArgs {
+  int batch, h_kv, gq, d, G, R, log2G, Gv, log2Gv, P, bits;
+  float scale_log2;
+  const uint8_t* kc;  // pool [n_pages][h_kv][P][d*bits/8]
+  const __half* ks;   // pool [n_pages][h_kv][P/G][d]
+  const __half* kz;
+  const uint8_t* vc;
+  const __half* vs;   // pool [n_pages][h_kv][P][d/Gv]
+  const __half* vz;
+  const int* table;   // [batch][max_pages]
+  int max_pages, n_pages;
+  const __half* kr;   // rings [batch][h_kv][R][d]
+  const __half* vr;
+  const __half* q;
+  __half* out;
+  float* part;        // [pairs][n_splits][gq][d + 2]
+  int* counters;      // [pairs]
+  int* err;           // workspace error word (timed-out waits)
+  int* page_err;      // the cache's error word (bad block-table entries)
+  int n_splits;       // records per (sequence, kv head) in the workspace
+  int tile_pp;        // tile tokens where K and V are both packed
+  int tile_mix;       // tile tokens where the ring is involved
+  int n_cols;         // grid columns (sum of n_split)
+  int n_seq;
+  PagedSeq seq[KVQ_MAX_SEQS];
+};
+
+__host__ __device__ inline int paged_run_tiles(int lo, int hi, int ts) {
+  return hi > lo ? (hi - 1) / ts - lo / ts + 1 : 0;
+}
+
+__host__ __device__ inline int paged_tiles(const PagedArgs& a, const PagedSeq& s) {
+  const int L = s.nk + s.nkr;
+  const int a0 = s.nk < s.nv ? s.nk : s.nv, a1 = s.nk < s.nv ? s.nv : s.nk;
+  return paged_run_tiles(0, a0, a.tile_pp) + paged_run_tiles(a0, a1, a.tile_mix) +
+         paged_run_tiles(a1, L, a.tile_mix);
+}
+
+// Tile t of sequence s: ku0/vu0 = packed row (absolute token index) when the
+// side is packed, else ring index; kseg/vseg = 0 packed, -1 ring.
+__host__ __device__ inline TileInfo paged_tile(const PagedArgs& a, const PagedSeq& s, int t) {
+  const int L = s.nk + s.nkr;
+  const int a0 = s.nk < s.nv ? s.nk : s.nv, a1 = s.nk < s.nv ? s.nv : s.nk;
+  const int n0 = paged_run_tiles(0, a0, a.tile_pp), n1 = paged_run_tiles(a0, a1, a.tile_mix);
+  int lo, hi, ts;
+  if (t < n0) {
+    lo = 0, hi = a0, ts = a.tile_pp;
+  } else if (t < n0 + n1) {
+    t -= n0, lo = a0, hi = a1, ts = a.tile_mix;
+  } else {
+    t -= n0 + n1, lo = a1, hi = L, ts = a.tile_mix;
+  }
+  int start = (lo / ts + t) * ts, end = start + ts;
+  start = start > lo ? start : lo;
+  end = end < hi ? end : hi;
+  const int D = a.d;
+  TileInfo ti;
+  ti.n = end - start;
+  ti.kseg = start < s.nk ? 0 : -1;
+  ti.vseg = start < s.nv ? 0 : -1;
+  ti.ku0 = ti.kseg == 0 ? start : start - s.nk;
+  ti.vu0 = ti.vseg == 0 ? start : start - s.nv;
+  ti.kbits = ti.kseg == 0 ? a.bits : 16;
+  ti.vbits = ti.vseg == 0 ? a.bits : 16;
+  uint32_t off = 0;
+  ti.k_off = off;
+  off += align16u((uint32_t)ti.n * (uint32_t)(D * ti.kbits / 8));
+  if (ti.kseg == 0) {
+    ti.g0 = ti.ku0 / a.G;
+    ti.ng = (ti.ku0 + ti.n - 1) / a.G - ti.g0 + 1;
+    ti.ks_off = off;
+    off += (uint32_t)ti.ng * D * 2;
+    ti.kz_off = off;
+    off += (uint32_t)ti.ng * D * 2;
+  } else {
+    ti.g0 = ti.ng = 0;
+    ti.ks_off = ti.kz_off = off;
+  }
+  ti.v_off = off;
+  off += align16u((uint32_t)ti.n * (uint32_t)(D * ti.vbits / 8));
+  if (ti.vseg == 0) {
+    const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.Gv) * 2u);
+    ti.vs_off = off;
+    off += sb;
+    ti.vz_off = off;
+    off += sb;
+  } else {
+    ti.vs_off = ti.vz_off = off;
+  }
+  ti.bytes = off;
+  return ti;
+}
+
+// Visit the bulk copies that stage paged tile `ti` of sequence b, kv head h:
+// f(src, dst_off, bytes).  page(row) maps a packed row to its pool page (the
+// caller checks the block-table entry).
+template <class Page, class F>
+__host__ __device__ inline void for_each_paged_copy(const PagedArgs& a, int b, int h, const PagedSeq& s,
+                                                    const TileInfo& ti, Page&& page, F&& f) {
+  const int D = a.d, P = a.P;
+  const size_t pair = (size_t)b * a.h_kv + h;
+  const int rb = D * a.bits / 8;
+  if (ti.kseg == 0) {
+    const size_t ph = (size_t)page(ti.ku0) * a.h_kv + h;
+    const int r = ti.ku0 % P;
+    f(a.kc + (ph * P + r) * rb, ti.k_off, (uint32_t)(ti.n * rb));
+    const size_t gbase = (ph * (size_t)(P / a.G) + r / a.G) * D;
+    f(a.ks + gbase, ti.ks_off, (uint32_t)(ti.ng * D * 2));
+    f(a.kz + gbase, ti.kz_off, (uint32_t)(ti.ng * D * 2));
+  } else {
+    const int s0 = (s.krs + ti.ku0) % a.R;
+    const int n1 = ti.n < a.R - s0 ? ti.n : a.R - s0;
+    const __half* ring = a.kr + pair * (size_t)a.R * D;
+    f(ring + (size_t)s0 * D, ti.k_off, (uint32_t)(n1 * D * 2));
+    if (n1 < ti.n) f(ring, ti.k_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2));
+  }
+  if (ti.vseg == 0) {
+    const size_t ph = (size_t)page(ti.vu0) * a.h_kv + h;
+    const int r = ti.vu0 % P;
+    f(a.vc + (ph * P + r) * rb, ti.v_off, (uint32_t)(ti.n * rb));
+    const size_t sbase = (ph * P + r) * (D / a.Gv);
+    const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.Gv) * 2u);
+    f(a.vs + sbase, ti.vs_off, sb);
+    f(a.vz + sbase, ti.vz_off, sb);
+  } else {
+    const int s0 = (s.vrs + ti.vu0) % a.R;
+    const int n1 = ti.n < a.R - s0 ? ti.n : a.R - s0;
+    const __half* ring = a.vr + pair * (size_t)a.R * D;
+    f(ring + (size_t)s0 * D, ti.v_off, (uint32_t)(n1 * D * 2));
+    if (n1 < ti.n) f(ring, ti.v_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2));
+  }
+}
+
+// Per-sequence append work (KIVI Algorithm 1 for one sequence), the fields
+// of AppendArgs that differ between sequences.
+struct PagedAppendSeq {
+  int t;              // new tokens of the sequence
+  int k_groups, k_nk0, k_ring_groups;
+  RowSrc ksrc;
+  int v_evict, v_nv0, v_ring_tokens;
+  RowSrc vsrc;
+  int k_first_ring, k_slot0, v_first_ring, v_slot0;
+};
+
+struct PagedAppendArgs {
+  int batch, h_kv, d, G, Gv, R, T, P, bits, intz;
+  const __half* k_new;  // [B][H][T][d]
+  const __half* v_new;
+  __half* kr;           // rings [B][H][R][d]
+  __half* vr;
+  uint8_t* kc;          // pool, as PagedArgs
+  __half* ks;
+  __half* kz;
+  uint8_t* vc;
+  __half* vs;
+  __half* vz;
+  const int* table;
+  int max_pages, n_pages;
+  int* page_err;
+  int chunks;           // CTAs per (sequence, kv head); chunk 0 does ring work
+  int flush;            // 1: K flush of the rings only (kvq_paged_flush_residual)
+  PagedAppendSeq seq[KVQ_MAX_SEQS];
+};
+
 // host helpers of kvq_api.cu used by other entry points
 void set_last_error(const char* msg);
 kvq_status check_cache(const kvq_cache* c);
@@ -265,6 +443,8 @@ size_t decode_smem_bytes(int gq, int d);
 cudaError_t launch_decode_mha(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, int form, cudaStream_t s);
 cudaError_t launch_decode_tc_merge(const DecodeArgs& a, int n_pairs, cudaStream_t s);
+cudaError_t launch_decode_paged(const PagedArgs& a, cudaStream_t s);
+cudaError_t launch_paged_append(const PagedAppendArgs& a, cudaStream_t s);
 int decode_tc_ctas_per_sm();
 size_t decode_mha_smem_bytes();
 

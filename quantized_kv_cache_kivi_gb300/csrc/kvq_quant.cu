@@ -349,6 +349,102 @@ __global__ void __launch_bounds__(kQuantThreads) ingest_kernel(const IngestArgs 
     quant_v_token<D, Z>(dst, dst.bits, a.Gv, pair, in_v + (size_t)(job.src_token + p) * D, job.dst + p);
 }
 
+// ---------------------------------------------------------------------------
+// Paged cache: KIVI Algorithm 1 per sequence.  Block (sequence, kv head,
+// chunk).  A pool page seen through a SegDev of capacity P with the kv head
+// as its "pair" index puts every row, K group and V scale row where the
+// pool layout [page][h_kv][P][...] wants it, so the quantizers above write
+// pages unchanged.  A block-table entry outside the pool writes nothing and
+// sets the cache's error word.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int paged_page(const PagedAppendArgs& a, int b, int row) {
+  const int j = row / a.P;
+  const int pg = j < a.max_pages ? a.table[(size_t)b * a.max_pages + j] : -1;
+  return (pg < 0 || pg >= a.n_pages) ? -1 : pg;
+}
+
+__device__ __forceinline__ SegDev paged_view(const PagedAppendArgs& a, int pg) {
+  const size_t rows = (size_t)pg * a.h_kv * a.P;
+  const int rb = a.d * a.bits / 8;
+  SegDev v;
+  v.kc = a.kc + rows * rb;
+  v.ks = a.ks + rows / a.G * a.d;
+  v.kz = a.kz + rows / a.G * a.d;
+  v.vc = a.vc + rows * rb;
+  v.vs = a.vs + rows * (a.d / a.Gv);
+  v.vz = a.vz + rows * (a.d / a.Gv);
+  v.bits = a.bits;
+  v.cap = a.P;
+  v.intz = a.intz;
+  return v;
+}
+
+template <int D, int Z>
+__device__ void paged_k_group(const PagedAppendArgs& a, int b, int h, const PagedAppendSeq& q,
+                              const __half* ring, const __half* in, int gi, const QuantSmem& qs) {
+  const int row = q.k_nk0 + gi * a.G;
+  const int pg = paged_page(a, b, row);  // the same in every thread
+  if (pg < 0) {
+    if (threadIdx.x == 0) atomicExch(a.page_err, 2);
+    return;
+  }
+  const int r = row % a.P;
+  quant_k_group_any<D, Z>(paged_view(a, pg), a.bits, a.G, a.R, (size_t)h, ring, in, q.ksrc, gi * a.G, r,
+                          r / a.G, qs);
+}
+
+template <int D, int Z>
+__device__ void paged_v_token(const PagedAppendArgs& a, int b, int h, const PagedAppendSeq& q,
+                              const __half* ring, const __half* in, int p) {
+  const int row = q.v_nv0 + p;
+  const int pg = paged_page(a, b, row);
+  if (pg < 0) {
+    if ((threadIdx.x & 31) == 0) atomicExch(a.page_err, 2);
+    return;
+  }
+  quant_v_token<D, Z>(paged_view(a, pg), a.bits, a.Gv, (size_t)h, src_row<D>(ring, in, a.R, q.vsrc, p),
+                      row % a.P);
+}
+
+template <int D, int Z>
+__global__ void __launch_bounds__(kQuantThreads) paged_append_kernel(const PagedAppendArgs a) {
+  extern __shared__ __align__(16) uint8_t qsm[];
+  const QuantSmem qs = quant_smem_view(qsm, a.G, D);
+  const int b = blockIdx.x, h = blockIdx.y, chunk = blockIdx.z;
+  const PagedAppendSeq& q = a.seq[b];
+  const size_t pair = (size_t)b * a.h_kv + h;
+  const __half* in_k = a.k_new + pair * (size_t)a.T * D;
+  const __half* in_v = a.v_new + pair * (size_t)a.T * D;
+  __half* ring_k = a.kr + pair * (size_t)a.R * D;
+  __half* ring_v = a.vr + pair * (size_t)a.R * D;
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  if (a.flush) {  // the ring's oldest K groups, one chunk per group
+    for (int gi = chunk; gi < q.k_groups; gi += a.chunks)
+      paged_k_group<D, Z>(a, b, h, q, ring_k, nullptr, gi, qs);
+    return;
+  }
+  if (chunk == 0) {
+    // work that reads old ring slots, then the new tokens into the ring
+    for (int gi = 0; gi < q.k_ring_groups; ++gi) paged_k_group<D, Z>(a, b, h, q, ring_k, in_k, gi, qs);
+    for (int p = warp; p < q.v_ring_tokens; p += nwarps) paged_v_token<D, Z>(a, b, h, q, ring_v, in_v, p);
+    __syncthreads();
+    if (q.k_first_ring < q.t)
+      copy_to_ring<D>(ring_k, a.R, q.k_slot0 + q.k_first_ring, in_k + (size_t)q.k_first_ring * D,
+                      q.t - q.k_first_ring);
+    if (q.v_first_ring < q.t)
+      copy_to_ring<D>(ring_v, a.R, q.v_slot0 + q.v_first_ring, in_v + (size_t)q.v_first_ring * D,
+                      q.t - q.v_first_ring);
+    if (a.chunks > 1) return;
+  }
+  // work that reads only new tokens, over chunks 1.. (or chunk 0 alone)
+  const int workers = a.chunks > 1 ? a.chunks - 1 : 1;
+  const int me = a.chunks > 1 ? chunk - 1 : 0;
+  for (int gi = q.k_ring_groups + me; gi < q.k_groups; gi += workers)
+    paged_k_group<D, Z>(a, b, h, q, ring_k, in_k, gi, qs);
+  for (int p = q.v_ring_tokens + me * nwarps + warp; p < q.v_evict; p += workers * nwarps)
+    paged_v_token<D, Z>(a, b, h, q, ring_v, in_v, p);
+}
+
 }  // namespace
 
 size_t quant_smem(int G, int d) { return quant_smem_bytes(G, d); }
@@ -658,6 +754,21 @@ cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s) {
   const int z = a.seg[0].intz;  // one zero-point mode per cache
   if (a.d == 128) return z ? launch_ingest_dz<128, 1>(a, s) : launch_ingest_dz<128, 0>(a, s);
   return z ? launch_ingest_dz<64, 1>(a, s) : launch_ingest_dz<64, 0>(a, s);
+}
+
+template <int D, int Z>
+cudaError_t launch_paged_append_dz(const PagedAppendArgs& a, cudaStream_t s) {
+  dim3 grid(a.batch, a.h_kv, a.chunks);
+  const size_t sm = quant_smem(a.G, a.d);
+  cudaError_t e;
+  if ((e = set_smem(paged_append_kernel<D, Z>, sm)) != cudaSuccess) return e;
+  paged_append_kernel<D, Z><<<grid, kQuantThreads, sm, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_paged_append(const PagedAppendArgs& a, cudaStream_t s) {
+  if (a.d == 128) return a.intz ? launch_paged_append_dz<128, 1>(a, s) : launch_paged_append_dz<128, 0>(a, s);
+  return a.intz ? launch_paged_append_dz<64, 1>(a, s) : launch_paged_append_dz<64, 0>(a, s);
 }
 
 }  // namespace kvq

@@ -26,6 +26,7 @@ KVQ_POLICY_FP16_TAIL = 1
 KVQ_ZERO_MIN, KVQ_ZERO_INT = 0, 1
 KVQ_MAX_SEGMENTS = 8
 KVQ_MAX_SPLITS = 128
+KVQ_MAX_SEQS = 256
 
 
 class kvq_segment(ctypes.Structure):
@@ -52,6 +53,28 @@ class kvq_window_plan(ctypes.Structure):
     _fields_ = [("window", ctypes.c_int32), ("n_windows", ctypes.c_int32),
                 ("bits", ctypes.POINTER(ctypes.c_int8)),
                 ("perm", ctypes.POINTER(ctypes.c_int32))]
+
+
+class kvq_seq_state(ctypes.Structure):
+    _fields_ = [("nk", ctypes.c_int32), ("nv", ctypes.c_int32),
+                ("nkr", ctypes.c_int32), ("nvr", ctypes.c_int32),
+                ("k_ring_start", ctypes.c_int32), ("v_ring_start", ctypes.c_int32)]
+
+
+class kvq_paged_cache(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("h_kv", ctypes.c_int32), ("h_q", ctypes.c_int32),
+                ("d_h", ctypes.c_int32), ("group", ctypes.c_int32), ("group_v", ctypes.c_int32),
+                ("resid_cap", ctypes.c_int32), ("bits", ctypes.c_int32),
+                ("zero_point", ctypes.c_int32), ("page_tokens", ctypes.c_int32),
+                ("n_pages", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float),
+                ("k_codes", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("k_zero", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("v_zero", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p),
+                ("k_resid", ctypes.c_void_p), ("v_resid", ctypes.c_void_p),
+                ("err", ctypes.c_void_p),
+                ("seq", kvq_seq_state * KVQ_MAX_SEQS)]
 
 
 _LIB = None
@@ -87,13 +110,21 @@ def lib():
             [ctypes.c_double, ctypes.c_double, ctypes.c_int32, _P, ctypes.c_size_t,
              ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(ctypes.c_int32),
              ctypes.POINTER(ctypes.c_double), _P]
+        pp = ctypes.POINTER(kvq_paged_cache)
+        L.kvq_paged_append.argtypes = [pp, _P, _P, ctypes.c_int32,
+                                       ctypes.POINTER(ctypes.c_int32), _P]
+        L.kvq_paged_flush_residual.argtypes = [pp, _P]
+        L.kvq_paged_workspace_bytes.argtypes = [pp, ctypes.c_int32]
+        L.kvq_paged_workspace_bytes.restype = ctypes.c_size_t
+        L.kvq_paged_decode_attention.argtypes = [pp, _P, _P, _P, ctypes.c_size_t, _P]
         L.kvq_status_string.argtypes = [ctypes.c_int]
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_last_error_string.argtypes = []
         L.kvq_last_error_string.restype = ctypes.c_char_p
         for name in ("kvq_quantize_append", "kvq_flush_residual", "kvq_workspace_init",
                      "kvq_decode_attention", "kvq_workspace_error", "kvq_window_assign",
-                     "kvq_window_assign_eq8"):
+                     "kvq_window_assign_eq8", "kvq_paged_append", "kvq_paged_flush_residual",
+                     "kvq_paged_decode_attention"):
             getattr(L, name).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -226,6 +257,35 @@ def kvq_window_assign_eq8(vision, text, S, layer_sim, alpha, first_window_fp16=F
     return bits, perm, sim
 
 
+def kvq_paged_append(cache, k_new, v_new, t_seq=None, stream=None):
+    """fp16 [B][H_kv][T][d] new tokens; sequence b takes its first t_seq[b]
+    (all T when None).  Returns KVQ_OK or KVQ_FLUSH_DUE."""
+    import numpy as np
+    T = int(k_new.shape[2])
+    ts = None
+    if t_seq is not None:
+        arr = np.ascontiguousarray(t_seq, np.int32)
+        ts = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    st = lib().kvq_paged_append(ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new), T, ts,
+                                _stream(stream))
+    return _check(st, "kvq_paged_append", ok=(KVQ_OK, KVQ_FLUSH_DUE))
+
+
+def kvq_paged_flush_residual(cache, stream=None):
+    return _check(lib().kvq_paged_flush_residual(ctypes.byref(cache.c), _stream(stream)),
+                  "kvq_paged_flush_residual")
+
+
+def kvq_paged_workspace_bytes(cache, max_splits=KVQ_MAX_SPLITS):
+    return int(lib().kvq_paged_workspace_bytes(ctypes.byref(cache.c), int(max_splits)))
+
+
+def kvq_paged_decode_attention(cache, q, out, ws, stream=None):
+    st = lib().kvq_paged_decode_attention(ctypes.byref(cache.c), _ptr(q), _ptr(out), _ptr(ws),
+                                          ws.numel() * ws.element_size(), _stream(stream))
+    return _check(st, "kvq_paged_decode_attention")
+
+
 def make_plan(window, bits, perm):
     """kvq_window_plan over numpy int8 bits / int32 perm (kept alive by the plan)."""
     import numpy as np
@@ -290,10 +350,59 @@ def alloc_cache(batch, h_kv, h_q, d_h, group, resid_cap, segments, policy=KVQ_PO
     return Cache(c, tensors)
 
 
+class PagedCache(Cache):
+    """A kvq_paged_cache struct plus the torch tensors that back it."""
+
+    def lengths(self, b):
+        s = self.c.seq[b]
+        return dict(nk=s.nk, nv=s.nv, nkr=s.nkr, nvr=s.nvr, krs=s.k_ring_start,
+                    vrs=s.v_ring_start)
+
+
+def alloc_paged_cache(batch, h_kv, h_q, d_h, group, resid_cap, bits, page_tokens, n_pages,
+                      max_pages, block_table=None, sm_scale=None, device="cuda", zero_point=0,
+                      group_v=0):
+    """Page pool, per-sequence rings, block table and error word of a paged
+    cache (layout of kvq.h).  block_table: int [batch][max_pages] pool page
+    ids (any order; -1 where unmapped); None maps sequence b's page j to pool
+    page b * max_pages + j.  Buffers are zero-filled."""
+    import numpy as np
+    import torch
+    c = kvq_paged_cache()
+    c.batch, c.h_kv, c.h_q, c.d_h, c.group, c.group_v = batch, h_kv, h_q, d_h, group, group_v
+    c.resid_cap, c.bits, c.zero_point = resid_cap, bits, zero_point
+    c.page_tokens, c.n_pages, c.max_pages = page_tokens, n_pages, max_pages
+    c.sm_scale = float(sm_scale if sm_scale is not None else 1.0 / math.sqrt(d_h))
+    gv = group_v or group
+    rows = n_pages * h_kv * page_tokens
+    rb = d_h * bits // 8
+    if block_table is None:
+        if n_pages < batch * max_pages:
+            raise ValueError("n_pages < batch * max_pages: pass a block_table")
+        block_table = np.arange(batch * max_pages, dtype=np.int32).reshape(batch, max_pages)
+    bt = np.ascontiguousarray(block_table, np.int32).reshape(batch, max_pages)
+    t = dict(
+        k_codes=torch.zeros(rows * rb, dtype=torch.uint8, device=device),
+        k_scale=torch.zeros(rows // group * d_h, dtype=torch.float16, device=device),
+        k_zero=torch.zeros(rows // group * d_h, dtype=torch.float16, device=device),
+        v_codes=torch.zeros(rows * rb, dtype=torch.uint8, device=device),
+        v_scale=torch.zeros(rows * (d_h // gv), dtype=torch.float16, device=device),
+        v_zero=torch.zeros(rows * (d_h // gv), dtype=torch.float16, device=device),
+        block_table=torch.from_numpy(bt.copy()).to(device),
+        k_resid=torch.zeros(batch * h_kv * resid_cap * d_h, dtype=torch.float16, device=device),
+        v_resid=torch.zeros(batch * h_kv * resid_cap * d_h, dtype=torch.float16, device=device),
+        err=torch.zeros(4, dtype=torch.int32, device=device))
+    for k, v in t.items():
+        setattr(c, k, v.data_ptr())
+    cache = PagedCache(c, t)
+    cache.table = bt
+    return cache
+
+
 def header_symbols():
     """Names of the functions include/kvq.h declares."""
     import re
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     with open(os.path.join(root, "include", "kvq.h")) as f:
         src = f.read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\s*\*?\s*(kvq_[a-z_]+)\s*\(", src, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\s*\*?\s*(kvq_[a-z0-9_]+)\s*\(", src, re.M)))

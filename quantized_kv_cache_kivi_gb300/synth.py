@@ -15,7 +15,7 @@ All values are rounded to fp16 (the pages' cache precision).
 """
 import numpy as np
 
-TAG_K, TAG_V, TAG_Q, TAG_OUTLIER, TAG_TEXT, TAG_DIR, TAG_STEP = 1, 2, 3, 4, 5, 6, 7
+TAG_K, TAG_V, TAG_Q, TAG_OUTLIER, TAG_TEXT, TAG_DIR, TAG_STEP, TAG_LEN = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 def rng(seed, tag, b=0, h=0, step=0):
@@ -113,4 +113,14 @@ WORKLOADS = {
                                  n_win=64, S=256, n_text=64, frac8=0.1, frac4=0.3, seed=3),
     "streaming": dict(batch=64, h_q=32, h_kv=32, d=128, bits=2, G=32, R=128,
                       prompt=8192, steps=256, n_out=3, factor=15.0, seed=4),
+    # per-sequence lengths in one paged cache: Llama-2-7B heads, prompt
+    # lengths drawn uniformly from [min_len, max_len] (ragged_lengths)
+    "ragged_paged": dict(batch=16, h_q=32, h_kv=32, d=128, bits=2, G=32, R=128, page=256,
+                         min_len=512, max_len=8192, n_out=3, factor=15.0, seed=5),
 }
+
+
+def ragged_lengths(w):
+    """Seeded per-sequence prompt lengths of a ragged workload."""
+    g = rng(w["seed"], TAG_LEN)
+    return g.integers(w["min_len"], w["max_len"] + 1, size=w["batch"]).astype(np.int32)
