@@ -155,3 +155,19 @@ def test_paged_decode_plan_passes_geometry_check(L, d, G, gv, R, bits, P, gq):
                                           ctypes.c_void_p(BASE // 2), ws, None)
         msg = L.kvq_last_error_string().decode()
         assert st == kvq.KVQ_ERR_CUDA, (st, msg, trial)
+
+
+def test_paged_tile_geometry_enumeration(tmp_path):
+    """Every consistent per-sequence state of several shapes through the
+    header's paged tile geometry (host build of tests/paged_geometry.cu)."""
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = tmp_path / "paged_geometry"
+    subprocess.run([nvcc, "-std=c++17", "-O2", "--expt-relaxed-constexpr", "-x", "cu",
+                    os.path.join(ROOT, "tests", "paged_geometry.cu"), "-o", str(exe)],
+                   check=True, capture_output=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:]
+    assert "bad 0" in r.stdout
