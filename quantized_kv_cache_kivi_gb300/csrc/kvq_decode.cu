@@ -265,7 +265,7 @@ __device__ inline void cta_issue(const PagedArgs& a, const CtaWork& w, int t, ui
     }
     return pg;
   };
-  for_each_paged_copy(a, w.b, w.hk, s, ti, page, [&](const void* src, uint32_t off, uint32_t bytes) {
+  for_each_paged_copy(a, w.b, w.hk, s, ti, page, [&](const void* src, uint32_t off, uint32_t bytes, int) {
     bulk_g2s(stage + off, src, bytes, bar);
   });
 }

@@ -1204,7 +1204,7 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
     for (int h = 0; h < HQ; ++h)
       if (h < nh)
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) a.out[out_base + h * D + lane + 32 * i] = __float2half_rn(O[h][i] / L[h]);
+        for (int i = 0; i < D / 32; ++i) a.out[out_base + h * D + lane + 32 * i] = __float2half_rn(L[h] > 0.f ? O[h][i] / L[h] : 0.f);
     return;
   }
   // records [pair][piece][head][REC]
@@ -1244,12 +1244,12 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
     float l = 0.f;
     for (int s = lane; s < pieces; s += 32) {
       const float* rr = recs + ((size_t)s * nh + h) * REC;
-      l += __ldcg(rr + D + 1) * exp2f(__ldcg(rr + D) - m);
+      if (m != -INFINITY) l += __ldcg(rr + D + 1) * exp2f(__ldcg(rr + D) - m);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(kFull, l, off);
     MM[h] = m;
-    IL[h] = 1.f / l;
+    IL[h] = l > 0.f ? 1.f / l : 0.f;  // l = 0: a sequence with no tokens, output 0
   }
   float OO[HQ][D / 32];
 #pragma unroll
@@ -1262,7 +1262,7 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
     for (int h = 0; h < HQ; ++h) {
       if (h >= nh) continue;
       const float* rr = recs + ((size_t)s * nh + h) * REC;
-      const float w = exp2f(__ldcg(rr + D) - MM[h]) * IL[h];
+      const float w = MM[h] == -INFINITY ? 0.f : exp2f(__ldcg(rr + D) - MM[h]) * IL[h];
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) OO[h][i] += __ldcg(rr + lane + 32 * i) * w;
     }
@@ -1275,8 +1275,19 @@ __device__ void finish_piece(const DecodeArgs& a, uint8_t* smem, int pair, int p
   if (lane == 0) a.counters[pair] = 0;
 }
 
-template <int B, int HQ>
-__global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel(const DecodeArgs a) {
+// Launch arguments of a paged cache (per-sequence lengths), or nothing.
+struct TcNoPaged {
+  int unused;
+};
+
+// PG: a paged cache.  Every (sequence, kv head) is padded to a.n_tiles tiles
+// (the longest sequence's count) so the stream-K ranges, owners and merges
+// keep their uniform tile index; a padding tile (t >= the sequence's own
+// count) takes no pipeline stage: the issue warp and the consumers skip it
+// by the same rule.
+template <int B, int HQ, bool PG>
+__global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm)
+    decode_tc_kernel(const DecodeArgs a, const typename std::conditional<PG, PagedArgs, TcNoPaged>::type p) {
   using SM = TcSmem<HQ>;
   constexpr int NCW = TcCfg<HQ>::NCW, NTH = TcCfg<HQ>::NTH, NSLOT = TcCfg<HQ>::NSLOT, NS = TcCfg<HQ>::NS;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -1325,9 +1336,9 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
     uint32_t bytes = 0;
     const void* src[6];
     uint32_t dst[6], nb[6];
-    int nissued = 0;
-    for (int j = 0; j < ntiles; ++j) {
-      const int st = j % NS;
+    int nissued = 0;  // stages used so far (live tiles issued)
+    unsigned live = 0u;  // live tiles among the 32 of the current batch
+    for (int j = 0, k = 0; j < ntiles; ++j) {
       if ((j & 31) == 0) {
         const int jl = j + lane;
 #pragma unroll
@@ -1335,10 +1346,8 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
           src[k] = nullptr;
           dst[k] = nb[k] = 0u;
         }
-        if (jl < ntiles) {
-          const int g = g_begin + jl;
-          pair = g / sa.n_tiles;
-          const TileInfo ti = tile_info(sa, g - pair * sa.n_tiles);
+        bool mine = false;
+        auto fill = [&](const TileInfo& ti) {
           rec.n = ti.n;
           rec.kq = ti.kseg >= 0;
           rec.vq = ti.vseg >= 0;
@@ -1352,23 +1361,60 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
           rec.kb = ti.kbits;
           rec.vb = ti.vbits;
           bytes = ti.bytes + (HQ == 1 ? 1 : sa.gq) * D * 2;
-          bool k2 = false, v2 = false;
-          for_each_tile_copy(sa, (size_t)pair, ti, [&](const void* s_, uint32_t off, uint32_t n_, int buf, int) {
-            const int slot = buf < 6 ? buf : (buf == 6 ? (k2 ? 1 : 0) : (v2 ? 4 : 3));
-            if (buf == 6) k2 = true;
-            if (buf == 7) v2 = true;
-            src[slot] = s_;
-            dst[slot] = off;
-            nb[slot] = n_;
-          });
+        };
+        if (jl < ntiles) {
+          const int g = g_begin + jl;
+          pair = g / sa.n_tiles;
+          const int t = g - pair * sa.n_tiles;
+          if constexpr (PG) {
+            const int b = pair / sa.h_kv, h = pair - b * sa.h_kv;
+            const PagedSeq& ps = p.seq[b];
+            mine = t < ps.n_tiles;
+            if (mine) {
+              const TileInfo ti = paged_tile(p, ps, t);
+              fill(ti);
+              // a block-table entry outside the pool is not followed: page
+              // 0 is read in its place and the cache's error word is set
+              auto page = [&](int row) {
+                const int jp = row / p.P;
+                const int pg = jp < p.max_pages ? p.table[(size_t)b * p.max_pages + jp] : -1;
+                if (pg < 0 || pg >= p.n_pages) {
+                  atomicExch(p.page_err, 2);
+                  return 0;
+                }
+                return pg;
+              };
+              for_each_paged_copy(p, b, h, ps, ti, page, [&](const void* s_, uint32_t off, uint32_t n_, int slot) {
+                src[slot] = s_;
+                dst[slot] = off;
+                nb[slot] = n_;
+              });
+            }
+          } else {
+            mine = true;
+            const TileInfo ti = tile_info(sa, t);
+            fill(ti);
+            bool k2 = false, v2 = false;
+            for_each_tile_copy(sa, (size_t)pair, ti, [&](const void* s_, uint32_t off, uint32_t n_, int buf, int) {
+              const int slot = buf < 6 ? buf : (buf == 6 ? (k2 ? 1 : 0) : (v2 ? 4 : 3));
+              if (buf == 6) k2 = true;
+              if (buf == 7) v2 = true;
+              src[slot] = s_;
+              dst[slot] = off;
+              nb[slot] = n_;
+            });
+          }
         }
+        live = __ballot_sync(kFull, mine);
       }
-      if (j >= NS) {
-        if (__any_sync(kFull, !wait_or_abort<true>(&empty[st], (uint32_t)(((j / NS) & 1) ^ 1), flags))) break;
+      if (!((live >> (j & 31)) & 1u)) continue;  // padding tile: no stage
+      const int st = k % NS;
+      if (k >= NS) {
+        if (__any_sync(kFull, !wait_or_abort<true>(&empty[st], (uint32_t)(((k / NS) & 1) ^ 1), flags))) break;
         // consumers that gave up release a stage without waiting for it
-        if (!mbar_drain_bounded(&full[st], (uint32_t)(((j / NS) & 1) ^ 1)) && lane == 0) atomicExch(sa.err, 1);
+        if (!mbar_drain_bounded(&full[st], (uint32_t)(((k / NS) & 1) ^ 1)) && lane == 0) atomicExch(sa.err, 1);
       }
-      nissued = j + 1;
+      nissued = ++k;
       if (lane == (j & 31)) {
         recs[st] = rec;
         uint8_t* stage = smem + SM::stages + st * kTcStageBytes;
@@ -1397,16 +1443,23 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
   int piece = 0;  // pieces (pairs) of this CTA's range finished so far
   int jstart = warp;  // this warp's first sub-tile of the next tile (round-robin)
   bool aborted = false;
-  for (int it = 0; it < ntiles; ++it) {
-    const int st = it % NS;
-    const uint32_t ph = (uint32_t)((it / NS) & 1);
+  auto live_tiles = [&](int pr) {
+    if constexpr (PG) return p.seq[pr / a.h_kv].n_tiles;
+    else return a.n_tiles;
+  };
+  int n_live = live_tiles(cur_pair);
+  for (int it = 0, k = 0; it < ntiles; ++it) {
     if (t_in_pair == a.n_tiles) {  // first tile of the next pair
       finish_piece<B, HQ>(a, smem, cur_pair, piece++, warp, lane, S, flags);
       reset();
       ++cur_pair;
       t_in_pair = 0;
+      n_live = live_tiles(cur_pair);
     }
-    ++t_in_pair;
+    if (t_in_pair++ >= n_live) continue;  // padding tile: no stage
+    const int st = k % NS;
+    const uint32_t ph = (uint32_t)((k / NS) & 1);
+    ++k;
     if (!aborted && __any_sync(kFull, !wait_or_abort<false>(&full[st], ph, flags))) aborted = true;
     if (!aborted) {
       const int4 r0 = *reinterpret_cast<const int4*>(&recs[st].n);
@@ -1441,20 +1494,20 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm) decode_tc_kernel
   if (ntiles > 0) finish_piece<B, HQ>(a, smem, cur_pair, piece, warp, lane, S, flags);
 }
 
-template <int B, int HQ>
-cudaError_t launch_tc_b(const DecodeArgs& a, cudaStream_t s) {
+template <int B, int HQ, bool PG = false, class PA = TcNoPaged>
+cudaError_t launch_tc_b(const DecodeArgs& a, cudaStream_t s, const PA& p = PA{}) {
   const int smem = TcSmem<HQ>::total;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<B, HQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<B, HQ, PG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<B, HQ><<<a.n_cta, TcCfg<HQ>::NTH, smem, s>>>(a);
+  decode_tc_kernel<B, HQ, PG><<<a.n_cta, TcCfg<HQ>::NTH, smem, s>>>(a, p);
   return cudaGetLastError();
 }
 
-template <int HQ>
-cudaError_t launch_tc_hq(const DecodeArgs& a, int bits, cudaStream_t s) {
-  if (bits == 2) return launch_tc_b<2, HQ>(a, s);
-  if (bits == 4) return launch_tc_b<4, HQ>(a, s);
-  return launch_tc_b<8, HQ>(a, s);
+template <int HQ, bool PG = false, class PA = TcNoPaged>
+cudaError_t launch_tc_hq(const DecodeArgs& a, int bits, cudaStream_t s, const PA& p = PA{}) {
+  if (bits == 2) return launch_tc_b<2, HQ, PG>(a, s, p);
+  if (bits == 4) return launch_tc_b<4, HQ, PG>(a, s, p);
+  return launch_tc_b<8, HQ, PG>(a, s, p);
 }
 
 // Merge of a pair's partial records in a launch of its own (many records):
@@ -1490,7 +1543,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_tc_kernel(const DecodeArg
   float l = 0.f;
   if (tid < pieces) {
     const float* rr = recs + (size_t)tid * nh * REC;
-    const float ws = exp2f(rr[D] - m);
+    const float ws = m == -INFINITY ? 0.f : exp2f(rr[D] - m);
     w[tid] = ws;
     l = rr[D + 1] * ws;
   }
@@ -1511,7 +1564,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_tc_kernel(const DecodeArg
   if (k == 0) {
 #pragma unroll
     for (int i = 1; i < kMergeThreads / D; ++i) o += part[i][c];
-    a.out[((size_t)pair * nh + h) * D + c] = __float2half_rn(o / l);
+    a.out[((size_t)pair * nh + h) * D + c] = __float2half_rn(l > 0.f ? o / l : 0.f);
   }
 }
 
@@ -1530,6 +1583,12 @@ int decode_tc_ctas_per_sm() { return kTcCtasPerSm; }
 cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, int form, cudaStream_t s) {
   if (form == 8) return launch_tc_b<0, 8>(a, s);
   return form == 1 ? launch_tc_hq<1>(a, bits, s) : launch_tc_hq<4>(a, bits, s);
+}
+
+// The same kernels over a paged cache (per-sequence lengths).
+cudaError_t launch_decode_tc_paged(const DecodeArgs& a, const PagedArgs& p, int bits, int form, cudaStream_t s) {
+  if (form == 8) return launch_tc_b<0, 8, true>(a, s, p);
+  return form == 1 ? launch_tc_hq<1, true>(a, bits, s, p) : launch_tc_hq<4, true>(a, bits, s, p);
 }
 
 }  // namespace kvq

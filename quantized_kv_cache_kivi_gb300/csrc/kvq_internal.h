@@ -360,7 +360,8 @@ __host__ __device__ inline TileInfo paged_tile(const PagedArgs& a, const PagedSe
 }
 
 // Visit the bulk copies that stage paged tile `ti` of sequence b, kv head h:
-// f(src, dst_off, bytes).  page(row) maps a packed row to its pool page (the
+// f(src, dst_off, bytes, slot), slot 0-2 the K side (codes, scales, zeros or
+// the ring's one or two pieces), 3-5 the V side.  page(row) maps a packed row to its pool page (the
 // caller checks the block-table entry).
 template <class Page, class F>
 __host__ __device__ inline void for_each_paged_copy(const PagedArgs& a, int b, int h, const PagedSeq& s,
@@ -371,31 +372,31 @@ __host__ __device__ inline void for_each_paged_copy(const PagedArgs& a, int b, i
   if (ti.kseg == 0) {
     const size_t ph = (size_t)page(ti.ku0) * a.h_kv + h;
     const int r = ti.ku0 % P;
-    f(a.kc + (ph * P + r) * rb, ti.k_off, (uint32_t)(ti.n * rb));
+    f(a.kc + (ph * P + r) * rb, ti.k_off, (uint32_t)(ti.n * rb), 0);
     const size_t gbase = (ph * (size_t)(P / a.G) + r / a.G) * D;
-    f(a.ks + gbase, ti.ks_off, (uint32_t)(ti.ng * D * 2));
-    f(a.kz + gbase, ti.kz_off, (uint32_t)(ti.ng * D * 2));
+    f(a.ks + gbase, ti.ks_off, (uint32_t)(ti.ng * D * 2), 1);
+    f(a.kz + gbase, ti.kz_off, (uint32_t)(ti.ng * D * 2), 2);
   } else {
     const int s0 = (s.krs + ti.ku0) % a.R;
     const int n1 = ti.n < a.R - s0 ? ti.n : a.R - s0;
     const __half* ring = a.kr + pair * (size_t)a.R * D;
-    f(ring + (size_t)s0 * D, ti.k_off, (uint32_t)(n1 * D * 2));
-    if (n1 < ti.n) f(ring, ti.k_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2));
+    f(ring + (size_t)s0 * D, ti.k_off, (uint32_t)(n1 * D * 2), 0);
+    if (n1 < ti.n) f(ring, ti.k_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2), 1);
   }
   if (ti.vseg == 0) {
     const size_t ph = (size_t)page(ti.vu0) * a.h_kv + h;
     const int r = ti.vu0 % P;
-    f(a.vc + (ph * P + r) * rb, ti.v_off, (uint32_t)(ti.n * rb));
+    f(a.vc + (ph * P + r) * rb, ti.v_off, (uint32_t)(ti.n * rb), 3);
     const size_t sbase = (ph * P + r) * (D / a.Gv);
     const uint32_t sb = align16u((uint32_t)ti.n * (uint32_t)(D / a.Gv) * 2u);
-    f(a.vs + sbase, ti.vs_off, sb);
-    f(a.vz + sbase, ti.vz_off, sb);
+    f(a.vs + sbase, ti.vs_off, sb, 4);
+    f(a.vz + sbase, ti.vz_off, sb, 5);
   } else {
     const int s0 = (s.vrs + ti.vu0) % a.R;
     const int n1 = ti.n < a.R - s0 ? ti.n : a.R - s0;
     const __half* ring = a.vr + pair * (size_t)a.R * D;
-    f(ring + (size_t)s0 * D, ti.v_off, (uint32_t)(n1 * D * 2));
-    if (n1 < ti.n) f(ring, ti.v_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2));
+    f(ring + (size_t)s0 * D, ti.v_off, (uint32_t)(n1 * D * 2), 3);
+    if (n1 < ti.n) f(ring, ti.v_off + (uint32_t)(n1 * D * 2), (uint32_t)((ti.n - n1) * D * 2), 4);
   }
 }
 
@@ -444,6 +445,7 @@ cudaError_t launch_decode_mha(const DecodeArgs& a, int n_pairs, int bits, cudaSt
 cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, int form, cudaStream_t s);
 cudaError_t launch_decode_tc_merge(const DecodeArgs& a, int n_pairs, cudaStream_t s);
 cudaError_t launch_decode_paged(const PagedArgs& a, cudaStream_t s);
+cudaError_t launch_decode_tc_paged(const DecodeArgs& a, const PagedArgs& p, int bits, int form, cudaStream_t s);
 cudaError_t launch_paged_append(const PagedAppendArgs& a, cudaStream_t s);
 int decode_tc_ctas_per_sm();
 size_t decode_mha_smem_bytes();

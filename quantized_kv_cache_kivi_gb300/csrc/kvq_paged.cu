@@ -96,6 +96,125 @@ bool tile_fits(int t, int kb, int vb, int d, int G, int Gv, int gq) {
   return kb == 16 || ((t + G - 1) / G + 1) * gq * d * 4 <= kvq::kQsBytes;
 }
 
+// Geometry check of a paged plan: every run's first and last tile of every
+// sequence (interior tiles repeat the aligned full-size shape) through the
+// kernels' own functions: tokens, stage bytes, no page crossed, 16-byte
+// copies inside their page (page 0 stands in) or ring, bytes as expected;
+// for the tensor-core kernel also the K groups a tile touches and 32-token
+// units inside one K group.
+kvq_status check_paged_plan(const kvq_paged_cache* c, const kvq::PagedArgs& a, uint32_t stage_cap, bool tc) {
+  const int d = a.d, G = a.G, Gv = a.Gv, rb = d * a.bits / 8;
+  const size_t n_pairs = (size_t)c->batch * c->h_kv;
+  const size_t page_k = (size_t)c->h_kv * a.P * rb;
+  const size_t ring = n_pairs * a.R * d * 2;
+  for (int b = 0; b < c->batch; ++b) {
+    const kvq::PagedSeq& q = a.seq[b];
+    const int L = q.nk + q.nkr;
+    const int a0 = std::min(q.nk, q.nv), a1 = std::max(q.nk, q.nv);
+    const int n0 = kvq::paged_run_tiles(0, a0, a.tile_pp), n1 = kvq::paged_run_tiles(a0, a1, a.tile_mix),
+              n2 = kvq::paged_run_tiles(a1, L, a.tile_mix);
+    const int ends[6] = {0, n0 - 1, n0, n0 + n1 - 1, n0 + n1, n0 + n1 + n2 - 1};
+    for (int t : ends) {
+      if (t < 0 || t >= q.n_tiles) continue;
+      const kvq::TileInfo ti = kvq::paged_tile(a, q, t);
+      if (ti.n < 1 || ti.bytes > stage_cap || ti.n > (tc ? 256 : 128))
+        return pfail(KVQ_ERR_UNSUPPORTED, "paged tile %d of sequence %d does not fit a stage", t, b);
+      if ((ti.kseg == 0 && (ti.ku0 / a.P != (ti.ku0 + ti.n - 1) / a.P)) ||
+          (ti.vseg == 0 && (ti.vu0 / a.P != (ti.vu0 + ti.n - 1) / a.P)))
+        return pfail(KVQ_ERR_UNSUPPORTED, "paged tile %d of sequence %d crosses a page", t, b);
+      if (tc && ti.kseg == 0 &&
+          (ti.ng > kvq::kTcMaxGroups || (ti.ku0 % 32 != 0 && ti.ku0 / 32 != (ti.ku0 + ti.n - 1) / 32)))
+        return pfail(KVQ_ERR_UNSUPPORTED, "paged tile %d of sequence %d: K groups or units", t, b);
+      uint32_t sum = 0;
+      bool ok = true;
+      kvq::for_each_paged_copy(a, b, c->h_kv - 1, q, ti, [](int) { return 0; },
+                               [&](const void* src, uint32_t off, uint32_t bytes, int slot) {
+                                 sum += bytes;
+                                 if (slot < 0 || slot > 5 || bytes % 16 || off % 16 || ((uintptr_t)src & 15u))
+                                   ok = false;
+                                 const uint8_t* p = static_cast<const uint8_t*>(src);
+                                 auto inside = [&](const void* base, size_t n) {
+                                   const uint8_t* b0 = static_cast<const uint8_t*>(base);
+                                   return p >= b0 && p + bytes <= b0 + n;
+                                 };
+                                 if (!(inside(a.kc, page_k) || inside(a.vc, page_k) ||
+                                       inside(a.ks, page_k / rb / G * d * 2) || inside(a.kz, page_k / rb / G * d * 2) ||
+                                       inside(a.vs, page_k / rb * (d / Gv) * 2) ||
+                                       inside(a.vz, page_k / rb * (d / Gv) * 2) || inside(a.kr, ring) ||
+                                       inside(a.vr, ring)))
+                                   ok = false;
+                               });
+      if (!ok || sum != ti.bytes)
+        return pfail(KVQ_ERR_UNSUPPORTED, "paged tile %d of sequence %d: copy geometry check failed", t, b);
+    }
+  }
+  return KVQ_OK;
+}
+
+// Stream-K ranges of the tensor-core kernel over a paged cache: every pair
+// padded to nt tiles; a live tile costs its 32-token units plus a quarter
+// unit, a padding tile nothing.  CTA i's range starts at the first tile
+// whose cost prefix reaches i/N of the total, kept non-empty.  Returns the
+// most ranges that meet one pair.
+int paged_tc_ranges(const kvq::PagedArgs& a, int h_kv, int nt, int N, int* bound) {
+  const int B = a.n_seq;
+  std::vector<std::vector<long long>> pre(B, std::vector<long long>(nt + 1, 0));
+  for (int b = 0; b < B; ++b)
+    for (int t = 0; t < nt; ++t) {
+      long long c = 0;
+      if (t < a.seq[b].n_tiles) c = 4 * ((kvq::paged_tile(a, a.seq[b], t).n + 31) / 32) + 1;
+      pre[b][t + 1] = pre[b][t] + c;
+    }
+  const long long n_pairs = (long long)B * h_kv, T = n_pairs * nt;
+  std::vector<long long> cum(n_pairs + 1, 0);
+  for (long long pr = 0; pr < n_pairs; ++pr) cum[pr + 1] = cum[pr] + pre[pr / h_kv][nt];
+  auto prefix = [&](long long g) {
+    const long long pr = g / nt;
+    return pr >= n_pairs ? cum[n_pairs] : cum[pr] + pre[pr / h_kv][g % nt];
+  };
+  const long long total = cum[n_pairs];
+  bound[0] = 0;
+  for (int i = 1; i < N; ++i) {
+    const long long target = total * i / N;
+    long long lo = 0, hi = T;
+    while (lo < hi) {
+      const long long mid = (lo + hi) / 2;
+      if (prefix(mid) >= target) hi = mid;
+      else lo = mid + 1;
+    }
+    lo = std::max<long long>(lo, bound[i - 1] + 1);
+    lo = std::min<long long>(lo, T - (N - i));
+    bound[i] = (int)lo;
+  }
+  bound[N] = (int)T;
+  int most = 1, run = 1;
+  long long run_pair = -1;
+  for (int i = 1; i < N; ++i) {
+    if (bound[i] % nt == 0) continue;
+    const long long pr = bound[i] / nt;
+    run = pr == run_pair ? run + 1 : 2;
+    run_pair = pr;
+    most = std::max(most, run);
+  }
+  return most;
+}
+
+// Tensor-core form for a paged cache (the uniform cache's rules): 1 = one
+// query head per kv head, 4 = 2-4 heads, 8 = up to 8 heads (no tile with
+// fp16 K beside packed V); 0 = the general kernel.
+int paged_tc_form(const kvq_paged_cache* c) {
+  const int gq = c->h_q / c->h_kv, d = c->d_h, G = c->group, Gv = gv_of(c);
+  if (d != 128 || G < 32) return 0;
+  if (gq == 1 && Gv >= d / 4) return 1;
+  if (gq >= 2 && gq <= 4 && Gv >= 64) return 4;
+  if (gq <= kvq::kMaxGq && Gv >= 16) {
+    for (int b = 0; b < c->batch; ++b)
+      if (c->seq[b].nv > c->seq[b].nk) return 0;
+    return 8;
+  }
+  return 0;
+}
+
 kvq::PagedAppendArgs append_base(const kvq_paged_cache* c, int T, const void* k_new, const void* v_new) {
   kvq::PagedAppendArgs a{};
   a.batch = c->batch;
@@ -270,18 +389,25 @@ kvq_status kvq_paged_decode_attention(const kvq_paged_cache* c, const void* q, v
   a.page_err = c->err;
   a.n_splits = ws_splits;
   // tiles: the largest power of two that fits a stage (packed K and V), and
-  // one for tiles that read a ring; both divide the page
+  // one for tiles that read a ring; both divide the page.  The tensor-core
+  // kernel takes 32-token tiles where a ring is involved (a tile starting
+  // inside a 32-token unit must end in it).
   const int G = a.G, Gv = a.Gv, bits = a.bits;
-  for (int t = 128; t >= 16 && !a.tile_pp; t >>= 1)
-    if (tile_fits(t, bits, bits, d, G, Gv, gq)) a.tile_pp = t;
-  for (int t = a.tile_pp; t >= 16 && !a.tile_mix; t >>= 1)
-    if (tile_fits(t, 16, 16, d, G, Gv, gq) && tile_fits(t, bits, 16, d, G, Gv, gq) &&
-        tile_fits(t, 16, bits, d, G, Gv, gq))
-      a.tile_mix = t;
+  const int form = paged_tc_form(c);
+  const bool tc = form != 0;
+  auto fits = [&](int t, int kb, int vb) {
+    if (tc)
+      return stage_bytes(t, kb, vb, d, G, Gv) <= kvq::kTcStageBytes &&
+             (kb == 16 || (t + G - 1) / G + 1 <= kvq::kTcMaxGroups);
+    return tile_fits(t, kb, vb, d, G, Gv, gq);
+  };
+  for (int t = tc ? 256 : 128; t >= (tc ? 32 : 16) && !a.tile_pp; t >>= 1)
+    if (a.P % t == 0 && fits(t, bits, bits)) a.tile_pp = t;
+  for (int t = tc ? 32 : a.tile_pp; t >= 16 && !a.tile_mix; t >>= 1)
+    if (t <= a.tile_pp && fits(t, 16, 16) && fits(t, bits, 16) && fits(t, 16, bits)) a.tile_mix = t;
   if (!a.tile_pp || !a.tile_mix) return pfail(KVQ_ERR_UNSUPPORTED, "no tile fits a pipeline stage");
-  // splits per sequence: about four CTAs per SM over all tiles, each CTA a
-  // contiguous range of one sequence's tiles
   long long total = 0;
+  int nt_max = 0;
   std::vector<int> nt(c->batch);
   for (int b = 0; b < c->batch; ++b) {
     kvq::PagedSeq& q = a.seq[b];
@@ -294,12 +420,69 @@ kvq_status kvq_paged_decode_attention(const kvq_paged_cache* c, const void* q, v
     q.vrs = cs.v_ring_start;
     nt[b] = kvq::paged_tiles(a, q);
     q.n_tiles = nt[b];
+    nt_max = std::max(nt_max, nt[b]);
     total += (long long)nt[b] * c->h_kv;
   }
+  a.n_seq = c->batch;
   if (total == 0) {
     const cudaError_t e = cudaMemsetAsync(out, 0, (size_t)c->batch * c->h_q * d * 2, s);
     return e == cudaSuccess ? KVQ_OK : pcuda(e, "zero output");
   }
+  st = check_paged_plan(c, a, tc ? (uint32_t)kvq::kTcStageBytes : (uint32_t)kvq::kStageBytes, tc);
+  if (st != KVQ_OK) return st;
+  if (tc) {
+    // the tensor-core kernel: persistent CTAs over all pairs' tiles, each
+    // pair padded to the longest sequence's tile count (padding tiles cost
+    // no stage)
+    if ((long long)n_pairs * nt_max >= (1LL << 31)) return pfail(KVQ_ERR_UNSUPPORTED, "more than 2^31 tiles");
+    kvq::DecodeArgs u{};
+    u.batch = c->batch;
+    u.h_kv = c->h_kv;
+    u.gq = gq;
+    u.d = d;
+    u.G = G;
+    u.log2G = a.log2G;
+    u.Gv = Gv;
+    u.log2Gv = a.log2Gv;
+    u.R = a.R;
+    u.scale_log2 = a.scale_log2;
+    u.n_seg = 1;
+    u.kr = a.kr;
+    u.vr = a.vr;
+    u.q = a.q;
+    u.out = a.out;
+    u.err = a.err;
+    u.counters = a.counters;
+    u.part = a.part;
+    u.n_tiles = nt_max;
+    u.n_splits = std::max(1, ws_splits);
+    const long long T = (long long)n_pairs * nt_max;
+    const int cap = std::max(ws_splits, 1);
+    long long N = std::min<long long>(T, (long long)sms() * kvq::decode_tc_ctas_per_sm());
+    N = std::min<long long>(N, kvq::kTcMaxCtas);
+    N = std::min<long long>(N, std::max<long long>(n_pairs, (long long)n_pairs * (cap - 1)));
+    while (true) {
+      const int most = paged_tc_ranges(a, c->h_kv, nt_max, (int)N, u.tc_bound);
+      u.tc_defer = most > 16;  // past 16 records a pair, a merge launch of its own
+      if (most <= cap) {
+        u.n_cta = (int)N;
+        u.tc_whole = 0;
+        break;
+      }
+      if (N <= n_pairs) {
+        u.n_cta = n_pairs;  // one pair per CTA: no records
+        u.tc_whole = 1;
+        u.tc_defer = 0;
+        break;
+      }
+      N = std::max<long long>(n_pairs, N - std::max<long long>(1, N / 32));
+    }
+    cudaError_t e = kvq::launch_decode_tc_paged(u, a, bits, form, s);
+    if (e == cudaSuccess && u.tc_defer) e = kvq::launch_decode_tc_merge(u, n_pairs, s);
+    return e == cudaSuccess ? KVQ_OK : pcuda(e, "paged decode launch");
+  }
+  // the general kernel: about four CTAs per SM over all tiles, each CTA a
+  // contiguous range of one sequence's tiles
   const long long per_cta = std::max<long long>(4, (total + 4LL * sms() - 1) / (4LL * sms()));
   int cols = 0;
   for (int b = 0; b < c->batch; ++b) {
@@ -310,50 +493,6 @@ kvq_status kvq_paged_decode_attention(const kvq_paged_cache* c, const void* q, v
     cols += q.n_split;
   }
   a.n_cols = cols;
-  a.n_seq = c->batch;
-  // every run's first and last tile of every sequence through the kernel's
-  // geometry (interior tiles repeat the aligned full-size shape): stage size,
-  // 16-byte copies, copies inside their page / ring, bytes as expected
-  const int rb = d * bits / 8;
-  for (int b = 0; b < c->batch; ++b) {
-    const kvq::PagedSeq& q = a.seq[b];
-    const int L = q.nk + q.nkr;
-    const int a0 = std::min(q.nk, q.nv), a1 = std::max(q.nk, q.nv);
-    const int n0 = kvq::paged_run_tiles(0, a0, a.tile_pp), n1 = kvq::paged_run_tiles(a0, a1, a.tile_mix),
-              n2 = kvq::paged_run_tiles(a1, L, a.tile_mix);
-    const int firsts[6] = {0, n0 - 1, n0, n0 + n1 - 1, n0 + n1, n0 + n1 + n2 - 1};
-    for (int t : firsts) {
-      if (t < 0 || t >= q.n_tiles) continue;
-      const kvq::TileInfo ti = kvq::paged_tile(a, q, t);
-      if (ti.n < 1 || ti.bytes > (uint32_t)kvq::kStageBytes || ti.n > 128)
-        return pfail(KVQ_ERR_UNSUPPORTED, "paged tile %d of sequence %d does not fit a stage", t, b);
-      if ((ti.kseg == 0 && (ti.ku0 / a.P != (ti.ku0 + ti.n - 1) / a.P)) ||
-          (ti.vseg == 0 && (ti.vu0 / a.P != (ti.vu0 + ti.n - 1) / a.P)))
-        return pfail(KVQ_ERR_UNSUPPORTED, "paged tile %d of sequence %d crosses a page", t, b);
-      uint32_t sum = 0;
-      bool ok = true;
-      const size_t page_k = (size_t)c->h_kv * a.P * rb;
-      for_each_paged_copy(a, b, c->h_kv - 1, q, ti, [](int) { return 0; },
-                          [&](const void* src, uint32_t off, uint32_t bytes) {
-                            sum += bytes;
-                            if (bytes % 16 || off % 16 || ((uintptr_t)src & 15u)) ok = false;
-                            const uint8_t* p = static_cast<const uint8_t*>(src);
-                            auto inside = [&](const void* base, size_t n) {
-                              const uint8_t* b0 = static_cast<const uint8_t*>(base);
-                              return p >= b0 && p + bytes <= b0 + n;
-                            };
-                            const size_t ring = (size_t)n_pairs * a.R * d * 2;
-                            if (!(inside(a.kc, page_k) || inside(a.vc, page_k) ||
-                                  inside(a.ks, page_k / rb / G * d * 2) || inside(a.kz, page_k / rb / G * d * 2) ||
-                                  inside(a.vs, page_k / rb * (d / Gv) * 2) ||
-                                  inside(a.vz, page_k / rb * (d / Gv) * 2) || inside(a.kr, ring) ||
-                                  inside(a.vr, ring)))
-                              ok = false;
-                          });
-      if (!ok || sum != ti.bytes)
-        return pfail(KVQ_ERR_UNSUPPORTED, "paged tile %d of sequence %d: copy geometry check failed", t, b);
-    }
-  }
   const cudaError_t e = kvq::launch_decode_paged(a, s);
   return e == cudaSuccess ? KVQ_OK : pcuda(e, "paged decode launch");
 }

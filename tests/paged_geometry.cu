@@ -66,7 +66,8 @@ int main() {
             for (int b = 0; b < B; ++b) for (int h = 0; h < a.h_kv; ++h) {
               uint32_t sum = 0;
               auto page = [&](int row) { return (row / a.P * 5 + b) % a.n_pages; };
-              for_each_paged_copy(a, b, h, s, ti, page, [&](const void* src, uint32_t off, uint32_t bytes) {
+              for_each_paged_copy(a, b, h, s, ti, page, [&](const void* src, uint32_t off, uint32_t bytes, int slot) {
+                if (slot < 0 || slot > 5) ok = false;
                 sum += bytes;
                 if (bytes % 16 || off % 16 || ((uintptr_t)src & 15)) ok = false;
                 if (off + bytes > ti.bytes) ok = false;

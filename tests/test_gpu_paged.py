@@ -180,6 +180,15 @@ def test_paged_integer_zero_point_and_v_group():
     assert pp.attention_error(_q(3, 3, 4, 128)) < TOL
 
 
+def test_paged_general_kernel_at_head_dim_128():
+    """K groups of 16 tokens keep d_h 128 on the general kernel's paged form
+    (the tensor-core forms need groups of 32 or more)."""
+    pp = PagedPair(batch=4, h_kv=2, h_q=4, d=128, G=16, R=32, bits=4, P=128, max_pages=5, seed=6)
+    _run_ragged(pp, 81, prompt=[400, 0, 90, 255], steps=33)
+    pp.assert_bit_exact()
+    assert pp.attention_error(_q(5, 4, 4, 128)) < TOL
+
+
 def test_paged_head_dim_64_and_eight_query_heads():
     pp = PagedPair(batch=3, h_kv=1, h_q=8, d=64, G=16, R=32, bits=2, P=128, max_pages=5, seed=2)
     _run_ragged(pp, 41, prompt=[500, 17, 33], steps=35)
