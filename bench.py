@@ -353,6 +353,7 @@ def per_workload_attention(device, flush_l2, peak, reps=20, only=None):
                                        "frac": nb / (us * 1e-6) / 1e9 / peak, "bytes": nb,
                                        "tokens": int(lens.sum()) * H}
         del K, V
+        torch.cuda.empty_cache()
         q = torch.randn(B, Hq, d, generator=torch.Generator(device=device).manual_seed(w["seed"] + 7),
                         device=device).half()
         out = torch.empty_like(q)

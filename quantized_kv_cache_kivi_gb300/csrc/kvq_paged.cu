@@ -152,17 +152,29 @@ kvq_status check_paged_plan(const kvq_paged_cache* c, const kvq::PagedArgs& a, u
 }
 
 // Stream-K ranges of the tensor-core kernel over a paged cache: every pair
-// padded to nt tiles; a live tile costs its 32-token units plus a quarter
-// unit, a padding tile nothing.  CTA i's range starts at the first tile
-// whose cost prefix reaches i/N of the total, kept non-empty.  Returns the
-// most ranges that meet one pair.
+// padded to nt tiles.  Cost of a live tile: 4 per 32-token unit plus 1 when
+// K and V are both packed; a tile that reads a ring (one 32-token unit of
+// fp16 K or V) costs 48, and a pair's first tile adds 16 for the pair's
+// merge; a padding tile costs nothing.  Such ring tiles keep one consumer
+// warp busy each while they hold a pipeline stage; measured on a ragged
+// batch (16 sequences, 644-7650 tokens, 2-bit), ring costs of 12 / 20 / 40
+// / 56 / 72 / 96 gave 133 / 117 / 94 / 93 / 94 / 101 us.  (In the uniform
+// cache every pair has the same mix of tiles, so the weights do not move
+// its ranges much; sequences of different lengths put very different mixes
+// into one CTA's range.)  CTA i's range starts at the first tile whose cost
+// prefix reaches i/N of the total, kept non-empty.  Returns the most ranges
+// that meet one pair.
 int paged_tc_ranges(const kvq::PagedArgs& a, int h_kv, int nt, int N, int* bound) {
   const int B = a.n_seq;
   std::vector<std::vector<long long>> pre(B, std::vector<long long>(nt + 1, 0));
   for (int b = 0; b < B; ++b)
     for (int t = 0; t < nt; ++t) {
       long long c = 0;
-      if (t < a.seq[b].n_tiles) c = 4 * ((kvq::paged_tile(a, a.seq[b], t).n + 31) / 32) + 1;
+      if (t < a.seq[b].n_tiles) {
+        const kvq::TileInfo ti = kvq::paged_tile(a, a.seq[b], t);
+        c = (ti.kseg == 0 && ti.vseg == 0) ? 4 * ((ti.n + 31) / 32) + 1 : 48;
+        if (t == 0) c += 16;
+      }
       pre[b][t + 1] = pre[b][t] + c;
     }
   const long long n_pairs = (long long)B * h_kv, T = n_pairs * nt;
