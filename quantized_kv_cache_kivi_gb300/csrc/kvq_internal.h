@@ -409,6 +409,7 @@ struct PagedAppendSeq {
   int v_evict, v_nv0, v_ring_tokens;
   RowSrc vsrc;
   int k_first_ring, k_slot0, v_first_ring, v_slot0;
+  int k_item0, v_item0;  // bulk kernels: first work item of the sequence
 };
 
 struct PagedAppendArgs {
@@ -428,6 +429,9 @@ struct PagedAppendArgs {
   int* page_err;
   int chunks;           // CTAs per (sequence, kv head); chunk 0 does ring work
   int flush;            // 1: K flush of the rings only (kvq_paged_flush_residual)
+  int bulk;             // 1: new-token groups and tokens go to the bulk kernels (d_h 128)
+  int k_items, v_items; // bulk kernels: (sequence, kv head, group / token) work items
+  int n_seq;
   PagedAppendSeq seq[KVQ_MAX_SEQS];
 };
 

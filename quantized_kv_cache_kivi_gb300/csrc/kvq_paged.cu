@@ -271,6 +271,7 @@ kvq_status kvq_paged_append(kvq_paged_cache* c, const void* k_new, const void* v
   kvq::PagedAppendArgs a = append_base(c, T, k_new, v_new);
   bool due = false;
   int most = 0;
+  long long k_items = 0, v_items = 0;
   // KIVI Algorithm 1 per sequence, as the uniform cache's append
   for (int b = 0; b < c->batch; ++b) {
     const kvq_seq_state& s = c->seq[b];
@@ -301,9 +302,20 @@ kvq_status kvq_paged_append(kvq_paged_cache* c, const void* k_new, const void* v
     q.v_first_ring = std::max(0, evict - s.nvr);
     q.v_slot0 = s.v_ring_start + s.nvr;
     const int in_k = q.k_groups - q.k_ring_groups, in_v = q.v_evict - q.v_ring_tokens;
+    q.k_item0 = (int)k_items;
+    q.v_item0 = (int)v_items;
+    k_items += (long long)in_k * c->h_kv;
+    v_items += (long long)in_v * c->h_kv;
     most = std::max(most, in_k + (in_v + 63) / 64);
   }
-  a.chunks = most > 0 ? 1 + std::min(256, most) : 1;
+  if (k_items >= INT_MAX || v_items >= INT_MAX) return pfail(KVQ_ERR_UNSUPPORTED, "append too large for one call");
+  a.n_seq = c->batch;
+  a.k_items = (int)k_items;
+  a.v_items = (int)v_items;
+  // the new-token work of a prompt-sized append goes to grid-wide kernels;
+  // the block kernel keeps the work that reads the old rings
+  a.bulk = c->d_h == 128 && k_items + v_items > 0;
+  a.chunks = (!a.bulk && most > 0) ? 1 + std::min(256, most) : 1;
   const cudaError_t e = kvq::launch_paged_append(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return pcuda(e, "paged append launch");
   for (int b = 0; b < c->batch; ++b) {

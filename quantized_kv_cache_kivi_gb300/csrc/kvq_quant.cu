@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kQuantThreads) paged_append_kernel(const Paged
     if (q.v_first_ring < q.t)
       copy_to_ring<D>(ring_v, a.R, q.v_slot0 + q.v_first_ring, in_v + (size_t)q.v_first_ring * D,
                       q.t - q.v_first_ring);
-    if (a.chunks > 1) return;
+    if (a.chunks > 1 || a.bulk) return;
   }
   // work that reads only new tokens, over chunks 1.. (or chunk 0 alone)
   const int workers = a.chunks > 1 ? a.chunks - 1 : 1;
@@ -619,6 +619,80 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_v_kernel(const AppendArgs a
   }
 }
 
+// Paged cache, bulk appends: the K groups and V tokens that read only new
+// tokens, as bulk_k_kernel / bulk_v_kernel, over the work items of all
+// sequences (sequence b's items start at k_item0 / v_item0; its kv heads
+// are consecutive).  Rows go to the sequence's pages; a block-table entry
+// outside the pool writes nothing and sets the cache's error word.
+__device__ __forceinline__ int paged_item_seq(const PagedAppendArgs& a, int it, bool k) {
+  int lo = 0, hi = a.n_seq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((k ? a.seq[mid].k_item0 : a.seq[mid].v_item0) <= it) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int BITS, int Z>
+__global__ void __launch_bounds__(kBulkThreads) paged_bulk_k_kernel(const PagedAppendArgs a) {
+  constexpr int D = 128;
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (kBulkThreads / 32);
+  for (int it = blockIdx.x * (kBulkThreads / 32) + (threadIdx.x >> 5); it < a.k_items; it += warps) {
+    const int b = paged_item_seq(a, it, true);
+    const PagedAppendSeq& q = a.seq[b];
+    const int per_head = q.k_groups - q.k_ring_groups;
+    const int local = it - q.k_item0;
+    const int h = local / per_head;
+    const int gi = q.k_ring_groups + local % per_head;
+    const int p0 = gi * a.G;
+    const int row = q.k_nk0 + p0;
+    const int pg = paged_page(a, b, row);
+    if (pg < 0) {
+      if (lane == 0) atomicExch(a.page_err, 2);
+      continue;
+    }
+    const size_t pair = (size_t)b * a.h_kv + h;
+    const __half* src = a.k_new + (pair * (size_t)a.T + (size_t)(p0 - q.ksrc.n_old)) * D;
+    const int r = row % a.P;
+    quant_group_warp<BITS, Z>(src, paged_view(a, pg), a.G, (size_t)h, r, r / a.G, lane);
+  }
+}
+
+template <int BITS, int Z>
+__global__ void __launch_bounds__(kBulkThreads) paged_bulk_v_kernel(const PagedAppendArgs a) {
+  constexpr int D = 128;
+  const int hl = threadIdx.x & 15;
+  const int halves_n = gridDim.x * (kBulkThreads / 16);
+  const int first = blockIdx.x * (kBulkThreads / 16) + (threadIdx.x >> 4);
+  const int rounds = (a.v_items + halves_n - 1) / halves_n;
+  // both halves of a warp run the same number of rounds (shuffles)
+  for (int k = 0; k < rounds; ++k) {
+    const int it = first + k * halves_n;
+    bool live = it < a.v_items;
+    int b = 0, h = 0, p = 0, pg = 0;
+    if (live) {
+      b = paged_item_seq(a, it, false);
+      const PagedAppendSeq& q = a.seq[b];
+      const int per_head = q.v_evict - q.v_ring_tokens;
+      const int local = it - q.v_item0;
+      h = local / per_head;
+      p = q.v_ring_tokens + local % per_head;
+      pg = paged_page(a, b, q.v_nv0 + p);
+      if (pg < 0) {
+        if (hl == 0) atomicExch(a.page_err, 2);
+        live = false;
+      }
+    }
+    const PagedAppendSeq& q = a.seq[b];
+    const size_t pair = (size_t)b * a.h_kv + h;
+    float f[8];
+    load8(a.v_new + (pair * (size_t)a.T + (size_t)(p - q.vsrc.n_old)) * D + 8 * hl, live, f);
+    quant_token_half<BITS, Z>(f, live, paged_view(a, live ? pg : 0), a.Gv, (size_t)h, (q.v_nv0 + p) % a.P, hl);
+  }
+}
+
 // WindowQuant reordered ingest: the K groups and V tokens of every quantized
 // window go to the rows its job names, in the segment of its width (rings
 // and the fp16 tail: ingest_kernel).  Work items are (pair, window, group)
@@ -756,6 +830,14 @@ cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s) {
   return z ? launch_ingest_dz<64, 1>(a, s) : launch_ingest_dz<64, 0>(a, s);
 }
 
+template <int BITS, int Z>
+cudaError_t launch_paged_bulk_b(const PagedAppendArgs& a, cudaStream_t s) {
+  const int cap = 4096;  // blocks: enough to fill any GPU, then the warps loop
+  if (a.k_items > 0) paged_bulk_k_kernel<BITS, Z><<<std::min(cap, (a.k_items + 7) / 8), kBulkThreads, 0, s>>>(a);
+  if (a.v_items > 0) paged_bulk_v_kernel<BITS, Z><<<std::min(cap, (a.v_items + 15) / 16), kBulkThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int D, int Z>
 cudaError_t launch_paged_append_dz(const PagedAppendArgs& a, cudaStream_t s) {
   dim3 grid(a.batch, a.h_kv, a.chunks);
@@ -763,7 +845,13 @@ cudaError_t launch_paged_append_dz(const PagedAppendArgs& a, cudaStream_t s) {
   cudaError_t e;
   if ((e = set_smem(paged_append_kernel<D, Z>, sm)) != cudaSuccess) return e;
   paged_append_kernel<D, Z><<<grid, kQuantThreads, sm, s>>>(a);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (D == 128 && a.bulk) {
+    if (a.bits == 2) return launch_paged_bulk_b<2, Z>(a, s);
+    if (a.bits == 4) return launch_paged_bulk_b<4, Z>(a, s);
+    return launch_paged_bulk_b<8, Z>(a, s);
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_paged_append(const PagedAppendArgs& a, cudaStream_t s) {
