@@ -2,6 +2,7 @@
 // (token runs, tiles, splits, append bookkeeping), and the launches.  All
 // state lives in the caller's kvq_cache struct and device buffers.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdarg>
@@ -108,12 +109,7 @@ kvq::SegDev seg_dev(const kvq_segment& g, int zero_point = KVQ_ZERO_MIN) {
   return d;
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-  return n > 0 ? n : 148;
-}
+int sm_count() { return kvq::sm_count_cached(); }
 
 // ---------------------------------------------------------------------------
 // decode planning: runs of uniform (K source, V source), tiles, splits
@@ -274,18 +270,18 @@ int tc_ranges(const kvq::DecodeArgs& a, int n_pairs, int N, int* bound, int nf =
   }
   const long long per_pair = pre[nt], T = (long long)n_pairs * nt;
   const long long total = per_pair * n_pairs;
-  auto prefix = [&](long long g) { return (g / nt) * per_pair + pre[g % nt]; };
   auto weight = [&](long long i) { return i <= nf ? w1 * i : w1 * (long long)nf + w2 * (i - nf); };
   const long long wn = weight(N);
   bound[0] = 0;
   for (int i = 1; i < N; ++i) {
     const long long target = total * weight(i) / wn;
-    long long lo = 0, hi = T;  // first g with prefix(g) >= target
-    while (lo < hi) {
-      const long long mid = (lo + hi) / 2;
-      if (prefix(mid) >= target) hi = mid;
-      else lo = mid + 1;
-    }
+    // first g with prefix(g) >= target, where prefix(g) = (g / nt) per_pair
+    // + pre[g % nt]: every pair has the same prefix, so the pair is
+    // target / per_pair and the tile the first one whose prefix reaches the
+    // rest (tile costs are >= 1, so pre rises strictly)
+    const long long p = target / per_pair, rest = target - p * per_pair;
+    long long lo = p * nt;
+    if (rest > 0) lo += std::lower_bound(pre.begin(), pre.end(), rest) - pre.begin();
     lo = std::max<long long>(lo, bound[i - 1] + 1);
     lo = std::min<long long>(lo, T - (N - i));
     bound[i] = (int)lo;
@@ -348,6 +344,17 @@ kvq_status verify_decode_plan(const kvq_cache* c, const kvq::DecodeArgs& a, int 
                                              : (uint32_t)kvq::kStageBytes;
   const int max_groups = kern == K_TC ? kvq::kTcMaxGroups : kvq::kMhaMaxGroups;
   const size_t P = (size_t)n_pairs, D = (size_t)a.d, G = (size_t)a.G, R = (size_t)a.R;
+  // The bulk copies are walked for the first and last tile of every run:
+  // a run's tiles in between have the first one's shape (their K groups
+  // can differ in count, checked for every tile below) and their copies lie
+  // between the two ends' addresses.
+  std::vector<char> walk(a.n_tiles, 0);
+  for (int i = 0; i < a.n_runs; ++i) {
+    const int t0 = a.runs[i].tile0;
+    const int t1 = (i + 1 < a.n_runs ? a.runs[i + 1].tile0 : a.n_tiles) - 1;
+    if (t0 >= 0 && t0 < a.n_tiles) walk[t0] = 1;
+    if (t1 >= 0 && t1 < a.n_tiles) walk[t1] = 1;
+  }
   for (int which = 0; which < 2; ++which) {
     const size_t pair = which == 0 ? 0 : P - 1;
     for (int t = 0; t < a.n_tiles; ++t) {
@@ -362,6 +369,7 @@ kvq_status verify_decode_plan(const kvq_cache* c, const kvq::DecodeArgs& a, int 
         return fail(KVQ_ERR_UNSUPPORTED, "tile %d: 32-token unit spans two K groups", t);
       if (mha && ti.kseg >= 0 && ti.ng > max_groups)
         return fail(KVQ_ERR_UNSUPPORTED, "tile %d: %d K groups > %d", t, ti.ng, max_groups);
+      if (!walk[t]) continue;
       struct Copy {
         const void* src;
         uint32_t dst_off, bytes;
@@ -570,6 +578,15 @@ kvq_status append_plan(kvq_cache* c, const void* k_new, const void* v_new, int T
 }  // namespace
 
 namespace kvq {
+int sm_count_cached() {
+  static std::atomic<int> cache[64];  // 0 = not looked up yet
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && (n = cache[dev].load(std::memory_order_relaxed)) > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 void set_last_error(const char* msg) { g_last_error = msg; }
 kvq_status check_cache(const kvq_cache* c) { return validate_cache(c); }
 }  // namespace kvq

@@ -523,8 +523,7 @@ cudaError_t launch_d(const DecodeArgs& a, int n_pairs, cudaStream_t s) {
   const dim3 grid(n_pairs * a.n_splits);
   cudaError_t e;
 #define KVQ_LAUNCH(GQV)                                                                   \
-  e = cudaFuncSetAttribute(decode_kernel<D, GQV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                           (int)smem);                                                    \
+  e = set_smem_once((const void*)decode_kernel<D, GQV>, (int)smem);                        \
   if (e != cudaSuccess) return e;                                                         \
   decode_kernel<D, GQV><<<grid, NT, smem, s>>>(a);
   if (a.gq == 1) { KVQ_LAUNCH(1) }
@@ -555,8 +554,7 @@ cudaError_t launch_paged_d(const PagedArgs& a, cudaStream_t s) {
   const dim3 grid(a.n_cols, a.h_kv);
   cudaError_t e;
 #define KVQ_LAUNCH(GQV)                                                                          \
-  e = cudaFuncSetAttribute(decode_paged_kernel<D, GQV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                           (int)smem);                                                           \
+  e = set_smem_once((const void*)decode_paged_kernel<D, GQV>, (int)smem);                         \
   if (e != cudaSuccess) return e;                                                                \
   decode_paged_kernel<D, GQV><<<grid, NT, smem, s>>>(a);
   if (a.gq == 1) { KVQ_LAUNCH(1) }

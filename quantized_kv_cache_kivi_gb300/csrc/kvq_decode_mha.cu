@@ -544,8 +544,7 @@ __global__ void __launch_bounds__(NTH, 2) decode_mha_kernel(const DecodeArgs a) 
 template <int D, int B>
 cudaError_t launch_mha_db(const DecodeArgs& a, int n_pairs, cudaStream_t s) {
   const int smem = MhaSmem::total;
-  cudaError_t e = cudaFuncSetAttribute(decode_mha_kernel<D, B>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once((const void*)decode_mha_kernel<D, B>, (int)smem);
   if (e != cudaSuccess) return e;
   decode_mha_kernel<D, B><<<n_pairs * a.n_splits, NTH, smem, s>>>(a);
   return cudaGetLastError();

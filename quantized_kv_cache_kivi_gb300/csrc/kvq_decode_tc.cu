@@ -1497,7 +1497,7 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm)
 template <int B, int HQ, bool PG = false, class PA = TcNoPaged>
 cudaError_t launch_tc_b(const DecodeArgs& a, cudaStream_t s, const PA& p = PA{}) {
   const int smem = TcSmem<HQ>::total;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<B, HQ, PG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once((const void*)decode_tc_kernel<B, HQ, PG>, smem);
   if (e != cudaSuccess) return e;
   decode_tc_kernel<B, HQ, PG><<<a.n_cta, TcCfg<HQ>::NTH, smem, s>>>(a, p);
   return cudaGetLastError();

@@ -6,6 +6,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <tuple>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -435,7 +439,25 @@ struct PagedAppendArgs {
   PagedAppendSeq seq[KVQ_MAX_SEQS];
 };
 
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device,
+// size): the attribute lives in the device's context, and a driver call on
+// every launch is host time the GPU waits for between launches.
+inline cudaError_t set_smem_once(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::set<std::tuple<const void*, int, int>> done;
+  const auto key = std::make_tuple(kernel, dev, bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
+}
+
 // host helpers of kvq_api.cu used by other entry points
+int sm_count_cached();  // SMs of the current device, looked up once per device
 void set_last_error(const char* msg);
 kvq_status check_cache(const kvq_cache* c);
 

@@ -72,12 +72,7 @@ kvq_status validate_paged(const kvq_paged_cache* c) {
   return KVQ_OK;
 }
 
-int sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-  return n > 0 ? n : 148;
-}
+int sms() { return kvq::sm_count_cached(); }
 
 size_t ws_head(int n_pairs) { return kvq::kWorkspaceHeader + (((size_t)n_pairs * 4 + 255) / 256) * 256; }
 

@@ -751,7 +751,7 @@ __global__ void __launch_bounds__(kBulkThreads) ingest_bulk_v_kernel(const Inges
 
 template <class K>
 cudaError_t set_smem(K kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  return set_smem_once((const void*)kernel, (int)bytes);
 }
 
 template <int BITS, int Z>
