@@ -6,9 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
 #include <mutex>
-#include <set>
-#include <tuple>
+#include <utility>
 
 #include "../../include/kvq.h"
 
@@ -439,20 +439,23 @@ struct PagedAppendArgs {
   PagedAppendSeq seq[KVQ_MAX_SEQS];
 };
 
-// Raise a kernel's dynamic shared-memory limit once per (kernel, device,
-// size): the attribute lives in the device's context, and a driver call on
-// every launch is host time the GPU waits for between launches.
+// Make a kernel's dynamic shared-memory limit at least `bytes` on the
+// current device.  The attribute is one maximum per (kernel, device) that
+// lives in the device's context; it is raised only when a launch needs more
+// than the largest value set so far (never lowered: a smaller value would
+// fail later launches that need more), so most launches make no driver call.
 inline cudaError_t set_smem_once(const void* kernel, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static std::mutex mu;
-  static std::set<std::tuple<const void*, int, int>> done;
-  const auto key = std::make_tuple(kernel, dev, bytes);
+  static std::map<std::pair<const void*, int>, int> raised;
+  const auto key = std::make_pair(kernel, dev);
   std::lock_guard<std::mutex> lock(mu);
-  if (done.count(key)) return cudaSuccess;
+  const auto it = raised.find(key);
+  if (it != raised.end() && it->second >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.insert(key);
+  if (e == cudaSuccess) raised[key] = bytes;
   return e;
 }
 
