@@ -122,22 +122,24 @@ kvq_status check_paged_plan(const kvq_paged_cache* c, const kvq::PagedArgs& a, u
         return pfail(KVQ_ERR_UNSUPPORTED, "paged tile %d of sequence %d: K groups or units", t, b);
       uint32_t sum = 0;
       bool ok = true;
+      // the buffer a copy must stay in follows from its slot and its side's
+      // source (page 0 stands in for the pool page)
+      const void* packed[6] = {a.kc, a.ks, a.kz, a.vc, a.vs, a.vz};
+      const size_t gsz = page_k / rb / G * d * 2, vsz = page_k / rb * (d / Gv) * 2;
+      const size_t psize[6] = {page_k, gsz, gsz, page_k, vsz, vsz};
       kvq::for_each_paged_copy(a, b, c->h_kv - 1, q, ti, [](int) { return 0; },
                                [&](const void* src, uint32_t off, uint32_t bytes, int slot) {
                                  sum += bytes;
-                                 if (slot < 0 || slot > 5 || bytes % 16 || off % 16 || ((uintptr_t)src & 15u))
+                                 if (slot < 0 || slot > 5 || bytes % 16 || off % 16 || ((uintptr_t)src & 15u)) {
                                    ok = false;
+                                   return;
+                                 }
+                                 const bool ring_side = slot < 3 ? ti.kseg != 0 : ti.vseg != 0;
+                                 const uint8_t* b0 = static_cast<const uint8_t*>(
+                                     ring_side ? (slot < 3 ? (const void*)a.kr : (const void*)a.vr) : packed[slot]);
+                                 const size_t n = ring_side ? ring : psize[slot];
                                  const uint8_t* p = static_cast<const uint8_t*>(src);
-                                 auto inside = [&](const void* base, size_t n) {
-                                   const uint8_t* b0 = static_cast<const uint8_t*>(base);
-                                   return p >= b0 && p + bytes <= b0 + n;
-                                 };
-                                 if (!(inside(a.kc, page_k) || inside(a.vc, page_k) ||
-                                       inside(a.ks, page_k / rb / G * d * 2) || inside(a.kz, page_k / rb / G * d * 2) ||
-                                       inside(a.vs, page_k / rb * (d / Gv) * 2) ||
-                                       inside(a.vz, page_k / rb * (d / Gv) * 2) || inside(a.kr, ring) ||
-                                       inside(a.vr, ring)))
-                                   ok = false;
+                                 if (p < b0 || p + bytes > b0 + n) ok = false;
                                });
       if (!ok || sum != ti.bytes)
         return pfail(KVQ_ERR_UNSUPPORTED, "paged tile %d of sequence %d: copy geometry check failed", t, b);
@@ -159,35 +161,45 @@ kvq_status check_paged_plan(const kvq_paged_cache* c, const kvq::PagedArgs& a, u
 // into one CTA's range.)  CTA i's range starts at the first tile whose cost
 // prefix reaches i/N of the total, kept non-empty.  Returns the most ranges
 // that meet one pair.
-int paged_tc_ranges(const kvq::PagedArgs& a, int h_kv, int nt, int N, int* bound) {
-  const int B = a.n_seq;
-  std::vector<std::vector<long long>> pre(B, std::vector<long long>(nt + 1, 0));
-  for (int b = 0; b < B; ++b)
+// Cost prefix of each sequence's tiles, padded to nt: [B][nt + 1], built
+// from the sequence's runs with arithmetic alone (tiles of the both-packed
+// run first, at 4 per 32-token unit + 1; every later tile reads a ring).
+std::vector<long long> paged_tc_costs(const kvq::PagedArgs& a, int nt) {
+  std::vector<long long> pre((size_t)a.n_seq * (nt + 1), 0);
+  for (int b = 0; b < a.n_seq; ++b) {
+    const kvq::PagedSeq& q = a.seq[b];
+    const int a0 = std::min(q.nk, q.nv), n0 = kvq::paged_run_tiles(0, a0, a.tile_pp);
+    long long* pb = pre.data() + (size_t)b * (nt + 1);
     for (int t = 0; t < nt; ++t) {
       long long c = 0;
-      if (t < a.seq[b].n_tiles) {
-        const kvq::TileInfo ti = kvq::paged_tile(a, a.seq[b], t);
-        c = (ti.kseg == 0 && ti.vseg == 0) ? 4 * ((ti.n + 31) / 32) + 1 : 48;
+      if (t < q.n_tiles) {
+        c = t < n0 ? 4 * ((std::min(a.tile_pp, a0 - t * a.tile_pp) + 31) / 32) + 1 : 48;
         if (t == 0) c += 16;
       }
-      pre[b][t + 1] = pre[b][t] + c;
+      pb[t + 1] = pb[t] + c;
     }
+  }
+  return pre;
+}
+
+int paged_tc_ranges(const std::vector<long long>& pre, int B, int h_kv, int nt, int N, int* bound) {
   const long long n_pairs = (long long)B * h_kv, T = n_pairs * nt;
   std::vector<long long> cum(n_pairs + 1, 0);
-  for (long long pr = 0; pr < n_pairs; ++pr) cum[pr + 1] = cum[pr] + pre[pr / h_kv][nt];
-  auto prefix = [&](long long g) {
-    const long long pr = g / nt;
-    return pr >= n_pairs ? cum[n_pairs] : cum[pr] + pre[pr / h_kv][g % nt];
-  };
+  for (long long pr = 0; pr < n_pairs; ++pr) cum[pr + 1] = cum[pr] + pre[(size_t)(pr / h_kv) * (nt + 1) + nt];
   const long long total = cum[n_pairs];
   bound[0] = 0;
+  // first g with prefix(g) >= target, prefix(pr nt + t) = cum[pr] + pre_b[t]:
+  // targets rise with i, so the pair that holds a target is found by
+  // walking forward (the first pair whose end reaches it), then the tile by
+  // a lower bound inside that pair
+  long long pr = 0;
   for (int i = 1; i < N; ++i) {
     const long long target = total * i / N;
-    long long lo = 0, hi = T;
-    while (lo < hi) {
-      const long long mid = (lo + hi) / 2;
-      if (prefix(mid) >= target) hi = mid;
-      else lo = mid + 1;
+    while (pr < n_pairs && cum[pr + 1] < target) ++pr;
+    long long lo = T;
+    if (pr < n_pairs) {
+      const long long* pb = pre.data() + (size_t)(pr / h_kv) * (nt + 1);
+      lo = pr * nt + (std::lower_bound(pb, pb + nt + 1, target - cum[pr]) - pb);
     }
     lo = std::max<long long>(lo, bound[i - 1] + 1);
     lo = std::min<long long>(lo, T - (N - i));
@@ -198,9 +210,9 @@ int paged_tc_ranges(const kvq::PagedArgs& a, int h_kv, int nt, int N, int* bound
   long long run_pair = -1;
   for (int i = 1; i < N; ++i) {
     if (bound[i] % nt == 0) continue;
-    const long long pr = bound[i] / nt;
-    run = pr == run_pair ? run + 1 : 2;
-    run_pair = pr;
+    const long long p = bound[i] / nt;
+    run = p == run_pair ? run + 1 : 2;
+    run_pair = p;
     most = std::max(most, run);
   }
   return most;
@@ -480,8 +492,9 @@ kvq_status kvq_paged_decode_attention(const kvq_paged_cache* c, const void* q, v
     long long N = std::min<long long>(T, (long long)sms() * kvq::decode_tc_ctas_per_sm());
     N = std::min<long long>(N, kvq::kTcMaxCtas);
     N = std::min<long long>(N, std::max<long long>(n_pairs, (long long)n_pairs * (cap - 1)));
+    const std::vector<long long> costs = paged_tc_costs(a, nt_max);
     while (true) {
-      const int most = paged_tc_ranges(a, c->h_kv, nt_max, (int)N, u.tc_bound);
+      const int most = paged_tc_ranges(costs, c->batch, c->h_kv, nt_max, (int)N, u.tc_bound);
       u.tc_defer = most > 16;  // past 16 records a pair, a merge launch of its own
       if (most <= cap) {
         u.n_cta = (int)N;
