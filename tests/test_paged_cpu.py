@@ -171,3 +171,86 @@ def test_paged_tile_geometry_enumeration(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-2000:]
     assert "bad 0" in r.stdout
+
+
+def test_paged_stream_k_planning_against_brute_force(tmp_path):
+    """The paged planner's run-based tile costs and forward range walk against
+    per-tile costs and a binary search (host build of tests/paged_ranges.cu)."""
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = tmp_path / "paged_ranges"
+    subprocess.run([nvcc, "-std=c++17", "-O2", "--expt-relaxed-constexpr", "-x", "cu",
+                    os.path.join(ROOT, "tests", "paged_ranges.cu"), "-o", str(exe)],
+                   check=True, capture_output=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:]
+    assert "bad 0" in r.stdout
+
+
+class _Lengths:
+    """KIVI Algorithm 1 lengths of one sequence (decoding updates, the K
+    block quantized when the ring holds R tokens), without the data."""
+
+    def __init__(self, R):
+        self.R = R
+        self.nk = self.nv = self.nkr = self.nvr = self.krs = self.vrs = 0
+
+    def push(self, n):
+        for _ in range(int(n)):
+            self.nkr += 1
+            self.nvr += 1
+            if self.nkr == self.R:
+                self.nk += self.R
+                self.nkr = 0
+            if self.nvr > self.R:
+                self.nv += 1
+                self.nvr -= 1
+                self.vrs = (self.vrs + 1) % self.R
+
+
+def test_paged_lengths_bookkeeping_matches_the_oracle():
+    import oracle
+    head, ln = oracle.KiviHead(128, 32, 64, 2), _Lengths(64)
+    z = np.zeros(128, np.float16)
+    for i in range(300):
+        head.decode_update(z, z)
+        ln.push(1)
+        assert (head.nk, head.nv, len(head.kr), len(head.vr), head.krs, head.vrs) == \
+            (ln.nk, ln.nv, ln.nkr, ln.nvr, ln.krs, ln.vrs), i
+
+
+@pytest.mark.parametrize("d,G,gv,R,bits,P,gq", [
+    (128, 32, 0, 64, 2, 128, 1), (128, 32, 0, 64, 8, 128, 4), (128, 64, 16, 128, 4, 256, 2),
+    (128, 16, 0, 32, 4, 128, 2), (64, 16, 0, 32, 2, 128, 8), (128, 32, 0, 128, 2, 256, 1)])
+def test_paged_decode_plan_on_algorithm1_histories(L, d, G, gv, R, bits, P, gq):
+    """States that KIVI Algorithm 1 reaches from ragged prompts and decode
+    steps with idle sequences pass the pre-launch checks and reach the
+    launch (without a GPU the launch then fails with KVQ_ERR_CUDA)."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("meaningful only without a GPU (the launch must fail)")
+    rng = np.random.default_rng(d + G + R + bits + gq)
+    B, max_pages = 6, 8
+    seqs = [_Lengths(R) for _ in range(B)]
+    prompt = rng.integers(0, max_pages * P - 3 * R, B)
+    prompt[0] = 0
+    for s, n in zip(seqs, prompt):
+        s.push(n)
+    c = fake_paged(batch=B, h_kv=2, gq=gq, d=d, G=G, R=R, bits=bits, P=P, n_pages=B * max_pages,
+                   max_pages=max_pages, group_v=gv)
+    for step in range(2 * R + 5):
+        for b, s in enumerate(seqs):
+            if not (b == 1 and step % 3 == 0):
+                s.push(1)
+        if step % 7 and step != 2 * R + 4:
+            continue
+        for b, s in enumerate(seqs):
+            set_seq(c, b, s.nk, s.nkr, s.nv, s.nvr, s.krs, s.vrs)
+        for splits in (64, 1):
+            ws = L.kvq_paged_workspace_bytes(ctypes.byref(c), splits)
+            st = L.kvq_paged_decode_attention(ctypes.byref(c), ctypes.c_void_p(BASE - 4096),
+                                              ctypes.c_void_p(BASE - 8192), ctypes.c_void_p(BASE // 2),
+                                              ws, None)
+            assert st == kvq.KVQ_ERR_CUDA, (st, L.kvq_last_error_string().decode(), step, splits)
