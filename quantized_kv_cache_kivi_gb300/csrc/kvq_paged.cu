@@ -10,6 +10,13 @@
 
 #include "kvq_internal.h"
 
+// The per-sequence tables travel as kernel parameters (by value, no upload),
+// which CUDA limits to 32,764 bytes per launch.
+static_assert(sizeof(kvq::PagedAppendArgs) <= 32000, "paged append arguments exceed the kernel parameter limit");
+static_assert(sizeof(kvq::PagedArgs) <= 32000, "paged decode arguments exceed the kernel parameter limit");
+static_assert(sizeof(kvq::DecodeArgs) + sizeof(kvq::PagedArgs) <= 32000,
+              "paged tensor-core arguments exceed the kernel parameter limit");
+
 namespace {
 
 kvq_status pfail(kvq_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
