@@ -51,7 +51,7 @@ def lib():
         L.orc_attention_dense.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p, _f64p,
                                           ctypes.c_double, _f64p, _f64p]
         pp = ctypes.POINTER(ctypes.c_void_p)
-        L.orc_dequant_head.argtypes = [ctypes.c_int] * 5 + [_i32p] * 3 + [pp] * 6 + \
+        L.orc_dequant_head.argtypes = [ctypes.c_int] * 5 + [_i32p] * 4 + [pp] * 6 + \
             [_u16p, _u16p] + [ctypes.c_int] * 4 + [_f64p, _f64p]
         L.orc_dequant_head.restype = ctypes.c_int
         L.orc_window_sims.argtypes = [_u16p, _u16p] + [ctypes.c_int] * 6 + [_f64p]
@@ -80,9 +80,10 @@ def _as_u16(x):
 # codec (KIVI "方法细节" first formula; WindowQuant §3.3.3 Eq.14, Eq.16)
 # ---------------------------------------------------------------------------
 def quantize_group(x, bits, intz=False):
-    """One group of fp16 values -> (codes uint8 [n], s fp16-bits, z fp16-bits).
-    intz: the integer-zero-point quantizer (WindowQuant Eq.14-16), z then
-    holds fp16(-s * z_int)."""
+    """One group of fp16 values -> (codes uint8 [n], s fp16-bits, z 16 bits).
+    KIVI: z = the fp16 minimum.  intz: the integer-zero-point quantizer
+    (WindowQuant Eq.14-16); z is then the integer zero point as int16 bits
+    (``zero_int`` reads it) and X' = s (Q - z) (Eq.15)."""
     x = _as_u16(x).ravel()
     codes = np.zeros(x.size, np.uint8)
     s = np.zeros(1, np.uint16)
@@ -139,9 +140,17 @@ def f2h(f):
     return int(lib().orc_f2h(float(f)))
 
 
-def dequant(codes, s, z):
-    """fp64 dequantization X' = Q * s + z (KIVI "方法细节")."""
+def zero_int(z):
+    """The integer zero point(s) stored in 16-bit zero slots (int16 bits)."""
+    return np.asarray(z, np.uint16).view(np.int16).astype(np.int64)
+
+
+def dequant(codes, s, z, intz=False):
+    """fp64 dequantization: X' = Q * s + z (KIVI "方法细节"), or with an
+    integer zero point X' = s (Q - z) (WindowQuant Eq.15)."""
     s64 = np.asarray(s, np.uint16).view(np.float16).astype(np.float64)
+    if intz:
+        return s64 * (codes.astype(np.int64) - zero_int(z)).astype(np.float64)
     z64 = np.asarray(z, np.uint16).view(np.float16).astype(np.float64)
     return codes.astype(np.float64) * s64 + z64
 
@@ -305,7 +314,7 @@ def _head_buffers(head, seg_bits, seg_caps, kg_lists, vg_lists):
             vc[u] = pack_row(codes, b)
             vs[u] = sc
             vz[u] = zc
-        out.append(dict(bits=b, nk=len(kg_lists[s]) * G, nv=len(vg_lists[s]),
+        out.append(dict(bits=b, nk=len(kg_lists[s]) * G, nv=len(vg_lists[s]), intz=bool(head.intz),
                         k_codes=kc, k_scale=ks, k_zero=kz, v_codes=vc, v_scale=vs, v_zero=vz))
     kr = np.zeros((R, D), np.uint16)
     vr = np.zeros((R, D), np.uint16)
@@ -330,6 +339,7 @@ def dequant_head(segs, kr, vr, nkr, nvr, krs, vrs, D, G, R, Gv=None):
     bits = np.array([s["bits"] for s in segs], np.int32)
     nk = np.array([s["nk"] for s in segs], np.int32)
     nv = np.array([s["nv"] for s in segs], np.int32)
+    intz = np.array([int(bool(s.get("intz", False))) for s in segs], np.int32)
     L = int(nk.sum()) + nkr
     K = np.zeros((max(L, 1), D), np.float64)
     V = np.zeros((max(L, 1), D), np.float64)
@@ -347,7 +357,8 @@ def dequant_head(segs, kr, vr, nkr, nvr, krs, vrs, D, G, R, Gv=None):
     vc, vs, vz = arr("v_codes", _u8p), arr("v_scale", _u16p), arr("v_zero", _u16p)
     kr = _as_u16(kr)
     vr = _as_u16(vr)
-    got = lib().orc_dequant_head(D, G, Gv or G, R, n, _p(bits, _i32p), _p(nk, _i32p), _p(nv, _i32p),
+    got = lib().orc_dequant_head(D, G, Gv or G, R, n, _p(bits, _i32p), _p(intz, _i32p), _p(nk, _i32p),
+                                 _p(nv, _i32p),
                                  kc, ks, kz, vc, vs, vz, _p(kr, _u16p), _p(vr, _u16p),
                                  nkr, nvr, krs, vrs, _p(K, _f64p), _p(V, _f64p))
     if got < 0:

@@ -76,13 +76,31 @@ void orc_quantize_group(const uint16_t* x, int n, int stride, int bits,
   *z_out = z_h;
 }
 
-/* ---- the integer-zero-point quantizer (WindowQuant page §3.3.3): Eq.16
- * s = (max - min) / (qmax - qmin), z = qmin - round(min / s); Eq.14
- * Q = clamp(round(x / s) + z, qmin, qmax); Eq.15 X' = s (Q - z); unsigned
- * range, qmin = 0.  s is stored as fp16 and used rounded, as in the KIVI
- * quantizer; the zero point is stored as the fp16 of -s z, so that
- * X' = Q s + stored zero as for the KIVI quantizer.  A constant group (s = 0)
- * keeps codes 0 and stores its value as the zero (exact reconstruction). */
+/* ---- the integer-zero-point quantizer (WindowQuant page §3.3.3) ----------
+ * Eq.16: s = (max - min) / (qmax - qmin), z = qmin - round(min / s);
+ * Eq.14: Q = clamp(round(x / s) + z, qmin, qmax);
+ * Eq.15: X' = s (Q - z);  unsigned range, qmin = 0.
+ * s is stored as fp16 and used rounded (as in the KIVI quantizer); z is an
+ * integer, stored as a 16-bit two's-complement value in the zero slot, and
+ * the codes are computed with exactly the stored s and z, so that Eq.15 of
+ * the stored values is the dequantization.  Where Eq.16 is undefined or z
+ * would not fit 16 bits the following readings hold:
+ *   - a constant group (max = min), or one whose s rounds to 0, takes
+ *     s = |min| (exact in fp16); Eq.16 then gives z = -sign(min) and Eq.14
+ *     codes 0 for the constant, so Eq.15 gives it back exactly (min = 0:
+ *     s = 0, z = 0, codes 0);
+ *   - if |round(min / s)| > 32767, s is raised to the smallest fp16 value
+ *     for which it is not: a coarser grid, whose step is still below an
+ *     fp16 ulp of min.  fp16 inputs give |min| / range < 2^11 and an fp16 s
+ *     is at least 2/3 of range / qmax, so this never happens at 2 bits, at
+ *     4 bits only with a subnormal s, at 8 bits for groups whose range is
+ *     below about |min| / 128. */
+static uint16_t f2h_up(float t) { /* smallest fp16 >= t, t >= 0 finite */
+  uint16_t h = f2h(t);
+  if (h2f(h) < t) ++h;
+  return h;
+}
+
 void orc_quantize_group_intz(const uint16_t* x, int n, int stride, int bits,
                              uint8_t* code, int code_stride, uint16_t* s_out,
                              uint16_t* z_out) {
@@ -98,20 +116,32 @@ void orc_quantize_group_intz(const uint16_t* x, int n, int stride, int bits,
   uint16_t s_h = f2h(s32);
   float s = h2f(s_h);
   if (s == 0.0f) {
-    for (int i = 0; i < n; ++i) code[(long)i * code_stride] = 0;
-    *s_out = s_h;
-    *z_out = f2h(mn);
-    return;
+    s_h = f2h(fabsf(mn));
+    s = h2f(s_h);
   }
-  float zi = 0.0f - rintf(mn / s); /* an integer */
+  float zr = 0.0f; /* round(min / s), an integer */
+  if (s != 0.0f) {
+    zr = rintf(mn / s);
+    if (fabsf(zr) > 32767.0f) {
+      s_h = f2h_up(fabsf(mn) / 32767.0f);
+      for (int k = 0; k < 8 && fabsf(rintf(mn / h2f(s_h))) > 32767.0f; ++k) ++s_h;
+      s = h2f(s_h);
+      zr = rintf(mn / s);
+    }
+  }
+  const int z = -(int)zr;
   for (int i = 0; i < n; ++i) {
-    float r = rintf(h2f(x[(long)i * stride]) / s) + zi;
-    if (r < 0.0f) r = 0.0f;
-    if (r > (float)qmax) r = (float)qmax;
-    code[(long)i * code_stride] = (uint8_t)(int)r;
+    int q = 0;
+    if (s != 0.0f) {
+      float r = rintf(h2f(x[(long)i * stride]) / s) + (float)z;
+      if (r < 0.0f) r = 0.0f;
+      if (r > (float)qmax) r = (float)qmax;
+      q = (int)r;
+    }
+    code[(long)i * code_stride] = (uint8_t)q;
   }
   *s_out = s_h;
-  *z_out = f2h(-(s * zi));
+  *z_out = (uint16_t)(int16_t)z;
 }
 
 /* K block of G tokens x D channels (row-major [G][D]): one group per channel;
@@ -178,6 +208,16 @@ void orc_attention_dense(int L, int D, const double* K, const double* V,
   free(a);
 }
 
+/* ---- fp64 dequantization of one code ------------------------------------
+ * KIVI float zero point: X' = Q s + z ("方法细节", first formula);
+ * integer zero point: X' = s (Q - z) (WindowQuant Eq.15), z the int16 in the
+ * zero slot. */
+static double dequant_value(int q, uint16_t s_h, uint16_t z_h, int intz) {
+  const double s = (double)h2f(s_h);
+  if (intz) return s * (double)(q - (int)(int16_t)z_h);
+  return (double)q * s + (double)h2f(z_h);
+}
+
 /* ---- dequantize one (batch, kv-head) cache into dense fp64 K and V --------
  * Per segment s: codes/scales/zeros point at this head's slice
  * (k_codes [cap][D*bits/8], k_scale/k_zero [cap/G][D], v_codes likewise,
@@ -187,7 +227,7 @@ void orc_attention_dense(int L, int D, const double* K, const double* V,
  * start slot.  Returns the token count L (same for K and V) or -1 if the
  * K and V counts differ. */
 int orc_dequant_head(int D, int G, int Gv, int R, int n_seg, const int* bits,
-                     const int* nk, const int* nv, const uint8_t* const* kc,
+                     const int* intz, const int* nk, const int* nv, const uint8_t* const* kc,
                      const uint16_t* const* ks, const uint16_t* const* kz,
                      const uint8_t* const* vc, const uint16_t* const* vs,
                      const uint16_t* const* vz, const uint16_t* kr,
@@ -207,8 +247,7 @@ int orc_dequant_head(int D, int G, int Gv, int R, int n_seg, const int* bits,
       orc_unpack_row(kc[s] + (long)u * rb, D, bits[s], codes);
       const int g = u / G;
       for (int c = 0; c < D; ++c)
-        K[(long)t * D + c] = (double)codes[c] * (double)h2f(ks[s][(long)g * D + c]) +
-                             (double)h2f(kz[s][(long)g * D + c]);
+        K[(long)t * D + c] = dequant_value(codes[c], ks[s][(long)g * D + c], kz[s][(long)g * D + c], intz[s]);
     }
   }
   for (int i = 0; i < nkr; ++i, ++t) {
@@ -222,8 +261,8 @@ int orc_dequant_head(int D, int G, int Gv, int R, int n_seg, const int* bits,
       orc_unpack_row(vc[s] + (long)u * rb, D, bits[s], codes);
       for (int c = 0; c < D; ++c) {
         const int g = c / Gv;
-        V[(long)t * D + c] = (double)codes[c] * (double)h2f(vs[s][(long)u * (D / Gv) + g]) +
-                             (double)h2f(vz[s][(long)u * (D / Gv) + g]);
+        V[(long)t * D + c] =
+            dequant_value(codes[c], vs[s][(long)u * (D / Gv) + g], vz[s][(long)u * (D / Gv) + g], intz[s]);
       }
     }
   }

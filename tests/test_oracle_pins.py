@@ -511,55 +511,127 @@ def _h(v):
 def test_intz_hand_worked_group(orc):
     """x = (0.5, 1, 1.75, 2), 2 bits: s = 0.5, z = -round(0.5 / 0.5) = -1,
     Q = round(x / s) + z = (0, 1, round(3.5) - 1 = 3, 4 - 1 -> clamp 3); the
-    stored zero is -s z = 0.5.  The KIVI quantizer rounds (x - min) / s
-    instead and puts 1.75 at code 2 (2.5 rounds to even)."""
+    zero slot holds the integer -1 and Eq.15 gives s (Q - z) = (0.5, 1, 2, 2).
+    The KIVI quantizer rounds (x - min) / s instead and puts 1.75 at code 2
+    (2.5 rounds to even)."""
     x = np.array([0.5, 1.0, 1.75, 2.0], np.float16)
     codes, s, z = orc.quantize_group(x, 2, intz=True)
     assert codes.tolist() == [0, 1, 3, 3]
-    assert orc.h2f(s) == 0.5 and orc.h2f(z) == 0.5
+    assert orc.h2f(s) == 0.5 and orc.zero_int(z) == -1
+    assert orc.dequant(codes, s, z, intz=True).tolist() == [0.5, 1.0, 2.0, 2.0]
     kcodes, _, kz = orc.quantize_group(x, 2)
     assert kcodes.tolist() == [0, 1, 2, 3] and orc.h2f(kz) == 0.5
 
 
+def _intz_groups(rng, bits):
+    """Groups near zero and far from it (|offset| 20..800, spread 0.01..1:
+    the outlier-channel case of a narrow range at a large magnitude)."""
+    for _ in range(150):
+        yield (rng.standard_normal(32) * rng.choice([0.01, 1.0, 30.0]) + rng.normal() * 5).astype(np.float16)
+    for _ in range(150):
+        off = rng.uniform(20.0, 800.0) * rng.choice([-1.0, 1.0])
+        yield (off + rng.uniform(0.01, 1.0) * rng.standard_normal(32)).astype(np.float16)
+
+
 def test_intz_grid_and_error_bounds(orc):
-    """Dequantized values s (Q - z_int) lie on the grid s Z; an unclamped code
-    is within s/2 of its input, the top code within 3s/2 (the rounded scale
-    and the two roundings can leave the range one step short), each plus the
-    rounding of the fp32 quotient x / s."""
+    """Through the stored values: the zero slot holds z = -round(min / s)
+    exactly (an integer, not a rounded product), Eq.15 s (Q - z) lies on the
+    grid s Z, an unclamped code is within s/2 of its input and the top code
+    within 3s/2 (the rounded scale can leave the range one step short), each
+    plus the rounding of the fp32 quotient x / s.  A zero stored as the fp16
+    of -s z (a float offset) fails this on the far-from-zero groups, where
+    that rounding is many steps s."""
     rng = np.random.default_rng(17)
     for bits in (2, 4, 8):
         qmax = (1 << bits) - 1
-        for _ in range(200):
-            x = (rng.standard_normal(32) * rng.choice([0.01, 1.0, 30.0]) + rng.normal() * 5).astype(np.float16)
+        for x in _intz_groups(rng, bits):
             codes, sh, zh = orc.quantize_group(x, bits, intz=True)
             s = Fraction(orc.h2f(sh))
-            if s == 0:
-                continue
-            zs = Fraction(orc.h2f(zh))  # fp16(-s z_int)
-            zi = -Fraction(round(Fraction(float(x.min())) / s))  # only to bound the stored zero
-            assert abs(zs - (-s * zi)) <= abs(s * zi) * Fraction(1, 2048)
+            assert s > 0
+            zi = int(orc.zero_int(zh))
+            # z = -round(min / s) up to the fp32 rounding of the quotient
+            ratio = Fraction(float(x.min())) / s
+            assert abs(-zi - ratio) <= Fraction(1, 2) + abs(ratio) * Fraction(1, 1 << 22)
             for xi, q in zip(x, codes):
                 assert 0 <= q <= qmax
                 xq = Fraction(float(xi))
                 deq = s * (int(q) - zi)
-                assert (deq / s).denominator == 1
-                # plus the rounding of the fp32 quotient x / s (|x| 2^-24 of a step)
+                assert Fraction(orc.dequant(np.array([q]), [sh], [zh], intz=True)[0]) == deq
                 bound = (s / 2 if q < qmax else 3 * s / 2) + abs(xq) * Fraction(1, 1 << 22)
                 assert abs(xq - deq) <= bound
 
 
 def test_intz_exact_grid_and_constant(orc):
-    """8 bits, inputs on the grid k s with s a power of two: exact; a constant
-    group stores its value as the zero with codes 0."""
+    """8 bits, inputs on the grid k s with s a power of two: exact, z = 40 in
+    the slot.  A constant group takes s = |x| and z = -sign(x): codes 0 and
+    an exact reconstruction; a zero group keeps s = 0, z = 0."""
     s = 0.25
     x = (np.arange(-40, 216, 1.0) * s).astype(np.float16)  # 256 points, range 255 s
     codes, sh, zh = orc.quantize_group(x, 8, intz=True)
-    assert orc.h2f(sh) == s
-    zi = 40  # -round(-10 / 0.25)
-    assert orc.h2f(zh) == -s * zi
-    assert np.array_equal(codes.astype(np.float64) * s - s * zi, x.astype(np.float64))
-    c, sh, zh = orc.quantize_group(np.full(8, -3.5, np.float16), 4, intz=True)
-    assert c.tolist() == [0] * 8 and orc.h2f(sh) == 0.0 and orc.h2f(zh) == -3.5
+    assert orc.h2f(sh) == s and orc.zero_int(zh) == 40  # -round(-10 / 0.25)
+    assert np.array_equal(orc.dequant(codes, sh, zh, intz=True), x.astype(np.float64))
+    for v, bits in ((-3.5, 4), (1000.0, 2), (0.0078125, 8)):
+        c, sh, zh = orc.quantize_group(np.full(8, v, np.float16), bits, intz=True)
+        assert c.tolist() == [0] * 8 and orc.h2f(sh) == abs(v)
+        assert orc.zero_int(zh) == (1 if v < 0 else -1)
+        assert orc.dequant(c, sh, zh, intz=True).tolist() == [v] * 8
+    c, sh, zh = orc.quantize_group(np.zeros(8, np.float16), 2, intz=True)
+    assert c.tolist() == [0] * 8 and orc.h2f(sh) == 0.0 and orc.zero_int(zh) == 0
+
+
+def _fp16_next(v):
+    with np.errstate(over="ignore"):
+        return float(np.nextafter(np.float16(v), np.float16(np.inf)))
+
+
+def test_intz_zero_fits_sixteen_bits(orc):
+    """The narrowest groups (min and the next fp16 above it) over the fp16
+    binades.  fp16 inputs give |min| / range < 2^11, and an fp16 s is at
+    least 2/3 of (max - min) / qmax (a subnormal s can round down by up to a
+    third), so at 2 bits Eq.16's s is always kept, with |z| <= 1.5 * 3 * 2^11;
+    at 4 bits it is kept whenever s is a normal fp16 (|z| <= 15 * 2^11).
+    Where Eq.16 would need more than 16 bits (8 bits; 4 bits with a
+    subnormal s), s is the smallest fp16 for which round(min / s) fits (the
+    next smaller one does not).  The reconstruction stays within s/2 (3s/2 at
+    the top code, whose step the rounded scale can leave short), and at 8
+    bits below an fp16 ulp of the input.  Where Eq.16's s rounds to 0 the
+    constant-group reading s = |min| holds."""
+    raised = {2: 0, 4: 0, 8: 0}
+    for e in range(-10, 16):
+        for m in (1.0, 1.5, 1.9990234375):
+            for sign in (1.0, -1.0):
+                lo = np.float16(sign * m * 2.0 ** e)
+                hi = np.float16(_fp16_next(lo))
+                if not np.isfinite(hi):
+                    continue
+                x = np.array([lo, hi] * 4, np.float16)
+                for bits in (2, 4, 8):
+                    qmax = (1 << bits) - 1
+                    codes, sh, zh = orc.quantize_group(x, bits, intz=True)
+                    s = orc.h2f(sh)
+                    zi = int(orc.zero_int(zh))
+                    assert abs(zi) <= 32767
+                    eq16 = orc.h2f(orc.f2h(np.float32(float(hi) - float(lo)) / np.float32(qmax)))
+                    if eq16 == 0.0:  # the range rounds to s = 0: the constant-group reading
+                        assert s == abs(float(lo))
+                    elif bits == 2:
+                        assert s == eq16 and abs(zi) <= 3 * 3072 + 1
+                    elif bits == 4 and eq16 >= 2.0 ** -14:
+                        assert s == eq16 and abs(zi) <= 15 * 2048 + 16
+                    else:
+                        assert s >= eq16
+                        if s > eq16:  # raised: the fp16 just below does not fit
+                            raised[bits] += 1
+                            prev = float(np.nextafter(np.float16(s), np.float16(0)))
+                            assert abs(np.rint(np.float32(lo) / np.float32(prev))) > 32767
+                    deq = orc.dequant(codes, sh, zh, intz=True)
+                    with np.errstate(over="ignore"):
+                        ulp = float(np.spacing(np.float16(abs(lo))))
+                    err = np.abs(deq - x.astype(np.float64))
+                    lim = np.where(codes < qmax, s / 2, 3 * s / 2) + abs(float(lo)) * 2.0 ** -22
+                    assert np.all(err <= lim)
+                    assert bits < 8 or eq16 == 0.0 or err.max() < ulp
+    assert raised[8] > 0  # the 8-bit rule is exercised
 
 
 def test_intz_block_and_token_use_the_group_quantizer(orc):
