@@ -422,6 +422,84 @@ size_t ws_fixed(int n_pairs) {
 }
 
 // ---------------------------------------------------------------------------
+// the warp kernel (one query head per kv head, one 2-bit segment, d_h 128)
+// ---------------------------------------------------------------------------
+constexpr bool kUseWarpKernel = false;
+
+bool warp_kernel_applies(const kvq_cache* c) {
+  const int Gv = group_v(c);
+  return c->h_q == c->h_kv && c->n_seg == 1 && c->d_h == 128 && c->seg[0].bits == 2 && c->group >= 32 &&
+         c->group % 32 == 0 && Gv >= 32 && 128 % Gv == 0 && c->seg[0].nk % 8 == 0 && c->seg[0].capacity % 32 == 0;
+}
+
+// Chunk counts, stream-K warps and the record stride of a cache's state;
+// false if the workspace cannot hold the records even for one warp per pair.
+bool plan_warp(const kvq_cache* c, kvq::WarpArgs& a, size_t ws_bytes) {
+  const int P = c->batch * c->h_kv;
+  a.nk = c->seg[0].nk;
+  a.nv = c->seg[0].nv;
+  a.L = a.nk + c->nkr;
+  a.npp = std::min(a.nk, a.nv);
+  a.npx = std::max(a.nk, a.nv);
+  a.n_pp = (a.npp + 31) / 32;
+  a.n_x1 = a.npx > a.npp ? (a.npx - 1) / 8 - a.npp / 8 + 1 : 0;
+  a.n_x2 = a.L > a.npx ? (a.L - 1) / 8 - a.npx / 8 + 1 : 0;
+  a.C = a.n_pp + a.n_x1 + a.n_x2;
+  a.wpp = 6;  // stream-K weights of a 32-token packed chunk and an 8-token ring chunk
+  a.wx = 5;
+  a.Cp = (long long)a.wpp * a.n_pp + (long long)a.wx * (a.n_x1 + a.n_x2);
+  a.P = P;
+  a.T = a.Cp * P;
+  // every warp's cost share at least the largest chunk cost: no empty range
+  long long nw = std::min<long long>((long long)sm_count() * kvq::kWarpWarps, a.T / std::max(a.wpp, a.wx));
+  nw = std::max<long long>(nw, 1);
+  const size_t room = ws_bytes > ws_fixed(P) ? ws_bytes - ws_fixed(P) : 0;
+  for (;;) {
+    a.n_warps = (int)nw;
+    int stride = 1;
+    for (int p = 0; p < P; ++p) {
+      const int f = kvq::warp_owner(a, (long long)p * a.C), l = kvq::warp_owner(a, (long long)p * a.C + a.C - 1);
+      stride = std::max(stride, l - f + 1);
+    }
+    a.rec_stride = stride;
+    if (stride == 1 || (size_t)P * stride * (128 + 2) * sizeof(float) <= room) return true;
+    if (nw == 1) return false;
+    nw = std::max<long long>(1, nw / 2);
+  }
+}
+
+// Every bulk copy of every chunk, walked for the first and the last pair
+// against its buffer (in bounds, 16-byte aligned, inside the slot).
+kvq_status verify_warp_plan(const kvq_cache* c, const kvq::WarpArgs& a) {
+  const int P = a.P, G = c->group;
+  const size_t rows = (size_t)P * a.cap;
+  const uint8_t* base[8] = {a.kc, (const uint8_t*)a.ks, (const uint8_t*)a.kz, a.vc, (const uint8_t*)a.vs,
+                            (const uint8_t*)a.vz, (const uint8_t*)a.kr, (const uint8_t*)a.vr};
+  const size_t ext[8] = {rows * 32, (size_t)P * (a.cap / G) * 256, (size_t)P * (a.cap / G) * 256, rows * 32,
+                         rows * a.ngv * 2, rows * a.ngv * 2, (size_t)P * a.R * 256, (size_t)P * a.R * 256};
+  const long long pairs[2] = {0, P - 1};
+  for (long long pair : pairs) {
+    for (int ci = 0; ci < a.C; ++ci) {
+      const kvq::WarpChunk ch = kvq::warp_chunk(a, ci);
+      if (ch.n < 1 || ch.n > (ch.pp ? 32 : 8) || ch.o0 < 0 || ch.o0 + ch.n > (ch.pp ? 32 : 8))
+        return fail(KVQ_ERR_UNSUPPORTED, "warp plan: chunk %d has a bad token range", ci);
+      bool ok = true;
+      uint32_t total = 0;
+      kvq::warp_chunk_copies(a, pair, ch, [&](const void* src, uint32_t dst, uint32_t n, int buf) {
+        const uint8_t* p = static_cast<const uint8_t*>(src);
+        total += n;
+        if (n == 0 || n % 16 || (uintptr_t)p % 16 || dst % 16 || dst + n > (uint32_t)kvq::kWarpSlot ||
+            p < base[buf] || p + n > base[buf] + ext[buf])
+          ok = false;
+      });
+      if (!ok || total >= (1u << 20))
+        return fail(KVQ_ERR_UNSUPPORTED, "warp plan: a copy of chunk %d leaves its buffer or the slot", ci);
+    }
+  }
+  return KVQ_OK;
+}
+
+// ---------------------------------------------------------------------------
 // append bookkeeping (KIVI Algorithm 1 over T pushed tokens)
 // ---------------------------------------------------------------------------
 kvq_status append_kivi(kvq_cache* c, const void* k_new, const void* v_new, int T,
@@ -685,6 +763,39 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
     return fail(KVQ_ERR_WORKSPACE, "workspace needs at least %zu bytes", ws_fixed(n_pairs));
   cudaStream_t s = as_stream(stream);
   const int gq = cache->h_q / cache->h_kv;
+  if (kUseWarpKernel && warp_kernel_applies(cache) && cache->seg[0].nk + cache->nkr > 0) {
+    kvq::WarpArgs w{};
+    w.cap = cache->seg[0].capacity;
+    w.R = cache->resid_cap;
+    w.krs = cache->k_ring_start;
+    w.vrs = cache->v_ring_start;
+    w.log2G = 0;
+    while ((1 << w.log2G) < cache->group) ++w.log2G;
+    w.ngv = cache->d_h / group_v(cache);
+    w.intz = cache->zero_point == KVQ_ZERO_INT;
+    w.scale_log2 = cache->sm_scale * 1.4426950408889634f;
+    const kvq_segment& sg = cache->seg[0];
+    w.kc = static_cast<const uint8_t*>(sg.k_codes);
+    w.ks = static_cast<const __half*>(sg.k_scale);
+    w.kz = static_cast<const __half*>(sg.k_zero);
+    w.vc = static_cast<const uint8_t*>(sg.v_codes);
+    w.vs = static_cast<const __half*>(sg.v_scale);
+    w.vz = static_cast<const __half*>(sg.v_zero);
+    w.kr = static_cast<const __half*>(cache->k_resid);
+    w.vr = static_cast<const __half*>(cache->v_resid);
+    w.q = static_cast<const __half*>(q);
+    w.out = static_cast<__half*>(out);
+    if (plan_warp(cache, w, ws_bytes)) {
+      uint8_t* wb = static_cast<uint8_t*>(ws);
+      w.err = reinterpret_cast<int*>(wb);
+      w.counters = reinterpret_cast<int*>(wb + kvq::kWorkspaceHeader);
+      w.part = reinterpret_cast<float*>(wb + ws_fixed(n_pairs));
+      st = verify_warp_plan(cache, w);
+      if (st != KVQ_OK) return st;
+      const cudaError_t e = kvq::launch_decode_warp(w, s);
+      return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "decode launch");
+    }
+  }
   kvq::DecodeArgs a{};
   std::vector<int> cost;
   // one query head per kv head, one segment, each lane's channel quarter
@@ -767,6 +878,7 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   while ((1 << a.log2Gv) < a.Gv) ++a.log2Gv;
   a.R = cache->resid_cap;
   a.scale_log2 = cache->sm_scale * 1.4426950408889634f;
+  a.intz = cache->zero_point == KVQ_ZERO_INT;
   a.n_seg = cache->n_seg;
   for (int i = 0; i < cache->n_seg; ++i) a.seg[i] = seg_dev(cache->seg[i], cache->zero_point);
   a.kr = static_cast<const __half*>(cache->k_resid);

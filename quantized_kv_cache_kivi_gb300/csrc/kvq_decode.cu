@@ -161,7 +161,7 @@ __device__ void pv_packed(const A& a, const TileInfo& ti, const uint8_t* stage,
     uint32_t lo, hi;
     load_chunk<B>(stage + ti.v_off + tok * RB + k * B, lo, hi);
     const float s = __half2float(vs[tok * ngrp + g]);
-    const float z = __half2float(vz[tok * ngrp + g]);
+    const float z = zero_add(__half_as_ushort(vz[tok * ngrp + g]), __half_as_ushort(vs[tok * ngrp + g]), a.intz);
     float c[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) c[j] = code8<B>(lo, hi, j);
@@ -349,7 +349,8 @@ __device__ __forceinline__ void decode_cta(const A& a) {
       for (int task = warp; task < ti.ng * a.gq; task += NT / 32) {
         const int gl = task / a.gq, h = task % a.gq;
         float s = 0.f;
-        for (int c = lane; c < D; c += 32) s += q_s[h * D + c] * __half2float(kz[gl * D + c]);
+        for (int c = lane; c < D; c += 32)
+          s += q_s[h * D + c] * zero_add(__half_as_ushort(kz[gl * D + c]), __half_as_ushort(ks[gl * D + c]), a.intz);
         for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
         if (lane == 0) bias[task] = s;
       }

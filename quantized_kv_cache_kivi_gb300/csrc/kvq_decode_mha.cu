@@ -251,7 +251,8 @@ __device__ __forceinline__ void consume_slice(const DecodeArgs& a, const TileInf
         const __half* vs = reinterpret_cast<const __half*>(stage + ti.vs_off);
         const __half* vz = reinterpret_cast<const __half*>(stage + ti.vz_off);
         const float ps = pt * __half2float(vs[tok * ngv + gv]);
-        S.zsum = fmaf(pt, __half2float(vz[tok * ngv + gv]), S.zsum);
+        S.zsum = fmaf(pt, zero_add(__half_as_ushort(vz[tok * ngv + gv]), __half_as_ushort(vs[tok * ngv + gv]), a.intz),
+                      S.zsum);
         const float2 ps2 = make_float2(ps, ps);
         const uint32_t* cw = reinterpret_cast<const uint32_t*>(
                                  stage + ti.v_off + (size_t)tok * (D * B / 8)) + cq * WPL;
@@ -389,8 +390,12 @@ __global__ void __launch_bounds__(NTH, 2) decode_mha_kernel(const DecodeArgs a) 
             const uint2 zr = *reinterpret_cast<const uint2*>(kz + gl * D + c0);
             const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sr.x));
             const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sr.y));
-            const float2 z01 = __half22float2(*reinterpret_cast<const __half2*>(&zr.x));
-            const float2 z23 = __half22float2(*reinterpret_cast<const __half2*>(&zr.y));
+            float2 z01 = __half22float2(*reinterpret_cast<const __half2*>(&zr.x));
+            float2 z23 = __half22float2(*reinterpret_cast<const __half2*>(&zr.y));
+            if (a.intz) {  // the additive zero -s z of the integer zero point
+              z01 = make_float2(-s01.x * (float)(short)(zr.x & 0xffffu), -s01.y * (float)(short)(zr.x >> 16));
+              z23 = make_float2(-s23.x * (float)(short)(zr.y & 0xffffu), -s23.y * (float)(short)(zr.y >> 16));
+            }
             *reinterpret_cast<float4*>(qt + (gl * 4 + c0 / CPL) * 36 + c0 % CPL) =
                 make_float4(qf[0] * s01.x, qf[1] * s01.y, qf[2] * s23.x, qf[3] * s23.y);
             bp[gl] = qz[0] * z01.x + qz[1] * z01.y + qz[2] * z23.x + qz[3] * z23.y;

@@ -42,11 +42,12 @@
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_mma.cuh"
 
 namespace kvq {
 namespace {
 
-constexpr int D = 128;
+using namespace mma;
 
 // HQ = query-head columns: 1 (one query head per kv head; every column of
 // the K operand carries it), 4 (2-4 query heads per kv head; lane tig of a
@@ -60,7 +61,6 @@ struct TcCfg {
   static constexpr int NS = HQ == 8 ? 3 : kTcStages;   // pipeline stages
   static constexpr int KTAB = 512 * HQ;                // bytes of a warp's K operand
 };
-constexpr uint32_t kFull = 0xffffffffu;
 
 // What the producer records about the tile it staged in a stage.
 struct TcRec {
@@ -99,118 +99,6 @@ static_assert(kTcCtasPerSm * (TcSmem<1>::total + 1024) <= 228 * 1024, "CTAs per 
 static_assert(kTcCtasPerSm * (TcSmem<4>::total + 1024) <= 228 * 1024, "CTAs per SM");
 static_assert(TcSmem<8>::q % 16 == 0 && TcSmem<8>::ktab % 16 == 0 && TcSmem<8>::rec % 16 == 0, "align");
 static_assert(kTcCtasPerSm * (TcSmem<8>::total + 1024) <= 228 * 1024, "CTAs per SM");
-
-// Token of row r of a 16-token sub-tile.  Swapping neighbours in the upper
-// half of each 8-row block keeps both the K row loads (rows gid) and the V
-// row loads (rows 2 tig, 2 tig + 1, ...) free of shared-memory bank conflicts.
-__host__ __device__ constexpr int sigma(int r) { return r ^ ((r >> 2) & 1); }
-
-// ---- code fields ------------------------------------------------------------
-// A 32-bit word holds 32/B codes: two 16-bit halves of 16/B fields each.
-// Fields inside bits 0..9 of a half are used in place (p = j B); the others
-// are taken from the word shifted right by 6 (p = j B - 6).  Either way the
-// field sits at bit p <= 8 with p + B <= 10, inside the fp16 mantissa.
-template <int B>
-struct Fields {
-  static constexpr int INPLACE = B == 2 ? 5 : (B == 4 ? 2 : 1);
-  __host__ __device__ static constexpr int pos(int j) { return j < INPLACE ? j * B : j * B - 6; }
-  // (code_lo 2^(p-24), code_hi 2^(p-24)) as a half2: field j of both halves
-  __device__ static __forceinline__ uint32_t get(uint32_t x, uint32_t x_shr6, int j) {
-    const uint32_t m = ((1u << B) - 1u) << pos(j);
-    return (j < INPLACE ? x : x_shr6) & (m | (m << 16));
-  }
-};
-
-// K: thread tig owns channels [32 tig, 32 tig + 32) of its rows; its h-th
-// half2 (h = 2 kt + e, e = 0 for k columns 2 tig.., 1 for 2 tig + 8..) holds
-// field j = h % PER_HALF of word w = h / PER_HALF: channels c_lo (low half)
-// and c_hi (high half).
-template <int B>
-__host__ __device__ constexpr void k_half2_channels(int tig, int h, int* c_lo, int* c_hi, int* p) {
-  constexpr int PH = 16 / B;
-  const int w = h / PH, j = h % PH;
-  const int base = 32 * tig + w * (32 / B);
-  *c_lo = base + j;
-  *c_hi = base + PH + j;
-  *p = Fields<B>::pos(j);
-}
-
-// V: thread gid owns channels [16 gid, 16 gid + 16) of its tokens; m-tile mt
-// = (word w, field j), w = mt / PER_HALF, j = mt % PER_HALF; row gid <- the
-// low-half channel, row gid + 8 <- the high-half channel.
-template <int B>
-__host__ __device__ constexpr void v_rows(int gid, int mt, int* c_row0, int* c_row8, int* p) {
-  constexpr int PH = 16 / B;
-  const int w = mt / PH, j = mt % PH;
-  const int base = 16 * gid + w * (32 / B);
-  *c_row0 = base + j;
-  *c_row8 = base + PH + j;
-  *p = Fields<B>::pos(j);
-}
-
-// Volatile on purpose: the source order of the MMAs is their issue order,
-// which is arranged so that two MMAs on one accumulator are several apart.
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// 8x8 b16 transpose across the warp: lane (gid, tig) passes row gid, columns
-// 2 tig, 2 tig + 1 and receives row gid of the transpose.
-__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
-  uint32_t y;
-  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-__device__ __forceinline__ uint32_t halves(uint32_t lo, uint32_t hi) {
-  return (lo & 0xffffu) | (hi << 16);
-}
-
-__device__ __forceinline__ bool try_wait_at(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// The same with a suspend-time hint: the waiting thread may sleep in the
-// barrier unit until the phase completes (or about `ns` nanoseconds pass)
-// instead of spinning through issue slots the working warps need.
-__device__ __forceinline__ bool try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
 
 // Bounded wait: about 2^31 SM clocks, then the abort flag is raised.  Every
 // warp waits inside the barrier unit (suspend-time hint) rather than
@@ -424,7 +312,9 @@ __device__ __forceinline__ float build_k_operand(const DecodeArgs& a, const uint
     float z = 0.f;
     if (live) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) z = fmaf(__half2float(qh[lane + 32 * i]), __half2float(zg[lane + 32 * i]), z);
+      for (int i = 0; i < 4; ++i)
+        z = fmaf(__half2float(qh[lane + 32 * i]),
+                 zero_add(__half_as_ushort(zg[lane + 32 * i]), __half_as_ushort(sg[lane + 32 * i]), a.intz), z);
     }
     zsum[h] = z;
   }
@@ -527,11 +417,13 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
     const int ngv = D >> a.log2Gv;
     const uint16_t* sp;
     const uint16_t* zp = nullptr;
+    const uint16_t* szp = nullptr;  // integer zero points: the scales beside the zero slots read
     int stride;
     if constexpr (HQ == 1) {
       const int g = gid & 3;
       if (g < ngv) {
         sp = reinterpret_cast<const uint16_t*>(stage + (gid < 4 ? r.vs_off : r.vz_off)) + (s0 * ngv + g);
+        if (gid >= 4) szp = reinterpret_cast<const uint16_t*>(stage + r.vs_off) + (s0 * ngv + g);
         stride = ngv;
       } else {
         sp = reinterpret_cast<const uint16_t*>(sm + SM::zero);
@@ -541,8 +433,10 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
       const int g = ngv == 1 ? 0 : (gid & 1);
       sp = reinterpret_cast<const uint16_t*>(stage + r.vs_off) + (s0 * ngv + g);
       zp = reinterpret_cast<const uint16_t*>(stage + r.vz_off) + (s0 * ngv + g);
+      szp = sp;
       stride = ngv;
     }
+    const bool zint = a.intz && szp != nullptr;
     uint32_t bv[2][2], bz[2][2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -550,11 +444,25 @@ __device__ __forceinline__ void sub_unit(const DecodeArgs& a, int st, const TcRe
       const uint32_t ka = (FULL || o + ta < nv) ? 0xffffu : 0u, kb = (FULL || o + tb < nv) ? 0xffffu : 0u;
       const uint32_t kc = (FULL || o + tc < nv) ? 0xffffu : 0u, kd = (FULL || o + td < nv) ? 0xffffu : 0u;
       // padding tokens: p = 0, and their stale scale bits must not make NaN
-      bv[h][0] = hmul2u(pp[h][0], halves(sp[(o + ta) * stride] & ka, sp[(o + tb) * stride] & kb));
-      bv[h][1] = hmul2u(pp[h][1], halves(sp[(o + tc) * stride] & kc, sp[(o + td) * stride] & kd));
+      const uint32_t e[4] = {sp[(o + ta) * stride] & ka, sp[(o + tb) * stride] & kb,
+                             sp[(o + tc) * stride] & kc, sp[(o + td) * stride] & kd};
+      if (HQ == 1 && zint) {  // columns 4..7: p times the additive zero -s z, one rounding
+        bv[h][0] = p_times_zero(pp[h][0], e[0], e[1], szp[(o + ta) * stride] & ka, szp[(o + tb) * stride] & kb);
+        bv[h][1] = p_times_zero(pp[h][1], e[2], e[3], szp[(o + tc) * stride] & kc, szp[(o + td) * stride] & kd);
+      } else {
+        bv[h][0] = hmul2u(pp[h][0], halves(e[0], e[1]));
+        bv[h][1] = hmul2u(pp[h][1], halves(e[2], e[3]));
+      }
       if constexpr (HQ != 1) {
-        bz[h][0] = hmul2u(pp[h][0], halves(zp[(o + ta) * stride] & ka, zp[(o + tb) * stride] & kb));
-        bz[h][1] = hmul2u(pp[h][1], halves(zp[(o + tc) * stride] & kc, zp[(o + td) * stride] & kd));
+        const uint32_t f[4] = {zp[(o + ta) * stride] & ka, zp[(o + tb) * stride] & kb,
+                               zp[(o + tc) * stride] & kc, zp[(o + td) * stride] & kd};
+        if (zint) {
+          bz[h][0] = p_times_zero(pp[h][0], f[0], f[1], e[0], e[1]);
+          bz[h][1] = p_times_zero(pp[h][1], f[2], f[3], e[2], e[3]);
+        } else {
+          bz[h][0] = hmul2u(pp[h][0], halves(f[0], f[1]));
+          bz[h][1] = hmul2u(pp[h][1], halves(f[2], f[3]));
+        }
       } else {
         bz[h][0] = bv[h][0];
         bz[h][1] = bv[h][1];
@@ -773,7 +681,9 @@ __device__ __forceinline__ float2 build_k_operand8(const DecodeArgs& a, const ui
     float zs = 0.f;
     if (live) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) zs = fmaf(__half2float(qh[lane + 32 * i]), __half2float(zg[lane + 32 * i]), zs);
+      for (int i = 0; i < 4; ++i)
+        zs = fmaf(__half2float(qh[lane + 32 * i]),
+                  zero_add(__half_as_ushort(zg[lane + 32 * i]), __half_as_ushort(sg[lane + 32 * i]), a.intz), zs);
     }
     z[h] = zs;
   }
@@ -963,8 +873,16 @@ __device__ __forceinline__ void sub_unit8(const DecodeArgs& a, int st, const TcR
       const uint32_t kc = (FULL || o + tc < nv) ? 0xffffu : 0u, kd = (FULL || o + td < nv) ? 0xffffu : 0u;
       sv[h][0] = halves(sp[(o + ta) * ngv] & ka, sp[(o + tb) * ngv] & kb);
       sv[h][1] = halves(sp[(o + tc) * ngv] & kc, sp[(o + td) * ngv] & kd);
-      zv[h][0] = halves(zp[(o + ta) * ngv] & ka, zp[(o + tb) * ngv] & kb);
-      zv[h][1] = halves(zp[(o + tc) * ngv] & kc, zp[(o + td) * ngv] & kd);
+      uint32_t f[4] = {zp[(o + ta) * ngv] & ka, zp[(o + tb) * ngv] & kb, zp[(o + tc) * ngv] & kc,
+                       zp[(o + td) * ngv] & kd};
+      if (a.intz) {  // the additive zero -s z of the integer zero point
+        f[0] = zero_add_h(f[0], sp[(o + ta) * ngv] & ka, true);
+        f[1] = zero_add_h(f[1], sp[(o + tb) * ngv] & kb, true);
+        f[2] = zero_add_h(f[2], sp[(o + tc) * ngv] & kc, true);
+        f[3] = zero_add_h(f[3], sp[(o + td) * ngv] & kd, true);
+      }
+      zv[h][0] = halves(f[0], f[1]);
+      zv[h][1] = halves(f[2], f[3]);
     }
     const uint8_t* vc = stage + r.v_off + s0 * RB + gid * (NW * 4);
 #pragma unroll

@@ -71,9 +71,15 @@ __device__ __forceinline__ uint32_t qcode_exact(float x, float z, float s) {
   return min(__float2uint_rn(rintf(__fdiv_rn(__fsub_rn(x, z), s))), (1u << BITS) - 1u);
 }
 
-// Integer zero point (WindowQuant §3.3.3 Eq.14-16, qmin = 0): p.z is the
-// integer zi = -rint(mn / s) as fp32, p.zh the stored zero fp16(-s zi); a
-// constant group (s = 0) stores mn and codes 0, as the KIVI quantizer.
+// Integer zero point (WindowQuant §3.3.3, qmin = 0): Eq.16 s = (max - min) /
+// qmax, z = -round(min / s); Eq.14 Q = clamp(round(x / s) + z, 0, qmax);
+// Eq.15 x' = s (Q - z).  s is stored as fp16 and used rounded; z is stored
+// as a 16-bit two's-complement integer in the zero slot (p.zh holds those
+// bits, p.z the integer as fp32).  Where Eq.16 is undefined or z would not
+// fit 16 bits: a constant group (or one whose s rounds to 0) takes
+// s = |min|, so z = -sign(min) and its codes are 0; if |round(min / s)|
+// exceeds 32767 (8 bits, or 4 bits with a subnormal s) s is raised to the
+// smallest fp16 value for which it does not.
 __device__ __forceinline__ QParams qparams_intz(float mn, float mx, int bits) {
   const float qmax = (float)((1 << bits) - 1);
   QParams p;
@@ -81,22 +87,39 @@ __device__ __forceinline__ QParams qparams_intz(float mn, float mx, int bits) {
   p.sh = __float2half_rn(s32);
   p.s = __half2float(p.sh);
   if (p.s == 0.0f) {
-    p.z = 0.0f;
-    p.zh = __float2half_rn(mn);
-  } else {
-    p.z = __fsub_rn(0.0f, rintf(__fdiv_rn(mn, p.s)));
-    p.zh = __float2half_rn(-__fmul_rn(p.s, p.z));
+    p.sh = __float2half_rn(fabsf(mn));  // exact: mn is an fp16 value
+    p.s = __half2float(p.sh);
   }
+  float zr = 0.0f;
+  if (p.s != 0.0f) {
+    zr = rintf(__fdiv_rn(mn, p.s));
+    if (fabsf(zr) > 32767.0f) {
+      const float t = __fdiv_rn(fabsf(mn), 32767.0f);
+      unsigned short h = __half_as_ushort(__float2half_rn(t));
+      if (__half2float(__ushort_as_half(h)) < t) ++h;  // smallest fp16 >= t
+      for (int k = 0; k < 8 && fabsf(rintf(__fdiv_rn(mn, __half2float(__ushort_as_half(h))))) > 32767.0f; ++k) ++h;
+      p.sh = __ushort_as_half(h);
+      p.s = __half2float(p.sh);
+      zr = rintf(__fdiv_rn(mn, p.s));
+    }
+  }
+  const int zi = -(int)zr;
+  p.z = (float)zi;
+  p.zh = __short_as_half((short)zi);
   return p;
 }
 
-// clamp(rint(x / s) + zi, 0, qmax): the product x * (1/s) decides unless it
-// lies within 1e-4 of a rounding tie, then the IEEE quotient does.
+// clamp(rint(x / s) + z, 0, qmax): the product x * (1/s) decides unless it
+// lies near a rounding tie, then the IEEE quotient does.  t = x * rcp and
+// the quotient both lie within |t| 2^-22.4 of the exact ratio (two and one
+// fp32 roundings), so they round alike when t is farther than |t| 2^-20
+// from a half-integer; |t| is up to ~2^15 here (x / s is not bounded by
+// qmax as (x - min) / s is), so the window scales with it.
 template <int BITS>
 __device__ __forceinline__ uint32_t qcode_intz_guess(float x, float zi, float rcp, bool& near_tie) {
   const float t = __fmul_rn(x, rcp);
   const float r = rintf(t);
-  near_tie = fabsf(t - r) > 0.4999f;
+  near_tie = fabsf(t - r) > 0.5f - fabsf(t) * 0x1p-20f;
   return (uint32_t)min(max(__float2int_rn(r + zi), 0), (1 << BITS) - 1);
 }
 template <int BITS>
@@ -109,6 +132,20 @@ __device__ __forceinline__ uint32_t qcode_intz_fast(float x, float zi, float s, 
   bool tie;
   const uint32_t c = qcode_intz_guess<BITS>(x, zi, rcp, tie);
   return tie ? qcode_intz_exact<BITS>(x, zi, s) : c;
+}
+
+// The additive zero of a dequantized value x' = code s + zero, from the 16
+// bits of a zero slot and of the matching scale: the stored fp16 zero
+// (KIVI, z = min), or -s z for an integer zero point z (WindowQuant Eq.15,
+// x' = s (code - z)), formed in fp32.
+__device__ __forceinline__ float zero_add(uint16_t zbits, uint16_t sbits, bool intz) {
+  if (!intz) return __half2float(__ushort_as_half(zbits));
+  return -__half2float(__ushort_as_half(sbits)) * (float)(short)zbits;
+}
+// The same rounded to fp16 bits, for fp16 tensor-core operands.
+__device__ __forceinline__ uint16_t zero_add_h(uint16_t zbits, uint16_t sbits, bool intz) {
+  if (!intz) return zbits;
+  return __half_as_ushort(__float2half_rn(-__half2float(__ushort_as_half(sbits)) * (float)(short)zbits));
 }
 
 // Either quantizer, by the destination's zero point.

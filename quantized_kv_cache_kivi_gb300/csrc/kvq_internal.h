@@ -66,6 +66,7 @@ struct DecodeArgs {
   int log2G;         // G is a power of two
   int Gv, log2Gv;    // V channel group and its log2
   float scale_log2;  // sm_scale * log2(e)
+  int intz;          // zero slots hold integer zero points (x' = s (code - z))
   int n_seg;
   SegDev seg[KVQ_MAX_SEGMENTS];
   const __half* kr;
@@ -257,6 +258,146 @@ __host__ __device__ inline void for_each_tile_copy(const DecodeArgs& a, size_t p
 }
 
 // ---------------------------------------------------------------------------
+// Decode with one query head per kv head over one 2-bit segment (the warp
+// kernel, kvq_decode_warp.cu): every warp runs a bulk-copy pipeline of its
+// own over a contiguous, cost-balanced range of chunks of the concatenated
+// (pair, chunk) list.  Per pair the token axis is cut into
+//   - PP chunks: 32 tokens [32u, 32u + 32) of [0, npp), K and V packed
+//     (npp = min(nk, nv)); the last one may be short;
+//   - X chunks: the rest, [npp, L), in the 8-token blocks of the token
+//     index, split at npx = max(nk, nv): one side packed below npx, both
+//     from the rings above.  An X chunk is staged as its whole 8-row block,
+//     its tokens at rows [o0, o0 + n).
+// ---------------------------------------------------------------------------
+constexpr int kWarpSlot = 4096;   // bytes of one pipeline slot
+constexpr int kWarpSlots = 3;     // slots per warp
+constexpr int kWarpWarps = 16;    // warps per CTA (one CTA per SM)
+// slot layout, PP chunk: K codes, K group scales / zeros, V codes, V token
+// scales / zeros (the zeros 32 bytes off a 256-byte stride, so the scale and
+// zero loads of one instruction hit different banks)
+constexpr int kPpKc = 0, kPpKs = 1024, kPpKz = 1280, kPpVc = 1536, kPpVs = 2560, kPpVz = 2848;
+// X chunk: K side at 0 (ring rows, or codes / group scales / zeros), V side
+// at 2048 (ring rows, or codes / token scales / zeros)
+constexpr int kXK = 0, kXV = 2048, kXKs = 256, kXKz = 512, kXVs = 256, kXVz = 320;
+
+struct WarpArgs {
+  const uint8_t* kc;  // segment 0: K codes [P][cap][32]
+  const __half* ks;   // [P][cap/G][128]
+  const __half* kz;
+  const uint8_t* vc;  // V codes [P][cap][32]
+  const __half* vs;   // [P][cap][128/Gv]
+  const __half* vz;
+  const __half* kr;   // rings [P][R][128]
+  const __half* vr;
+  const __half* q;    // [P][128] (one query head per pair)
+  __half* out;
+  float* part;        // records [P][rec_stride][130]
+  int* counters;      // [P]
+  int* err;
+  int cap, R, krs, vrs, log2G, ngv, intz;
+  float scale_log2;
+  int nk, nv, L, npp, npx;
+  int n_pp, n_x1, n_x2, C;  // chunks per pair
+  int wpp, wx;              // chunk costs (stream-K weights)
+  long long Cp, T;          // cost of a pair, of all pairs
+  int P, n_warps, rec_stride;
+};
+
+struct WarpChunk {
+  int t0, n, o0;  // first token, tokens, row of t0 in the staged block
+  int kq, vq, pp;
+};
+
+__host__ __device__ inline WarpChunk warp_chunk(const WarpArgs& a, int c) {
+  WarpChunk ch;
+  if (c < a.n_pp) {
+    ch.pp = 1;
+    ch.t0 = 32 * c;
+    ch.n = a.npp - ch.t0 < 32 ? a.npp - ch.t0 : 32;
+    ch.o0 = 0;
+    ch.kq = ch.vq = 1;
+    return ch;
+  }
+  const bool r1 = c < a.n_pp + a.n_x1;
+  const int lo = r1 ? a.npp : a.npx, hi = r1 ? a.npx : a.L;
+  const int blk = lo / 8 + (c - (r1 ? a.n_pp : a.n_pp + a.n_x1));
+  const int s = 8 * blk > lo ? 8 * blk : lo;
+  const int e = 8 * blk + 8 < hi ? 8 * blk + 8 : hi;
+  ch.pp = 0;
+  ch.t0 = s;
+  ch.n = e - s;
+  ch.o0 = s - 8 * blk;
+  ch.kq = s < a.nk;
+  ch.vq = s < a.nv;
+  return ch;
+}
+
+// First global chunk of warp w's range (w = n_warps gives P * C): the first
+// chunk whose cost offset reaches T * w / n_warps.
+__host__ __device__ inline long long warp_bound(const WarpArgs& a, int w) {
+  const long long target = a.T * (long long)w / a.n_warps;
+  const long long pair = target / a.Cp;
+  const long long r = target - pair * a.Cp;
+  const long long pp_cost = (long long)a.wpp * a.n_pp;
+  const long long c = r <= pp_cost ? (r + a.wpp - 1) / a.wpp : a.n_pp + (r - pp_cost + a.wx - 1) / a.wx;
+  return pair * a.C + c;
+}
+
+// The warp whose range holds global chunk g (ranges are never empty).
+__host__ __device__ inline int warp_owner(const WarpArgs& a, long long g) {
+  int lo = 0, hi = a.n_warps - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (warp_bound(a, mid) <= g) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// The bulk copies that stage chunk c of `pair` in a slot: f(src, dst_off,
+// bytes, buf) with buf 0..5 = K codes, K scales, K zeros, V codes, V scales,
+// V zeros and 6/7 = the K / V ring.
+template <class F>
+__host__ __device__ inline void warp_chunk_copies(const WarpArgs& a, long long pair, const WarpChunk& ch, F&& f) {
+  const int G = 1 << a.log2G;
+  const long long ksb = (pair * (a.cap / G) + (ch.t0 >> a.log2G)) * 128;  // K group, in halves
+  if (ch.pp) {
+    const long long row = pair * a.cap + ch.t0;
+    const uint32_t sb = (uint32_t)((ch.n * a.ngv * 2 + 15) & ~15);
+    f(a.kc + row * 32, kPpKc, (uint32_t)ch.n * 32u, 0);
+    f(a.ks + ksb, kPpKs, 256u, 1);
+    f(a.kz + ksb, kPpKz, 256u, 2);
+    f(a.vc + row * 32, kPpVc, (uint32_t)ch.n * 32u, 3);
+    f(a.vs + row * a.ngv, kPpVs, sb, 4);
+    f(a.vz + row * a.ngv, kPpVz, sb, 5);
+    return;
+  }
+  const long long blk = pair * a.cap + (ch.t0 - ch.o0);  // the chunk's 8-row block
+  if (ch.kq) {
+    f(a.kc + blk * 32, kXK, 256u, 0);
+    f(a.ks + ksb, kXK + kXKs, 256u, 1);
+    f(a.kz + ksb, kXK + kXKz, 256u, 2);
+  } else {
+    const int s0 = (a.krs + (ch.t0 - a.nk)) % a.R;
+    const int n1 = ch.n < a.R - s0 ? ch.n : a.R - s0;
+    const __half* ring = a.kr + pair * a.R * 128;
+    f(ring + (long long)s0 * 128, kXK + ch.o0 * 256, (uint32_t)n1 * 256u, 6);
+    if (n1 < ch.n) f(ring, kXK + (ch.o0 + n1) * 256, (uint32_t)(ch.n - n1) * 256u, 6);
+  }
+  if (ch.vq) {
+    f(a.vc + blk * 32, kXV, 256u, 3);
+    f(a.vs + blk * a.ngv, kXV + kXVs, (uint32_t)(16 * a.ngv), 4);
+    f(a.vz + blk * a.ngv, kXV + kXVz, (uint32_t)(16 * a.ngv), 5);
+  } else {
+    const int s0 = (a.vrs + (ch.t0 - a.nv)) % a.R;
+    const int n1 = ch.n < a.R - s0 ? ch.n : a.R - s0;
+    const __half* ring = a.vr + pair * a.R * 128;
+    f(ring + (long long)s0 * 128, kXV + ch.o0 * 256, (uint32_t)n1 * 256u, 7);
+    if (n1 < ch.n) f(ring, kXV + (ch.o0 + n1) * 256, (uint32_t)(ch.n - n1) * 256u, 7);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Paged cache with per-sequence lengths.  A sequence's token axis is cut into
 // three runs -- both packed [0, min(nk, nv)), one side packed [min, max),
 // both ring [max, L) -- and each run into tiles aligned to multiples of the
@@ -273,6 +414,7 @@ struct PagedSeq {
 struct PagedArgs {
   int batch, h_kv, gq, d, G, R, log2G, Gv, log2Gv, P, bits;
   float scale_log2;
+  int intz;           // zero slots hold integer zero points (x' = s (code - z))
   const uint8_t* kc;  // pool [n_pages][h_kv][P][d*bits/8]
   const __half* ks;   // pool [n_pages][h_kv][P/G][d]
   const __half* kz;
@@ -473,6 +615,7 @@ size_t decode_smem_bytes(int gq, int d);
 cudaError_t launch_decode_mha(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, int form, cudaStream_t s);
 cudaError_t launch_decode_tc_merge(const DecodeArgs& a, int n_pairs, cudaStream_t s);
+cudaError_t launch_decode_warp(const WarpArgs& a, cudaStream_t s);
 cudaError_t launch_decode_paged(const PagedArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tc_paged(const DecodeArgs& a, const PagedArgs& p, int bits, int form, cudaStream_t s);
 cudaError_t launch_paged_append(const PagedAppendArgs& a, cudaStream_t s);

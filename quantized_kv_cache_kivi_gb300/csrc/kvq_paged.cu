@@ -407,6 +407,7 @@ kvq_status kvq_paged_decode_attention(const kvq_paged_cache* c, const void* q, v
   a.P = c->page_tokens;
   a.bits = c->bits;
   a.scale_log2 = c->sm_scale * 1.4426950408889634f;
+  a.intz = c->zero_point == KVQ_ZERO_INT;
   a.kc = static_cast<const uint8_t*>(c->k_codes);
   a.ks = static_cast<const __half*>(c->k_scale);
   a.kz = static_cast<const __half*>(c->k_zero);
@@ -484,6 +485,7 @@ kvq_status kvq_paged_decode_attention(const kvq_paged_cache* c, const void* q, v
     u.log2Gv = a.log2Gv;
     u.R = a.R;
     u.scale_log2 = a.scale_log2;
+    u.intz = a.intz;
     u.n_seg = 1;
     u.kr = a.kr;
     u.vr = a.vr;

@@ -15,7 +15,7 @@ All values are rounded to fp16 (the pages' cache precision).
 """
 import numpy as np
 
-TAG_K, TAG_V, TAG_Q, TAG_OUTLIER, TAG_TEXT, TAG_DIR, TAG_STEP, TAG_LEN = 1, 2, 3, 4, 5, 6, 7, 8
+TAG_K, TAG_V, TAG_Q, TAG_OUTLIER, TAG_TEXT, TAG_DIR, TAG_STEP, TAG_LEN, TAG_OFFSET = 1, 2, 3, 4, 5, 6, 7, 8, 9
 
 
 def rng(seed, tag, b=0, h=0, step=0):
@@ -60,6 +60,26 @@ def kv_block(seed, batch, h_kv, n, d, n_out, factor, step=0):
         for h in range(h_kv):
             K[b, h] = keys(seed, b, h, n, d, n_out, factor, step)
             V[b, h] = values(seed, b, h, n, d, step)
+    return K, V
+
+
+def offset_block(seed, batch, h_kv, n, d, Gv, step=0):
+    """K, V [batch][h_kv][n][d] fp16 far from zero with narrow spreads (the
+    large-magnitude, narrow-range groups of an outlier channel): K channel c
+    of a head is o_c + w_c N(0,1), V channel group j of token t is
+    o_tj + w_tj N(0,1), with |o| uniform in [20, 800] (random sign) and w
+    uniform in [0.01, 1]."""
+    K = np.empty((batch, h_kv, n, d), np.float16)
+    V = np.empty((batch, h_kv, n, d), np.float16)
+    for b in range(batch):
+        for h in range(h_kv):
+            g = rng(seed, TAG_OFFSET, b, h, step)
+            ok = g.uniform(20.0, 800.0, d) * g.choice([-1.0, 1.0], d)
+            wk = g.uniform(0.01, 1.0, d)
+            K[b, h] = (ok + wk * g.standard_normal((n, d))).astype(np.float16)
+            ov = np.repeat(g.uniform(20.0, 800.0, (n, d // Gv)) * g.choice([-1.0, 1.0], (n, d // Gv)), Gv, axis=1)
+            wv = np.repeat(g.uniform(0.01, 1.0, (n, d // Gv)), Gv, axis=1)
+            V[b, h] = (ov + wv * g.standard_normal((n, d))).astype(np.float16)
     return K, V
 
 

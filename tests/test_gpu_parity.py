@@ -136,6 +136,31 @@ def test_integer_zero_point_bit_exact_and_attention(d, G, R, bits, gq):
     assert pair.attention_error(_q(8, B, H * gq, d)) < TOL
 
 
+@pytest.mark.parametrize("d,G,R,bits,gq", [(128, 32, 64, 2, 1), (128, 32, 64, 4, 4), (128, 32, 32, 8, 7),
+                                           (128, 64, 128, 8, 2), (64, 16, 32, 8, 1), (64, 32, 64, 4, 8)])
+def test_integer_zero_point_far_from_zero_bit_exact(d, G, R, bits, gq):
+    """Groups far from zero with narrow ranges (x = +-(20..800) + 0.01..1
+    N(0,1)): x / s reaches ~2^15, so the quantizer's product x (1/s) can fall
+    next to a rounding tie that the IEEE quotient decides differently, and
+    the integer zero point is large.  Codes, scales and integer zeros
+    bit-exact through the bulk prefill kernels (d 128: warp per K group,
+    half-warp per V token), the decode-step block kernels (V evictions, K
+    flushes) and a bulk append; attention within tolerance on every decode
+    form (one, four and eight query-head columns; d 64)."""
+    B, H = 2, 2
+    pair = KiviPair(B, H, H * gq, d, G, R, bits, cap=2048, zero_point=kvq.KVQ_ZERO_INT)
+    l = 6 * R + 9
+    K, V = synth.offset_block(71 + bits, B, H, l + 2 * R + 40, d, G)
+    pair.prefill(K[:, :, :l], V[:, :, :l])
+    pair.assert_buffers_bit_exact()
+    for t in range(l, l + R + 3):
+        pair.append(K[:, :, t:t + 1], V[:, :, t:t + 1])
+    pair.assert_buffers_bit_exact()
+    pair.append(K[:, :, l + R + 3:], V[:, :, l + R + 3:])
+    pair.assert_buffers_bit_exact()
+    assert pair.attention_error(_q(18, B, H * gq, d)) < TOL
+
+
 @pytest.mark.parametrize("d,G,Gv,R,bits,gq", [(128, 64, 32, 128, 2, 1), (128, 256, 128, 256, 4, 4),
                                               (128, 32, 16, 64, 4, 7), (64, 32, 16, 64, 2, 1),
                                               (128, 16, 64, 32, 8, 2), (128, 32, 8, 64, 2, 3)])
@@ -347,33 +372,43 @@ def test_window_assign_matches_oracle():
 
 
 def _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed, first16=False, bits=None, perm=None, zero_point=0,
-              group_v=0):
-    vis, txt = synth.window_keys(seed, B, H, n_win, S, n_text, d)
-    M = n_win * S
-    Vv = np.stack([np.stack([synth.values(seed, b, h, M, d) for h in range(H)]) for b in range(B)])
-    Vt = np.stack([np.stack([synth.values(seed + 1, b, h, n_text, d) for h in range(H)])
-                   for b in range(B)])
+              group_v=0, tail=5, data=None, heads=None, R=None):
+    """A WindowQuant cache on the GPU (ranked or given widths, reordered
+    ingest, text tokens into the ring) and oracle heads fed the same tokens.
+    data = (vision K, vision V, text K, text V) replaces the seeded keys;
+    heads = the (batch, kv head) pairs the oracle builds (all by default)."""
+    if data is None:
+        vis, txt = synth.window_keys(seed, B, H, n_win, S, n_text, d)
+        M = n_win * S
+        Vv = np.stack([np.stack([synth.values(seed, b, h, M, d) for h in range(H)]) for b in range(B)])
+        Vt = np.stack([np.stack([synth.values(seed + 1, b, h, n_text, d) for h in range(H)])
+                       for b in range(B)])
+    else:
+        vis, Vv, txt, Vt = data
     if bits is None:
         sim = oracle.window_sims(vis, txt, S)
         bits, perm = oracle.window_assign(sim, 0.1, 0.3, first_window_fp16=first16)
     caps = [(b, int(((bits == b).sum() * S + G - 1) // G * G) or G) for b in (8, 4, 2)]
-    R = -(-(128 + int((bits == 16).sum()) * S) // G) * G
+    if R is None:
+        R = -(-(128 + int((bits == 16).sum()) * S) // G) * G
     c = kvq.alloc_cache(B, H, H * gq, d, G, R, caps, policy=kvq.KVQ_POLICY_FP16_TAIL, zero_point=zero_point,
                         group_v=group_v)
     plan = kvq.make_plan(S, bits, perm)
-    tail = 5  # vision tokens past the last whole window stay fp16
+    # vision tokens past the last whole window stay fp16
     extra_k = np.concatenate([vis, vis[:, :, :tail]], axis=2)
     extra_v = np.concatenate([Vv, Vv[:, :, :tail]], axis=2)
     kvq.kvq_quantize_append(c, to_dev(extra_k), to_dev(extra_v), plan=plan)
     kvq.kvq_quantize_append(c, to_dev(txt), to_dev(Vt))
-    heads = {}
+    out = {}
     for b in range(B):
         for h in range(H):
+            if heads is not None and (b, h) not in heads:
+                continue
             o = oracle.Segmented(d, G, R, [8, 4, 2], intz=zero_point == kvq.KVQ_ZERO_INT, Gv=group_v or G)
             o.ingest_windows(extra_k[b, h], extra_v[b, h], S, bits, perm)
             o.append_fp16(txt[b, h], Vt[b, h])
-            heads[(b, h)] = o
-    return c, heads, caps, R
+            out[(b, h)] = o
+    return c, out, caps, R
 
 
 def _eq8_inputs(seed, B, n_win, S, N, dim):
@@ -436,10 +471,13 @@ def test_windowquant_window_groups(zero_point):
 
 
 def _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, seed, first16, bits, perm, zero_point=0,
-                        group_v=0):
+                        group_v=0, **kw):
+    """Every array the reordered ingest writes (codes, scales and zeros of
+    each width's segment, the fp16 ring slots) bit-exact against the
+    oracle's serialized heads, then mixed-width attention within tolerance."""
     Gv = group_v or G
     c, heads, caps, R = _wq_setup(n_win, S, n_text, B, H, gq, d, G, seed=seed, first16=first16,
-                                  bits=bits, perm=perm, zero_point=zero_point, group_v=group_v)
+                                  bits=bits, perm=perm, zero_point=zero_point, group_v=group_v, **kw)
     torch.cuda.synchronize()
     P = B * H
     q = synth.q_block(9, B, H * gq, d)
@@ -448,6 +486,9 @@ def _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, seed, first16, bits, p
     ws = torch.zeros(kvq.kvq_workspace_bytes(c, 64), dtype=torch.uint8, device="cuda")
     kvq.kvq_decode_attention(c, qd, out, ws)
     got = out.cpu().numpy()
+    assert kvq.kvq_workspace_error(ws) == 0
+    kr_all = c.t["k_resid"].cpu().numpy().view(np.uint16).reshape(P, R, d)
+    vr_all = c.t["v_resid"].cpu().numpy().view(np.uint16).reshape(P, R, d)
     errs = []
     for (b, h), o in heads.items():
         p = b * H + h
@@ -458,16 +499,51 @@ def _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, seed, first16, bits, p
             rb = d * bits // 8
             n = c.c.seg[s].nk
             assert n == seg["nk"] == c.c.seg[s].nv
-            kc = t["k_codes"].cpu().numpy().reshape(P, cap, rb)[p, :n]
-            assert np.array_equal(kc, seg["k_codes"][:n])
-            ks = t["k_scale"].cpu().numpy().view(np.uint16).reshape(P, cap // G, d)[p, :n // G]
-            assert np.array_equal(ks, seg["k_scale"][:n // G])
-            vc = t["v_codes"].cpu().numpy().reshape(P, cap, rb)[p, :n]
-            assert np.array_equal(vc, seg["v_codes"][:n])
-            vz = t["v_zero"].cpu().numpy().view(np.uint16).reshape(P, cap, d // Gv)[p, :n]
-            assert np.array_equal(vz, seg["v_zero"][:n])
+            arrays = dict(
+                k_codes=t["k_codes"].cpu().numpy().reshape(P, cap, rb)[p, :n],
+                k_scale=t["k_scale"].cpu().numpy().view(np.uint16).reshape(P, cap // G, d)[p, :n // G],
+                k_zero=t["k_zero"].cpu().numpy().view(np.uint16).reshape(P, cap // G, d)[p, :n // G],
+                v_codes=t["v_codes"].cpu().numpy().reshape(P, cap, rb)[p, :n],
+                v_scale=t["v_scale"].cpu().numpy().view(np.uint16).reshape(P, cap, d // Gv)[p, :n],
+                v_zero=t["v_zero"].cpu().numpy().view(np.uint16).reshape(P, cap, d // Gv)[p, :n])
+            for name, a in arrays.items():
+                want = seg[name][:n // G] if name in ("k_scale", "k_zero") else seg[name][:n]
+                assert np.array_equal(a, want), (name, bits, b, h)
         assert c.c.nkr == len(o.kr) and c.c.nvr == len(o.vr)
-        K, V = oracle.dequant_head(segs, kr, vr, len(o.kr), len(o.vr), 0, 0, d, G, R, Gv)
+        for i in range(c.c.nkr):
+            slot = (c.c.k_ring_start + i) % R
+            assert np.array_equal(kr_all[p, slot], kr[slot]), ("k ring", b, h, i)
+        for i in range(c.c.nvr):
+            slot = (c.c.v_ring_start + i) % R
+            assert np.array_equal(vr_all[p, slot], vr[slot]), ("v ring", b, h, i)
+        K, V = oracle.dequant_head(segs, kr, vr, len(o.kr), len(o.vr), c.c.k_ring_start, c.c.v_ring_start,
+                                   d, G, R, Gv)
         ref = oracle.attention_head(K, V, q[b, h * gq:(h + 1) * gq].astype(np.float64), c.c.sm_scale)
         errs.append(max_abs_rel(got[b, h * gq:(h + 1) * gq], ref))
     assert max(errs) < TOL
+    return max(errs)
+
+
+def test_windowquant_ingest_far_from_zero_bit_exact():
+    """The reordered ingest's quantizers (ingest_bulk_k / ingest_bulk_v) with
+    the integer zero point on groups far from zero with narrow ranges, at
+    all three widths and fp16 windows: every array bit-exact."""
+    n_win, S, n_text, B, H, gq, d, G = 12, 64, 16, 1, 2, 7, 128, 32
+    K, V = synth.offset_block(91, B, H, n_win * S + n_text, d, G)
+    data = (K[:, :, :n_win * S], V[:, :, :n_win * S], K[:, :, n_win * S:], V[:, :, n_win * S:])
+    bits = np.array([8, 2, 4, 2, 16, 8, 2, 4, 2, 2, 16, 4], np.int8)
+    perm = np.array(sorted(range(n_win), key=lambda w: (-bits[w], w)), np.int32)
+    _wq_attention_check(n_win, S, n_text, B, H, gq, d, G, 0, False, bits, perm, kvq.KVQ_ZERO_INT, data=data)
+
+
+def test_windowquant_workload_full_shape():
+    """The LLaVA-OneVision-shaped WindowQuant workload at its full size:
+    batch 1, 28 query heads over 4 kv heads, 64 windows x 256 vision tokens
+    ranked by the rank rule into INT8 / INT4 / INT2 segments and reordered,
+    64 fp16 text tokens in a ring of 128.  The cache holds all four kv heads;
+    the oracle checks every array and the attention of two of them."""
+    w = synth.WORKLOADS["windowquant_llava_ov"]
+    err = _wq_attention_check(w["n_win"], w["S"], w["n_text"], w["batch"], w["h_kv"], w["h_q"] // w["h_kv"],
+                              w["d"], w["G"], w["seed"], False, None, None, tail=0, heads={(0, 0), (0, 3)},
+                              R=w["R"])
+    assert err < TOL
