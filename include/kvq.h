@@ -371,6 +371,14 @@ kvq_status kvq_paged_decode_attention(const kvq_paged_cache* cache,
 kvq_status kvq_decode_attention_noalloc(const kvq_cache* cache, const void* q,
                                         void* out, void* stream);
 
+/* Error word of that static scratch on the current device (0 = none;
+ * nonzero = a bounded wait timed out inside a decode kernel, the output is
+ * not valid), as kvq_workspace_error reports it for a caller workspace.
+ * Each kvq_decode_attention_noalloc call clears the word first, so read it
+ * after every call whose result matters.  Synchronizes `stream`.  No
+ * counterpart in the pages. */
+kvq_status kvq_noalloc_error(int32_t* err_out, void* stream);
+
 /* Static description of a status code. */
 const char* kvq_status_string(kvq_status status);
 

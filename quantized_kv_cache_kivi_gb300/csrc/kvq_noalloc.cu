@@ -79,3 +79,20 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_cache* cache, const
   }
   return kvq_decode_attention(cache, q, out, scratch, (size_t)KVQ_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+// The error word of the static scratch (its first int32), which the decode
+// kernels raise when a bounded wait runs out: the caller of the entry point
+// above has no pointer to it.  Reads it after the work queued on `stream`.
+extern "C" kvq_status kvq_noalloc_error(int32_t* err_out, void* stream) {
+  if (!err_out) {
+    kvq::set_last_error("NULL argument");
+    return KVQ_ERR_INVALID_ARG;
+  }
+  void* scratch = nullptr;
+  cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) {
+    kvq::set_last_error(cudaGetErrorString(e));
+    return KVQ_ERR_CUDA;
+  }
+  return kvq_workspace_error(scratch, err_out, stream);
+}

@@ -98,6 +98,8 @@ def lib():
         L.kvq_workspace_error.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
         L.kvq_decode_attention_noalloc.argtypes = [cp, _P, _P, _P]
         L.kvq_decode_attention_noalloc.restype = ctypes.c_int
+        L.kvq_noalloc_error.argtypes = [ctypes.POINTER(ctypes.c_int32), _P]
+        L.kvq_noalloc_error.restype = ctypes.c_int
         L.kvq_window_assign_workspace_bytes.argtypes = [ctypes.c_int32] * 5
         L.kvq_window_assign_workspace_bytes.restype = ctypes.c_size_t
         L.kvq_window_assign.argtypes = [_P, _P] + [ctypes.c_int32] * 6 + \
@@ -192,6 +194,13 @@ def kvq_decode_attention_noalloc(cache, q, out, stream=None):
     st = lib().kvq_decode_attention_noalloc(ctypes.byref(cache.c), _ptr(q), _ptr(out),
                                             _stream(stream))
     return _check(st, "kvq_decode_attention_noalloc")
+
+
+def kvq_noalloc_error(stream=None):
+    """Error word of the static scratch after the last no-workspace call."""
+    v = ctypes.c_int32(0)
+    _check(lib().kvq_noalloc_error(ctypes.byref(v), _stream(stream)), "kvq_noalloc_error")
+    return v.value
 
 
 def kvq_workspace_error(ws, stream=None):

@@ -38,6 +38,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         kvq.kvq_decode_attention(pair.gpu, q, ref, ws)
         kvq.kvq_decode_attention_noalloc(pair.gpu, q, got)
         torch.cuda.synchronize()
+        assert kvq.kvq_noalloc_error() == 0, call  # no bounded wait ran out
+        assert kvq.kvq_workspace_error(ws) == 0, call
         g = got.cpu().numpy().astype(np.float64)
         r = ref.cpu().numpy().astype(np.float64)
         assert np.isfinite(g).all()
