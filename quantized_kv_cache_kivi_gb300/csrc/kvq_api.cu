@@ -424,7 +424,7 @@ size_t ws_fixed(int n_pairs) {
 // ---------------------------------------------------------------------------
 // the warp kernel (one query head per kv head, one 2-bit segment, d_h 128)
 // ---------------------------------------------------------------------------
-constexpr bool kUseWarpKernel = false;
+constexpr bool kUseWarpKernel = true;
 
 bool warp_kernel_applies(const kvq_cache* c) {
   const int Gv = group_v(c);
@@ -445,20 +445,19 @@ bool plan_warp(const kvq_cache* c, kvq::WarpArgs& a, size_t ws_bytes) {
   a.n_x1 = a.npx > a.npp ? (a.npx - 1) / 8 - a.npp / 8 + 1 : 0;
   a.n_x2 = a.L > a.npx ? (a.L - 1) / 8 - a.npx / 8 + 1 : 0;
   a.C = a.n_pp + a.n_x1 + a.n_x2;
-  a.wpp = 6;  // stream-K weights of a 32-token packed chunk and an 8-token ring chunk
-  a.wx = 5;
-  a.Cp = (long long)a.wpp * a.n_pp + (long long)a.wx * (a.n_x1 + a.n_x2);
+  a.Cp = (long long)kvq::kWarpWpp * a.n_pp + (long long)kvq::kWarpWx * (a.n_x1 + a.n_x2);
   a.P = P;
   a.T = a.Cp * P;
   // every warp's cost share at least the largest chunk cost: no empty range
-  long long nw = std::min<long long>((long long)sm_count() * kvq::kWarpWarps, a.T / std::max(a.wpp, a.wx));
+  long long nw = std::min<long long>((long long)sm_count() * kvq::kWarpWarps,
+                                     a.T / std::max(kvq::kWarpWpp, kvq::kWarpWx));
   nw = std::max<long long>(nw, 1);
   const size_t room = ws_bytes > ws_fixed(P) ? ws_bytes - ws_fixed(P) : 0;
   for (;;) {
     a.n_warps = (int)nw;
     int stride = 1;
     for (int p = 0; p < P; ++p) {
-      const int f = kvq::warp_owner(a, (long long)p * a.C), l = kvq::warp_owner(a, (long long)p * a.C + a.C - 1);
+      const int f = kvq::warp_owner(a, p, 0), l = kvq::warp_owner(a, p, a.C - 1);
       stride = std::max(stride, l - f + 1);
     }
     a.rec_stride = stride;

@@ -18,13 +18,15 @@
 // chunks (32 tokens with K and V packed; 8-token blocks where a ring is
 // involved: kvq_internal.h, warp_chunk) and the concatenated chunk list of
 // all pairs into one contiguous, cost-balanced range per warp (stream-K over
-// warps, computed in closed form from the uniform lengths).  A warp stages
-// its chunks itself: one lane issues the bulk copies (TMA engine, mbarrier
-// completion) of the next chunks into the warp's own slots while the warp
-// computes on the current one.  No warp ever waits for another: there is no
-// producer warp, no stage release and no CTA-wide barrier after set-up.
-// Each warp leaves a partial (o, m, l) record per pair it touched; the last
-// warp of a pair to finish (atomic counter) merges the records.
+// warps, computed in closed form from the uniform lengths).  Each warp is a
+// CTA of its own (kWarpWarps of them resident per SM) and stages its own
+// chunks, kWarpSlots ahead, into its own slots: one lane issues the bulk
+// copies (TMA engine, mbarrier completion); with one warp per CTA every
+// shared-memory and barrier address is warp-uniform, so the copies take
+// their operands straight from uniform registers.  No warp ever waits for
+// another: there is no producer warp, no stage release and no CTA-wide
+// barrier.  Each warp leaves a partial (o, m, l) record per pair it touched;
+// the last warp of a pair to finish (atomic counter) merges the records.
 #include <float.h>
 
 #include "kvq_device.cuh"
@@ -38,19 +40,20 @@ using namespace mma;
 
 constexpr int kWB = 2;                   // packed width of this kernel
 constexpr int kRB = D * kWB / 8;         // packed row bytes (32)
-constexpr int kPad = 2048;               // past the last slot: masked rows of the last slot's short chunks
 constexpr int kKtab = 512;               // one K operand table (bytes)
 constexpr int kRec = D + 2;              // record (o[D], m, l)
 
+// Shared memory of a CTA (one warp): its slots, two K operand tables, the
+// pair's query and the slots' mbarriers.
 struct WarpSmem {
-  static constexpr int slots = 0;                                              // [warp][slot][kWarpSlot]
-  static constexpr int ktab = slots + kWarpWarps * kWarpSlots * kWarpSlot + kPad;  // [warp][2][kKtab]
-  static constexpr int qbuf = ktab + kWarpWarps * 2 * kKtab;                   // [warp][D] f16
-  static constexpr int bars = qbuf + kWarpWarps * D * 2;                       // [warp][slot] mbarrier
-  static constexpr int total = bars + kWarpWarps * kWarpSlots * 8;
+  static constexpr int slots = 0;                             // [slot][kWarpSlot]
+  static constexpr int ktab = slots + kWarpSlots * kWarpSlot;  // [2][kKtab]
+  static constexpr int qbuf = ktab + 2 * kKtab;                      // [D] f16
+  static constexpr int bars = qbuf + D * 2;                          // [slot] mbarrier
+  static constexpr int total = bars + kWarpSlots * 8;
 };
 static_assert(WarpSmem::ktab % 16 == 0 && WarpSmem::qbuf % 16 == 0 && WarpSmem::bars % 8 == 0, "align");
-static_assert(WarpSmem::total <= 227 * 1024, "one CTA per SM");
+static_assert(kWarpWarps * (WarpSmem::total + 1024) <= 228 * 1024, "CTAs per SM");
 
 struct WState {
   float m;  // running max (log2 domain), warp-uniform
@@ -152,8 +155,9 @@ __device__ __forceinline__ PairQ pair_query(const WarpArgs& a, const __half* qsm
 // reads the 16 words of its own column.  Returns the bias q . z (log2
 // domain) of the group.  tab: this unit's table (two alternate per unit, so
 // one __syncwarp separates writes from reads).
-__device__ __forceinline__ float build_kop(const WarpArgs& a, const uint8_t* ks, const uint8_t* kz, const PairQ& Q,
-                                           const LaneC& L, uint8_t* tab, uint32_t (&bq)[16]) {
+template <bool INTZ>
+__device__ __forceinline__ float build_kop(const uint8_t* ks, const uint8_t* kz, const PairQ& Q, const LaneC& L,
+                                           uint8_t* tab, uint32_t (&bq)[16]) {
   const uint32_t s_lo = *reinterpret_cast<const uint32_t*>(ks + 2 * L.c_lo0);        // s[c_lo0], s[c_lo0 + 1]
   const uint32_t s_hi = *reinterpret_cast<const uint32_t*>(ks + 2 * (L.c_lo0 + 8));  // s[c_hi0], s[c_hi0 + 1]
   const uint32_t z_lo = *reinterpret_cast<const uint32_t*>(kz + 2 * L.c_lo0);
@@ -169,7 +173,7 @@ __device__ __forceinline__ float build_kop(const WarpArgs& a, const uint8_t* ks,
   *reinterpret_cast<uint2*>(tab + L.wr_hi) = make_uint2(h01, h23);
   *reinterpret_cast<uint2*>(tab + L.wr_lo) = make_uint2(l01, l23);
   float zl0, zl1, zh0, zh1;
-  if (!a.intz) {
+  if constexpr (!INTZ) {
     const float2 zl = __half22float2(*reinterpret_cast<const __half2*>(&z_lo));
     const float2 zh = __half22float2(*reinterpret_cast<const __half2*>(&z_hi));
     zl0 = zl.x, zl1 = zl.y, zh0 = zh.x, zh1 = zh.y;
@@ -293,14 +297,14 @@ __device__ __forceinline__ void softmax_step(WState& S, const float (&x)[2][2], 
 // row t at vc + t * 32), token scales / zeros at vs / vz ([token][ngv]).
 // Rows whose token lies outside [lo, hi) of the staged block are padding:
 // p = 0 there and their stale scale / zero bits are masked (no NaN).
-template <int NH, bool FULL>
-__device__ __forceinline__ void pv_packed(const WarpArgs& a, const uint8_t* vc, const uint8_t* vs, const uint8_t* vz,
-                                          int lo, int hi, const LaneC& L, const uint32_t (&pp)[2][2], WState& S) {
+template <int NH, bool FULL, int NGV, bool INTZ>
+__device__ __forceinline__ void pv_packed(const uint8_t* vc, const uint8_t* vs, const uint8_t* vz, int lo, int hi,
+                                          const LaneC& L, const uint32_t (&pp)[2][2], WState& S) {
   const int g = L.gid & 3;
-  const bool live = g < a.ngv;  // columns of groups past d / Gv stay zero
+  const bool live = NGV == 4 || g < NGV;  // columns of groups past d / Gv stay zero
   const uint16_t* sp = reinterpret_cast<const uint16_t*>(L.gid < 4 ? vs : vz) + g;
   const uint16_t* szp = reinterpret_cast<const uint16_t*>(vs) + g;
-  const int st = a.ngv;
+  constexpr int st = NGV;
   uint32_t bv[2][2];
 #pragma unroll
   for (int h = 0; h < NH; ++h) {
@@ -312,7 +316,7 @@ __device__ __forceinline__ void pv_packed(const WarpArgs& a, const uint8_t* vc, 
       m[i] = (live && (FULL || (t[i] >= lo && t[i] < hi))) ? 0xffffu : 0u;
       e[i] = live ? (uint32_t)sp[t[i] * st] & m[i] : 0u;
     }
-    if (a.intz && L.gid >= 4 && live) {  // columns 4..7: p times the additive zero -s z, one rounding
+    if (INTZ && L.gid >= 4 && live) {  // columns 4..7: p times the additive zero -s z, one rounding
       bv[h][0] = p_times_zero(pp[h][0], e[0], e[1], szp[t[0] * st] & m[0], szp[t[1] * st] & m[1]);
       bv[h][1] = p_times_zero(pp[h][1], e[2], e[3], szp[t[2] * st] & m[2], szp[t[3] * st] & m[3]);
     } else {
@@ -344,9 +348,10 @@ __device__ __forceinline__ void pv_packed(const WarpArgs& a, const uint8_t* vc, 
   for (int h = 0; h < NH; ++h) mma16816(S.accz, ONES, ONES, ONES, ONES, bv[h][0], bv[h][1]);
 }
 
-// PV over one 16-row half of fp16 ring V at vr (row stride 256 bytes): A
+// PV over an 8-row block of fp16 ring V at vr (row stride 256 bytes): A
 // rows are the channels of the 2-bit row map, gathered from the lane's 16
-// channels of each token; rows outside [lo, hi) read as zeros.
+// channels of each token; rows outside [lo, hi) read as zeros, and rows 8..15
+// of the MMA's 16 (tokens tc, td) lie past the block: zeros, not read.
 __device__ __forceinline__ void pv_ring(const uint8_t* vr, int lo, int hi, const LaneC& L, const uint32_t (&pp)[2],
                                         WState& S) {
   if (!S.vring) {
@@ -356,10 +361,7 @@ __device__ __forceinline__ void pv_ring(const uint8_t* vr, int lo, int hi, const
   const uint8_t* vg = vr + L.gid * 32;
   const uint32_t* va = reinterpret_cast<const uint32_t*>(vg + L.ta * (D * 2));
   const uint32_t* vb = reinterpret_cast<const uint32_t*>(vg + L.tb * (D * 2));
-  const uint32_t* vcc = reinterpret_cast<const uint32_t*>(vg + L.tc * (D * 2));
-  const uint32_t* vd = reinterpret_cast<const uint32_t*>(vg + L.td * (D * 2));
   const uint32_t ma = (L.ta >= lo && L.ta < hi) ? kFull : 0u, mb = (L.tb >= lo && L.tb < hi) ? kFull : 0u;
-  const uint32_t mc = (L.tc >= lo && L.tc < hi) ? kFull : 0u, md = (L.td >= lo && L.td < hi) ? kFull : 0u;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     int c0, c8, p;
@@ -367,18 +369,16 @@ __device__ __forceinline__ void pv_ring(const uint8_t* vr, int lo, int hi, const
     const uint32_t s0sel = (c0 & 1) ? 0x7632u : 0x5410u;
     const uint32_t s8sel = (c8 & 1) ? 0x7632u : 0x5410u;
     mma16816(S.acc[mt], __byte_perm(va[c0 >> 1] & ma, vb[c0 >> 1] & mb, s0sel),
-             __byte_perm(va[c8 >> 1] & ma, vb[c8 >> 1] & mb, s8sel),
-             __byte_perm(vcc[c0 >> 1] & mc, vd[c0 >> 1] & md, s0sel),
-             __byte_perm(vcc[c8 >> 1] & mc, vd[c8 >> 1] & md, s8sel), pp[0], pp[1]);
+             __byte_perm(va[c8 >> 1] & ma, vb[c8 >> 1] & mb, s8sel), 0u, 0u, pp[0], pp[1]);
   }
 }
 
 // A 32-token chunk with K and V packed (n tokens valid, 32 when FULL).
-template <bool FULL>
-__device__ __forceinline__ void run_pp(const WarpArgs& a, const uint8_t* slot, int n, const PairQ& Q, const LaneC& L,
-                                       uint8_t* tab, WState& S) {
+template <bool FULL, int NGV, bool INTZ>
+__device__ __forceinline__ void run_pp(const uint8_t* slot, int n, const PairQ& Q, const LaneC& L, uint8_t* tab,
+                                       WState& S) {
   uint32_t bq[16];
-  const float bias = build_kop(a, slot + kPpKs, slot + kPpKz, Q, L, tab, bq);
+  const float bias = build_kop<INTZ>(slot + kPpKs, slot + kPpKz, Q, L, tab, bq);
   float x[2][2];
   k_scores_packed<2>(slot + kPpKc, L, bq, bias, x);  // rows past n read stale codes: masked below
   if (!FULL) {
@@ -389,19 +389,20 @@ __device__ __forceinline__ void run_pp(const WarpArgs& a, const uint8_t* slot, i
   }
   uint32_t pp[2][2];
   softmax_step<2>(S, x, pp);
-  pv_packed<2, FULL>(a, slot + kPpVc, slot + kPpVs, slot + kPpVz, 0, n, L, pp, S);
+  pv_packed<2, FULL, NGV, INTZ>(slot + kPpVc, slot + kPpVs, slot + kPpVz, 0, n, L, pp, S);
 }
 
 // A chunk of at most 8 tokens at rows [o0, o0 + n) of its staged 8-row
 // block (rows 8..15 of the MMA half are padding), K and V each packed or
 // from the ring.
+template <int NGV, bool INTZ>
 __device__ __forceinline__ void run_x(const WarpArgs& a, const uint8_t* slot, const WarpChunk& ch, const PairQ& Q,
                                       const LaneC& L, const uint8_t* qsm, uint8_t* tab, WState& S) {
   const int lo = ch.o0, hi = ch.o0 + ch.n;
   float x[2][2];
   if (ch.kq) {
     uint32_t bq[16];
-    const float bias = build_kop(a, slot + kXK + kXKs, slot + kXK + kXKz, Q, L, tab, bq);
+    const float bias = build_kop<INTZ>(slot + kXK + kXKs, slot + kXK + kXKz, Q, L, tab, bq);
     k_scores_packed<1>(slot + kXK, L, bq, bias, x);
   } else {
     k_scores_ring(slot + kXK, qsm, L, a.scale_log2, x[0][0], x[0][1]);
@@ -411,14 +412,51 @@ __device__ __forceinline__ void run_x(const WarpArgs& a, const uint8_t* slot, co
   x[1][0] = x[1][1] = -INFINITY;
   uint32_t pp[2][2];
   softmax_step<1>(S, x, pp);
-  if (ch.vq) pv_packed<1, false>(a, slot + kXV, slot + kXV + kXVs, slot + kXV + kXVz, lo, hi, L, pp, S);
+  if (ch.vq) pv_packed<1, false, NGV, INTZ>(slot + kXV, slot + kXV + kXVs, slot + kXV + kXVz, lo, hi, L, pp, S);
   else pv_ring(slot + kXV, lo, hi, L, pp[0], S);
 }
 
-// Issue the copies of global chunk gc into a slot (one lane).
-__device__ __forceinline__ void issue_chunk(const WarpArgs& a, long long gc, uint8_t* slot, uint64_t* bar) {
-  const long long pair = gc / a.C;
-  const WarpChunk ch = warp_chunk(a, (int)(gc - pair * a.C));
+// Base addresses of one pair's slices of the cache arrays.
+struct PairPtrs {
+  const uint8_t *kc, *vc;
+  const __half *ks, *kz, *vs, *vz, *kr, *vr;
+};
+
+__device__ __forceinline__ PairPtrs pair_ptrs(const WarpArgs& a, long long pair) {
+  PairPtrs p;
+  const long long rows = pair * a.cap;
+  p.kc = a.kc + rows * kRB;
+  p.vc = a.vc + rows * kRB;
+  p.ks = a.ks + (rows >> a.log2G) * D;
+  p.kz = a.kz + (rows >> a.log2G) * D;
+  p.vs = a.vs + rows * a.ngv;
+  p.vz = a.vz + rows * a.ngv;
+  p.kr = a.kr + pair * a.R * D;
+  p.vr = a.vr + pair * a.R * D;
+  return p;
+}
+
+// Stage chunk c of a pair into a slot: one lane issues the bulk copies
+// (TMA engine) and the mbarrier's expected byte count.  The CTA is one warp,
+// so every address here is warp-uniform.  A full 32-token chunk with K and V
+// packed takes the short path; anything else walks the general copy list
+// (warp_chunk_copies, the list the host checked).
+template <int NGV>
+__device__ __forceinline__ void stage_chunk(const WarpArgs& a, const PairPtrs& pp, long long pair, int c,
+                                            uint8_t* slot, uint64_t* bar) {
+  if (c < a.npp / 32) {
+    const int t0 = 32 * c;
+    constexpr uint32_t sb = 32 * NGV * 2;
+    mbar_arrive_expect_tx(bar, 2 * 1024 + 2 * 256 + 2 * sb);
+    bulk_g2s(slot + kPpKc, pp.kc + t0 * kRB, 1024, bar);
+    bulk_g2s(slot + kPpKs, pp.ks + (t0 >> a.log2G) * D, 256, bar);
+    bulk_g2s(slot + kPpKz, pp.kz + (t0 >> a.log2G) * D, 256, bar);
+    bulk_g2s(slot + kPpVc, pp.vc + t0 * kRB, 1024, bar);
+    bulk_g2s(slot + kPpVs, pp.vs + t0 * NGV, sb, bar);
+    bulk_g2s(slot + kPpVz, pp.vz + t0 * NGV, sb, bar);
+    return;
+  }
+  const WarpChunk ch = warp_chunk(a, c);
   uint32_t bytes = 0;
   warp_chunk_copies(a, pair, ch, [&](const void*, uint32_t, uint32_t n, int) { bytes += n; });
   mbar_arrive_expect_tx(bar, bytes);
@@ -428,14 +466,15 @@ __device__ __forceinline__ void issue_chunk(const WarpArgs& a, long long gc, uin
 // End of a warp's share of a pair: its partial (o, m, l) as a record, or the
 // output when the warp holds the whole pair; the last record of the pair to
 // arrive merges them all.
+template <int NGV>
 __device__ void finish_pair(const WarpArgs& a, long long pair, int gw, int lane, const LaneC& L, WState& S) {
   if (!S.vring) unscale_acc2(S);
   float l = S.l;  // sum over the lanes of one tig (rows gid)
   l += __shfl_xor_sync(kFull, l, 4);
   l += __shfl_xor_sync(kFull, l, 8);
   l += __shfl_xor_sync(kFull, l, 16);
-  const int first = warp_owner(a, pair * a.C);
-  const int last = warp_owner(a, pair * a.C + a.C - 1);
+  const int first = warp_owner(a, pair, 0);
+  const int last = warp_owner(a, pair, a.C - 1);
   const int nrec = last - first + 1;
   // o of channel c: column g(c) of its row (lanes tig = g / 2) plus the z sum
   // of group g (column 4 + g, lanes tig = 2 + g / 2)
@@ -445,7 +484,7 @@ __device__ void finish_pair(const WarpArgs& a, long long pair, int gw, int lane,
   for (int mt = 0; mt < 8; ++mt) {
     int c0, c8, p;
     v_rows<2>(L.gid, mt, &c0, &c8, &p);
-    const int g = (c0 * a.ngv) >> 7;  // c0 and c8 share their group
+    const int g = (c0 * NGV) >> 7;  // c0 and c8 share their group
     const float z0 = __shfl_sync(kFull, S.accz[0], (lane & ~3) | (2 + (g >> 1)));
     const float z1 = __shfl_sync(kFull, S.accz[1], (lane & ~3) | (2 + (g >> 1)));
     const float zg = (g & 1) ? z1 : z0;
@@ -504,46 +543,62 @@ __device__ __forceinline__ void load_query(const WarpArgs& a, long long pair, in
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(kWarpWarps * 32, 1) decode_warp_kernel(const WarpArgs a) {
+// One warp per CTA, kWarpWarps CTAs per SM: CTA gw takes the range of warp gw.
+template <int NGV, bool INTZ>
+__global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kWarpWarps + warp;
-  if (gw >= a.n_warps) return;  // warps are independent: no CTA-wide barrier follows
-  uint8_t* slots = smem + WarpSmem::slots + warp * kWarpSlots * kWarpSlot;
-  uint8_t* tab0 = smem + WarpSmem::ktab + warp * 2 * kKtab;
-  __half* qsm = reinterpret_cast<__half*>(smem + WarpSmem::qbuf + warp * D * 2);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WarpSmem::bars) + warp * kWarpSlots;
+  const int lane = threadIdx.x;
+  const int gw = blockIdx.x;
+  uint8_t* slots = smem + WarpSmem::slots;
+  uint8_t* tab0 = smem + WarpSmem::ktab;
+  __half* qsm = reinterpret_cast<__half*>(smem + WarpSmem::qbuf);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WarpSmem::bars);
   const long long c0 = warp_bound(a, gw), c1 = warp_bound(a, gw + 1);
+  const int n = (int)(c1 - c0);  // chunks of this warp
+  const long long pair0 = c0 / a.C;
+  const int cc0 = (int)(c0 - pair0 * a.C);
+  // staging position, kWarpSlots chunks ahead of the consumed one
+  long long ip = pair0;
+  int ic = cc0;
+  PairPtrs ipp = pair_ptrs(a, ip);
   if (lane == 0) {
     for (int s = 0; s < kWarpSlots; ++s) mbar_init(&bars[s], 1);
     mbar_fence_init();
-    for (int s = 0; s < kWarpSlots && c0 + s < c1; ++s) issue_chunk(a, c0 + s, slots + s * kWarpSlot, &bars[s]);
   }
   __syncwarp();
+  for (int s = 0; s < kWarpSlots && s < n; ++s) {
+    if (lane == 0) stage_chunk<NGV>(a, ipp, ip, ic, slots + s * kWarpSlot, &bars[s]);
+    if (++ic == a.C) {
+      ic = 0;
+      ipp = pair_ptrs(a, ++ip);
+    }
+  }
   const LaneC L = lane_consts(lane);
   WState S;
   reset_state(S);
   PairQ Q;
-  long long cur = -1;
-  int unit = 0;
-  for (long long gc = c0; gc < c1; ++gc) {
-    const int k = (int)(gc - c0), s = k % kWarpSlots;
-    const long long pair = gc / a.C;
+  long long pair = pair0, cur = -1;
+  int c = cc0, s = 0;
+  uint32_t ph = 0;
+  const int n_full = a.npp / 32;  // full 32-token chunks with K and V packed
+  for (int k = 0; k < n; ++k) {
     if (pair != cur) {
       if (cur >= 0) {
-        finish_pair(a, cur, gw, lane, L, S);
+        finish_pair<NGV>(a, cur, gw, lane, L, S);
         reset_state(S);
       }
       cur = pair;
       load_query(a, pair, lane, qsm);
       Q = pair_query(a, qsm, L);
     }
-    // wait for the chunk's copies (bounded: about 2^31 clocks)
-    const uint32_t ph = (uint32_t)((k / kWarpSlots) & 1);
-    if (!mbar_try_wait(&bars[s], ph)) {
+    // wait for the chunk's copies (bounded: about 2^31 clocks), inside the
+    // barrier unit (suspend-time hint) rather than spinning through issue
+    // slots the other warps of the SM need
+    const uint32_t bar_addr = smem_u32(&bars[s]);
+    if (!try_wait_at(bar_addr, ph)) {
       const long long t0 = clock64();
       bool ok = true;
-      while (!mbar_try_wait(&bars[s], ph)) {
+      while (!try_wait_sleep(bar_addr, ph, 20000u)) {
         if (clock64() - t0 > (1ll << 31)) {
           ok = false;
           break;
@@ -553,40 +608,53 @@ __global__ void __launch_bounds__(kWarpWarps * 32, 1) decode_warp_kernel(const W
         if (lane == 0) {
           atomicExch(a.err, 1);
           // the copies still in flight land before the block may exit
-          for (int j = k + 1; j < k + kWarpSlots && c0 + j < c1; ++j)
+          for (int j = k; j < k + kWarpSlots && j < n; ++j)
             (void)mbar_drain_bounded(&bars[j % kWarpSlots], (uint32_t)((j / kWarpSlots) & 1));
         }
         return;
       }
     }
     const uint8_t* slot = slots + s * kWarpSlot;
-    uint8_t* tab = tab0 + (unit & 1) * kKtab;
-    ++unit;
-    const WarpChunk ch = warp_chunk(a, (int)(gc - pair * a.C));
-    if (ch.pp) {
-      if (ch.n == 32) run_pp<true>(a, slot, 32, Q, L, tab, S);
-      else run_pp<false>(a, slot, ch.n, Q, L, tab, S);
+    uint8_t* tab = tab0 + (k & 1) * kKtab;
+    if (c < n_full) {
+      run_pp<true, NGV, INTZ>(slot, 32, Q, L, tab, S);
     } else {
-      run_x(a, slot, ch, Q, L, reinterpret_cast<const uint8_t*>(qsm), tab, S);
+      const WarpChunk ch = warp_chunk(a, c);
+      if (ch.pp) run_pp<false, NGV, INTZ>(slot, ch.n, Q, L, tab, S);
+      else run_x<NGV, INTZ>(a, slot, ch, Q, L, reinterpret_cast<const uint8_t*>(qsm), tab, S);
     }
     __syncwarp();  // every lane has read the slot
-    if (lane == 0 && gc + kWarpSlots < c1) {
-      fence_proxy_async_smem();
-      issue_chunk(a, gc + kWarpSlots, slots + s * kWarpSlot, &bars[s]);
+    if (k + kWarpSlots < n) {
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        stage_chunk<NGV>(a, ipp, ip, ic, slots + s * kWarpSlot, &bars[s]);
+      }
+      if (++ic == a.C) {
+        ic = 0;
+        ipp = pair_ptrs(a, ++ip);
+      }
     }
+    if (++c == a.C) c = 0, ++pair;
+    if (++s == kWarpSlots) s = 0, ph ^= 1u;
   }
-  if (cur >= 0) finish_pair(a, cur, gw, lane, L, S);
+  if (cur >= 0) finish_pair<NGV>(a, cur, gw, lane, L, S);
 }
 
 }  // namespace
 
-cudaError_t launch_decode_warp(const WarpArgs& a, cudaStream_t s) {
+template <int NGV, bool INTZ>
+static cudaError_t launch_warp_t(const WarpArgs& a, cudaStream_t s) {
   const int bytes = WarpSmem::total;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_warp_kernel), bytes);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_warp_kernel<NGV, INTZ>), bytes);
   if (e != cudaSuccess) return e;
-  const int ctas = (a.n_warps + kWarpWarps - 1) / kWarpWarps;
-  decode_warp_kernel<<<ctas, kWarpWarps * 32, bytes, s>>>(a);
+  decode_warp_kernel<NGV, INTZ><<<a.n_warps, 32, bytes, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode_warp(const WarpArgs& a, cudaStream_t s) {
+  if (a.ngv == 4) return a.intz ? launch_warp_t<4, true>(a, s) : launch_warp_t<4, false>(a, s);
+  if (a.ngv == 2) return a.intz ? launch_warp_t<2, true>(a, s) : launch_warp_t<2, false>(a, s);
+  return a.intz ? launch_warp_t<1, true>(a, s) : launch_warp_t<1, false>(a, s);
 }
 
 }  // namespace kvq

@@ -269,9 +269,15 @@ __host__ __device__ inline void for_each_tile_copy(const DecodeArgs& a, size_t p
 //     from the rings above.  An X chunk is staged as its whole 8-row block,
 //     its tokens at rows [o0, o0 + n).
 // ---------------------------------------------------------------------------
-constexpr int kWarpSlot = 4096;   // bytes of one pipeline slot
-constexpr int kWarpSlots = 3;     // slots per warp
-constexpr int kWarpWarps = 16;    // warps per CTA (one CTA per SM)
+#ifndef KVQ_WARP_SLOTS
+#define KVQ_WARP_SLOTS 2
+#endif
+#ifndef KVQ_WARP_WARPS
+#define KVQ_WARP_WARPS 16
+#endif
+constexpr int kWarpSlot = 4096;               // bytes of one pipeline slot
+constexpr int kWarpSlots = KVQ_WARP_SLOTS;    // slots per warp
+constexpr int kWarpWarps = KVQ_WARP_WARPS;    // warps (one-warp CTAs) per SM
 // slot layout, PP chunk: K codes, K group scales / zeros, V codes, V token
 // scales / zeros (the zeros 32 bytes off a 256-byte stride, so the scale and
 // zero loads of one instruction hit different banks)
@@ -298,8 +304,7 @@ struct WarpArgs {
   float scale_log2;
   int nk, nv, L, npp, npx;
   int n_pp, n_x1, n_x2, C;  // chunks per pair
-  int wpp, wx;              // chunk costs (stream-K weights)
-  long long Cp, T;          // cost of a pair, of all pairs
+  long long Cp, T;          // stream-K cost of a pair, of all pairs
   int P, n_warps, rec_stride;
 };
 
@@ -332,26 +337,38 @@ __host__ __device__ inline WarpChunk warp_chunk(const WarpArgs& a, int c) {
   return ch;
 }
 
+// Stream-K weights of a 32-token packed chunk and of an 8-token ring chunk.
+#ifndef KVQ_WARP_WPP
+#define KVQ_WARP_WPP 6
+#endif
+#ifndef KVQ_WARP_WX
+#define KVQ_WARP_WX 8
+#endif
+constexpr int kWarpWpp = KVQ_WARP_WPP, kWarpWx = KVQ_WARP_WX;
+
+// Cost offset of chunk c of `pair` in the concatenated list.
+__host__ __device__ inline long long warp_chunk_start(const WarpArgs& a, long long pair, int c) {
+  const long long in = c <= a.n_pp ? (long long)kWarpWpp * c
+                                   : (long long)kWarpWpp * a.n_pp + (long long)kWarpWx * (c - a.n_pp);
+  return pair * a.Cp + in;
+}
+
 // First global chunk of warp w's range (w = n_warps gives P * C): the first
-// chunk whose cost offset reaches T * w / n_warps.
+// chunk whose cost offset reaches floor(T * w / n_warps).
 __host__ __device__ inline long long warp_bound(const WarpArgs& a, int w) {
   const long long target = a.T * (long long)w / a.n_warps;
   const long long pair = target / a.Cp;
   const long long r = target - pair * a.Cp;
-  const long long pp_cost = (long long)a.wpp * a.n_pp;
-  const long long c = r <= pp_cost ? (r + a.wpp - 1) / a.wpp : a.n_pp + (r - pp_cost + a.wx - 1) / a.wx;
+  const long long pp_cost = (long long)kWarpWpp * a.n_pp;
+  const long long c = r <= pp_cost ? (r + kWarpWpp - 1) / kWarpWpp : a.n_pp + (r - pp_cost + kWarpWx - 1) / kWarpWx;
   return pair * a.C + c;
 }
 
-// The warp whose range holds global chunk g (ranges are never empty).
-__host__ __device__ inline int warp_owner(const WarpArgs& a, long long g) {
-  int lo = 0, hi = a.n_warps - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (warp_bound(a, mid) <= g) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
+// The warp whose range holds chunk c of `pair`: the largest w with
+// floor(T w / n_warps) <= start, i.e. T w < n_warps (start + 1).  Ranges are
+// never empty (every warp's share is at least the largest chunk cost).
+__host__ __device__ inline int warp_owner(const WarpArgs& a, long long pair, int c) {
+  return (int)(((long long)a.n_warps * (warp_chunk_start(a, pair, c) + 1) - 1) / a.T);
 }
 
 // The bulk copies that stage chunk c of `pair` in a slot: f(src, dst_off,
