@@ -432,8 +432,9 @@ bool warp_kernel_applies(const kvq_cache* c) {
          c->group % 32 == 0 && Gv >= 32 && 128 % Gv == 0 && c->seg[0].nk % 8 == 0 && c->seg[0].capacity % 32 == 0;
 }
 
-// Chunk counts, stream-K warps and the record stride of a cache's state;
-// false if the workspace cannot hold the records even for one warp per pair.
+// Chunk counts and warps per pair of a cache's state: as many warps per
+// pair as the GPU holds (kWarpWarps per SM), each piece at least the largest
+// chunk's cost; fewer if the workspace cannot hold the pieces' records.
 bool plan_warp(const kvq_cache* c, kvq::WarpArgs& a, size_t ws_bytes) {
   const int P = c->batch * c->h_kv;
   a.nk = c->seg[0].nk;
@@ -447,24 +448,14 @@ bool plan_warp(const kvq_cache* c, kvq::WarpArgs& a, size_t ws_bytes) {
   a.C = a.n_pp + a.n_x1 + a.n_x2;
   a.Cp = (long long)kvq::kWarpWpp * a.n_pp + (long long)kvq::kWarpWx * (a.n_x1 + a.n_x2);
   a.P = P;
-  a.T = a.Cp * P;
-  // every warp's cost share at least the largest chunk cost: no empty range
-  long long nw = std::min<long long>((long long)sm_count() * kvq::kWarpWarps,
-                                     a.T / std::max(kvq::kWarpWpp, kvq::kWarpWx));
-  nw = std::max<long long>(nw, 1);
+  long long k = (long long)sm_count() * kvq::kWarpWarps / P;
+  k = std::min<long long>(k, a.Cp / std::max(kvq::kWarpWpp, kvq::kWarpWx));
   const size_t room = ws_bytes > ws_fixed(P) ? ws_bytes - ws_fixed(P) : 0;
-  for (;;) {
-    a.n_warps = (int)nw;
-    int stride = 1;
-    for (int p = 0; p < P; ++p) {
-      const int f = kvq::warp_owner(a, p, 0), l = kvq::warp_owner(a, p, a.C - 1);
-      stride = std::max(stride, l - f + 1);
-    }
-    a.rec_stride = stride;
-    if (stride == 1 || (size_t)P * stride * (128 + 2) * sizeof(float) <= room) return true;
-    if (nw == 1) return false;
-    nw = std::max<long long>(1, nw / 2);
-  }
+  k = std::min<long long>(k, (long long)(room / ((size_t)P * (128 + 2) * sizeof(float))));
+  if (k < 1) k = 1;  // one warp per pair writes its output directly: no records
+  if ((long long)P * k >= (1LL << 31)) return false;
+  a.k = (int)k;
+  return true;
 }
 
 // Every bulk copy of every chunk, walked for the first and the last pair

@@ -16,17 +16,18 @@
 //
 // Work split.  The token axis of every (batch, kv head) pair is cut into
 // chunks (32 tokens with K and V packed; 8-token blocks where a ring is
-// involved: kvq_internal.h, warp_chunk) and the concatenated chunk list of
-// all pairs into one contiguous, cost-balanced range per warp (stream-K over
-// warps, computed in closed form from the uniform lengths).  Each warp is a
-// CTA of its own (kWarpWarps of them resident per SM) and stages its own
-// chunks, kWarpSlots ahead, into its own slots: one lane issues the bulk
-// copies (TMA engine, mbarrier completion); with one warp per CTA every
-// shared-memory and barrier address is warp-uniform, so the copies take
-// their operands straight from uniform registers.  No warp ever waits for
-// another: there is no producer warp, no stage release and no CTA-wide
-// barrier.  Each warp leaves a partial (o, m, l) record per pair it touched;
-// the last warp of a pair to finish (atomic counter) merges the records.
+// involved: kvq_internal.h, warp_chunk) and each pair's chunk list into k
+// contiguous pieces of equal cost, k as large as the GPU's resident warps
+// allow (kWarpWarps per SM).  Each piece is a one-warp CTA that stages its
+// own chunks, kWarpSlots ahead, into its own slots: the K and V codes by
+// bulk copies (TMA engine, mbarrier completion) that one lane issues, the
+// small scale / zero arrays by 16-byte cp.async pieces of every lane
+// tracked on the same mbarrier.  With one warp per CTA every shared-memory
+// and barrier address is warp-uniform.  No warp ever waits for another:
+// there is no producer warp, no stage release and no CTA-wide barrier, and
+// a warp loads its pair's query once.  Each piece leaves a partial
+// (o, m, l) record; the last piece of a pair to finish (atomic counter)
+// merges the records.
 #include <float.h>
 
 #include "kvq_device.cuh"
@@ -436,46 +437,60 @@ __device__ __forceinline__ PairPtrs pair_ptrs(const WarpArgs& a, long long pair)
   return p;
 }
 
-// Stage chunk c of a pair into a slot: one lane issues the bulk copies
-// (TMA engine) and the mbarrier's expected byte count.  The CTA is one warp,
-// so every address here is warp-uniform.  A full 32-token chunk with K and V
-// packed takes the short path; anything else walks the general copy list
-// (warp_chunk_copies, the list the host checked).
+// Stage chunk c of a pair into a slot.  A full 32-token chunk with K and V
+// packed: every lane copies its 16-byte pieces of the K group's scales /
+// zeros and the tokens' V scales / zeros (cp.async, tracked by the slot's
+// mbarrier), then one lane issues the K and V code copies (TMA engine)
+// with the barrier's byte count: two bulk copies per chunk, as the engine
+// issues small copies at a limited rate per SM.  Anything else (ring blocks,
+// a short last chunk) walks the general copy list (warp_chunk_copies, the
+// list the host checked) with bulk copies only.  The CTA is one warp, so
+// every address here is warp-uniform.
 template <int NGV>
 __device__ __forceinline__ void stage_chunk(const WarpArgs& a, const PairPtrs& pp, long long pair, int c,
-                                            uint8_t* slot, uint64_t* bar) {
+                                            uint8_t* slot, uint64_t* bar, int lane) {
   if (c < a.npp / 32) {
     const int t0 = 32 * c;
-    constexpr uint32_t sb = 32 * NGV * 2;
-    mbar_arrive_expect_tx(bar, 2 * 1024 + 2 * 256 + 2 * sb);
-    bulk_g2s(slot + kPpKc, pp.kc + t0 * kRB, 1024, bar);
-    bulk_g2s(slot + kPpKs, pp.ks + (t0 >> a.log2G) * D, 256, bar);
-    bulk_g2s(slot + kPpKz, pp.kz + (t0 >> a.log2G) * D, 256, bar);
-    bulk_g2s(slot + kPpVc, pp.vc + t0 * kRB, 1024, bar);
-    bulk_g2s(slot + kPpVs, pp.vs + t0 * NGV, sb, bar);
-    bulk_g2s(slot + kPpVz, pp.vz + t0 * NGV, sb, bar);
+    const uint32_t sl = smem_u32(slot);
+    const int h = lane & 15;
+    const bool lo = lane < 16;
+    cp16(sl + (lo ? kPpKs : kPpKz) + h * 16, (lo ? pp.ks : pp.kz) + (t0 >> a.log2G) * D + h * 8);
+    constexpr int VB = 32 * NGV * 2;  // bytes of the chunk's token scales (zeros)
+    if (h * 16 < VB) cp16(sl + (lo ? kPpVs : kPpVz) + h * 16, (lo ? pp.vs : pp.vz) + t0 * NGV + h * 8);
+    cp_mbar_arrive(bar);
+    __syncwarp();  // every lane's pending arrival is counted before the phase can end
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, 2 * 1024);
+      bulk_g2s(slot + kPpKc, pp.kc + t0 * kRB, 1024, bar);
+      bulk_g2s(slot + kPpVc, pp.vc + t0 * kRB, 1024, bar);
+    }
     return;
   }
-  const WarpChunk ch = warp_chunk(a, c);
-  uint32_t bytes = 0;
-  warp_chunk_copies(a, pair, ch, [&](const void*, uint32_t, uint32_t n, int) { bytes += n; });
-  mbar_arrive_expect_tx(bar, bytes);
-  warp_chunk_copies(a, pair, ch, [&](const void* src, uint32_t dst, uint32_t n, int) { bulk_g2s(slot + dst, src, n, bar); });
+  if (lane == 0) {
+    const WarpChunk ch = warp_chunk(a, c);
+    uint32_t bytes = 0;
+    warp_chunk_copies(a, pair, ch, [&](const void*, uint32_t, uint32_t n, int) { bytes += n; });
+    mbar_arrive_expect_tx(bar, bytes);
+    warp_chunk_copies(a, pair, ch,
+                      [&](const void* src, uint32_t dst, uint32_t n, int) { bulk_g2s(slot + dst, src, n, bar); });
+  }
 }
 
-// End of a warp's share of a pair: its partial (o, m, l) as a record, or the
-// output when the warp holds the whole pair; the last record of the pair to
-// arrive merges them all.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// End of a warp's piece of a pair: its partial (o, m, l) as the piece's
+// record, made visible and counted (lane 0 gets the count found, `ticket`),
+// or the output itself when the pair has one piece.  Returns the pair's
+// number of records (1: output written).
 template <int NGV>
-__device__ void finish_pair(const WarpArgs& a, long long pair, int gw, int lane, const LaneC& L, WState& S) {
+__device__ int write_piece(const WarpArgs& a, long long pair, int piece, int lane, const LaneC& L, WState& S,
+                           int& ticket) {
   if (!S.vring) unscale_acc2(S);
   float l = S.l;  // sum over the lanes of one tig (rows gid)
   l += __shfl_xor_sync(kFull, l, 4);
   l += __shfl_xor_sync(kFull, l, 8);
   l += __shfl_xor_sync(kFull, l, 16);
-  const int first = warp_owner(a, pair, 0);
-  const int last = warp_owner(a, pair, a.C - 1);
-  const int nrec = last - first + 1;
+  const int nrec = a.k;
   // o of channel c: column g(c) of its row (lanes tig = g / 2) plus the z sum
   // of group g (column 4 + g, lanes tig = 2 + g / 2)
   float o16[16];
@@ -498,9 +513,9 @@ __device__ void finish_pair(const WarpArgs& a, long long pair, int gw, int lane,
 #pragma unroll
     for (int i = 0; i < 16; ++i)
       if (c16[i] >= 0) a.out[pair * D + c16[i]] = __float2half_rn(o16[i] * il);
-    return;
+    return 1;
   }
-  float* rec = a.part + (pair * a.rec_stride + (gw - first)) * kRec;
+  float* rec = a.part + (pair * a.k + piece) * kRec;
 #pragma unroll
   for (int i = 0; i < 16; ++i)
     if (c16[i] >= 0) rec[c16[i]] = o16[i];
@@ -508,13 +523,18 @@ __device__ void finish_pair(const WarpArgs& a, long long pair, int gw, int lane,
     rec[D] = S.m;
     rec[D + 1] = l;
   }
-  __threadfence();
+  fence_acq_rel_gpu();  // the record is visible before it is counted
   __syncwarp();
-  int is_last = 0;
-  if (lane == 0) is_last = atomicAdd(&a.counters[pair], 1) == nrec - 1;
-  if (!__shfl_sync(kFull, is_last, 0)) return;
-  __threadfence();
-  const float* recs = a.part + pair * a.rec_stride * kRec;
+  if (lane == 0) ticket = atomicAdd(&a.counters[pair], 1);
+  return nrec;
+}
+
+// The piece that found nrec - 1 (the last of the pair to arrive) merges the
+// pair's records and writes the output.
+__device__ __noinline__ void merge_if_last(const WarpArgs& a, long long pair, int nrec, int ticket, int lane) {
+  if (!__shfl_sync(kFull, ticket == nrec - 1 ? 1 : 0, 0)) return;
+  fence_acq_rel_gpu();  // the other records are visible after their counts
+  const float* recs = a.part + pair * a.k * kRec;
   float m = -INFINITY;
   for (int s = lane; s < nrec; s += 32) m = fmaxf(m, __ldcg(recs + s * kRec + D));
 #pragma unroll
@@ -526,6 +546,7 @@ __device__ void finish_pair(const WarpArgs& a, long long pair, int gw, int lane,
   for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(kFull, ls, off);
   const float il = ls > 0.f ? 1.f / ls : 0.f;
   float oo[D / 32] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
   for (int s = 0; s < nrec; ++s) {
     const float* rr = recs + s * kRec;
     const float w = m == -INFINITY ? 0.f : exp2f(__ldcg(rr + D) - m) * il;
@@ -537,60 +558,38 @@ __device__ void finish_pair(const WarpArgs& a, long long pair, int gw, int lane,
   if (lane == 0) a.counters[pair] = 0;  // ready for the next call on this workspace
 }
 
-__device__ __forceinline__ void load_query(const WarpArgs& a, long long pair, int lane, __half* qsm) {
-  const uint2 v = reinterpret_cast<const uint2*>(a.q + pair * D)[lane];  // 8 bytes per lane
-  reinterpret_cast<uint2*>(qsm)[lane] = v;
-  __syncwarp();
-}
-
-// One warp per CTA, kWarpWarps CTAs per SM: CTA gw takes the range of warp gw.
+// One warp per CTA, kWarpWarps CTAs per SM: CTA gw takes piece gw % k of
+// pair gw / k.
 template <int NGV, bool INTZ>
 __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x;
-  const int gw = blockIdx.x;
+  const long long pair = blockIdx.x / a.k;
+  const int piece = (int)(blockIdx.x - pair * a.k);
   uint8_t* slots = smem + WarpSmem::slots;
   uint8_t* tab0 = smem + WarpSmem::ktab;
   __half* qsm = reinterpret_cast<__half*>(smem + WarpSmem::qbuf);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WarpSmem::bars);
-  const long long c0 = warp_bound(a, gw), c1 = warp_bound(a, gw + 1);
-  const int n = (int)(c1 - c0);  // chunks of this warp
-  const long long pair0 = c0 / a.C;
-  const int cc0 = (int)(c0 - pair0 * a.C);
-  // staging position, kWarpSlots chunks ahead of the consumed one
-  long long ip = pair0;
-  int ic = cc0;
-  PairPtrs ipp = pair_ptrs(a, ip);
+  const int c0 = warp_piece_start(a, piece), c1 = warp_piece_start(a, piece + 1);
+  const int n = c1 - c0;  // chunks of this piece (at least one)
+  const PairPtrs pp = pair_ptrs(a, pair);
   if (lane == 0) {
     for (int s = 0; s < kWarpSlots; ++s) mbar_init(&bars[s], 1);
     mbar_fence_init();
   }
   __syncwarp();
-  for (int s = 0; s < kWarpSlots && s < n; ++s) {
-    if (lane == 0) stage_chunk<NGV>(a, ipp, ip, ic, slots + s * kWarpSlot, &bars[s]);
-    if (++ic == a.C) {
-      ic = 0;
-      ipp = pair_ptrs(a, ++ip);
-    }
-  }
+  for (int s = 0; s < kWarpSlots && s < n; ++s) stage_chunk<NGV>(a, pp, pair, c0 + s, slots + s * kWarpSlot, &bars[s], lane);
+  reinterpret_cast<uint2*>(qsm)[lane] = __ldg(reinterpret_cast<const uint2*>(a.q + pair * D) + lane);
+  __syncwarp();
   const LaneC L = lane_consts(lane);
+  const PairQ Q = pair_query(a, qsm, L);
   WState S;
   reset_state(S);
-  PairQ Q;
-  long long pair = pair0, cur = -1;
-  int c = cc0, s = 0;
-  uint32_t ph = 0;
   const int n_full = a.npp / 32;  // full 32-token chunks with K and V packed
+  int s = 0;
+  uint32_t ph = 0;
   for (int k = 0; k < n; ++k) {
-    if (pair != cur) {
-      if (cur >= 0) {
-        finish_pair<NGV>(a, cur, gw, lane, L, S);
-        reset_state(S);
-      }
-      cur = pair;
-      load_query(a, pair, lane, qsm);
-      Q = pair_query(a, qsm, L);
-    }
+    const int c = c0 + k;
     // wait for the chunk's copies (bounded: about 2^31 clocks), inside the
     // barrier unit (suspend-time hint) rather than spinning through issue
     // slots the other warps of the SM need
@@ -625,19 +624,14 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
     }
     __syncwarp();  // every lane has read the slot
     if (k + kWarpSlots < n) {
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        stage_chunk<NGV>(a, ipp, ip, ic, slots + s * kWarpSlot, &bars[s]);
-      }
-      if (++ic == a.C) {
-        ic = 0;
-        ipp = pair_ptrs(a, ++ip);
-      }
+      if (lane == 0) fence_proxy_async_smem();
+      stage_chunk<NGV>(a, pp, pair, c + kWarpSlots, slots + s * kWarpSlot, &bars[s], lane);
     }
-    if (++c == a.C) c = 0, ++pair;
     if (++s == kWarpSlots) s = 0, ph ^= 1u;
   }
-  if (cur >= 0) finish_pair<NGV>(a, cur, gw, lane, L, S);
+  int ticket = 0;
+  const int nrec = write_piece<NGV>(a, pair, piece, lane, L, S, ticket);
+  if (nrec > 1) merge_if_last(a, pair, nrec, ticket, lane);
 }
 
 }  // namespace
@@ -647,7 +641,7 @@ static cudaError_t launch_warp_t(const WarpArgs& a, cudaStream_t s) {
   const int bytes = WarpSmem::total;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_warp_kernel<NGV, INTZ>), bytes);
   if (e != cudaSuccess) return e;
-  decode_warp_kernel<NGV, INTZ><<<a.n_warps, 32, bytes, s>>>(a);
+  decode_warp_kernel<NGV, INTZ><<<(unsigned)(a.P * a.k), 32, bytes, s>>>(a);
   return cudaGetLastError();
 }
 

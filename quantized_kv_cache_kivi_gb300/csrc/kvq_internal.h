@@ -259,9 +259,9 @@ __host__ __device__ inline void for_each_tile_copy(const DecodeArgs& a, size_t p
 
 // ---------------------------------------------------------------------------
 // Decode with one query head per kv head over one 2-bit segment (the warp
-// kernel, kvq_decode_warp.cu): every warp runs a bulk-copy pipeline of its
-// own over a contiguous, cost-balanced range of chunks of the concatenated
-// (pair, chunk) list.  Per pair the token axis is cut into
+// kernel, kvq_decode_warp.cu): every pair is cut into k pieces of equal
+// cost, one per warp, and every warp runs a bulk-copy pipeline of its own
+// over its piece's chunks.  Per pair the token axis is cut into
 //   - PP chunks: 32 tokens [32u, 32u + 32) of [0, npp), K and V packed
 //     (npp = min(nk, nv)); the last one may be short;
 //   - X chunks: the rest, [npp, L), in the 8-token blocks of the token
@@ -304,8 +304,8 @@ struct WarpArgs {
   float scale_log2;
   int nk, nv, L, npp, npx;
   int n_pp, n_x1, n_x2, C;  // chunks per pair
-  long long Cp, T;          // stream-K cost of a pair, of all pairs
-  int P, n_warps, rec_stride;
+  long long Cp;             // cost of a pair (kWarpWpp, kWarpWx)
+  int P, k;                 // pairs, warps per pair (pieces; records when k > 1)
 };
 
 struct WarpChunk {
@@ -337,7 +337,8 @@ __host__ __device__ inline WarpChunk warp_chunk(const WarpArgs& a, int c) {
   return ch;
 }
 
-// Stream-K weights of a 32-token packed chunk and of an 8-token ring chunk.
+// Weights of a 32-token packed chunk and of an 8-token ring chunk (about
+// their bytes) for cutting a pair into pieces of equal cost.
 #ifndef KVQ_WARP_WPP
 #define KVQ_WARP_WPP 6
 #endif
@@ -346,29 +347,13 @@ __host__ __device__ inline WarpChunk warp_chunk(const WarpArgs& a, int c) {
 #endif
 constexpr int kWarpWpp = KVQ_WARP_WPP, kWarpWx = KVQ_WARP_WX;
 
-// Cost offset of chunk c of `pair` in the concatenated list.
-__host__ __device__ inline long long warp_chunk_start(const WarpArgs& a, long long pair, int c) {
-  const long long in = c <= a.n_pp ? (long long)kWarpWpp * c
-                                   : (long long)kWarpWpp * a.n_pp + (long long)kWarpWx * (c - a.n_pp);
-  return pair * a.Cp + in;
-}
-
-// First global chunk of warp w's range (w = n_warps gives P * C): the first
-// chunk whose cost offset reaches floor(T * w / n_warps).
-__host__ __device__ inline long long warp_bound(const WarpArgs& a, int w) {
-  const long long target = a.T * (long long)w / a.n_warps;
-  const long long pair = target / a.Cp;
-  const long long r = target - pair * a.Cp;
+// First chunk of piece j of a pair cut into `k` pieces of equal cost (j = k
+// gives C): the first chunk whose cost offset reaches floor(Cp * j / k).
+__host__ __device__ inline int warp_piece_start(const WarpArgs& a, int j) {
+  const long long r = a.Cp * (long long)j / a.k;
   const long long pp_cost = (long long)kWarpWpp * a.n_pp;
   const long long c = r <= pp_cost ? (r + kWarpWpp - 1) / kWarpWpp : a.n_pp + (r - pp_cost + kWarpWx - 1) / kWarpWx;
-  return pair * a.C + c;
-}
-
-// The warp whose range holds chunk c of `pair`: the largest w with
-// floor(T w / n_warps) <= start, i.e. T w < n_warps (start + 1).  Ranges are
-// never empty (every warp's share is at least the largest chunk cost).
-__host__ __device__ inline int warp_owner(const WarpArgs& a, long long pair, int c) {
-  return (int)(((long long)a.n_warps * (warp_chunk_start(a, pair, c) + 1) - 1) / a.T);
+  return (int)(c < a.C ? c : a.C);
 }
 
 // The bulk copies that stage chunk c of `pair` in a slot: f(src, dst_off,
