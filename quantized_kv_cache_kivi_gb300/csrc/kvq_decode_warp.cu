@@ -44,12 +44,12 @@ constexpr int kRB = D * kWB / 8;         // packed row bytes (32)
 constexpr int kKtab = 512;               // one K operand table (bytes)
 constexpr int kRec = D + 2;              // record (o[D], m, l)
 
-// Shared memory of a CTA (one warp): its slots, two K operand tables, the
+// Shared memory of a CTA (one warp): its slots, the K operand table, the
 // pair's query and the slots' mbarriers.
 struct WarpSmem {
-  static constexpr int slots = 0;                             // [slot][kWarpSlot]
-  static constexpr int ktab = slots + kWarpSlots * kWarpSlot;  // [2][kKtab]
-  static constexpr int qbuf = ktab + 2 * kKtab;                      // [D] f16
+  static constexpr int slots = 0;                              // [slot][kWarpSlot]
+  static constexpr int ktab = slots + kWarpSlots * kWarpSlot;  // [kKtab]
+  static constexpr int qbuf = ktab + kKtab;                    // [D] f16
   static constexpr int bars = qbuf + D * 2;                          // [slot] mbarrier
   static constexpr int total = bars + kWarpSlots * 8;
 };
@@ -154,8 +154,8 @@ __device__ __forceinline__ PairQ pair_query(const WarpArgs& a, const __half* qsm
 // slot): each lane computes its four entries, splits them into an fp16 high
 // part and the fp16 rest, writes both to the warp's table; every lane then
 // reads the 16 words of its own column.  Returns the bias q . z (log2
-// domain) of the group.  tab: this unit's table (two alternate per unit, so
-// one __syncwarp separates writes from reads).
+// domain) of the group.  tab: the warp's table (the __syncwarp that ends
+// each chunk separates one chunk's reads from the next one's writes).
 template <bool INTZ>
 __device__ __forceinline__ float build_kop(const uint8_t* ks, const uint8_t* kz, const PairQ& Q, const LaneC& L,
                                            uint8_t* tab, uint32_t (&bq)[16]) {
@@ -437,15 +437,21 @@ __device__ __forceinline__ PairPtrs pair_ptrs(const WarpArgs& a, long long pair)
   return p;
 }
 
-// Stage chunk c of a pair into a slot.  A full 32-token chunk with K and V
-// packed: every lane copies its 16-byte pieces of the K group's scales /
-// zeros and the tokens' V scales / zeros (cp.async, tracked by the slot's
-// mbarrier), then one lane issues the K and V code copies (TMA engine)
-// with the barrier's byte count: two bulk copies per chunk, as the engine
-// issues small copies at a limited rate per SM.  Anything else (ring blocks,
-// a short last chunk) walks the general copy list (warp_chunk_copies, the
-// list the host checked) with bulk copies only.  The CTA is one warp, so
-// every address here is warp-uniform.
+// Stage chunk c of a pair into a slot.  A slot's mbarrier expects 33
+// arrivals per phase: one from each lane and one, with the byte count of the
+// bulk copies, from lane 0, in any order.  A full 32-token chunk with K and
+// V packed: every lane copies its 16-byte pieces of the K group's scales /
+// zeros and the tokens' V scales / zeros (cp.async) and arrives when they
+// have landed; lane 0 issues the K and V code copies (TMA engine) -- two
+// bulk copies per chunk, as the engine issues small copies at a limited
+// rate per SM.  Anything else (ring blocks, a short last chunk) walks the
+// general copy list (warp_chunk_copies, the list the host checked) with
+// bulk copies only.  The CTA is one warp, so every address is warp-uniform.
+// No proxy fence precedes the copies into a slot the warp has just read:
+// every shared load of the slot has returned its value (the loop's
+// __syncwarp follows the last use) before lane 0 issues them.
+constexpr uint32_t kSlotArrivals = 33;
+
 template <int NGV>
 __device__ __forceinline__ void stage_chunk(const WarpArgs& a, const PairPtrs& pp, long long pair, int c,
                                             uint8_t* slot, uint64_t* bar, int lane) {
@@ -457,8 +463,7 @@ __device__ __forceinline__ void stage_chunk(const WarpArgs& a, const PairPtrs& p
     cp16(sl + (lo ? kPpKs : kPpKz) + h * 16, (lo ? pp.ks : pp.kz) + (t0 >> a.log2G) * D + h * 8);
     constexpr int VB = 32 * NGV * 2;  // bytes of the chunk's token scales (zeros)
     if (h * 16 < VB) cp16(sl + (lo ? kPpVs : kPpVz) + h * 16, (lo ? pp.vs : pp.vz) + t0 * NGV + h * 8);
-    cp_mbar_arrive(bar);
-    __syncwarp();  // every lane's pending arrival is counted before the phase can end
+    cp_mbar_arrive_noinc(bar);
     if (lane == 0) {
       mbar_arrive_expect_tx(bar, 2 * 1024);
       bulk_g2s(slot + kPpKc, pp.kc + t0 * kRB, 1024, bar);
@@ -466,6 +471,7 @@ __device__ __forceinline__ void stage_chunk(const WarpArgs& a, const PairPtrs& p
     }
     return;
   }
+  mbar_arrive_plain(bar);
   if (lane == 0) {
     const WarpChunk ch = warp_chunk(a, c);
     uint32_t bytes = 0;
@@ -558,8 +564,8 @@ __device__ __noinline__ void merge_if_last(const WarpArgs& a, long long pair, in
   if (lane == 0) a.counters[pair] = 0;  // ready for the next call on this workspace
 }
 
-// One warp per CTA, kWarpWarps CTAs per SM: CTA gw takes piece gw % k of
-// pair gw / k.
+// One warp per CTA, kWarpWarps CTAs per SM: CTA i takes piece i % k of
+// pair i / k.
 template <int NGV, bool INTZ>
 __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -567,19 +573,20 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
   const long long pair = blockIdx.x / a.k;
   const int piece = (int)(blockIdx.x - pair * a.k);
   uint8_t* slots = smem + WarpSmem::slots;
-  uint8_t* tab0 = smem + WarpSmem::ktab;
+  uint8_t* tab = smem + WarpSmem::ktab;
   __half* qsm = reinterpret_cast<__half*>(smem + WarpSmem::qbuf);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WarpSmem::bars);
   const int c0 = warp_piece_start(a, piece), c1 = warp_piece_start(a, piece + 1);
   const int n = c1 - c0;  // chunks of this piece (at least one)
   const PairPtrs pp = pair_ptrs(a, pair);
+  const uint2 qv = __ldg(reinterpret_cast<const uint2*>(a.q + pair * D) + lane);
   if (lane == 0) {
-    for (int s = 0; s < kWarpSlots; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < kWarpSlots; ++s) mbar_init(&bars[s], kSlotArrivals);
     mbar_fence_init();
   }
   __syncwarp();
   for (int s = 0; s < kWarpSlots && s < n; ++s) stage_chunk<NGV>(a, pp, pair, c0 + s, slots + s * kWarpSlot, &bars[s], lane);
-  reinterpret_cast<uint2*>(qsm)[lane] = __ldg(reinterpret_cast<const uint2*>(a.q + pair * D) + lane);
+  reinterpret_cast<uint2*>(qsm)[lane] = qv;
   __syncwarp();
   const LaneC L = lane_consts(lane);
   const PairQ Q = pair_query(a, qsm, L);
@@ -614,7 +621,6 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
       }
     }
     const uint8_t* slot = slots + s * kWarpSlot;
-    uint8_t* tab = tab0 + (k & 1) * kKtab;
     if (c < n_full) {
       run_pp<true, NGV, INTZ>(slot, 32, Q, L, tab, S);
     } else {
@@ -623,10 +629,7 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
       else run_x<NGV, INTZ>(a, slot, ch, Q, L, reinterpret_cast<const uint8_t*>(qsm), tab, S);
     }
     __syncwarp();  // every lane has read the slot
-    if (k + kWarpSlots < n) {
-      if (lane == 0) fence_proxy_async_smem();
-      stage_chunk<NGV>(a, pp, pair, c + kWarpSlots, slots + s * kWarpSlot, &bars[s], lane);
-    }
+    if (k + kWarpSlots < n) stage_chunk<NGV>(a, pp, pair, c + kWarpSlots, slots + s * kWarpSlot, &bars[s], lane);
     if (++s == kWarpSlots) s = 0, ph ^= 1u;
   }
   int ticket = 0;

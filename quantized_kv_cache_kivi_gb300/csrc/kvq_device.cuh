@@ -236,11 +236,13 @@ __device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Make an mbarrier's current phase also wait for this thread's cp.async
-// copies issued so far (the pending count is raised now and lowered when
-// they complete, so the barrier's initial count is unchanged).
-__device__ __forceinline__ void cp_mbar_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+// An arrival on an mbarrier once this thread's cp.async copies issued so far
+// have completed (.noinc: counted in the barrier's expected arrivals).
+__device__ __forceinline__ void cp_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_wait() {

@@ -270,7 +270,7 @@ __host__ __device__ inline void for_each_tile_copy(const DecodeArgs& a, size_t p
 //     its tokens at rows [o0, o0 + n).
 // ---------------------------------------------------------------------------
 #ifndef KVQ_WARP_SLOTS
-#define KVQ_WARP_SLOTS 2
+#define KVQ_WARP_SLOTS 3
 #endif
 #ifndef KVQ_WARP_WARPS
 #define KVQ_WARP_WARPS 16
@@ -297,8 +297,8 @@ struct WarpArgs {
   const __half* vr;
   const __half* q;    // [P][128] (one query head per pair)
   __half* out;
-  float* part;        // records [P][rec_stride][130]
-  int* counters;      // [P]
+  float* part;        // records [P][k][130]
+  int* counters;      // [P] pieces of a pair finished (merge)
   int* err;
   int cap, R, krs, vrs, log2G, ngv, intz;
   float scale_log2;
