@@ -493,7 +493,7 @@ kvq_status verify_warp_plan(const kvq_cache* c, const kvq::WarpArgs& a) {
 // append bookkeeping (KIVI Algorithm 1 over T pushed tokens)
 // ---------------------------------------------------------------------------
 kvq_status append_kivi(kvq_cache* c, const void* k_new, const void* v_new, int T,
-                       cudaStream_t st) {
+                       cudaStream_t st, bool pdl = false) {
   const int R = c->resid_cap, G = c->group;
   kvq_segment& last = c->seg[c->n_seg - 1];
   kvq::AppendArgs a{};
@@ -553,7 +553,7 @@ kvq_status append_kivi(kvq_cache* c, const void* k_new, const void* v_new, int T
   if (a.chunks == 2 && a.k_ring_groups == 0 && a.v_ring_tokens == 0 && a.k_first_ring >= T &&
       a.v_first_ring >= T)
     a.chunks = 1;
-  const cudaError_t e = kvq::launch_append(a, st);
+  const cudaError_t e = kvq::launch_append(a, st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
   // new lengths
   last.nk += fb * R;
@@ -688,9 +688,51 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* 
   return append_kivi(cache, k_new, v_new, T, as_stream(stream));
 }
 
+namespace {
+kvq_status flush_impl(kvq_cache* cache, cudaStream_t stream, bool pdl);
+kvq_status decode_attention_impl(const kvq_cache* cache, const void* q, void* out, void* ws, size_t ws_bytes,
+                                 cudaStream_t s, bool pdl);
+}  // namespace
+
 kvq_status kvq_flush_residual(kvq_cache* cache, void* stream) {
   kvq_status st = validate_cache(cache);
   if (st != KVQ_OK) return st;
+  return flush_impl(cache, as_stream(stream), false);
+}
+
+kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out, void* ws, size_t ws_bytes,
+                                void* stream) {
+  kvq_status st = validate_cache(cache);
+  if (st != KVQ_OK) return st;
+  return decode_attention_impl(cache, q, out, ws, ws_bytes, as_stream(stream), false);
+}
+
+kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_new, const void* q, void* out,
+                           void* ws, size_t ws_bytes, void* stream) {
+  kvq_status st = validate_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+    return fail(KVQ_ERR_INVALID_ARG, "k_new/v_new must be non-NULL and 16-byte aligned");
+  if (!q || !out || !aligned16(q) || !aligned16(out))
+    return fail(KVQ_ERR_INVALID_ARG, "q/out must be non-NULL and 16-byte aligned");
+  const int n_pairs = cache->batch * cache->h_kv;
+  if (!ws || !aligned16(ws) || ws_bytes < ws_fixed(n_pairs))
+    return fail(KVQ_ERR_WORKSPACE, "workspace needs at least %zu bytes", ws_fixed(n_pairs));
+  cudaStream_t s = as_stream(stream);
+  const kvq_cache before = *cache;
+  const kvq_status ap = append_kivi(cache, k_new, v_new, 1, s, true);
+  if (ap < 0) return ap;
+  st = decode_attention_impl(cache, q, out, ws, ws_bytes, s, true);
+  if (st != KVQ_OK) {
+    *cache = before;  // nothing of the step counts: the caller may retry it
+    return st;
+  }
+  if (ap == KVQ_FLUSH_DUE) return flush_impl(cache, s, true);
+  return KVQ_OK;
+}
+
+namespace {
+kvq_status flush_impl(kvq_cache* cache, cudaStream_t stream, bool pdl) {
   const int G = cache->group, R = cache->resid_cap;
   const int n = (cache->nkr / G) * G;
   if (n == 0) return KVQ_OK;
@@ -710,13 +752,15 @@ kvq_status kvq_flush_residual(kvq_cache* cache, void* stream) {
   a.k_groups = n / G;
   a.k_nk0 = last.nk;
   a.ksrc = {INT_MAX, cache->k_ring_start};
-  const cudaError_t e = kvq::launch_flush(a, as_stream(stream));
+  const cudaError_t e = kvq::launch_flush(a, stream, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "flush launch");
   last.nk += n;
   cache->nkr -= n;
   cache->k_ring_start = (cache->k_ring_start + n) % R;
   return KVQ_OK;
 }
+
+}  // namespace
 
 size_t kvq_workspace_bytes(const kvq_cache* cache, int32_t max_splits) {
   if (!cache || cache->batch < 1 || cache->h_kv < 1 || cache->h_q < cache->h_kv) return 0;
@@ -742,16 +786,16 @@ kvq_status kvq_workspace_error(const void* ws, int32_t* err_out, void* stream) {
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "reading the workspace error word");
 }
 
-kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out, void* ws,
-                                size_t ws_bytes, void* stream) {
-  kvq_status st = validate_cache(cache);
-  if (st != KVQ_OK) return st;
+namespace {
+kvq_status decode_attention_impl(const kvq_cache* cache, const void* q, void* out, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream, bool pdl) {
+  kvq_status st = KVQ_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out))
     return fail(KVQ_ERR_INVALID_ARG, "q/out must be non-NULL and 16-byte aligned");
   const int n_pairs = cache->batch * cache->h_kv;
   if (!ws || !aligned16(ws) || ws_bytes < ws_fixed(n_pairs))
     return fail(KVQ_ERR_WORKSPACE, "workspace needs at least %zu bytes", ws_fixed(n_pairs));
-  cudaStream_t s = as_stream(stream);
+  cudaStream_t s = stream;
   const int gq = cache->h_q / cache->h_kv;
   if (kUseWarpKernel && warp_kernel_applies(cache) && cache->seg[0].nk + cache->nkr > 0) {
     kvq::WarpArgs w{};
@@ -782,7 +826,7 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
       w.part = reinterpret_cast<float*>(wb + ws_fixed(n_pairs));
       st = verify_warp_plan(cache, w);
       if (st != KVQ_OK) return st;
-      const cudaError_t e = kvq::launch_decode_warp(w, s);
+      const cudaError_t e = kvq::launch_decode_warp(w, s, pdl);
       return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "decode launch");
     }
   }
@@ -889,6 +933,8 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
   if (e == cudaSuccess && kern == K_TC && a.tc_defer) e = kvq::launch_decode_tc_merge(a, n_pairs, s);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "decode launch");
 }
+
+}  // namespace
 
 size_t kvq_window_assign_workspace_bytes(int32_t batch, int32_t h_kv, int32_t d_h, int32_t M,
                                          int32_t S) {

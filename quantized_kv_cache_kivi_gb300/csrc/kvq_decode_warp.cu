@@ -579,11 +579,15 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
   const int c0 = warp_piece_start(a, piece), c1 = warp_piece_start(a, piece + 1);
   const int n = c1 - c0;  // chunks of this piece (at least one)
   const PairPtrs pp = pair_ptrs(a, pair);
-  const uint2 qv = __ldg(reinterpret_cast<const uint2*>(a.q + pair * D) + lane);
   if (lane == 0) {
     for (int s = 0; s < kWarpSlots; ++s) mbar_init(&bars[s], kSlotArrivals);
     mbar_fence_init();
   }
+  // inside a decode step: the append's writes first; then the step's K
+  // flush may start beside this grid (it touches nothing read here)
+  grid_dep_wait();
+  grid_dep_launch();
+  const uint2 qv = __ldg(reinterpret_cast<const uint2*>(a.q + pair * D) + lane);
   __syncwarp();
   for (int s = 0; s < kWarpSlots && s < n; ++s) stage_chunk<NGV>(a, pp, pair, c0 + s, slots + s * kWarpSlot, &bars[s], lane);
   reinterpret_cast<uint2*>(qsm)[lane] = qv;
@@ -640,18 +644,17 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
 }  // namespace
 
 template <int NGV, bool INTZ>
-static cudaError_t launch_warp_t(const WarpArgs& a, cudaStream_t s) {
+static cudaError_t launch_warp_t(const WarpArgs& a, cudaStream_t s, bool pdl) {
   const int bytes = WarpSmem::total;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_warp_kernel<NGV, INTZ>), bytes);
   if (e != cudaSuccess) return e;
-  decode_warp_kernel<NGV, INTZ><<<(unsigned)(a.P * a.k), 32, bytes, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(decode_warp_kernel<NGV, INTZ>, dim3((unsigned)(a.P * a.k)), dim3(32), (size_t)bytes, s, pdl, a);
 }
 
-cudaError_t launch_decode_warp(const WarpArgs& a, cudaStream_t s) {
-  if (a.ngv == 4) return a.intz ? launch_warp_t<4, true>(a, s) : launch_warp_t<4, false>(a, s);
-  if (a.ngv == 2) return a.intz ? launch_warp_t<2, true>(a, s) : launch_warp_t<2, false>(a, s);
-  return a.intz ? launch_warp_t<1, true>(a, s) : launch_warp_t<1, false>(a, s);
+cudaError_t launch_decode_warp(const WarpArgs& a, cudaStream_t s, bool pdl) {
+  if (a.ngv == 4) return a.intz ? launch_warp_t<4, true>(a, s, pdl) : launch_warp_t<4, false>(a, s, pdl);
+  if (a.ngv == 2) return a.intz ? launch_warp_t<2, true>(a, s, pdl) : launch_warp_t<2, false>(a, s, pdl);
+  return a.intz ? launch_warp_t<1, true>(a, s, pdl) : launch_warp_t<1, false>(a, s, pdl);
 }
 
 }  // namespace kvq

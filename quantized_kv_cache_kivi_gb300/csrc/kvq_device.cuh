@@ -230,6 +230,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their writes are visible (returns at once for a grid launched
+// without the attribute), and let the grid launched after this one start.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 16-byte asynchronous global -> shared copy cached in L2 only (cp.async.cg),
 // its group commit and the wait for all but the N most recent groups.
 __device__ __forceinline__ void cp16(uint32_t dst, const void* src) {

@@ -603,21 +603,41 @@ inline cudaError_t set_smem_once(const void* kernel, int bytes) {
   return e;
 }
 
+// Launch a kernel on stream s; with pdl, allowed to start before the previous
+// kernel of the stream completes (programmatic stream serialization): such a
+// kernel executes griddepcontrol.wait before it touches anything that kernel
+// writes.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // host helpers of kvq_api.cu used by other entry points
 int sm_count_cached();  // SMs of the current device, looked up once per device
 void set_last_error(const char* msg);
 kvq_status check_cache(const kvq_cache* c);
 
 // kernels' launchers (return cudaGetLastError())
-cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
-cudaError_t launch_flush(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_flush(const AppendArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_ingest(const IngestArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int n_pairs, cudaStream_t s);
 size_t decode_smem_bytes(int gq, int d);
 cudaError_t launch_decode_mha(const DecodeArgs& a, int n_pairs, int bits, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, int bits, int form, cudaStream_t s);
 cudaError_t launch_decode_tc_merge(const DecodeArgs& a, int n_pairs, cudaStream_t s);
-cudaError_t launch_decode_warp(const WarpArgs& a, cudaStream_t s);
+cudaError_t launch_decode_warp(const WarpArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_decode_paged(const PagedArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tc_paged(const DecodeArgs& a, const PagedArgs& p, int bits, int form, cudaStream_t s);
 cudaError_t launch_paged_append(const PagedAppendArgs& a, cudaStream_t s);

@@ -251,6 +251,9 @@ __global__ void __launch_bounds__(kQuantThreads) append_kernel(const AppendArgs 
   __half* ring_k = a.kr + pair * (size_t)a.R * D;
   __half* ring_v = a.vr + pair * (size_t)a.R * D;
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  // launched after a kernel of the same decode step: its writes first
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (chunk == 0) {
     // A few new tokens (a decode step) are read into registers first, so
@@ -309,8 +312,15 @@ __global__ void __launch_bounds__(kQuantThreads) flush_kernel(const AppendArgs a
   const size_t pair = blockIdx.x;
   const int gi = blockIdx.y;
   const __half* ring_k = a.kr + pair * (size_t)a.R * D;
+  // Inside a decode step this grid may start while the decode attention
+  // still runs: it reads ring slots and writes packed rows that the attention
+  // leaves alone, and the append it reads from completed before the
+  // attention let it start.  It completes only after the attention does
+  // (the wait at the end), so a kernel waiting on it waits on both.
+  grid_dep_launch();
   quant_k_group_any<D, Z>(a.dst, a.bits, a.G, a.R, pair, ring_k, nullptr, a.ksrc, gi * a.G,
                    a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
+  grid_dep_wait();
 }
 
 // WindowQuant ingest: block (pair, job); job n_jobs is the fp16 tail.
@@ -765,13 +775,13 @@ cudaError_t launch_bulk_b(const AppendArgs& a, cudaStream_t s) {
 }
 
 template <int D, int Z>
-cudaError_t launch_append_dz(const AppendArgs& a, cudaStream_t s) {
+cudaError_t launch_append_dz(const AppendArgs& a, cudaStream_t s, bool pdl) {
   dim3 grid(a.batch * a.h_kv, a.chunks);
   const size_t sm = quant_smem(a.G, a.d);
   cudaError_t e;
   if ((e = set_smem(append_kernel<D, Z>, sm)) != cudaSuccess) return e;
-  append_kernel<D, Z><<<grid, kQuantThreads, sm, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_kernel(append_kernel<D, Z>, grid, dim3(kQuantThreads), sm, s, pdl && !a.bulk, a)) != cudaSuccess)
+    return e;
   if (D == 128 && a.bulk) {
     if (a.bits == 2) return launch_bulk_b<2, Z>(a, s);
     if (a.bits == 4) return launch_bulk_b<4, Z>(a, s);
@@ -780,25 +790,24 @@ cudaError_t launch_append_dz(const AppendArgs& a, cudaStream_t s) {
   return cudaSuccess;
 }
 
-cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
-  if (a.d == 128) return a.dst.intz ? launch_append_dz<128, 1>(a, s) : launch_append_dz<128, 0>(a, s);
-  return a.dst.intz ? launch_append_dz<64, 1>(a, s) : launch_append_dz<64, 0>(a, s);
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, bool pdl) {
+  if (a.d == 128) return a.dst.intz ? launch_append_dz<128, 1>(a, s, pdl) : launch_append_dz<128, 0>(a, s, pdl);
+  return a.dst.intz ? launch_append_dz<64, 1>(a, s, pdl) : launch_append_dz<64, 0>(a, s, pdl);
 }
 
 template <int D, int Z>
-cudaError_t launch_flush_dz(const AppendArgs& a, cudaStream_t s) {
+cudaError_t launch_flush_dz(const AppendArgs& a, cudaStream_t s, bool pdl) {
   dim3 grid(a.batch * a.h_kv, a.k_groups);
   const size_t sm = quant_smem(a.G, a.d);
   cudaError_t e;
   if ((e = set_smem(flush_kernel<D, Z>, sm)) != cudaSuccess) return e;
-  flush_kernel<D, Z><<<grid, kQuantThreads, sm, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(flush_kernel<D, Z>, grid, dim3(kQuantThreads), sm, s, pdl, a);
 }
 
-cudaError_t launch_flush(const AppendArgs& a, cudaStream_t s) {
+cudaError_t launch_flush(const AppendArgs& a, cudaStream_t s, bool pdl) {
   if (a.k_groups <= 0) return cudaSuccess;
-  if (a.d == 128) return a.dst.intz ? launch_flush_dz<128, 1>(a, s) : launch_flush_dz<128, 0>(a, s);
-  return a.dst.intz ? launch_flush_dz<64, 1>(a, s) : launch_flush_dz<64, 0>(a, s);
+  if (a.d == 128) return a.dst.intz ? launch_flush_dz<128, 1>(a, s, pdl) : launch_flush_dz<128, 0>(a, s, pdl);
+  return a.dst.intz ? launch_flush_dz<64, 1>(a, s, pdl) : launch_flush_dz<64, 0>(a, s, pdl);
 }
 
 template <int D, int Z>

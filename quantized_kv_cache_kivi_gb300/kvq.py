@@ -96,6 +96,8 @@ def lib():
         L.kvq_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
         L.kvq_decode_attention.argtypes = [cp, _P, _P, _P, ctypes.c_size_t, _P]
         L.kvq_workspace_error.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
+        L.kvq_decode_step.argtypes = [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+        L.kvq_decode_step.restype = ctypes.c_int
         L.kvq_decode_attention_noalloc.argtypes = [cp, _P, _P, _P]
         L.kvq_decode_attention_noalloc.restype = ctypes.c_int
         L.kvq_noalloc_error.argtypes = [ctypes.POINTER(ctypes.c_int32), _P]
@@ -187,6 +189,13 @@ def kvq_decode_attention(cache, q, out, ws, stream=None):
     st = lib().kvq_decode_attention(ctypes.byref(cache.c), _ptr(q), _ptr(out), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream))
     return _check(st, "kvq_decode_attention")
+
+
+def kvq_decode_step(cache, k_new, v_new, q, out, ws, stream=None):
+    """Append one token per head, decode attention, and the K flush if due."""
+    st = lib().kvq_decode_step(ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream))
+    return _check(st, "kvq_decode_step")
 
 
 def kvq_decode_attention_noalloc(cache, q, out, stream=None):

@@ -547,3 +547,48 @@ def test_windowquant_workload_full_shape():
                               w["d"], w["G"], w["seed"], False, None, None, tail=0, heads={(0, 0), (0, 3)},
                               R=w["R"])
     assert err < TOL
+
+
+def test_decode_step_matches_separate_calls_and_oracle():
+    """kvq_decode_step (append, attention, the due K flush, chained with
+    programmatic dependent launch) against the three calls in order on a
+    second cache: identical outputs every step and identical buffers after
+    80 steps that cross a flush; against the oracle's Algorithm 1 decoding
+    (the flush after the attention) within tolerance."""
+    B, H, d, G, R = 2, 4, 128, 32, 64
+    a = KiviPair(B, H, H, d, G, R, 2, cap=1024)
+    b = KiviPair(B, H, H, d, G, R, 2, cap=1024, heads=[])
+    K, V = kv(81, B, H, 380, d)
+    a.prefill(K[:, :, :300], V[:, :, :300])
+    b.prefill(K[:, :, :300], V[:, :, :300])
+    ws_a, ws_b = a.workspace(), b.workspace()
+    flushes = 0
+    for t in range(300, 380):
+        q = _q(200 + t, B, H, d)
+        qd = to_dev(q)
+        out_a, out_b = torch.empty_like(qd), torch.empty_like(qd)
+        kt, vt = to_dev(K[:, :, t:t + 1]), to_dev(V[:, :, t:t + 1])
+        kvq.kvq_decode_step(a.gpu, kt, vt, qd, out_a, ws_a)
+        st = kvq.kvq_quantize_append(b.gpu, kt, vt)
+        kvq.kvq_decode_attention(b.gpu, qd, out_b, ws_b)
+        if st == kvq.KVQ_FLUSH_DUE:
+            kvq.kvq_flush_residual(b.gpu)
+            flushes += 1
+        torch.cuda.synchronize()
+        assert np.array_equal(out_a.cpu().numpy(), out_b.cpu().numpy()), t
+        for (bb, h), head in a.orc.items():
+            head.decode_update(K[bb, h, t], V[bb, h, t], flush_k=False)
+        if t % 16 == 0 or len(next(iter(a.orc.values())).kr) == R:
+            ref = a.oracle_attention(q)
+            got = out_a.cpu().numpy()
+            err = max(max_abs_rel(got[bb, h], ref[(bb, h)][0]) for (bb, h) in ref)
+            assert err < TOL, (t, err)
+        for head in a.orc.values():
+            if len(head.kr) == R:
+                head.flush_k(R)
+    assert flushes >= 1
+    assert kvq.kvq_workspace_error(ws_a) == 0
+    a.assert_buffers_bit_exact()
+    ga, gb = a.gpu_buffers(), b.gpu_buffers()
+    for name in ga:
+        assert np.array_equal(ga[name], gb[name]), name
