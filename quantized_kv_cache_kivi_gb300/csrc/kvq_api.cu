@@ -426,6 +426,7 @@ size_t ws_fixed(int n_pairs) {
 // ---------------------------------------------------------------------------
 constexpr bool kUseWarpKernel = true;
 
+
 bool warp_kernel_applies(const kvq_cache* c) {
   const int Gv = group_v(c);
   return c->h_q == c->h_kv && c->n_seg == 1 && c->d_h == 128 && c->seg[0].bits == 2 && c->group >= 32 &&
@@ -691,7 +692,8 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* 
 namespace {
 kvq_status flush_impl(kvq_cache* cache, cudaStream_t stream, bool pdl);
 kvq_status decode_attention_impl(const kvq_cache* cache, const void* q, void* out, void* ws, size_t ws_bytes,
-                                 cudaStream_t s, bool pdl);
+                                 cudaStream_t s, bool pdl, int dep_t0 = 0);
+void flush_bookkeeping(kvq_cache* cache, int n);
 }  // namespace
 
 kvq_status kvq_flush_residual(kvq_cache* cache, void* stream) {
@@ -722,7 +724,16 @@ kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_ne
   const kvq_cache before = *cache;
   const kvq_status ap = append_kivi(cache, k_new, v_new, 1, s, true);
   if (ap < 0) return ap;
-  st = decode_attention_impl(cache, q, out, ws, ws_bytes, s, true);
+  // first token position whose K or V the append wrote: the new token, and
+  // the rows it quantized (one segment; else every chunk waits)
+  int dep_t0 = 0;
+  if (cache->n_seg == 1) {
+    long long d = (long long)cache->seg[0].nk + cache->nkr - 1;
+    if (cache->seg[0].nk != before.seg[0].nk) d = std::min<long long>(d, before.seg[0].nk);
+    if (cache->seg[0].nv != before.seg[0].nv) d = std::min<long long>(d, before.seg[0].nv);
+    dep_t0 = (int)std::max(0LL, d);
+  }
+  st = decode_attention_impl(cache, q, out, ws, ws_bytes, s, true, dep_t0);
   if (st != KVQ_OK) {
     *cache = before;  // nothing of the step counts: the caller may retry it
     return st;
@@ -754,10 +765,15 @@ kvq_status flush_impl(kvq_cache* cache, cudaStream_t stream, bool pdl) {
   a.ksrc = {INT_MAX, cache->k_ring_start};
   const cudaError_t e = kvq::launch_flush(a, stream, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "flush launch");
-  last.nk += n;
-  cache->nkr -= n;
-  cache->k_ring_start = (cache->k_ring_start + n) % R;
+  flush_bookkeeping(cache, n);
   return KVQ_OK;
+}
+
+// n oldest K ring tokens now packed at the end of the last segment
+void flush_bookkeeping(kvq_cache* cache, int n) {
+  cache->seg[cache->n_seg - 1].nk += n;
+  cache->nkr -= n;
+  cache->k_ring_start = (cache->k_ring_start + n) % cache->resid_cap;
 }
 
 }  // namespace
@@ -788,7 +804,7 @@ kvq_status kvq_workspace_error(const void* ws, int32_t* err_out, void* stream) {
 
 namespace {
 kvq_status decode_attention_impl(const kvq_cache* cache, const void* q, void* out, void* ws, size_t ws_bytes,
-                                 cudaStream_t stream, bool pdl) {
+                                 cudaStream_t stream, bool pdl, int dep_t0) {
   kvq_status st = KVQ_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out))
     return fail(KVQ_ERR_INVALID_ARG, "q/out must be non-NULL and 16-byte aligned");
@@ -826,6 +842,21 @@ kvq_status decode_attention_impl(const kvq_cache* cache, const void* q, void* ou
       w.part = reinterpret_cast<float*>(wb + ws_fixed(n_pairs));
       st = verify_warp_plan(cache, w);
       if (st != KVQ_OK) return st;
+      // the first chunk that ends past dep_t0 (chunks run in token order)
+      int dc = 0;
+      if (dep_t0 > 0) {
+        if (dep_t0 < w.npp) {
+          dc = dep_t0 / 32;
+        } else {
+          dc = w.n_pp;
+          while (dc < w.C) {
+            const kvq::WarpChunk ch = kvq::warp_chunk(w, dc);
+            if (ch.t0 + ch.n > dep_t0) break;
+            ++dc;
+          }
+        }
+      }
+      w.dep_c = dc;
       const cudaError_t e = kvq::launch_decode_warp(w, s, pdl);
       return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "decode launch");
     }

@@ -583,13 +583,24 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
     for (int s = 0; s < kWarpSlots; ++s) mbar_init(&bars[s], kSlotArrivals);
     mbar_fence_init();
   }
-  // inside a decode step: the append's writes first; then the step's K
-  // flush may start beside this grid (it touches nothing read here)
-  grid_dep_wait();
+  // Inside a decode step this grid starts while the step's append runs.
+  // Chunks from a.dep_c on hold tokens the append writes (its evicted V row,
+  // the new ring token), so staging the first of them waits for the append
+  // grid; the chunks before it are packed rows that no kernel of the step
+  // writes, and the kernels before the append had completed before the
+  // append let this grid start.
+  bool waited = false;
+  auto stage = [&](int c, int s) {
+    if (!waited && c >= a.dep_c) {
+      grid_dep_wait();
+      waited = true;
+    }
+    stage_chunk<NGV>(a, pp, pair, c, slots + s * kWarpSlot, &bars[s], lane);
+  };
   grid_dep_launch();
   const uint2 qv = __ldg(reinterpret_cast<const uint2*>(a.q + pair * D) + lane);
   __syncwarp();
-  for (int s = 0; s < kWarpSlots && s < n; ++s) stage_chunk<NGV>(a, pp, pair, c0 + s, slots + s * kWarpSlot, &bars[s], lane);
+  for (int s = 0; s < kWarpSlots && s < n; ++s) stage(c0 + s, s);
   reinterpret_cast<uint2*>(qsm)[lane] = qv;
   __syncwarp();
   const LaneC L = lane_consts(lane);
@@ -633,7 +644,7 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
       else run_x<NGV, INTZ>(a, slot, ch, Q, L, reinterpret_cast<const uint8_t*>(qsm), tab, S);
     }
     __syncwarp();  // every lane has read the slot
-    if (k + kWarpSlots < n) stage_chunk<NGV>(a, pp, pair, c + kWarpSlots, slots + s * kWarpSlot, &bars[s], lane);
+    if (k + kWarpSlots < n) stage(c + kWarpSlots, s);
     if (++s == kWarpSlots) s = 0, ph ^= 1u;
   }
   int ticket = 0;

@@ -306,6 +306,9 @@ struct WarpArgs {
   int n_pp, n_x1, n_x2, C;  // chunks per pair
   long long Cp;             // cost of a pair (kWarpWpp, kWarpWx)
   int P, k;                 // pairs, warps per pair (pieces; records when k > 1)
+  // first chunk holding a token that the decode step's append wrote (its
+  // staging waits for the append grid); 0 outside a decode step
+  int dep_c;
 };
 
 struct WarpChunk {
@@ -598,6 +601,16 @@ inline cudaError_t set_smem_once(const void* kernel, int bytes) {
   std::lock_guard<std::mutex> lock(mu);
   const auto it = raised.find(key);
   if (it != raised.end() && it->second >= bytes) return cudaSuccess;
+  if (it == raised.end()) {
+    // Every kernel of the library asks for the largest shared-memory
+    // carveout: an SM runs CTAs of two kernels side by side only under one
+    // L1/shared split, so a small quantize kernel with a small carveout would
+    // keep the decode kernel (which needs most of the SM's shared memory)
+    // off the SM until it drains, and a dependent launch could not overlap.
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) raised[key] = bytes;
   return e;

@@ -549,22 +549,33 @@ def test_windowquant_workload_full_shape():
     assert err < TOL
 
 
-def test_decode_step_matches_separate_calls_and_oracle():
-    """kvq_decode_step (append, attention, the due K flush, chained with
-    programmatic dependent launch) against the three calls in order on a
-    second cache: identical outputs every step and identical buffers after
-    80 steps that cross a flush; against the oracle's Algorithm 1 decoding
-    (the flush after the attention) within tolerance."""
-    B, H, d, G, R = 2, 4, 128, 32, 64
-    a = KiviPair(B, H, H, d, G, R, 2, cap=1024)
-    b = KiviPair(B, H, H, d, G, R, 2, cap=1024, heads=[])
+@pytest.mark.parametrize("G,zp,gq,offset", [
+    (32, kvq.KVQ_ZERO_MIN, 1, False),   # one query head per kv head: the warp kernel
+    (64, kvq.KVQ_ZERO_INT, 1, True),    # the same, 64-token groups, integer zero, offset K channels
+    (32, kvq.KVQ_ZERO_MIN, 2, False),   # two query heads per kv head: the tensor-core kernel
+])
+def test_decode_step_matches_separate_calls_and_oracle(G, zp, gq, offset):
+    """kvq_decode_step (append, attention and the due K flush, chained with
+    programmatic dependent launch; the attention's chunks that hold no token
+    the append writes start before the append completes) against the three
+    calls in order on a second cache: identical outputs
+    every step and identical buffers after 80 steps that cross a flush;
+    against the oracle's Algorithm 1 decoding (the flush after the
+    attention) within tolerance."""
+    B, H, d, R = 2, 4, 128, 64
+    Hq = H * gq
+    a = KiviPair(B, H, Hq, d, G, R, 2, cap=1024, zero_point=zp)
+    b = KiviPair(B, H, Hq, d, G, R, 2, cap=1024, heads=[], zero_point=zp)
     K, V = kv(81, B, H, 380, d)
+    if offset:  # K channels far from zero with a narrow range (outlier channels)
+        K = (K.astype(np.float32) * np.float32(0.25)
+             + np.linspace(-100, 100, d, dtype=np.float32)).astype(np.float16)
     a.prefill(K[:, :, :300], V[:, :, :300])
     b.prefill(K[:, :, :300], V[:, :, :300])
     ws_a, ws_b = a.workspace(), b.workspace()
     flushes = 0
     for t in range(300, 380):
-        q = _q(200 + t, B, H, d)
+        q = _q(200 + t, B, Hq, d)
         qd = to_dev(q)
         out_a, out_b = torch.empty_like(qd), torch.empty_like(qd)
         kt, vt = to_dev(K[:, :, t:t + 1]), to_dev(V[:, :, t:t + 1])
@@ -581,7 +592,8 @@ def test_decode_step_matches_separate_calls_and_oracle():
         if t % 16 == 0 or len(next(iter(a.orc.values())).kr) == R:
             ref = a.oracle_attention(q)
             got = out_a.cpu().numpy()
-            err = max(max_abs_rel(got[bb, h], ref[(bb, h)][0]) for (bb, h) in ref)
+            err = max(max_abs_rel(got[bb, h * gq + j], ref[(bb, h)][j]) for (bb, h) in ref
+                      for j in range(gq))
             assert err < TOL, (t, err)
         for head in a.orc.values():
             if len(head.kr) == R:
