@@ -536,31 +536,51 @@ __device__ int write_piece(const WarpArgs& a, long long pair, int piece, int lan
 }
 
 // The piece that found nrec - 1 (the last of the pair to arrive) merges the
-// pair's records and writes the output.
+// pair's records and writes the output.  Records are taken 16 at a time with
+// every load of a block (o of 16 records, m and l in lanes 0..15) in flight
+// together; the running maximum rescales the sums of earlier blocks.
 __device__ __noinline__ void merge_if_last(const WarpArgs& a, long long pair, int nrec, int ticket, int lane) {
   if (!__shfl_sync(kFull, ticket == nrec - 1 ? 1 : 0, 0)) return;
   fence_acq_rel_gpu();  // the other records are visible after their counts
   const float* recs = a.part + pair * a.k * kRec;
-  float m = -INFINITY;
-  for (int s = lane; s < nrec; s += 32) m = fmaxf(m, __ldcg(recs + s * kRec + D));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-  float ls = 0.f;
-  for (int s = lane; s < nrec; s += 32)
-    if (m != -INFINITY) ls += __ldcg(recs + s * kRec + D + 1) * exp2f(__ldcg(recs + s * kRec + D) - m);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(kFull, ls, off);
-  const float il = ls > 0.f ? 1.f / ls : 0.f;
+  constexpr int kBlk = 16;
+  float m = -INFINITY, ls = 0.f;
   float oo[D / 32] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-  for (int s = 0; s < nrec; ++s) {
-    const float* rr = recs + s * kRec;
-    const float w = m == -INFINITY ? 0.f : exp2f(__ldcg(rr + D) - m) * il;
+  for (int s0 = 0; s0 < nrec; s0 += kBlk) {
+    const int nb = nrec - s0 < kBlk ? nrec - s0 : kBlk;
+    float ov[kBlk][D / 32];
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) oo[i] += __ldcg(rr + lane + 32 * i) * w;
+    for (int j = 0; j < kBlk; ++j)
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) ov[j][i] = j < nb ? __ldcg(recs + (s0 + j) * kRec + lane + 32 * i) : 0.f;
+    float mj = -INFINITY, lj = 0.f;
+    if (lane < nb) {
+      mj = __ldcg(recs + (s0 + lane) * kRec + D);
+      lj = __ldcg(recs + (s0 + lane) * kRec + D + 1);
+    }
+    float mb = mj;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
+    const float mn = fmaxf(m, mb);
+    const float sc = m == -INFINITY ? 0.f : exp2f(m - mn);
+    const float wj = mj == -INFINITY ? 0.f : exp2f(mj - mn);
+    float lw = lj * wj;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(kFull, lw, off);
+    ls = ls * sc + lw;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) oo[i] *= sc;
+#pragma unroll
+    for (int j = 0; j < kBlk; ++j) {
+      const float w = __shfl_sync(kFull, wj, j);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) oo[i] = fmaf(ov[j][i], w, oo[i]);
+    }
+    m = mn;
   }
+  const float il = ls > 0.f ? 1.f / ls : 0.f;
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) a.out[pair * D + lane + 32 * i] = __float2half_rn(oo[i]);
+  for (int i = 0; i < D / 32; ++i) a.out[pair * D + lane + 32 * i] = __float2half_rn(oo[i] * il);
   if (lane == 0) a.counters[pair] = 0;  // ready for the next call on this workspace
 }
 
@@ -570,8 +590,21 @@ template <int NGV, bool INTZ>
 __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x;
-  const long long pair = blockIdx.x / a.k;
-  const int piece = (int)(blockIdx.x - pair * a.k);
+  // CTAs [0, P kb): the large pieces of every pair (one wave); then the
+  // small pieces, which take the SMs' slots as the large ones finish
+  long long pair;
+  int piece;
+  {
+    const long long b = blockIdx.x, nb = (long long)a.P * a.kb;
+    if (b < nb) {
+      pair = b / a.kb;
+      piece = (int)(b - pair * a.kb);
+    } else {
+      const int ks = a.k - a.kb;
+      pair = (b - nb) / ks;
+      piece = a.kb + (int)(b - nb - pair * ks);
+    }
+  }
   uint8_t* slots = smem + WarpSmem::slots;
   uint8_t* tab = smem + WarpSmem::ktab;
   __half* qsm = reinterpret_cast<__half*>(smem + WarpSmem::qbuf);
