@@ -425,14 +425,6 @@ size_t ws_fixed(int n_pairs) {
 // the warp kernel (one query head per kv head, one 2-bit segment, d_h 128)
 // ---------------------------------------------------------------------------
 constexpr bool kUseWarpKernel = true;
-#ifndef KVQ_WARP_SMALL
-#define KVQ_WARP_SMALL 0
-#endif
-#ifndef KVQ_WARP_BIG_FRAC
-#define KVQ_WARP_BIG_FRAC 48
-#endif
-constexpr int kWarpSmall = KVQ_WARP_SMALL;       // small pieces per pair after the first wave
-constexpr int kWarpBigFrac = KVQ_WARP_BIG_FRAC;  // 64ths of a pair's cost in its first-wave pieces
 
 
 bool warp_kernel_applies(const kvq_cache* c) {
@@ -462,20 +454,8 @@ bool plan_warp(const kvq_cache* c, kvq::WarpArgs& a, size_t ws_bytes) {
   const size_t room = ws_bytes > ws_fixed(P) ? ws_bytes - ws_fixed(P) : 0;
   k = std::min<long long>(k, (long long)(room / ((size_t)P * (128 + 2) * sizeof(float))));
   if (k < 1) k = 1;  // one warp per pair writes its output directly: no records
-  // Small pieces after the first wave: the last part of each pair's cost
-  // cut finer, so the SMs whose warps finish early take more of the work.
-  long long ks = 0, Cb = a.Cp;
-  if (kWarpSmall > 0 && k > 1) {
-    const long long wmax = std::max(kvq::kWarpWpp, kvq::kWarpWx);
-    Cb = a.Cp * kWarpBigFrac / 64;
-    ks = std::min<long long>((long long)kWarpSmall, (a.Cp - Cb) / wmax);
-    ks = std::min<long long>(ks, (long long)(room / ((size_t)P * (128 + 2) * sizeof(float))) - k);
-    if (ks <= 0 || Cb / wmax < k) ks = 0, Cb = a.Cp;  // every piece keeps at least one chunk
-  }
-  if ((long long)P * (k + ks) >= (1LL << 31)) return false;
-  a.kb = (int)k;
-  a.k = (int)(k + ks);
-  a.Cb = Cb;
+  if ((long long)P * k >= (1LL << 31)) return false;
+  a.k = (int)k;
   return true;
 }
 

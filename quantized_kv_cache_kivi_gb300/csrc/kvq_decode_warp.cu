@@ -590,21 +590,8 @@ template <int NGV, bool INTZ>
 __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x;
-  // CTAs [0, P kb): the large pieces of every pair (one wave); then the
-  // small pieces, which take the SMs' slots as the large ones finish
-  long long pair;
-  int piece;
-  {
-    const long long b = blockIdx.x, nb = (long long)a.P * a.kb;
-    if (b < nb) {
-      pair = b / a.kb;
-      piece = (int)(b - pair * a.kb);
-    } else {
-      const int ks = a.k - a.kb;
-      pair = (b - nb) / ks;
-      piece = a.kb + (int)(b - nb - pair * ks);
-    }
-  }
+  const long long pair = blockIdx.x / a.k;
+  const int piece = (int)(blockIdx.x - pair * a.k);
   uint8_t* slots = smem + WarpSmem::slots;
   uint8_t* tab = smem + WarpSmem::ktab;
   __half* qsm = reinterpret_cast<__half*>(smem + WarpSmem::qbuf);

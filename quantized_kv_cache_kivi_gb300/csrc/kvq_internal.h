@@ -306,8 +306,6 @@ struct WarpArgs {
   int n_pp, n_x1, n_x2, C;  // chunks per pair
   long long Cp;             // cost of a pair (kWarpWpp, kWarpWx)
   int P, k;                 // pairs, pieces per pair (records when k > 1)
-  int kb;                   // the first kb pieces share the first Cb of the cost, the rest the remainder
-  long long Cb;
   // first chunk holding a token that the decode step's append wrote (its
   // staging waits for the append grid); 0 outside a decode step
   int dep_c;
@@ -352,12 +350,10 @@ __host__ __device__ inline WarpChunk warp_chunk(const WarpArgs& a, int c) {
 #endif
 constexpr int kWarpWpp = KVQ_WARP_WPP, kWarpWx = KVQ_WARP_WX;
 
-// First chunk of piece j of a pair (j = k gives C): pieces 0..kb-1 cut the
-// first Cb of the pair's cost into equal parts and pieces kb..k-1 the rest;
-// piece j starts at the first chunk whose cost offset reaches its share.
+// First chunk of piece j of a pair cut into `k` pieces of equal cost (j = k
+// gives C): the first chunk whose cost offset reaches floor(Cp * j / k).
 __host__ __device__ inline int warp_piece_start(const WarpArgs& a, int j) {
-  const long long r = j <= a.kb ? a.Cb * (long long)j / a.kb
-                                : a.Cb + (a.Cp - a.Cb) * (long long)(j - a.kb) / (a.k - a.kb);
+  const long long r = a.Cp * (long long)j / a.k;
   const long long pp_cost = (long long)kWarpWpp * a.n_pp;
   const long long c = r <= pp_cost ? (r + kWarpWpp - 1) / kWarpWpp : a.n_pp + (r - pp_cost + kWarpWx - 1) / kWarpWx;
   return (int)(c < a.C ? c : a.C);
