@@ -219,6 +219,21 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q,
 kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_new, const void* q,
                            void* out, void* workspace, size_t ws_bytes, void* stream);
 
+/* kvq_decode_step fed from host memory: the step's inputs are copied from
+ * host_in to dev_in, the step runs on them, and its output is copied from
+ * dev_out to host_out, all enqueued on `stream` (asynchronous: synchronize
+ * the stream before reading host_out).
+ *   host_in, dev_in  fp16 [new K: batch*h_kv*d_h | new V: batch*h_kv*d_h |
+ *                    q: batch*h_q*d_h], contiguous (the K and V parts in the
+ *                    [batch][h_kv][1][d_h] layout of kvq_decode_step)
+ *   host_out         fp16 [batch][h_q][d_h]; dev_out device, the same shape
+ * Host buffers should be page-locked for the copies to be asynchronous;
+ * device buffers 16-byte aligned.  workspace, ws_bytes: as for
+ * kvq_decode_step.  Returns what kvq_decode_step returns, or
+ * KVQ_ERR_INVALID_ARG / KVQ_ERR_CUDA for the arguments and the copies. */
+kvq_status kvq_decode_step_host(kvq_cache* cache, const void* host_in, void* host_out, void* dev_in,
+                                void* dev_out, void* workspace, size_t ws_bytes, void* stream);
+
 /* Device error word of a workspace (0 = none; nonzero = a bounded wait timed
  * out inside a kernel).  Synchronizes `stream`. */
 kvq_status kvq_workspace_error(const void* workspace, int32_t* err_out,

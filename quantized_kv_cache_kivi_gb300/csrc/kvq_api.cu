@@ -459,8 +459,10 @@ bool plan_warp(const kvq_cache* c, kvq::WarpArgs& a, size_t ws_bytes) {
   return true;
 }
 
-// Every bulk copy of every chunk, walked for the first and the last pair
-// against its buffer (in bounds, 16-byte aligned, inside the slot).
+// Every bulk copy of the chunks of the first and the last pair, walked
+// against its buffer (in bounds, 16-byte aligned, inside the slot).  The
+// full packed chunks' copies are a fixed size at addresses affine in the
+// chunk index, so the first and the last of them bound the rest.
 kvq_status verify_warp_plan(const kvq_cache* c, const kvq::WarpArgs& a) {
   const int P = a.P, G = c->group;
   const size_t rows = (size_t)P * a.cap;
@@ -469,8 +471,10 @@ kvq_status verify_warp_plan(const kvq_cache* c, const kvq::WarpArgs& a) {
   const size_t ext[8] = {rows * 32, (size_t)P * (a.cap / G) * 256, (size_t)P * (a.cap / G) * 256, rows * 32,
                          rows * a.ngv * 2, rows * a.ngv * 2, (size_t)P * a.R * 256, (size_t)P * a.R * 256};
   const long long pairs[2] = {0, P - 1};
+  const int n_full = a.npp / 32;  // full packed chunks: copies affine in the chunk index
   for (long long pair : pairs) {
     for (int ci = 0; ci < a.C; ++ci) {
+      if (ci > 0 && ci < n_full - 1) continue;  // between the first and the last full chunk
       const kvq::WarpChunk ch = kvq::warp_chunk(a, ci);
       if (ch.n < 1 || ch.n > (ch.pp ? 32 : 8) || ch.o0 < 0 || ch.o0 + ch.n > (ch.pp ? 32 : 8))
         return fail(KVQ_ERR_UNSUPPORTED, "warp plan: chunk %d has a bad token range", ci);
@@ -740,6 +744,27 @@ kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_ne
   }
   if (ap == KVQ_FLUSH_DUE) return flush_impl(cache, s, true);
   return KVQ_OK;
+}
+
+kvq_status kvq_decode_step_host(kvq_cache* cache, const void* host_in, void* host_out, void* dev_in,
+                                void* dev_out, void* ws, size_t ws_bytes, void* stream) {
+  kvq_status st = validate_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!host_in || !host_out || !dev_in || !dev_out)
+    return fail(KVQ_ERR_INVALID_ARG, "host_in, host_out, dev_in and dev_out must be non-NULL");
+  if (!aligned16(dev_in) || !aligned16(dev_out))
+    return fail(KVQ_ERR_INVALID_ARG, "dev_in/dev_out must be 16-byte aligned");
+  const size_t kv = (size_t)cache->batch * cache->h_kv * cache->d_h * sizeof(__half);  // new K (= new V)
+  const size_t qb = (size_t)cache->batch * cache->h_q * cache->d_h * sizeof(__half);
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = cudaMemcpyAsync(dev_in, host_in, 2 * kv + qb, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "input copy");
+  uint8_t* d = static_cast<uint8_t*>(dev_in);
+  st = kvq_decode_step(cache, d, d + kv, d + 2 * kv, dev_out, ws, ws_bytes, stream);
+  if (st < 0) return st;
+  e = cudaMemcpyAsync(host_out, dev_out, qb, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "output copy");
+  return st;
 }
 
 namespace {

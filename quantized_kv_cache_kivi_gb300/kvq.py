@@ -98,6 +98,8 @@ def lib():
         L.kvq_workspace_error.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
         L.kvq_decode_step.argtypes = [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
         L.kvq_decode_step.restype = ctypes.c_int
+        L.kvq_decode_step_host.argtypes = [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+        L.kvq_decode_step_host.restype = ctypes.c_int
         L.kvq_decode_attention_noalloc.argtypes = [cp, _P, _P, _P]
         L.kvq_decode_attention_noalloc.restype = ctypes.c_int
         L.kvq_noalloc_error.argtypes = [ctypes.POINTER(ctypes.c_int32), _P]
@@ -196,6 +198,14 @@ def kvq_decode_step(cache, k_new, v_new, q, out, ws, stream=None):
     st = lib().kvq_decode_step(ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out), _ptr(ws),
                                ws.numel() * ws.element_size(), _stream(stream))
     return _check(st, "kvq_decode_step")
+
+
+def kvq_decode_step_host(cache, host_in, host_out, dev_in, dev_out, ws, stream=None):
+    """kvq_decode_step with its inputs copied from host memory and its output
+    copied back (host_in / dev_in: [new K | new V | q] fp16)."""
+    st = lib().kvq_decode_step_host(ctypes.byref(cache.c), _ptr(host_in), _ptr(host_out), _ptr(dev_in),
+                                    _ptr(dev_out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    return _check(st, "kvq_decode_step_host")
 
 
 def kvq_decode_attention_noalloc(cache, q, out, stream=None):

@@ -604,3 +604,38 @@ def test_decode_step_matches_separate_calls_and_oracle(G, zp, gq, offset):
     ga, gb = a.gpu_buffers(), b.gpu_buffers()
     for name in ga:
         assert np.array_equal(ga[name], gb[name]), name
+
+
+def test_decode_step_host_matches_device_step():
+    """kvq_decode_step_host (the step's inputs copied from page-locked host
+    memory, its output copied back, all on the stream) against
+    kvq_decode_step on a twin cache: identical outputs every step (new
+    inputs each step, so a copy racing the kernels would show) and identical
+    buffers after 40 steps that cross a flush."""
+    B, H, d, G, R = 2, 4, 128, 32, 64
+    a = KiviPair(B, H, H, d, G, R, 2, cap=1024, heads=[])
+    b = KiviPair(B, H, H, d, G, R, 2, cap=1024, heads=[])
+    K, V = kv(83, B, H, 340, d)
+    a.prefill(K[:, :, :300], V[:, :, :300])
+    b.prefill(K[:, :, :300], V[:, :, :300])
+    ws_a, ws_b = a.workspace(), b.workspace()
+    n_kv, n_q = B * H * d, B * H * d
+    h_in = torch.empty(2 * n_kv + n_q, dtype=torch.float16).pin_memory()
+    h_out = torch.empty(B, H, d, dtype=torch.float16).pin_memory()
+    d_in = torch.empty(2 * n_kv + n_q, dtype=torch.float16, device="cuda")
+    d_out = torch.empty(B, H, d, dtype=torch.float16, device="cuda")
+    for t in range(300, 340):
+        q = _q(500 + t, B, H, d)
+        h_in[:n_kv] = torch.from_numpy(np.ascontiguousarray(K[:, :, t]).reshape(-1))
+        h_in[n_kv:2 * n_kv] = torch.from_numpy(np.ascontiguousarray(V[:, :, t]).reshape(-1))
+        h_in[2 * n_kv:] = torch.from_numpy(np.ascontiguousarray(q).reshape(-1))
+        kvq.kvq_decode_step_host(a.gpu, h_in, h_out, d_in, d_out, ws_a)
+        torch.cuda.current_stream().synchronize()
+        out_b = torch.empty_like(d_out)
+        kvq.kvq_decode_step(b.gpu, to_dev(K[:, :, t:t + 1]), to_dev(V[:, :, t:t + 1]), to_dev(q), out_b, ws_b)
+        torch.cuda.synchronize()
+        assert np.array_equal(h_out.numpy(), out_b.cpu().numpy()), t
+    assert kvq.kvq_workspace_error(ws_a) == 0
+    ga, gb = a.gpu_buffers(), b.gpu_buffers()
+    for name in ga:
+        assert np.array_equal(ga[name], gb[name]), name
