@@ -1230,6 +1230,9 @@ __global__ void __launch_bounds__(TcCfg<HQ>::NTH, kTcCtasPerSm)
     mbar_fence_init();
   }
   if (tid < 16) reinterpret_cast<uint32_t*>(smem + SM::zero)[tid] = 0u;
+  // a record merge launched after this grid may start launching now (it
+  // waits for this grid's completion before reading the records)
+  grid_dep_launch();
   if (tid < NSLOT) {
     reinterpret_cast<int*>(smem + SM::slot_owner)[tid] = tid;
     reinterpret_cast<int*>(smem + SM::slot_count)[tid] = 0;
@@ -1441,6 +1444,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_tc_kernel(const DecodeArg
   __shared__ float part[kMergeThreads / D][D];
   const int pair = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nh = a.gq;
+  grid_dep_wait();  // launched as a dependent of the decode grid: its records first
   const long long nt = a.n_tiles;
   const int first = tc_owner(a.tc_bound, a.n_cta, (long long)pair * nt);
   const int last = tc_owner(a.tc_bound, a.n_cta, (long long)pair * nt + nt - 1);
@@ -1489,8 +1493,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_tc_kernel(const DecodeArg
 }  // namespace
 
 cudaError_t launch_decode_tc_merge(const DecodeArgs& a, int n_pairs, cudaStream_t s) {
-  merge_tc_kernel<<<dim3(n_pairs, a.gq), kMergeThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(merge_tc_kernel, dim3(n_pairs, a.gq), dim3(kMergeThreads), 0, s, true, a);
 }
 
 int decode_tc_ctas_per_sm() { return kTcCtasPerSm; }
