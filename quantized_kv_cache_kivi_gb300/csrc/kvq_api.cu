@@ -425,6 +425,10 @@ size_t ws_fixed(int n_pairs) {
 // the warp kernel (one query head per kv head, one 2-bit segment, d_h 128)
 // ---------------------------------------------------------------------------
 constexpr bool kUseWarpKernel = true;
+#ifndef KVQ_WARP_FILL
+#define KVQ_WARP_FILL 1
+#endif
+constexpr bool kWarpFill = KVQ_WARP_FILL;  // pieces per pair that fill every warp slot
 
 
 bool warp_kernel_applies(const kvq_cache* c) {
@@ -449,13 +453,24 @@ bool plan_warp(const kvq_cache* c, kvq::WarpArgs& a, size_t ws_bytes) {
   a.C = a.n_pp + a.n_x1 + a.n_x2;
   a.Cp = (long long)kvq::kWarpWpp * a.n_pp + (long long)kvq::kWarpWx * (a.n_x1 + a.n_x2);
   a.P = P;
-  long long k = (long long)sm_count() * kvq::kWarpWarps / P;
-  k = std::min<long long>(k, a.Cp / std::max(kvq::kWarpWpp, kvq::kWarpWx));
+  const long long slots = (long long)sm_count() * kvq::kWarpWarps;
+  const long long kcost = a.Cp / std::max(kvq::kWarpWpp, kvq::kWarpWx);  // every piece keeps a chunk
   const size_t room = ws_bytes > ws_fixed(P) ? ws_bytes - ws_fixed(P) : 0;
-  k = std::min<long long>(k, (long long)(room / ((size_t)P * (128 + 2) * sizeof(float))));
-  if (k < 1) k = 1;  // one warp per pair writes its output directly: no records
+  const long long krec = (long long)(room / ((size_t)P * (128 + 2) * sizeof(float)));
+  // Every slot of the GPU filled: P1 pairs get k pieces and the rest k - 1,
+  // so that no SM holds a warp more than the others; else k pieces a pair.
+  const long long k_hi = (slots + P - 1) / P;
+  long long k, P1 = P;
+  if (kWarpFill && k_hi >= 2 && k_hi <= kcost && k_hi <= krec) {
+    k = k_hi;
+    P1 = slots - (long long)P * (k_hi - 1);
+  } else {
+    k = std::min(std::min(slots / P, kcost), krec);
+    if (k < 1) k = 1;  // one warp per pair writes its output directly: no records
+  }
   if ((long long)P * k >= (1LL << 31)) return false;
   a.k = (int)k;
+  a.P1 = (int)P1;
   return true;
 }
 

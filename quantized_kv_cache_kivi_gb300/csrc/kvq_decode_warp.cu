@@ -489,14 +489,14 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 // or the output itself when the pair has one piece.  Returns the pair's
 // number of records (1: output written).
 template <int NGV>
-__device__ int write_piece(const WarpArgs& a, long long pair, int piece, int lane, const LaneC& L, WState& S,
-                           int& ticket) {
+__device__ int write_piece(const WarpArgs& a, long long pair, int piece, int kp, int lane, const LaneC& L,
+                           WState& S, int& ticket) {
   if (!S.vring) unscale_acc2(S);
   float l = S.l;  // sum over the lanes of one tig (rows gid)
   l += __shfl_xor_sync(kFull, l, 4);
   l += __shfl_xor_sync(kFull, l, 8);
   l += __shfl_xor_sync(kFull, l, 16);
-  const int nrec = a.k;
+  const int nrec = kp;
   // o of channel c: column g(c) of its row (lanes tig = g / 2) plus the z sum
   // of group g (column 4 + g, lanes tig = 2 + g / 2)
   float o16[16];
@@ -590,13 +590,21 @@ template <int NGV, bool INTZ>
 __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x;
-  const long long pair = blockIdx.x / a.k;
-  const int piece = (int)(blockIdx.x - pair * a.k);
+  // CTAs [0, P1 k): pairs with k pieces; then pairs with k - 1
+  long long pair;
+  int piece, kp;
+  {
+    const long long b = blockIdx.x, n1 = (long long)a.P1 * a.k;
+    kp = b < n1 ? a.k : a.k - 1;
+    const long long p0 = b < n1 ? 0 : a.P1, b0 = b < n1 ? 0 : n1;
+    pair = p0 + (b - b0) / kp;
+    piece = (int)((b - b0) % kp);
+  }
   uint8_t* slots = smem + WarpSmem::slots;
   uint8_t* tab = smem + WarpSmem::ktab;
   __half* qsm = reinterpret_cast<__half*>(smem + WarpSmem::qbuf);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + WarpSmem::bars);
-  const int c0 = warp_piece_start(a, piece), c1 = warp_piece_start(a, piece + 1);
+  const int c0 = warp_piece_start(a, kp, piece), c1 = warp_piece_start(a, kp, piece + 1);
   const int n = c1 - c0;  // chunks of this piece (at least one)
   const PairPtrs pp = pair_ptrs(a, pair);
   if (lane == 0) {
@@ -668,7 +676,7 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
     if (++s == kWarpSlots) s = 0, ph ^= 1u;
   }
   int ticket = 0;
-  const int nrec = write_piece<NGV>(a, pair, piece, lane, L, S, ticket);
+  const int nrec = write_piece<NGV>(a, pair, piece, kp, lane, L, S, ticket);
   if (nrec > 1) merge_if_last(a, pair, nrec, ticket, lane);
 }
 
@@ -679,7 +687,8 @@ static cudaError_t launch_warp_t(const WarpArgs& a, cudaStream_t s, bool pdl) {
   const int bytes = WarpSmem::total;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_warp_kernel<NGV, INTZ>), bytes);
   if (e != cudaSuccess) return e;
-  return launch_kernel(decode_warp_kernel<NGV, INTZ>, dim3((unsigned)(a.P * a.k)), dim3(32), (size_t)bytes, s, pdl, a);
+  const long long grid = (long long)a.P1 * a.k + (long long)(a.P - a.P1) * (a.k - 1);
+  return launch_kernel(decode_warp_kernel<NGV, INTZ>, dim3((unsigned)grid), dim3(32), (size_t)bytes, s, pdl, a);
 }
 
 cudaError_t launch_decode_warp(const WarpArgs& a, cudaStream_t s, bool pdl) {

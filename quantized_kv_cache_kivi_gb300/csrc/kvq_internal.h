@@ -306,6 +306,7 @@ struct WarpArgs {
   int n_pp, n_x1, n_x2, C;  // chunks per pair
   long long Cp;             // cost of a pair (kWarpWpp, kWarpWx)
   int P, k;                 // pairs, pieces per pair (records when k > 1)
+  int P1;                   // pairs [0, P1) have k pieces, pairs [P1, P) k - 1
   // first chunk holding a token that the decode step's append wrote (its
   // staging waits for the append grid); 0 outside a decode step
   int dep_c;
@@ -350,10 +351,10 @@ __host__ __device__ inline WarpChunk warp_chunk(const WarpArgs& a, int c) {
 #endif
 constexpr int kWarpWpp = KVQ_WARP_WPP, kWarpWx = KVQ_WARP_WX;
 
-// First chunk of piece j of a pair cut into `k` pieces of equal cost (j = k
-// gives C): the first chunk whose cost offset reaches floor(Cp * j / k).
-__host__ __device__ inline int warp_piece_start(const WarpArgs& a, int j) {
-  const long long r = a.Cp * (long long)j / a.k;
+// First chunk of piece j of a pair cut into `kp` pieces of equal cost (j =
+// kp gives C): the first chunk whose cost offset reaches floor(Cp * j / kp).
+__host__ __device__ inline int warp_piece_start(const WarpArgs& a, int kp, int j) {
+  const long long r = a.Cp * (long long)j / kp;
   const long long pp_cost = (long long)kWarpWpp * a.n_pp;
   const long long c = r <= pp_cost ? (r + kWarpWpp - 1) / kWarpWpp : a.n_pp + (r - pp_cost + kWarpWx - 1) / kWarpWx;
   return (int)(c < a.C ? c : a.C);
