@@ -1435,24 +1435,48 @@ cudaError_t launch_tc_hq(const DecodeArgs& a, int bits, cudaStream_t s, const PA
 // block (pair, head) of 4 x 128 threads.  The records' weights
 // 2^(m_s - M) / L first (threads over records), then channel c = thread % 128
 // summed over a quarter of the records by each of the 4 thread groups.
-constexpr int kMergeThreads = 512;
+constexpr int kMergeThreads = 1024;
+constexpr int kMergeGroups = kMergeThreads / D;  // record groups: thread (k, c) sums records k, k + 8, ...
+constexpr int kMergeRegs = 10;                    // records a thread holds per pass
 
+// Merge of one (pair, head)'s records.  Every load of a pass is issued
+// before any is used: the (m, l) of the records (one per thread) and each
+// thread's o values of up to kMergeRegs records, so a pass costs one round
+// trip to L2; the weights then need two block reductions.
 __global__ void __launch_bounds__(kMergeThreads) merge_tc_kernel(const DecodeArgs a) {
   constexpr int REC = D + 2;
-  __shared__ float w[KVQ_MAX_SPLITS];
+  __shared__ float w[KVQ_MAX_SPLITS];  // records of a pair: at most KVQ_MAX_SPLITS (the workspace stride)
   __shared__ float red[kMergeThreads / 32];
-  __shared__ float part[kMergeThreads / D][D];
+  __shared__ float part[kMergeGroups][D];
+  __shared__ int bound[kTcMaxCtas + 1];
   const int pair = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nh = a.gq;
+  // the range table in shared memory: one parallel read of the parameter
+  // array instead of a search whose every step would wait on the constant
+  // cache
+  for (int i = tid; i <= a.n_cta; i += kMergeThreads) bound[i] = a.tc_bound[i];
+  __syncthreads();
   grid_dep_wait();  // launched as a dependent of the decode grid: its records first
   const long long nt = a.n_tiles;
-  const int first = tc_owner(a.tc_bound, a.n_cta, (long long)pair * nt);
-  const int last = tc_owner(a.tc_bound, a.n_cta, (long long)pair * nt + nt - 1);
+  const int first = tc_owner(bound, a.n_cta, (long long)pair * nt);
+  const int last = tc_owner(bound, a.n_cta, (long long)pair * nt + nt - 1);
   const int pieces = last - first + 1;
   if (pieces == 1) return;  // written by the decode launch itself
   const float* recs = a.part + (size_t)pair * a.n_splits * nh * REC + (size_t)h * REC;
+  const int c = tid % D, k = tid / D;
+  float ov[kMergeRegs];
+#pragma unroll
+  for (int i = 0; i < kMergeRegs; ++i) {
+    const int s = k + i * kMergeGroups;
+    ov[i] = s < pieces ? __ldcg(recs + (size_t)s * nh * REC + c) : 0.f;
+  }
+  float mt = -INFINITY, lt = 0.f;
+  if (tid < pieces) {
+    mt = __ldcg(recs + (size_t)tid * nh * REC + D);
+    lt = __ldcg(recs + (size_t)tid * nh * REC + D + 1);
+  }
   // M
-  float m = tid < pieces ? recs[(size_t)tid * nh * REC + D] : -INFINITY;
+  float m = mt;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
   if (lane == 0) red[warp] = m;
@@ -1461,14 +1485,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_tc_kernel(const DecodeArg
 #pragma unroll
   for (int i = 1; i < kMergeThreads / 32; ++i) m = fmaxf(m, red[i]);
   __syncthreads();
-  // L and the weights
-  float l = 0.f;
-  if (tid < pieces) {
-    const float* rr = recs + (size_t)tid * nh * REC;
-    const float ws = m == -INFINITY ? 0.f : exp2f(rr[D] - m);
-    w[tid] = ws;
-    l = rr[D + 1] * ws;
-  }
+  // weights and L
+  const float wt = (tid < pieces && m != -INFINITY) ? exp2f(mt - m) : 0.f;
+  if (tid < pieces) w[tid] = wt;
+  float l = lt * wt;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(kFull, l, off);
   if (lane == 0) red[warp] = l;
@@ -1476,16 +1496,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_tc_kernel(const DecodeArg
   l = 0.f;
 #pragma unroll
   for (int i = 0; i < kMergeThreads / 32; ++i) l += red[i];
-  // O: group k sums records k, k + 4, ...
-  const int c = tid % D, k = tid / D;
+  // O
   float o = 0.f;
-#pragma unroll 8
-  for (int s = k; s < pieces; s += kMergeThreads / D) o += recs[(size_t)s * nh * REC + c] * w[s];
+#pragma unroll
+  for (int i = 0; i < kMergeRegs; ++i) {
+    const int s = k + i * kMergeGroups;
+    if (s < pieces) o = fmaf(ov[i], w[s], o);
+  }
+  for (int s = k + kMergeRegs * kMergeGroups; s < pieces; s += kMergeGroups)  // past 80 records
+    o = fmaf(__ldcg(recs + (size_t)s * nh * REC + c), w[s], o);
   part[k][c] = o;
   __syncthreads();
   if (k == 0) {
 #pragma unroll
-    for (int i = 1; i < kMergeThreads / D; ++i) o += part[i][c];
+    for (int i = 1; i < kMergeGroups; ++i) o += part[i][c];
     a.out[((size_t)pair * nh + h) * D + c] = __float2half_rn(l > 0.f ? o / l : 0.f);
   }
 }
