@@ -203,16 +203,22 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q,
                                 void* out, void* workspace, size_t ws_bytes,
                                 void* stream);
 
-/* One decode step of KIVI Algorithm 1's decoding branch (KIVI page, "附录细节"
- * Algorithm 1): the new token of every (batch, kv head) is appended as by
- * kvq_quantize_append with T = 1 (k_new, v_new fp16 [batch][h_kv][1][d_h]);
- * decode attention then runs over the cache as the append left it, as by
- * kvq_decode_attention (q, out, workspace: as there); the K flush that the
- * append made due follows, as by kvq_flush_residual.  The results equal
- * those of the three calls in that order.  The kernels are chained with
- * programmatic dependent launch: each starts while the previous one ends,
- * and the flush, which touches nothing the attention reads, runs beside the
- * attention's last warps.  Asynchronous on `stream`.  Returns KVQ_OK, or a
+/* One decode step in the manner of KIVI Algorithm 1's decoding branch (KIVI
+ * page, "附录细节" Algorithm 1): the new token of every (batch, kv head) is
+ * appended as by kvq_quantize_append with T = 1 (k_new, v_new fp16
+ * [batch][h_kv][1][d_h]); decode attention then runs over the cache as the
+ * append left it, as by kvq_decode_attention (q, out, workspace: as there);
+ * the K flush that the append made due follows, as by kvq_flush_residual.
+ * The results equal those of the three calls in that order.  Algorithm 1
+ * quantizes a K ring that reached R before its attention; this call
+ * attends first (the ring of R fp16 K tokens is the state the attention
+ * sees), so those tokens enter one step's attention at full precision;
+ * kvq_quantize_append, kvq_flush_residual, kvq_decode_attention in that
+ * order give Algorithm 1's.  The kernels are chained with programmatic
+ * dependent launch: each starts while the previous one ends, and the flush,
+ * which touches nothing the attention reads and takes the new token from
+ * k_new (k_new must stay unchanged until the step completes), runs beside
+ * the attention's last warps.  Asynchronous on `stream`.  Returns KVQ_OK, or a
  * negative status; if the attention fails after the append was enqueued
  * the cache's host lengths are restored, but the append's device writes
  * (ring slot, evicted V row) have happened. */

@@ -709,7 +709,7 @@ kvq_status kvq_quantize_append(kvq_cache* cache, const void* k_new, const void* 
 }
 
 namespace {
-kvq_status flush_impl(kvq_cache* cache, cudaStream_t stream, bool pdl);
+kvq_status flush_impl(kvq_cache* cache, cudaStream_t stream, bool pdl, const void* k_new = nullptr);
 kvq_status decode_attention_impl(const kvq_cache* cache, const void* q, void* out, void* ws, size_t ws_bytes,
                                  cudaStream_t s, bool pdl, int dep_t0 = 0);
 void flush_bookkeeping(kvq_cache* cache, int n);
@@ -757,7 +757,9 @@ kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_ne
     *cache = before;  // nothing of the step counts: the caller may retry it
     return st;
   }
-  if (ap == KVQ_FLUSH_DUE) return flush_impl(cache, s, true);
+  // the flush may start before the append completes: it takes the step's
+  // new token from k_new rather than from the ring slot the append writes
+  if (ap == KVQ_FLUSH_DUE) return flush_impl(cache, s, true, k_new);
   return KVQ_OK;
 }
 
@@ -783,7 +785,9 @@ kvq_status kvq_decode_step_host(kvq_cache* cache, const void* host_in, void* hos
 }
 
 namespace {
-kvq_status flush_impl(kvq_cache* cache, cudaStream_t stream, bool pdl) {
+// k_new (a decode step's new tokens, [batch][h_kv][1][d_h]): the newest ring
+// token is read from there instead of its ring slot.
+kvq_status flush_impl(kvq_cache* cache, cudaStream_t stream, bool pdl, const void* k_new) {
   const int G = cache->group, R = cache->resid_cap;
   const int n = (cache->nkr / G) * G;
   if (n == 0) return KVQ_OK;
@@ -803,6 +807,11 @@ kvq_status flush_impl(kvq_cache* cache, cudaStream_t stream, bool pdl) {
   a.k_groups = n / G;
   a.k_nk0 = last.nk;
   a.ksrc = {INT_MAX, cache->k_ring_start};
+  if (k_new && cache->nkr >= 1 && cache->nkr - 1 < n) {  // the newest token is among those flushed
+    a.k_new = static_cast<const __half*>(k_new);
+    a.T = 1;
+    a.ksrc.n_old = cache->nkr - 1;
+  }
   const cudaError_t e = kvq::launch_flush(a, stream, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "flush launch");
   flush_bookkeeping(cache, n);

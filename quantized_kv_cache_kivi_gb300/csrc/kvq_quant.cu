@@ -313,12 +313,15 @@ __global__ void __launch_bounds__(kQuantThreads) flush_kernel(const AppendArgs a
   const int gi = blockIdx.y;
   const __half* ring_k = a.kr + pair * (size_t)a.R * D;
   // Inside a decode step this grid may start while the decode attention
-  // still runs: it reads ring slots and writes packed rows that the attention
-  // leaves alone, and the append it reads from completed before the
-  // attention let it start.  It completes only after the attention does
-  // (the wait at the end), so a kernel waiting on it waits on both.
+  // still runs, and even before the step's append has finished: it reads
+  // only ring slots written by earlier steps (tokens p >= ksrc.n_old, the
+  // step's new one, come from the step's input k_new, not from the ring slot
+  // the append is writing) and writes packed rows that the attention and the
+  // append leave alone.  It completes only after the attention does (the
+  // wait at the end), so a kernel waiting on it waits on both.
   grid_dep_launch();
-  quant_k_group_any<D, Z>(a.dst, a.bits, a.G, a.R, pair, ring_k, nullptr, a.ksrc, gi * a.G,
+  const __half* in_k = a.k_new ? a.k_new + pair * (size_t)a.T * D : nullptr;
+  quant_k_group_any<D, Z>(a.dst, a.bits, a.G, a.R, pair, ring_k, in_k, a.ksrc, gi * a.G,
                    a.k_nk0 + gi * a.G, a.k_nk0 / a.G + gi, qs);
   grid_dep_wait();
 }
