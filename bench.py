@@ -636,12 +636,13 @@ def run_ours(args, rank, world, local_rank):
     oh = torch.empty(B, Hq, d, dtype=torch.float16).pin_memory()
     e2e_s = []
     n_e2e = min(args.steps, 500)
+    rows = [host_in[j] for j in range(pool)]
     for i in range(n_e2e):
         j = i % pool
         flush_l2(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        kvq.kvq_decode_step_host(cache, host_in[j], oh, dev_in, out, ws)
+        kvq.kvq_decode_step_host(cache, rows[j], oh, dev_in, out, ws, stream)
         stream.synchronize()
         e2e_s.append(time.perf_counter() - t0)
         reset()
