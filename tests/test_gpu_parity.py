@@ -198,6 +198,23 @@ def test_attention_many_pairs_repeatable(G, bits, gq, ws_splits):
         assert np.array_equal(pair.gpu_attention(q, ws=ws), first)
 
 
+def test_attention_pairs_of_one_and_two_pieces():
+    """More pairs than half the GPU's warp slots: the one-query-head kernel
+    gives some pairs two pieces (a merge) and the rest one (the output
+    written directly), so that every slot is filled.  Sampled heads of both
+    kinds against the oracle, and repeated calls identical."""
+    B, H, d, G, R = 50, 32, 128, 32, 64
+    heads = [(0, 0), (0, 31), (13, 5), (26, 0), (49, 31)]  # pairs 0, 31, 421, 832, 1599
+    pair = KiviPair(B, H, H, d, G, R, 2, cap=256, heads=heads)
+    K, V = kv(61, B, H, 150, d)
+    pair.prefill(K, V)
+    q = _q(11, B, H, d)
+    ws = pair.workspace()
+    assert pair.attention_error(q, ws=ws) < TOL
+    first = pair.gpu_attention(q, ws=ws)
+    assert np.array_equal(pair.gpu_attention(q, ws=ws), first)
+
+
 @pytest.mark.parametrize("gq,G,bits", [(1, 32, 2), (7, 32, 4), (4, 64, 4)])
 def test_attention_one_long_head(gq, G, bits):
     """One kv head with a long context: its tiles spread over more CTAs than
