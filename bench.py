@@ -642,7 +642,7 @@ def run_ours(args, rank, world, local_rank):
         flush_l2(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        kvq.kvq_decode_step_host(cache, rows[j], oh, dev_in, out, ws, stream)
+        kvq.kvq_decode_step_host(cache, rows[j], oh, dev_in, out, ws, stream=stream)
         stream.synchronize()
         e2e_s.append(time.perf_counter() - t0)
         reset()

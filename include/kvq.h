@@ -203,27 +203,33 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q,
                                 void* out, void* workspace, size_t ws_bytes,
                                 void* stream);
 
-/* One decode step in the manner of KIVI Algorithm 1's decoding branch (KIVI
- * page, "附录细节" Algorithm 1): the new token of every (batch, kv head) is
- * appended as by kvq_quantize_append with T = 1 (k_new, v_new fp16
- * [batch][h_kv][1][d_h]); decode attention then runs over the cache as the
- * append left it, as by kvq_decode_attention (q, out, workspace: as there);
- * the K flush that the append made due follows, as by kvq_flush_residual.
- * The results equal those of the three calls in that order.  Algorithm 1
- * quantizes a K ring that reached R before its attention; this call
- * attends first (the ring of R fp16 K tokens is the state the attention
- * sees), so those tokens enter one step's attention at full precision;
- * kvq_quantize_append, kvq_flush_residual, kvq_decode_attention in that
- * order give Algorithm 1's.  The kernels are chained with programmatic
- * dependent launch: each starts while the previous one ends, and the flush,
- * which touches nothing the attention reads and takes the new token from
- * k_new (k_new must stay unchanged until the step completes), runs beside
- * the attention's last warps.  Asynchronous on `stream`.  Returns KVQ_OK, or a
- * negative status; if the attention fails after the append was enqueued
- * the cache's host lengths are restored, but the append's device writes
- * (ring slot, evicted V row) have happened. */
+/* Order of a decode step's attention and its due K flush. */
+typedef enum {
+  KVQ_STEP_ATTEND_FIRST = 0, /* attention over the ring of R fp16 K tokens, then the flush */
+  KVQ_STEP_FLUSH_FIRST = 1   /* the flush, then the attention (KIVI Algorithm 1's order) */
+} kvq_step_order;
+
+/* One decode step of KIVI Algorithm 1's decoding branch (KIVI page,
+ * "附录细节" Algorithm 1): the new token of every (batch, kv head) is appended
+ * as by kvq_quantize_append with T = 1 (k_new, v_new fp16
+ * [batch][h_kv][1][d_h]); the K flush that the append made due runs as by
+ * kvq_flush_residual, and decode attention as by kvq_decode_attention (q,
+ * out, workspace: as there).  `order` KVQ_STEP_FLUSH_FIRST is Algorithm 1's
+ * order (a K ring that reached R is quantized before the attention);
+ * KVQ_STEP_ATTEND_FIRST attends over the state the append left (R fp16 K
+ * tokens) and flushes after.  The results equal those of the three calls
+ * in the same order.  The kernels are chained with programmatic dependent
+ * launch: each starts while the previous one ends; the attention's chunks
+ * that hold no token the append or the flush writes start at once; the
+ * flush takes the step's new token from k_new (unchanged until the step
+ * completes), and after the attention it runs beside the attention's last
+ * warps.  Asynchronous on `stream`.  Returns KVQ_OK, or a negative status
+ * (KVQ_ERR_INVALID_ARG also for an unknown order); if a launch fails after
+ * the append was enqueued the cache's host lengths are restored, but the
+ * device writes already enqueued (ring slot, evicted V row, flushed rows)
+ * happen. */
 kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_new, const void* q,
-                           void* out, void* workspace, size_t ws_bytes, void* stream);
+                           void* out, void* workspace, size_t ws_bytes, int32_t order, void* stream);
 
 /* kvq_decode_step fed from host memory: the step's inputs are copied from
  * host_in to dev_in, the step runs on them, and its output is copied from
@@ -234,11 +240,12 @@ kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_ne
  *                    [batch][h_kv][1][d_h] layout of kvq_decode_step)
  *   host_out         fp16 [batch][h_q][d_h]; dev_out device, the same shape
  * Host buffers should be page-locked for the copies to be asynchronous;
- * device buffers 16-byte aligned.  workspace, ws_bytes: as for
+ * device buffers 16-byte aligned.  workspace, ws_bytes, order: as for
  * kvq_decode_step.  Returns what kvq_decode_step returns, or
  * KVQ_ERR_INVALID_ARG / KVQ_ERR_CUDA for the arguments and the copies. */
 kvq_status kvq_decode_step_host(kvq_cache* cache, const void* host_in, void* host_out, void* dev_in,
-                                void* dev_out, void* workspace, size_t ws_bytes, void* stream);
+                                void* dev_out, void* workspace, size_t ws_bytes, int32_t order,
+                                void* stream);
 
 /* Device error word of a workspace (0 = none; nonzero = a bounded wait timed
  * out inside a kernel).  Synchronizes `stream`. */

@@ -729,9 +729,11 @@ kvq_status kvq_decode_attention(const kvq_cache* cache, const void* q, void* out
 }
 
 kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_new, const void* q, void* out,
-                           void* ws, size_t ws_bytes, void* stream) {
+                           void* ws, size_t ws_bytes, int32_t order, void* stream) {
   kvq_status st = validate_cache(cache);
   if (st != KVQ_OK) return st;
+  if (order != KVQ_STEP_ATTEND_FIRST && order != KVQ_STEP_FLUSH_FIRST)
+    return fail(KVQ_ERR_INVALID_ARG, "unknown step order %d", (int)order);
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
     return fail(KVQ_ERR_INVALID_ARG, "k_new/v_new must be non-NULL and 16-byte aligned");
   if (!q || !out || !aligned16(q) || !aligned16(out))
@@ -743,8 +745,19 @@ kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_ne
   const kvq_cache before = *cache;
   const kvq_status ap = append_kivi(cache, k_new, v_new, 1, s, true);
   if (ap < 0) return ap;
-  // first token position whose K or V the append wrote: the new token, and
-  // the rows it quantized (one segment; else every chunk waits)
+  // The flush takes the step's new token from k_new rather than from the
+  // ring slot the append writes, so it may start before the append ends.
+  const bool flush_first = order == KVQ_STEP_FLUSH_FIRST;
+  if (flush_first && ap == KVQ_FLUSH_DUE) {
+    st = flush_impl(cache, s, true, k_new);
+    if (st != KVQ_OK) {
+      *cache = before;
+      return st;
+    }
+  }
+  // first token position whose K or V the append (or the flush) wrote: the
+  // new token, and the rows they quantized (one segment; else every chunk
+  // waits)
   int dep_t0 = 0;
   if (cache->n_seg == 1) {
     long long d = (long long)cache->seg[0].nk + cache->nkr - 1;
@@ -757,14 +770,12 @@ kvq_status kvq_decode_step(kvq_cache* cache, const void* k_new, const void* v_ne
     *cache = before;  // nothing of the step counts: the caller may retry it
     return st;
   }
-  // the flush may start before the append completes: it takes the step's
-  // new token from k_new rather than from the ring slot the append writes
-  if (ap == KVQ_FLUSH_DUE) return flush_impl(cache, s, true, k_new);
+  if (!flush_first && ap == KVQ_FLUSH_DUE) return flush_impl(cache, s, true, k_new);
   return KVQ_OK;
 }
 
 kvq_status kvq_decode_step_host(kvq_cache* cache, const void* host_in, void* host_out, void* dev_in,
-                                void* dev_out, void* ws, size_t ws_bytes, void* stream) {
+                                void* dev_out, void* ws, size_t ws_bytes, int32_t order, void* stream) {
   kvq_status st = validate_cache(cache);
   if (st != KVQ_OK) return st;
   if (!host_in || !host_out || !dev_in || !dev_out)
@@ -777,7 +788,7 @@ kvq_status kvq_decode_step_host(kvq_cache* cache, const void* host_in, void* hos
   cudaError_t e = cudaMemcpyAsync(dev_in, host_in, 2 * kv + qb, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "input copy");
   uint8_t* d = static_cast<uint8_t*>(dev_in);
-  st = kvq_decode_step(cache, d, d + kv, d + 2 * kv, dev_out, ws, ws_bytes, stream);
+  st = kvq_decode_step(cache, d, d + kv, d + 2 * kv, dev_out, ws, ws_bytes, order, stream);
   if (st < 0) return st;
   e = cudaMemcpyAsync(host_out, dev_out, qb, cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) return cuda_fail(e, "output copy");

@@ -24,6 +24,7 @@ KVQ_ERR_WORKSPACE = -5
 KVQ_POLICY_KIVI = 0
 KVQ_POLICY_FP16_TAIL = 1
 KVQ_ZERO_MIN, KVQ_ZERO_INT = 0, 1
+KVQ_STEP_ATTEND_FIRST, KVQ_STEP_FLUSH_FIRST = 0, 1
 KVQ_MAX_SEGMENTS = 8
 KVQ_MAX_SPLITS = 128
 KVQ_MAX_SEQS = 256
@@ -96,9 +97,9 @@ def lib():
         L.kvq_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
         L.kvq_decode_attention.argtypes = [cp, _P, _P, _P, ctypes.c_size_t, _P]
         L.kvq_workspace_error.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
-        L.kvq_decode_step.argtypes = [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+        L.kvq_decode_step.argtypes = [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_int32, _P]
         L.kvq_decode_step.restype = ctypes.c_int
-        L.kvq_decode_step_host.argtypes = [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+        L.kvq_decode_step_host.argtypes = [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_int32, _P]
         L.kvq_decode_step_host.restype = ctypes.c_int
         L.kvq_decode_attention_noalloc.argtypes = [cp, _P, _P, _P]
         L.kvq_decode_attention_noalloc.restype = ctypes.c_int
@@ -193,18 +194,21 @@ def kvq_decode_attention(cache, q, out, ws, stream=None):
     return _check(st, "kvq_decode_attention")
 
 
-def kvq_decode_step(cache, k_new, v_new, q, out, ws, stream=None):
-    """Append one token per head, decode attention, and the K flush if due."""
+def kvq_decode_step(cache, k_new, v_new, q, out, ws, stream=None, order=KVQ_STEP_ATTEND_FIRST):
+    """Append one token per head, then decode attention and the K flush if
+    due, in `order` (KVQ_STEP_FLUSH_FIRST: KIVI Algorithm 1's)."""
     st = lib().kvq_decode_step(ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out), _ptr(ws),
-                               ws.numel() * ws.element_size(), _stream(stream))
+                               ws.numel() * ws.element_size(), order, _stream(stream))
     return _check(st, "kvq_decode_step")
 
 
-def kvq_decode_step_host(cache, host_in, host_out, dev_in, dev_out, ws, stream=None):
+def kvq_decode_step_host(cache, host_in, host_out, dev_in, dev_out, ws, stream=None,
+                         order=KVQ_STEP_ATTEND_FIRST):
     """kvq_decode_step with its inputs copied from host memory and its output
     copied back (host_in / dev_in: [new K | new V | q] fp16)."""
     st = lib().kvq_decode_step_host(ctypes.byref(cache.c), _ptr(host_in), _ptr(host_out), _ptr(dev_in),
-                                    _ptr(dev_out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+                                    _ptr(dev_out), _ptr(ws), ws.numel() * ws.element_size(), order,
+                                    _stream(stream))
     return _check(st, "kvq_decode_step_host")
 
 

@@ -566,21 +566,24 @@ def test_windowquant_workload_full_shape():
     assert err < TOL
 
 
-@pytest.mark.parametrize("G,zp,gq,offset", [
-    (32, kvq.KVQ_ZERO_MIN, 1, False),   # one query head per kv head: the warp kernel
-    (64, kvq.KVQ_ZERO_INT, 1, True),    # the same, 64-token groups, integer zero, offset K channels
-    (32, kvq.KVQ_ZERO_MIN, 2, False),   # two query heads per kv head: the tensor-core kernel
+@pytest.mark.parametrize("G,zp,gq,offset,order", [
+    (32, kvq.KVQ_ZERO_MIN, 1, False, kvq.KVQ_STEP_ATTEND_FIRST),  # one query head per kv head: the warp kernel
+    (64, kvq.KVQ_ZERO_INT, 1, True, kvq.KVQ_STEP_ATTEND_FIRST),   # 64-token groups, integer zero, offset K
+    (32, kvq.KVQ_ZERO_MIN, 2, False, kvq.KVQ_STEP_ATTEND_FIRST),  # two query heads: the tensor-core kernel
+    (32, kvq.KVQ_ZERO_MIN, 1, False, kvq.KVQ_STEP_FLUSH_FIRST),   # KIVI Algorithm 1's order
+    (64, kvq.KVQ_ZERO_INT, 2, True, kvq.KVQ_STEP_FLUSH_FIRST),
 ])
-def test_decode_step_matches_separate_calls_and_oracle(G, zp, gq, offset):
-    """kvq_decode_step (append, attention and the due K flush, chained with
-    programmatic dependent launch; the attention's chunks that hold no token
-    the append writes start before the append completes) against the three
-    calls in order on a second cache: identical outputs
-    every step and identical buffers after 80 steps that cross a flush;
-    against the oracle's Algorithm 1 decoding (the flush after the
-    attention) within tolerance."""
+def test_decode_step_matches_separate_calls_and_oracle(G, zp, gq, offset, order):
+    """kvq_decode_step (append, attention and the due K flush in either
+    order, chained with programmatic dependent launch; the attention's
+    chunks that hold no token the append or the flush writes start before
+    those complete) against the three calls in the same order on a second
+    cache: identical outputs every step and identical buffers after 80
+    steps that cross flushes; against the oracle's decoding (Algorithm 1:
+    the flush before the attention; else after it) within tolerance."""
     B, H, d, R = 2, 4, 128, 64
     Hq = H * gq
+    flush_first = order == kvq.KVQ_STEP_FLUSH_FIRST
     a = KiviPair(B, H, Hq, d, G, R, 2, cap=1024, zero_point=zp)
     b = KiviPair(B, H, Hq, d, G, R, 2, cap=1024, heads=[], zero_point=zp)
     K, V = kv(81, B, H, 380, d)
@@ -596,17 +599,20 @@ def test_decode_step_matches_separate_calls_and_oracle(G, zp, gq, offset):
         qd = to_dev(q)
         out_a, out_b = torch.empty_like(qd), torch.empty_like(qd)
         kt, vt = to_dev(K[:, :, t:t + 1]), to_dev(V[:, :, t:t + 1])
-        kvq.kvq_decode_step(a.gpu, kt, vt, qd, out_a, ws_a)
+        kvq.kvq_decode_step(a.gpu, kt, vt, qd, out_a, ws_a, order=order)
         st = kvq.kvq_quantize_append(b.gpu, kt, vt)
+        if st == kvq.KVQ_FLUSH_DUE and flush_first:
+            kvq.kvq_flush_residual(b.gpu)
         kvq.kvq_decode_attention(b.gpu, qd, out_b, ws_b)
         if st == kvq.KVQ_FLUSH_DUE:
-            kvq.kvq_flush_residual(b.gpu)
+            if not flush_first:
+                kvq.kvq_flush_residual(b.gpu)
             flushes += 1
         torch.cuda.synchronize()
         assert np.array_equal(out_a.cpu().numpy(), out_b.cpu().numpy()), t
         for (bb, h), head in a.orc.items():
-            head.decode_update(K[bb, h, t], V[bb, h, t], flush_k=False)
-        if t % 16 == 0 or len(next(iter(a.orc.values())).kr) == R:
+            head.decode_update(K[bb, h, t], V[bb, h, t], flush_k=flush_first)
+        if t % 16 == 0 or len(next(iter(a.orc.values())).kr) in (0, R):
             ref = a.oracle_attention(q)
             got = out_a.cpu().numpy()
             err = max(max_abs_rel(got[bb, h * gq + j], ref[(bb, h)][j]) for (bb, h) in ref
@@ -621,6 +627,19 @@ def test_decode_step_matches_separate_calls_and_oracle(G, zp, gq, offset):
     ga, gb = a.gpu_buffers(), b.gpu_buffers()
     for name in ga:
         assert np.array_equal(ga[name], gb[name]), name
+
+
+def test_decode_step_rejects_unknown_order():
+    B, H, d, G, R = 1, 2, 128, 32, 64
+    a = KiviPair(B, H, H, d, G, R, 2, cap=256, heads=[])
+    K, V = kv(85, B, H, 100, d)
+    a.prefill(K, V)
+    before = (a.gpu.c.seg[0].nk, a.gpu.c.seg[0].nv, a.gpu.c.nkr, a.gpu.c.nvr)
+    q = to_dev(_q(5, B, H, d))
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_decode_step(a.gpu, to_dev(K[:, :, :1]), to_dev(V[:, :, :1]), q, torch.empty_like(q),
+                            a.workspace(), order=7)
+    assert (a.gpu.c.seg[0].nk, a.gpu.c.seg[0].nv, a.gpu.c.nkr, a.gpu.c.nvr) == before
 
 
 def test_decode_step_host_matches_device_step():
