@@ -17,8 +17,9 @@
 // Work split.  The token axis of every (batch, kv head) pair is cut into
 // chunks (32 tokens with K and V packed; 8-token blocks where a ring is
 // involved: kvq_internal.h, warp_chunk) and each pair's chunk list into k
-// contiguous pieces of equal cost, k as large as the GPU's resident warps
-// allow (kWarpWarps per SM).  Each piece is a one-warp CTA that stages its
+// or k - 1 contiguous pieces of equal cost, so that the pieces of all pairs
+// fill the GPU's resident warp slots (kWarpWarps per SM).  Each piece is a
+// one-warp CTA that stages its
 // own chunks, kWarpSlots ahead, into its own slots: the K and V codes by
 // bulk copies (TMA engine, mbarrier completion) that one lane issues, the
 // small scale / zero arrays by 16-byte cp.async pieces of every lane
@@ -584,8 +585,9 @@ __device__ __noinline__ void merge_if_last(const WarpArgs& a, long long pair, in
   if (lane == 0) a.counters[pair] = 0;  // ready for the next call on this workspace
 }
 
-// One warp per CTA, kWarpWarps CTAs per SM: CTA i takes piece i % k of
-// pair i / k.
+// One warp per CTA, kWarpWarps CTAs per SM: CTAs [0, P1 k) take the pieces
+// of the pairs cut into k, pair by pair; the rest those of the pairs cut
+// into k - 1.
 template <int NGV, bool INTZ>
 __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -611,12 +613,14 @@ __global__ void __launch_bounds__(32, kWarpWarps) decode_warp_kernel(const WarpA
     for (int s = 0; s < kWarpSlots; ++s) mbar_init(&bars[s], kSlotArrivals);
     mbar_fence_init();
   }
-  // Inside a decode step this grid starts while the step's append runs.
-  // Chunks from a.dep_c on hold tokens the append writes (its evicted V row,
-  // the new ring token), so staging the first of them waits for the append
-  // grid; the chunks before it are packed rows that no kernel of the step
-  // writes, and the kernels before the append had completed before the
-  // append let this grid start.
+  // Inside a decode step this grid starts while the kernel before it (the
+  // step's append, or its flush) runs.  Chunks from a.dep_c on hold tokens
+  // those write (the evicted V row, the new ring token, the flushed K
+  // rows), so staging the first of them waits for that grid, whose
+  // completion implies the step's earlier kernels' (each waits for its own
+  // predecessor before it completes); the chunks before it are packed rows
+  // that no kernel of the step writes, and the kernels of earlier steps had
+  // completed before the step's first kernel let the next one start.
   bool waited = false;
   auto stage = [&](int c, int s) {
     if (!waited && c >= a.dep_c) {

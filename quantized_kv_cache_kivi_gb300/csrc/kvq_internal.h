@@ -307,8 +307,9 @@ struct WarpArgs {
   long long Cp;             // cost of a pair (kWarpWpp, kWarpWx)
   int P, k;                 // pairs, pieces per pair (records when k > 1)
   int P1;                   // pairs [0, P1) have k pieces, pairs [P1, P) k - 1
-  // first chunk holding a token that the decode step's append wrote (its
-  // staging waits for the append grid); 0 outside a decode step
+  // first chunk holding a token that the decode step's append (or flush)
+  // wrote (its staging waits for the kernel before this grid); 0 outside a
+  // decode step
   int dep_c;
 };
 
