@@ -87,3 +87,21 @@ def test_plan_detects_a_short_buffer():
     c = fake_cache(1, 1, 1, 128, 32, 64, [(2, 256, 256, 200)], 8, 64, 0, 0)
     c.seg[0].nk = 288  # beyond capacity
     assert decode_status(c) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_decode_step_checks_arguments_before_any_launch():
+    """kvq_decode_step / kvq_decode_step_host reject an unknown order and
+    missing buffers before anything is enqueued, and leave the cache's
+    lengths as they were."""
+    L = kvq.lib()
+    c = fake_cache(2, 3, 1, 128, 32, 64, [(2, 256, 128, 96)], 16, 48, 0, 0)
+    before = (c.seg[0].nk, c.seg[0].nv, c.nkr, c.nvr, c.k_ring_start, c.v_ring_start)
+    ws = L.kvq_workspace_bytes(ctypes.byref(c), 8)
+    p = ctypes.c_void_p
+    st = L.kvq_decode_step(ctypes.byref(c), p(BASE - 4096 * 4), p(BASE - 4096 * 3), p(BASE - 4096 * 2),
+                           p(BASE - 4096), p(BASE // 2), ws, 7, None)
+    assert st == kvq.KVQ_ERR_INVALID_ARG
+    st = L.kvq_decode_step_host(ctypes.byref(c), None, None, p(BASE - 4096), p(BASE - 8192), p(BASE // 2), ws,
+                                kvq.KVQ_STEP_ATTEND_FIRST, None)
+    assert st == kvq.KVQ_ERR_INVALID_ARG
+    assert (c.seg[0].nk, c.seg[0].nv, c.nkr, c.nvr, c.k_ring_start, c.v_ring_start) == before
