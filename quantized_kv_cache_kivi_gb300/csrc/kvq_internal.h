@@ -342,13 +342,15 @@ __host__ __device__ inline WarpChunk warp_chunk(const WarpArgs& a, int c) {
   return ch;
 }
 
-// Weights of a 32-token packed chunk and of an 8-token ring chunk (about
-// their bytes) for cutting a pair into pieces of equal cost.
+// Weights of a 32-token packed chunk and of an 8-token ring chunk for
+// cutting a pair into pieces of equal cost: about their bytes (6 : 8), the
+// ring chunk raised to 10 by measured warp times (a ring chunk took ~18 %
+// more time per unit of byte cost than a packed one).
 #ifndef KVQ_WARP_WPP
 #define KVQ_WARP_WPP 6
 #endif
 #ifndef KVQ_WARP_WX
-#define KVQ_WARP_WX 8
+#define KVQ_WARP_WX 10
 #endif
 constexpr int kWarpWpp = KVQ_WARP_WPP, kWarpWx = KVQ_WARP_WX;
 
