@@ -192,12 +192,12 @@ def paged_bytes(cache):
 
 def streaming_steps(cache, w, device, flush_l2, peak, to_prompt):
     """The streaming workload as specified: after the prompt, `steps`
-    generated tokens, each step = quantize-append of the new token, the K
-    flush when the ring reaches R (KIVI Algorithm 1), and decode attention;
-    new K, V and q drawn per step (seed = step).  L2 is flushed before every
-    step; each step is timed with CUDA events around its calls.  The cache
-    given holds the prompt; `to_prompt()` puts its lengths back to the
-    state right after the prompt's ingest."""
+    generated tokens, each step one kvq_decode_step call in KIVI Algorithm
+    1's order: quantize-append of the new token, the K flush when the ring
+    reaches R, decode attention; new K, V and q drawn per step (seed =
+    step).  L2 is flushed before every step; each step is timed with CUDA
+    events around the call.  The cache given holds the prompt; `to_prompt()`
+    puts its lengths back to the state right after the prompt's ingest."""
     import torch
     from quantized_kv_cache_kivi_gb300 import kvq
 
@@ -218,13 +218,12 @@ def streaming_steps(cache, w, device, flush_l2, peak, to_prompt):
     torch.cuda.synchronize()
     for t, (k, v, q) in enumerate(toks):
         flush_l2(t)
+        nkr = cache.c.nkr
         ev[t][0].record()
-        if kvq.kvq_quantize_append(cache, k, v) == kvq.KVQ_FLUSH_DUE:
-            kvq.kvq_flush_residual(cache)
-            flushes += 1
-        nbytes.append(cache_bytes(cache))
-        kvq.kvq_decode_attention(cache, q, out, ws)
+        kvq.kvq_decode_step(cache, k, v, q, out, ws, order=kvq.KVQ_STEP_FLUSH_FIRST)
         ev[t][1].record()
+        flushes += cache.c.nkr <= nkr  # the ring did not grow: it was flushed
+        nbytes.append(cache_bytes(cache))  # the state the attention read
     torch.cuda.synchronize()
     if kvq.kvq_workspace_error(ws):
         raise RuntimeError("decode kernel reported a timed-out wait")
@@ -233,7 +232,8 @@ def streaming_steps(cache, w, device, flush_l2, peak, to_prompt):
     return {"steps": n, "us_per_step_mean": float(us.mean()), "us_per_step_max": float(us.max()),
             "us_per_step_min": float(us.min()), "flushes": flushes, "bytes_per_step_mean": float(np.mean(nbytes)),
             "GB/s": gbs, "frac": gbs / peak,
-            "note": "step = append + flush when due + attention, L2 flushed before each step"}
+            "note": "step = one kvq_decode_step (append, flush when due, attention: Algorithm 1's order), "
+                    "L2 flushed before each step"}
 
 
 def per_workload_attention(device, flush_l2, peak, reps=20, only=None):
@@ -357,7 +357,7 @@ def per_workload_attention(device, flush_l2, peak, reps=20, only=None):
         torch.cuda.synchronize()
         if only != "prefill_streaming":
             res[name] = timed(cache, B, Hq, d, w["seed"])
-        if name == "streaming" and only is None:
+        if name == "streaming" and only in (None, "streaming"):
             res["streaming_steps"] = streaming_steps(cache, w, device, flush_l2, peak,
                                                      lambda: set_lengths(cache, st_prompt))
         del cache
