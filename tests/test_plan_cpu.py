@@ -105,3 +105,19 @@ def test_decode_step_checks_arguments_before_any_launch():
                                 kvq.KVQ_STEP_ATTEND_FIRST, None)
     assert st == kvq.KVQ_ERR_INVALID_ARG
     assert (c.seg[0].nk, c.seg[0].nv, c.nkr, c.nvr, c.k_ring_start, c.v_ring_start) == before
+
+
+@pytest.mark.parametrize("B,H,L", [(64, 32, 8256), (50, 32, 150), (1, 1, 4160)])
+def test_plan_one_head_kernel_fills_the_slots(B, H, L):
+    """The one-query-head kernel's plan for many pairs (pairs cut into k and
+    k - 1 pieces to fill every warp slot), for a pair count near the slot
+    count, and for one long pair: the plan passes the pre-launch copy check
+    and reaches the launch."""
+    G, d, R = 32, 128, 128
+    nkr = L % G if L % G else G  # K: whole groups packed, the rest in the ring
+    nk = L - nkr
+    nvr = min(L, R)  # V: the newest R tokens in the ring
+    nv = L - nvr
+    cap = (L // G + 2) * G
+    c = fake_cache(B, H, 1, d, G, R, [(2, cap, nk, nv)], nkr, nvr, 5, 7)
+    assert decode_status(c) == kvq.KVQ_ERR_CUDA, kvq.lib().kvq_last_error_string()
