@@ -5,8 +5,9 @@ belongs to another allocator).  Its workspace is the library's own static
 device array, so the call needs no buffer from the caller.
 
 Checked through the C ABI against kvq_decode_attention with a caller
-workspace (itself checked against the oracle elsewhere), on two calls in a
-row, so the second call runs on the array the first one left behind."""
+workspace and, on two sampled (batch, kv head) pairs, against the oracle, on
+two calls in a row, so the second call runs on the array the first one left
+behind."""
 import ctypes
 
 import numpy as np
@@ -25,14 +26,15 @@ from quantized_kv_cache_kivi_gb300 import kvq, synth  # noqa: E402
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
     B, H, gq, d, G, R = 4, 8, 4, 128, 32, 128
-    pair = KiviPair(B, H, H * gq, d, G, R, 2, cap=3072, heads=[])
+    pair = KiviPair(B, H, H * gq, d, G, R, 2, cap=3072, heads=[(0, 0), (3, 7)])
     K, V = kv(71, B, H, 2600, d)
     pair.prefill(K[:, :, :2599], V[:, :, :2599])
     pair.append(K[:, :, 2599:], V[:, :, 2599:], flush=False)  # packed + full fp16 ring
     ws = torch.zeros(kvq.kvq_workspace_bytes(pair.gpu, kvq.KVQ_MAX_SPLITS), dtype=torch.uint8,
                      device="cuda")
     for call in range(2):
-        q = to_dev(synth.q_block(72, B, H * gq, d, step=call))
+        qh = synth.q_block(72, B, H * gq, d, step=call)
+        q = to_dev(qh)
         ref = torch.empty_like(q)
         got = torch.full_like(q, float("nan"))
         kvq.kvq_decode_attention(pair.gpu, q, ref, ws)
@@ -44,6 +46,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         r = ref.cpu().numpy().astype(np.float64)
         assert np.isfinite(g).all()
         assert max_abs_rel(g, r) < TOL, call
+        orc = pair.oracle_attention(qh)
+        for (b, h), o in orc.items():
+            assert max_abs_rel(g[b, h * gq:(h + 1) * gq], o) < TOL, (call, b, h)
 
 
 def test_noalloc_rejects_caches_beyond_the_static_array():
