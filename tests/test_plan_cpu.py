@@ -121,3 +121,23 @@ def test_plan_one_head_kernel_fills_the_slots(B, H, L):
     cap = (L // G + 2) * G
     c = fake_cache(B, H, 1, d, G, R, [(2, cap, nk, nv)], nkr, nvr, 5, 7)
     assert decode_status(c) == kvq.KVQ_ERR_CUDA, kvq.lib().kvq_last_error_string()
+
+
+def test_warp_chunk_geometry_enumeration(tmp_path):
+    """Many cache states, ring starts, group sizes and pair counts through
+    the one-query-head kernel's chunk, piece and copy geometry (host build
+    of tests/warp_geometry.cu)."""
+    import os
+    import shutil
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = tmp_path / "warp_geometry"
+    subprocess.run([nvcc, "-std=c++17", "-O2", "--expt-relaxed-constexpr", "-x", "cu",
+                    os.path.join(root, "tests", "warp_geometry.cu"), "-o", str(exe)],
+                   check=True, capture_output=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:]
+    assert "bad 0" in r.stdout
